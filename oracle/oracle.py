@@ -1,0 +1,209 @@
+"""NumPy front end of the C oracle (test infrastructure).
+
+Each function copies its inputs, calls the single-threaded C statement of the
+method in ``gc_oracle.c`` and returns fresh NumPy arrays.  Nothing here does
+arithmetic of the method; it only marshals buffers.
+
+Mode and rounding numbers are the oracle's own:
+MINMAX = 0, QSGD = 1, TERN = 2; NEAREST_EVEN = 0, STOCHASTIC = 1.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+MINMAX, QSGD, TERN = 0, 1, 2
+NEAREST_EVEN, STOCHASTIC = 0, 1
+MODES = {"minmax": MINMAX, "qsgd": QSGD, "tern": TERN}
+ROUNDINGS = {"nearest_even": NEAREST_EVEN, "stochastic": STOCHASTIC}
+
+_lib = None
+
+_f32p = ctypes.POINTER(ctypes.c_float)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_u32p = ctypes.POINTER(ctypes.c_uint32)
+_i64 = ctypes.c_int64
+_u64 = ctypes.c_uint64
+_int = ctypes.c_int
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def lib():
+    """Loads (building first if needed) ``libgc_oracle.so``."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not os.path.exists(path) or (
+                os.path.getmtime(path) < os.path.getmtime(_build.SRC)):
+            _build.build()
+        L = ctypes.CDLL(path)
+        L.orc_philox4x32_10.argtypes = [_u32p, _u32p, _u32p]
+        L.orc_philox4x32_10.restype = None
+        L.orc_uniform.argtypes = [_u64, _u64, _u64]
+        L.orc_uniform.restype = ctypes.c_float
+        L.orc_codes_bytes.argtypes = [_i64, _int, _int]
+        L.orc_codes_bytes.restype = _i64
+        L.orc_scales_floats.argtypes = [_i64, _i64, _int]
+        L.orc_scales_floats.restype = _i64
+        L.orc_ef_topk.argtypes = [_f32p, _f32p, _i64, _i64, _i32p, _f32p]
+        L.orc_ef_topk.restype = _int
+        L.orc_quant.argtypes = [_f32p, _i64, _int, _i64, _int, _int, _u64,
+                                _u64, _u8p, _f32p]
+        L.orc_quant.restype = _int
+        L.orc_dequant.argtypes = [_u8p, _f32p, _i64, _int, _i64, _int, _f32p]
+        L.orc_dequant.restype = _int
+        L.orc_ef_quant.argtypes = [_f32p, _f32p, _i64, _int, _i64, _int, _int,
+                                   _u64, _u64, _u8p, _f32p]
+        L.orc_ef_quant.restype = _int
+        L.orc_ef_topk_quant.argtypes = [_f32p, _f32p, _i64, _i64, _int, _i64,
+                                        _int, _u64, _u64, _i32p, _u8p, _f32p]
+        L.orc_ef_topk_quant.restype = _int
+        L.orc_powersgd_step.argtypes = [_f32p, _f32p, _i64, _i64, _int, _f32p,
+                                        _f32p]
+        L.orc_powersgd_step.restype = _int
+        _lib = L
+    return _lib
+
+
+def _p(a, t):
+    return a.ctypes.data_as(t) if a is not None else None
+
+
+def _f32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32)).copy()
+
+
+def _check(st, what):
+    if st != 0:
+        raise OracleError("%s failed with status %d" % (what, st))
+
+
+def _mode(mode):
+    return MODES[mode] if isinstance(mode, str) else int(mode)
+
+
+def _rounding(r):
+    return ROUNDINGS[r] if isinstance(r, str) else int(r)
+
+
+def philox4x32_10(counter, key):
+    """Philox-4x32-10 block: 4 counter words, 2 key words -> 4 words."""
+    c = np.asarray(counter, dtype=np.uint32).copy()
+    k = np.asarray(key, dtype=np.uint32).copy()
+    out = np.zeros(4, dtype=np.uint32)
+    lib().orc_philox4x32_10(_p(c, _u32p), _p(k, _u32p), _p(out, _u32p))
+    return out
+
+
+def uniform(seed, step, i):
+    """The stochastic-rounding draw u in [0, 1) of element i."""
+    return float(lib().orc_uniform(seed, step, i))
+
+
+def codes_bytes(n, bits, mode):
+    return int(lib().orc_codes_bytes(n, bits, _mode(mode)))
+
+
+def scales_floats(n, group, mode):
+    return int(lib().orc_scales_floats(n, group, _mode(mode)))
+
+
+def ef_topk(grad, err, k):
+    """EF + Top-K.  Returns (idx int32[k], val float32[k], err' or None)."""
+    g = _f32(grad)
+    e = _f32(err) if err is not None else None
+    n = g.size
+    idx = np.zeros(max(k, 1), dtype=np.int32)
+    val = np.zeros(max(k, 1), dtype=np.float32)
+    _check(lib().orc_ef_topk(_p(g, _f32p), _p(e, _f32p), n, k,
+                             _p(idx, _i32p), _p(val, _f32p)), "orc_ef_topk")
+    return idx[:k], val[:k], e
+
+
+def quant(x, bits, group, mode, rounding="nearest_even", seed=0, step=0):
+    """Quantise x.  Returns (codes uint8[codes_bytes], scales float32[...])."""
+    xs = _f32(x)
+    n = xs.size
+    m = _mode(mode)
+    cb = codes_bytes(n, bits, m)
+    sf = scales_floats(n, group, m)
+    if cb < 0 or sf < 0:
+        raise OracleError("bad quantisation arguments")
+    codes = np.zeros(max(cb, 1), dtype=np.uint8)
+    scales = np.zeros(max(sf, 1), dtype=np.float32)
+    _check(lib().orc_quant(_p(xs, _f32p), n, bits, group, m,
+                           _rounding(rounding), seed, step, _p(codes, _u8p),
+                           _p(scales, _f32p)), "orc_quant")
+    return codes[:cb], scales[:sf]
+
+
+def dequant(codes, scales, n, bits, group, mode):
+    c = np.ascontiguousarray(codes, dtype=np.uint8).copy()
+    s = _f32(scales)
+    out = np.zeros(max(n, 1), dtype=np.float32)
+    if c.size == 0:
+        c = np.zeros(1, dtype=np.uint8)
+    if s.size == 0:
+        s = np.zeros(1, dtype=np.float32)
+    _check(lib().orc_dequant(_p(c, _u8p), _p(s, _f32p), n, bits, group,
+                             _mode(mode), _p(out, _f32p)), "orc_dequant")
+    return out[:n]
+
+
+def ef_quant(grad, err, bits, group, mode, rounding="nearest_even", seed=0,
+             step=0):
+    """EF + quantise.  Returns (codes, scales, err')."""
+    g = _f32(grad)
+    e = _f32(err)
+    n = g.size
+    m = _mode(mode)
+    cb = codes_bytes(n, bits, m)
+    sf = scales_floats(n, group, m)
+    codes = np.zeros(max(cb, 1), dtype=np.uint8)
+    scales = np.zeros(max(sf, 1), dtype=np.float32)
+    _check(lib().orc_ef_quant(_p(g, _f32p), _p(e, _f32p), n, bits, group, m,
+                              _rounding(rounding), seed, step,
+                              _p(codes, _u8p), _p(scales, _f32p)),
+           "orc_ef_quant")
+    return codes[:cb], scales[:sf], e
+
+
+def ef_topk_quant(grad, err, k, bits, group, rounding="nearest_even", seed=0,
+                  step=0):
+    """EF + Top-K + QSGD on the kept values.
+
+    Returns (idx int32[k], codes, scales, err')."""
+    g = _f32(grad)
+    e = _f32(err)
+    n = g.size
+    cb = codes_bytes(k, bits, QSGD)
+    sf = scales_floats(k, group, QSGD)
+    idx = np.zeros(max(k, 1), dtype=np.int32)
+    codes = np.zeros(max(cb, 1), dtype=np.uint8)
+    scales = np.zeros(max(sf, 1), dtype=np.float32)
+    _check(lib().orc_ef_topk_quant(_p(g, _f32p), _p(e, _f32p), n, k, bits,
+                                   group, _rounding(rounding), seed, step,
+                                   _p(idx, _i32p), _p(codes, _u8p),
+                                   _p(scales, _f32p)), "orc_ef_topk_quant")
+    return idx[:k], codes[:cb], scales[:sf], e
+
+
+def powersgd_step(grad, err, Q, r):
+    """One PowerSGD step on an m x n matrix.  Returns (P_hat, Q', err')."""
+    g = _f32(grad)
+    if g.ndim != 2:
+        raise OracleError("powersgd_step wants a 2-D gradient")
+    m, n = g.shape
+    e = _f32(err).reshape(m, n)
+    q = _f32(Q).reshape(n, r)
+    P = np.zeros((m, r), dtype=np.float32)
+    _check(lib().orc_powersgd_step(_p(g, _f32p), _p(e, _f32p), m, n, r,
+                                   _p(P, _f32p), _p(q, _f32p)),
+           "orc_powersgd_step")
+    return P, q, e
