@@ -13,7 +13,8 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libgc_oracle.so")
 
 CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
-          "-fno-strict-aliasing", "-fPIC", "-Wall", "-Wextra"]
+          "-fno-strict-aliasing", "-fPIC", "-Wall", "-Wextra",
+          "-Wno-maybe-uninitialized"]
 
 
 def build(force=False):

@@ -381,9 +381,10 @@ static float dequant_one(uint32_t q, int negative, group_param p, int mode) {
  * gives q = 0 without dividing.  A sign is recorded only when q != 0, so a
  * zero code always dequantises to +0.
  */
-static int quant_core(const float* x, int64_t n, int bits, int64_t group,
-                      int mode, int rounding, uint64_t seed, uint64_t step,
-                      uint8_t* codes_out, float* scales_out, float* x_hat) {
+static int quant_core(const float* x, int64_t n, int64_t base, int bits,
+                      int64_t group, int mode, int rounding, uint64_t seed,
+                      uint64_t step, uint8_t* codes_out, float* scales_out,
+                      float* x_hat) {
   int st = check_quant_args(n, bits, group, mode, rounding);
   if (st != ORC_OK) return st;
   int64_t total = orc_codes_bytes(n, bits, mode);
@@ -414,7 +415,8 @@ static int quant_core(const float* x, int64_t n, int bits, int64_t group,
         t = p.scale == 0.0f ? 0.0f : fabsf(x[i]) / p.scale;
       uint32_t q = p.scale == 0.0f
                        ? 0u
-                       : round_level(t, rounding, seed, step, (uint64_t)i, top);
+                       : round_level(t, rounding, seed, step,
+                                     (uint64_t)(base + i), top);
       int negative = (mode != ORC_MINMAX) && q != 0 && x[i] < 0.0f;
       if (mode == ORC_TERN) {
         put_bits(codes_out, i, 2, ((uint32_t)negative << 1) | q);
@@ -432,8 +434,23 @@ static int quant_core(const float* x, int64_t n, int bits, int64_t group,
 int orc_quant(const float* x, int64_t n, int bits, int64_t group, int mode,
               int rounding, uint64_t seed, uint64_t step, uint8_t* codes_out,
               float* scales_out) {
-  return quant_core(x, n, bits, group, mode, rounding, seed, step, codes_out,
-                    scales_out, NULL);
+  return quant_core(x, n, 0, bits, group, mode, rounding, seed, step,
+                    codes_out, scales_out, NULL);
+}
+
+/*
+ * Same as orc_quant on the slice x[0..n) of a larger call whose element 0
+ * is element `base` of that call: the groups are taken relative to the
+ * slice (so the slice must start on a group boundary of the call) and the
+ * stochastic draw of slice element i is that of call element base + i.
+ * Lets a test check a sampled range of a call too large for the oracle.
+ */
+int orc_quant_at(const float* x, int64_t n, int64_t base, int bits,
+                 int64_t group, int mode, int rounding, uint64_t seed,
+                 uint64_t step, uint8_t* codes_out, float* scales_out) {
+  if (base < 0) return ORC_EINVAL;
+  return quant_core(x, n, base, bits, group, mode, rounding, seed, step,
+                    codes_out, scales_out, NULL);
 }
 
 /* Inverse of the packing above: g_hat from codes and scales. */
@@ -480,13 +497,13 @@ int orc_ef_quant(const float* grad, float* err, int64_t n, int bits,
                  uint64_t step, uint8_t* codes_out, float* scales_out) {
   int st = check_quant_args(n, bits, group, mode, rounding);
   if (st != ORC_OK) return st;
-  if (n == 0) return quant_core(grad, 0, bits, group, mode, rounding, seed,
+  if (n == 0) return quant_core(grad, 0, 0, bits, group, mode, rounding, seed,
                                 step, codes_out, scales_out, NULL);
   float* c = (float*)malloc((size_t)n * sizeof(float));
   float* g_hat = (float*)malloc((size_t)n * sizeof(float));
   if (!c || !g_hat) { free(c); free(g_hat); return ORC_ENOMEM; }
   for (int64_t i = 0; i < n; ++i) c[i] = grad[i] + err[i];
-  st = quant_core(c, n, bits, group, mode, rounding, seed, step, codes_out,
+  st = quant_core(c, n, 0, bits, group, mode, rounding, seed, step, codes_out,
                   scales_out, g_hat);
   if (st == ORC_OK)
     for (int64_t i = 0; i < n; ++i) err[i] = c[i] - g_hat[i];
@@ -515,7 +532,7 @@ int orc_ef_topk_quant(const float* grad, float* err, int64_t n, int64_t k,
   if (!val || !g_hat) { free(val); free(g_hat); return ORC_ENOMEM; }
   st = orc_ef_topk(grad, err, n, k, idx_out, val); /* err := c, kept -> 0 */
   if (st == ORC_OK)
-    st = quant_core(val, k, bits, group, ORC_QSGD, rounding, seed, step,
+    st = quant_core(val, k, 0, bits, group, ORC_QSGD, rounding, seed, step,
                     codes_out, scales_out, g_hat);
   if (st == ORC_OK)
     for (int64_t j = 0; j < k; ++j) err[idx_out[j]] = val[j] - g_hat[j];

@@ -56,6 +56,9 @@ def lib():
         L.orc_quant.argtypes = [_f32p, _i64, _int, _i64, _int, _int, _u64,
                                 _u64, _u8p, _f32p]
         L.orc_quant.restype = _int
+        L.orc_quant_at.argtypes = [_f32p, _i64, _i64, _int, _i64, _int, _int,
+                                   _u64, _u64, _u8p, _f32p]
+        L.orc_quant_at.restype = _int
         L.orc_dequant.argtypes = [_u8p, _f32p, _i64, _int, _i64, _int, _f32p]
         L.orc_dequant.restype = _int
         L.orc_ef_quant.argtypes = [_f32p, _f32p, _i64, _int, _i64, _int, _int,
@@ -140,6 +143,24 @@ def quant(x, bits, group, mode, rounding="nearest_even", seed=0, step=0):
     _check(lib().orc_quant(_p(xs, _f32p), n, bits, group, m,
                            _rounding(rounding), seed, step, _p(codes, _u8p),
                            _p(scales, _f32p)), "orc_quant")
+    return codes[:cb], scales[:sf]
+
+
+def quant_at(x, base, bits, group, mode, rounding="nearest_even", seed=0,
+             step=0):
+    """quant() of a group-aligned slice that starts at element ``base`` of
+    a larger call (the stochastic draws follow the call's indices)."""
+    xs = _f32(x)
+    n = xs.size
+    m = _mode(mode)
+    cb = codes_bytes(n, bits, m)
+    sf = scales_floats(n, group, m)
+    codes = np.zeros(max(cb, 1), dtype=np.uint8)
+    scales = np.zeros(max(sf, 1), dtype=np.float32)
+    _check(lib().orc_quant_at(_p(xs, _f32p), n, base, bits, group, m,
+                              _rounding(rounding), seed, step,
+                              _p(codes, _u8p), _p(scales, _f32p)),
+           "orc_quant_at")
     return codes[:cb], scales[:sf]
 
 

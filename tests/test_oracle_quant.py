@@ -246,3 +246,20 @@ def test_rejects_bad_arguments():
         oracle.quant(x, 3, 0, "minmax")
     with pytest.raises(oracle.OracleError):
         oracle.quant(x, 4, 0, "tern")
+
+
+def test_quant_at_matches_full_call():
+    """A group-aligned slice quantised with its call offset reproduces the
+    corresponding bytes of the full call (what the sampled full-size parity
+    tests rely on)."""
+    r = np.random.default_rng(31)
+    x = r.standard_normal(64 * 40 + 24).astype(np.float32)
+    for mode, bits in (("minmax", 4), ("qsgd", 8), ("minmax", 1)):
+        full_c, full_s = oracle.quant(x, bits, 64, mode, "stochastic", 5, 6)
+        g0, g1 = 7, 23
+        c, s = oracle.quant_at(x[g0 * 64:g1 * 64], g0 * 64, bits, 64, mode,
+                               "stochastic", 5, 6)
+        per = 2 if mode == "minmax" else 1
+        assert np.array_equal(s, full_s[g0 * per:g1 * per])
+        nb = 64 * bits // 8
+        assert np.array_equal(c[:(g1 - g0) * nb], full_c[g0 * nb:g1 * nb])
