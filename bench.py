@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""Throughput of the GB300 error-feedback gradient compressor.
+
+Default workload: a flat fp32 gradient of 134,217,728 elements (512 MiB) cut
+into 25 MiB buckets (20 x 6,553,600 + 1 x 3,145,728), Student-t (nu = 3)
+values x 1e-3 with temporally correlated steps g_t = 0.9 g_{t-1} + 0.436
+fresh_t.  One step is one pass of the whole compressor over every bucket:
+error feedback + Top-K 1 % + 8-bit QSGD (groups of 64, stochastic rounding)
+on the kept values + dequantisation + residual write-back
+(gc_ef_topk_quant), buckets spread over several contexts / CUDA streams.
+
+The metric is fp32 gradient GB/s through the compressor (4 bytes per
+gradient element per step), whole job over all GPUs.  Also reported: the
+roofline fraction of the dominant kernel (CUDA-event durations of every
+launch, measured in a second pass over the same steps), an end-to-end
+number through the C ABI with host buffers (pinned H2D of the gradient and
+D2H of the compressed result inside the timed region), the single-threaded
+CPU oracle on a bounded sample, and SM clocks sampled during the timed
+region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+    torchrun --nproc-per-node N bench.py --gpus N ...   (one rank per GPU)
+"""
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from gradient_compression_ef_gb300 import inputs  # noqa: E402
+
+METRIC = "fp32 gradient GB/s through EF+Top-K+quant compressor; % of GB300 HBM roofline"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["gc", "reference"], default="gc")
+    p.add_argument("--streams", type=int, default=4, help="contexts/streams for the buckets")
+    p.add_argument("--ratio", type=int, default=10, help="Top-K ratio in per mille")
+    p.add_argument("--distinct", type=int, default=3, help="distinct correlated gradients")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region (NVML through ctypes; reads only)
+# ---------------------------------------------------------------------------
+REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    """Polls the SM clock and clock-event reasons of one GPU every ~2 ms."""
+
+    def __init__(self, pci_bus_id):
+        self.samples, self.reasons = [], 0
+        self.max_mhz = None
+        self.ok = False
+        try:
+            nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if nvml.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if nvml.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if nvml.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = int(mx.value)
+            self.nvml, self.h = nvml, h
+            self.reason_fn = getattr(nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _run(self):
+        mhz = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(int(mhz.value))
+            if self.reason_fn(self.h, ctypes.byref(rs)) == 0:
+                self.reasons |= int(rs.value)
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "source": "unavailable"}
+        names = [v for b, v in REASON_BITS.items() if self.reasons & b and b != 0x1]
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples),
+                "source": "nvml"}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# the default workload
+# ---------------------------------------------------------------------------
+class BucketWorkload:
+    """134,217,728 fp32 elements in 25 MiB buckets; one step = EF + Top-K +
+    8-bit QSGD over every bucket."""
+
+    BITS, GROUP = 8, 64
+
+    def __init__(self, torch, gc, dev, ratio_per_mille, streams, distinct, seed):
+        self.torch, self.gc, self.dev = torch, gc, dev
+        self.n = inputs.FLAT_ELEMS
+        self.bounds = inputs.bucket_bounds(self.n)
+        self.ks = [inputs.ratio_k(length, ratio_per_mille, 1000) for _, length in self.bounds]
+        self.grads = inputs.correlated_steps_device(self.n, distinct, dev, seed=seed)
+        self.err = torch.zeros(self.n, dtype=torch.float32, device=dev)
+        # outputs of all buckets in three contiguous buffers (16-byte aligned slices)
+        self.slices = []
+        oi = oc = os_ = 0
+        for (start, length), k in zip(self.bounds, self.ks):
+            nb = gc.codes_bytes(k, self.BITS, "qsgd")
+            ns = gc.scales_floats(k, self.GROUP, "qsgd")
+            self.slices.append((oi, oc, os_, k, nb, ns))
+            oi += -(-k // 4) * 4
+            oc += -(-nb // 16) * 16
+            os_ += -(-ns // 4) * 4
+        self.idx = torch.empty(oi, dtype=torch.int32, device=dev)
+        self.codes = torch.empty(oc, dtype=torch.uint8, device=dev)
+        self.scales = torch.empty(os_, dtype=torch.float32, device=dev)
+        self.streams = [torch.cuda.Stream(device=dev) for _ in range(streams)]
+        self.ctxs = [gc.Context(max(l for _, l in self.bounds), stream=s) for s in self.streams]
+        self.main = torch.cuda.current_stream(dev)
+
+    def out_bytes(self):
+        return (self.idx.numel() * 4 + self.codes.numel() + self.scales.numel() * 4)
+
+    def algorithmic_bytes(self):
+        """Bytes the method must move per step: read g and e, write e' (12 B
+        per element) plus, per kept entry, its index (4 B), code (b/8 B),
+        sign (1/8 B) and 4/64 B of scale."""
+        kept = sum(self.ks)
+        return 12 * self.n + kept * (4 + self.BITS / 8 + 1 / 8 + 4 / self.GROUP)
+
+    def launch_step(self, t, grad=None):
+        """Enqueues one step: every bucket on its context's stream, forked
+        from and joined back into the main stream."""
+        torch, gc = self.torch, self.gc
+        g = self.grads[t % len(self.grads)] if grad is None else grad
+        fork = torch.cuda.Event()
+        fork.record(self.main)
+        for s in self.streams:
+            s.wait_event(fork)
+        for b, ((start, length), (oi, oc, os_, k, nb, ns)) in enumerate(zip(self.bounds, self.slices)):
+            ctx = self.ctxs[b % len(self.ctxs)]
+            gc.ef_topk_quant(ctx, g[start:start + length], self.err[start:start + length], k,
+                             self.BITS, self.GROUP, "stochastic", 1000 + b, t,
+                             self.idx[oi:oi + k], self.codes[oc:oc + nb],
+                             self.scales[os_:os_ + ns], n=length)
+        for s in self.streams:
+            j = torch.cuda.Event()
+            j.record(s)
+            self.main.wait_event(j)
+
+    def launches(self):
+        return sum(c.launch_count() for c in self.ctxs)
+
+    def check(self):
+        for c in self.ctxs:
+            c.check()
+
+
+def kernel_timing(wl, steps, warmup_step):
+    """Per-phase CUDA-event durations over `steps` more steps."""
+    per_step = 8 * len(wl.bounds)
+    for c in wl.ctxs:
+        c.enable_timing(per_step * steps)
+    for t in range(steps):
+        wl.launch_step(warmup_step + t)
+    phases = {}
+    for c in wl.ctxs:
+        for name, (ms, cnt) in c.read_timing().items():
+            a = phases.setdefault(name, [0.0, 0])
+            a[0] += ms
+            a[1] += cnt
+        c.enable_timing(0)
+    return phases
+
+
+def cpu_baseline(budget_s=12.0, seed=7):
+    """The oracle (single-threaded C) on whole buckets of the workload until
+    about budget_s seconds of CPU work; GB/s of fp32 gradient."""
+    import oracle
+    r = inputs.rng(seed)
+    length = inputs.BUCKET_ELEMS
+    k = inputs.ratio_k(length, 10, 1000)
+    done, elapsed, buckets = 0, 0.0, 0
+    while buckets == 0 or elapsed < budget_s:
+        g = inputs.student_t(r, length)
+        e = (0.1 * inputs.student_t(r, length)).astype(np.float32)
+        t0 = time.perf_counter()
+        oracle.ef_topk_quant(g, e, k, 8, 64, "stochastic", 1000 + buckets, 0)
+        elapsed += time.perf_counter() - t0
+        done += length
+        buckets += 1
+        if buckets >= 8:
+            break
+    return {"value": 4.0 * done / elapsed / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%d bucket(s) of 6,553,600 elements, EF + Top-K 1%% + 8-bit QSGD, "
+                      "%.1f s single-threaded" % (buckets, elapsed)}
+
+
+def config(args, wl=None):
+    cfg = {"workload": "flat fp32 gradient 134,217,728 elements in 25 MiB buckets "
+                       "(20 x 6,553,600 + 3,145,728), Student-t nu=3 x 1e-3, correlated steps; "
+                       "per bucket EF + Top-K %g%% + 8-bit QSGD (groups of 64, stochastic) on the "
+                       "kept values" % (args.ratio / 10),
+           "total_elems": inputs.FLAT_ELEMS, "bucket_elems": inputs.BUCKET_ELEMS,
+           "buckets": len(inputs.bucket_bounds()), "topk_per_mille": args.ratio,
+           "quant": "qsgd 8-bit g64 stochastic",
+           "l2": "inputs larger than L2: each step reads a 512 MiB gradient and the 512 MiB "
+                 "residual, no flush", "parallelism": "dp%d" % args.gpus}
+    if wl is not None:
+        cfg["streams"] = len(wl.streams)
+        cfg["distinct_gradients"] = len(wl.grads)
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    r = inputs.rng(11)
+    length = inputs.BUCKET_ELEMS
+    k = inputs.ratio_k(length, args.ratio, 1000)
+    g = inputs.student_t(r, length)
+    e = np.zeros(length, np.float32)
+    times = []
+    for t in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        _, _, _, e = oracle.ef_topk_quant(g, e, k, 8, 64, "stochastic", 1000, t)
+        dt = time.perf_counter() - t0
+        if t >= args.warmup:
+            times.append(dt)
+    sec = sum(times) / len(times)
+    value = 4.0 * length / sec / 1e9
+    sample = ("one 6,553,600-element bucket (1/21 of the 134,217,728-element step) per step, "
+              "EF + Top-K %g%% + 8-bit QSGD, single-threaded C oracle" % (args.ratio / 10))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config(args),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from gradient_compression_ef_gb300 import gc
+
+    wl = BucketWorkload(torch, gc, dev, args.ratio, args.streams, args.distinct, seed=42 + rank)
+    torch.cuda.synchronize(dev)
+    for t in range(args.warmup):
+        wl.launch_step(t)
+    wl.check()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    props = torch.cuda.get_device_properties(dev)
+    pci = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0),
+                                 getattr(props, "pci_bus_id", 0),
+                                 getattr(props, "pci_device_id", 0))
+    sampler = ClockSampler(pci)
+    launches0 = wl.launches()
+    barrier()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with sampler:
+        start.record(wl.main)
+        for t in range(args.steps):
+            wl.launch_step(args.warmup + t)
+        stop.record(wl.main)
+        torch.cuda.synchronize(dev)
+    barrier()
+    ms = start.elapsed_time(stop)
+    launches = wl.launches() - launches0
+    wl.check()
+    if world > 1:
+        tmax = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tmax.item())
+    ms_per_step = ms / args.steps
+    value = world * 4.0 * wl.n / (ms_per_step * 1e-3) / 1e9
+
+    # per-kernel durations (second pass over the same kind of steps)
+    phases = kernel_timing(wl, args.steps, args.warmup + args.steps)
+    top = max(phases.items(), key=lambda kv: kv[1][0])
+    peak, peak_src = measured_peaks()
+    per_launch_ms = {name: ms_ / cnt for name, (ms_, cnt) in phases.items()}
+    # algorithmic bytes per launch of each Top-K phase, per 6,553,600-element
+    # bucket: pass 1 reads g and e and writes c (12 B per element)
+    n_avg = wl.n / len(wl.bounds)
+    algo_per_launch = {"ef_hist": 12.0 * n_avg}
+    roofline = None
+    if top[0] in algo_per_launch:
+        achieved = algo_per_launch[top[0]] / (per_launch_ms[top[0]] * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": top[0], "achieved": achieved, "peak": peak,
+                    "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
+                    "traffic": None}
+    step_achieved = wl.algorithmic_bytes() / (ms_per_step * 1e-3) / 1e9
+
+    # end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        hosts = [g.cpu().pin_memory() for g in wl.grads[:2]]
+        dev_in = torch.empty(wl.n, dtype=torch.float32, device=dev)
+        out_i = torch.empty(wl.idx.numel(), dtype=torch.int32).pin_memory()
+        out_c = torch.empty(wl.codes.numel(), dtype=torch.uint8).pin_memory()
+        out_s = torch.empty(wl.scales.numel(), dtype=torch.float32).pin_memory()
+        e2e_steps = max(3, min(args.steps, 20))
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(wl.main)
+        with torch.cuda.stream(wl.main):
+            for t in range(e2e_steps):
+                dev_in.copy_(hosts[t % 2], non_blocking=True)
+                wl.launch_step(t, grad=dev_in)
+                out_i.copy_(wl.idx, non_blocking=True)
+                out_c.copy_(wl.codes, non_blocking=True)
+                out_s.copy_(wl.scales, non_blocking=True)
+        e1.record(wl.main)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e_ms = e0.elapsed_time(e1) / e2e_steps
+        if world > 1:
+            tm = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(tm, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(tm.item())
+        e2e = {"value": world * 4.0 * wl.n / (e_ms * 1e-3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": 4 * wl.n, "d2h_bytes_per_step": wl.out_bytes(),
+               "ms_per_step": e_ms}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": config(args, wl), "roofline": roofline,
+            "step_roofline": {"algorithmic_bytes_per_step": wl.algorithmic_bytes(),
+                              "achieved": step_achieved, "peak": peak, "unit": "GB/s",
+                              "frac": step_achieved / peak},
+            "kernels": {name: {"launches": cnt, "total_ms": ms_,
+                               "avg_us": 1e3 * ms_ / cnt} for name, (ms_, cnt) in phases.items()},
+            "e2e": e2e, "clocks": sampler.summary(), "gpu_launches": launches}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

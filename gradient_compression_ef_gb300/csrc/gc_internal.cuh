@@ -1,0 +1,263 @@
+// gc_internal.cuh -- shared definitions of the CUDA compressor (sm_103a).
+//
+// Everything here is internal to libgc.so; the public surface is the C ABI
+// in include/gc.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gc.h"
+
+namespace gc {
+
+// ---------------------------------------------------------------------------
+// Tunables shared by host and device code.
+// ---------------------------------------------------------------------------
+
+// Top-K radix select over the 31-bit magnitude key (IEEE bits of |c|).
+constexpr int kHistBits = 12;                    // bits 30..19: 8 exponent + 4 mantissa
+constexpr int kHistBins = 1 << kHistBits;
+constexpr int kHistShift = 31 - kHistBits;       // 19
+constexpr int kMidBits = 11;                     // bits 18..8
+constexpr int kMidBins = 1 << kMidBits;
+constexpr int kLowBits = 8;                      // bits 7..0
+constexpr int kLowBins = 1 << kLowBits;
+constexpr int kTopkThreads = 512;
+constexpr int kTopkSub = kTopkThreads * 4;       // elements per block step
+constexpr int kMaxTiles = 4096;                  // tiles of the ordered compaction
+
+// Device status bits (OR-ed into the context's status word).
+constexpr uint32_t kStatusTopkCount = 1u << 0;   // candidate count mismatch
+constexpr uint32_t kStatusTopkSelect = 1u << 1;  // threshold search failed
+constexpr uint32_t kStatusTopkOverflow = 1u << 2;  // more than k entries kept
+constexpr uint32_t kStatusScatterIndex = 1u << 3;  // residual index out of range
+
+// Per-context Top-K selection state in device memory.
+struct TopkSel {
+  uint32_t bin;         // first-level threshold bin B
+  uint32_t above;       // elements whose bin is above B
+  uint32_t need1;       // k - above: how many of bin B are kept
+  uint32_t cand_total;  // elements in bin B
+  uint32_t T;           // exact threshold key
+  uint32_t need_T;      // entries with key == T to keep (smallest indices)
+  uint32_t ticket_hist; // last-block ticket of the histogram pass
+  uint32_t ticket_coll; // last-block ticket of the collection pass
+  uint32_t cand_count;  // fill counter of the candidate buffer
+  uint32_t pad[7];
+};
+
+// Device scratch of one context (all pointers into one allocation).
+struct Workspace {
+  uint32_t* hist;        // [kHistBins], zero between calls
+  TopkSel* sel;          // one record
+  uint32_t* status;      // device status word
+  uint32_t* tile_above;  // [kMaxTiles]
+  uint32_t* tile_out;    // [kMaxTiles] exclusive output offsets
+  uint32_t* tile_tie;    // [kMaxTiles] exclusive tie offsets
+  uint2* cand;           // [max_n] (key, index) candidates
+  float* vals;           // [max_n] kept values of the hybrid call
+  float4* partials;      // [max_partials] chunk statistics of quantisation
+  int64_t max_n;
+  int64_t max_partials;
+};
+
+struct PsgdWorkspace {
+  float* q_part;         // [splits][max_n][max_r] partial sums of M^T P
+  uint32_t* tickets;     // [strips] last-block tickets
+  int64_t max_m, max_n;
+  int max_r;
+  int64_t bytes;
+};
+
+}  // namespace gc
+
+struct gc_ctx {
+  int device;
+  int num_sms;
+  cudaStream_t stream;
+  void* ws_base;
+  gc::Workspace ws;
+  void* psgd_base;
+  gc::PsgdWorkspace psgd;
+  // per-kernel timing (gc_ctx_enable_timing)
+  int timing_cap;           // event pairs available, 0 = off
+  int timing_used;          // pairs recorded in the current window
+  cudaEvent_t* ev_start;
+  cudaEvent_t* ev_stop;
+  int* ev_phase;
+  int64_t launches;         // kernels launched by this context
+};
+
+namespace gc {
+
+// ---------------------------------------------------------------------------
+// Device helpers.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t mag_key(float x) {
+  return __float_as_uint(x) & 0x7fffffffu;
+}
+
+// Philox-4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
+// Easy as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplies whose
+// halves are mixed with the other two words and the round key; the key is
+// advanced by the golden-ratio and sqrt(3)-1 Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint2 key) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * x.x;
+    const uint32_t hi0 = __umulhi(0xD2511F53u, x.x);
+    const uint32_t lo1 = 0xCD9E8D57u * x.z;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, x.z);
+    x = make_uint4(hi1 ^ x.y ^ key.x, lo1, hi0 ^ x.w ^ key.y, lo0);
+    key.x += 0x9E3779B9u;
+    key.y += 0xBB67AE85u;
+  }
+  return x;
+}
+
+// The four draws of elements 4b .. 4b+3 of a call: word j of Philox at
+// counter (b, step) and key seed, top 24 bits scaled by 2^-24.
+__device__ __forceinline__ void uniform4(uint64_t block, uint64_t seed,
+                                         uint64_t step, float u[4]) {
+  const uint4 r = philox4x32_10(
+      make_uint4((uint32_t)block, (uint32_t)(block >> 32), (uint32_t)step,
+                 (uint32_t)(step >> 32)),
+      make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+  u[0] = __fmul_rn(__uint2float_rn(r.x >> 8), 0x1p-24f);
+  u[1] = __fmul_rn(__uint2float_rn(r.y >> 8), 0x1p-24f);
+  u[2] = __fmul_rn(__uint2float_rn(r.z >> 8), 0x1p-24f);
+  u[3] = __fmul_rn(__uint2float_rn(r.w >> 8), 0x1p-24f);
+}
+
+// Level of one element: t >= 0 is its position on the level grid.
+// Nearest-even: rint(t).  Stochastic: floor(t) + [u < t - floor(t)].
+// Clamped to [0, top].
+__device__ __forceinline__ uint32_t round_level(float t, bool stochastic,
+                                                float u, uint32_t top) {
+  float q;
+  if (stochastic) {
+    const float fl = floorf(t);
+    q = __fadd_rn(fl, (u < __fsub_rn(t, fl)) ? 1.0f : 0.0f);
+  } else {
+    q = rintf(t);
+  }
+  if (!(q > 0.0f)) return 0u;
+  if (q >= (float)top) return top;
+  return (uint32_t)q;
+}
+
+// Quantise one value c against its group parameters; returns the code
+// level, the sign flag (QSGD/TernGrad, only when q != 0) and g_hat.
+template <int MODE>
+__device__ __forceinline__ uint32_t quantize_one(float c, float scale,
+                                                 float offset, bool stochastic,
+                                                 float u, uint32_t top,
+                                                 bool* negative, float* ghat) {
+  uint32_t q = 0u;
+  if (scale != 0.0f) {
+    const float t = (MODE == GC_MINMAX) ? __fdiv_rn(__fsub_rn(c, offset), scale)
+                                        : __fdiv_rn(fabsf(c), scale);
+    q = round_level(t, stochastic, u, top);
+  }
+  const float mag = __fmul_rn((float)q, scale);
+  if (MODE == GC_MINMAX) {
+    *negative = false;
+    *ghat = __fadd_rn(mag, offset);
+  } else {
+    *negative = (q != 0u) && (c < 0.0f);
+    *ghat = *negative ? -mag : mag;
+  }
+  return q;
+}
+
+// Pack four b-bit codes of consecutive elements into the low 4b bits.
+template <int BITS>
+__device__ __forceinline__ uint32_t pack4(const uint32_t q[4]) {
+  return q[0] | (q[1] << BITS) | (q[2] << (2 * BITS)) | (q[3] << (3 * BITS));
+}
+
+// Stores the packed codes of elements i0..i0+3 (i0 % 4 == 0).  Every lane of
+// the warp must call it (1-bit codes pair neighbouring lanes).
+template <int BITS>
+__device__ __forceinline__ void store_codes4(uint8_t* codes, int64_t i0,
+                                             bool lane_active, uint32_t bits4) {
+  if (BITS == 8) {
+    if (lane_active) *reinterpret_cast<uint32_t*>(codes + i0) = bits4;
+  } else if (BITS == 4) {
+    if (lane_active) *reinterpret_cast<uint16_t*>(codes + (i0 >> 1)) = (uint16_t)bits4;
+  } else if (BITS == 2) {
+    if (lane_active) codes[i0 >> 2] = (uint8_t)bits4;
+  } else {  // BITS == 1: two lanes form one byte
+    const uint32_t hi = __shfl_down_sync(0xffffffffu, bits4, 1);
+    if (lane_active && ((i0 >> 2) & 1) == 0)
+      codes[i0 >> 3] = (uint8_t)(bits4 | (hi << 4));
+  }
+}
+
+__device__ __forceinline__ float warp_sum_tree(float s, int lanes) {
+  // Butterfly over `lanes` consecutive lanes: with offsets 1, 2, 4 ... the
+  // value after offset o is the sum of an aligned block of 2o lanes, formed
+  // from its two aligned halves -- the adjacent-pair binary tree.
+  for (int o = 1; o < lanes; o <<= 1)
+    s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
+  return s;
+}
+
+// Brackets one kernel launch: counts it and, when timing is on, records a
+// start / stop event pair on the context's stream around it.
+struct LaunchScope {
+  gc_ctx* ctx;
+  int slot;
+  LaunchScope(gc_ctx* c, int phase) : ctx(c), slot(-1) {
+    ++ctx->launches;
+    if (ctx->timing_cap > 0 && ctx->timing_used < ctx->timing_cap) {
+      slot = ctx->timing_used++;
+      ctx->ev_phase[slot] = phase;
+      cudaEventRecord(ctx->ev_start[slot], ctx->stream);
+    }
+  }
+  ~LaunchScope() {
+    if (slot >= 0) cudaEventRecord(ctx->ev_stop[slot], ctx->stream);
+  }
+};
+
+// Host helpers.
+inline int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Launchers implemented in the .cu files (return GC_OK or GC_ERR_CUDA).
+gc_status launch_ef_topk(gc_ctx* ctx, const float* grad, float* err, int64_t n,
+                         int64_t k, int32_t* idx_out, float* val_out);
+// scatter_idx != NULL: x holds kept values and the residual of element j
+// goes to err[scatter_idx[j]] (err has scatter_n elements).
+gc_status launch_quant(gc_ctx* ctx, const float* x, float* err,
+                       const int32_t* scatter_idx, int64_t scatter_n, int64_t n,
+                       int bits, int64_t group, int mode, int rounding, uint64_t seed,
+                       uint64_t step, uint8_t* codes_out, float* scales_out);
+gc_status launch_dequant(gc_ctx* ctx, const uint8_t* codes,
+                         const float* scales, int64_t n, int bits,
+                         int64_t group, int mode, float* x_out);
+gc_status launch_powersgd(gc_ctx* ctx, const float* grad, float* err,
+                          int64_t m, int64_t n, int r, float* P_out,
+                          float* Q_inout);
+
+// Bytes of PowerSGD scratch for matrices up to max_m x max_n, rank max_r.
+int64_t psgd_workspace_bytes(int64_t max_m, int64_t max_n, int max_r, int num_sms);
+
+// Whether (group, n) runs in the fused single-pass quantisation kernel.
+inline bool quant_is_fused(int64_t n, int64_t group) {
+  const int64_t G = group == 0 ? n : group;
+  return G >= 4 && G <= 128 && (G & (G - 1)) == 0;
+}
+
+// Chunking of the multi-pass quantisation (groups the fused kernel does
+// not take): a group is cut into chunks of `chunk` elements (a power of two
+// >= 1024 when the group is larger than that, else the whole group).
+struct QuantPlan {
+  int64_t G, ngroups, chunk, chunks_per_group, nchunks;
+};
+QuantPlan quant_plan(int64_t n, int64_t group);
+
+}  // namespace gc

@@ -1,0 +1,654 @@
+// gc_quant.cu -- group-wise quantisation, bit packing, dequantisation and
+// the error-feedback residual.
+//
+// Formulas ("分布式训练中的梯度压缩算法" 二.1 线性量化 and 三 误差补偿;
+// "gradient-compression-quantization-sparsification" 1.1 QSGD / TernGrad,
+// 1.2 groups and rounding):
+//   min-max : scale = (max - min) / (2^b - 1), t = (c - min) / scale,
+//             g_hat = q * scale + min
+//   QSGD    : scale = ||c_group||_2 / (2^b - 1), t = |c| / scale,
+//             g_hat = sign * q * scale  (sum of squares as the adjacent-pair
+//             binary tree over the group)
+//   TernGrad: scale = max |c_group|, t = |c| / scale, q in {0, 1}
+//   q = rint(t) or floor(t) + [u < frac(t)], clamped; e' = c - g_hat.
+//
+// Kernels:
+//   quant_fused  : groups of 4..128 elements (a power of two).  One pass:
+//                  each lane holds 4 consecutive elements, a group is G/4
+//                  lanes and its statistics are warp butterflies.  Reads g
+//                  and e (or x), writes codes, scales and e'.  The hybrid
+//                  call runs it over the kept values and scatters e'.
+//   quant_stats  : other group sizes.  One warp per chunk of a group (the
+//                  whole group, or power-of-two chunks of a large group);
+//                  with error feedback it also writes c over e.
+//   quant_combine: combines the chunk statistics of large groups in the same
+//                  tree order.
+//   quant_apply  : elementwise quantise + pack (+ e' = c - g_hat).
+//   dequant      : elementwise g_hat from codes and scales.
+#include <algorithm>
+
+#include "gc_internal.cuh"
+
+namespace gc {
+
+QuantPlan quant_plan(int64_t n, int64_t group) {
+  QuantPlan p;
+  p.G = group == 0 ? n : group;
+  if (p.G < 1) p.G = 1;
+  p.ngroups = n == 0 ? 0 : ceil_div(n, p.G);
+  if (p.G <= 1024) {
+    p.chunk = p.G;
+    p.chunks_per_group = 1;
+  } else {
+    int64_t target = ceil_div(p.G, 8192);
+    int64_t c = 1024;
+    while (c < target) c <<= 1;
+    p.chunk = c;
+    p.chunks_per_group = ceil_div(p.G, c);
+  }
+  p.nchunks = p.ngroups == 0 ? 0
+                             : (p.ngroups - 1) * p.chunks_per_group +
+                                   ceil_div(n - (p.ngroups - 1) * p.G, p.chunk);
+  return p;
+}
+
+namespace {
+
+constexpr int kQThreads = 256;
+
+enum IoKind { IO_PLAIN = 0, IO_EF = 1, IO_SCATTER = 2 };
+
+struct QuantOut {
+  uint8_t* codes;
+  uint8_t* signs;        // QSGD sign plane (NULL otherwise)
+  float* scales;
+  int64_t zero_begin, zero_end;    // padding bytes of the code section
+  int64_t szero_begin, szero_end;  // padding bytes of the sign plane
+  int64_t scatter_n;               // length of err for the scattered residual
+  uint32_t* status;                // device status word
+};
+
+__device__ __forceinline__ void zero_padding(const QuantOut& o) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    for (int64_t b = o.zero_begin; b < o.zero_end; ++b) o.codes[b] = 0;
+    if (o.signs)
+      for (int64_t b = o.szero_begin; b < o.szero_end; ++b) o.signs[b] = 0;
+  }
+}
+
+template <int MODE, int BITS>
+__device__ __forceinline__ uint32_t code_bits4(const uint32_t q[4], const bool neg[4]) {
+  if (MODE == GC_TERN) {
+    uint32_t t[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) t[j] = q[j] | ((uint32_t)neg[j] << 1);
+    return pack4<2>(t);
+  }
+  return pack4<BITS>(q);
+}
+
+// ---------------------------------------------------------------------------
+// Fused single-pass kernel for groups of G = 4 * LPG elements.
+// ---------------------------------------------------------------------------
+template <int MODE, int BITS, int LPG, int IO>
+__global__ void __launch_bounds__(kQThreads) quant_fused_kernel(
+    const float* __restrict__ x, float* __restrict__ err,
+    const int32_t* __restrict__ scatter_idx, int64_t n, QuantOut o,
+    int stochastic, uint64_t seed, uint64_t step) {
+  constexpr int G = 4 * LPG;
+  constexpr uint32_t top = (MODE == GC_TERN) ? 1u : ((1u << BITS) - 1u);
+  const float levels = (float)top;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = ((int64_t)blockIdx.x * kQThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kQThreads) >> 5;
+  zero_padding(o);
+
+  for (int64_t base = warp_id * 128; base < n; base += nwarps * 128) {
+    const int64_t i0 = base + 4 * lane;
+    const bool active = i0 < n;
+    float c[4];
+    bool valid[4];
+    if (i0 + 3 < n) {
+      const float4 v = IO == IO_EF ? __ldcs(reinterpret_cast<const float4*>(x + i0))
+                                   : *reinterpret_cast<const float4*>(x + i0);
+      c[0] = v.x; c[1] = v.y; c[2] = v.z; c[3] = v.w;
+      valid[0] = valid[1] = valid[2] = valid[3] = true;
+      if (IO == IO_EF) {
+        const float4 e = *reinterpret_cast<const float4*>(err + i0);
+        c[0] = __fadd_rn(c[0], e.x);
+        c[1] = __fadd_rn(c[1], e.y);
+        c[2] = __fadd_rn(c[2], e.z);
+        c[3] = __fadd_rn(c[3], e.w);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        valid[j] = i0 + j < n;
+        c[j] = valid[j] ? x[i0 + j] : 0.0f;
+        if (IO == IO_EF && valid[j]) c[j] = __fadd_rn(c[j], err[i0 + j]);
+      }
+    }
+
+    // group statistics (lanes of a group are LPG consecutive lanes)
+    float scale, offset = 0.0f;
+    if (MODE == GC_MINMAX) {
+      float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (valid[j]) { mn = fminf(mn, c[j]); mx = fmaxf(mx, c[j]); }
+#pragma unroll
+      for (int o2 = 1; o2 < LPG; o2 <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+      }
+      mn = __fadd_rn(mn, 0.0f);
+      mx = __fadd_rn(mx, 0.0f);
+      scale = __fdiv_rn(__fsub_rn(mx, mn), levels);
+      offset = mn;
+    } else if (MODE == GC_QSGD) {
+      float s = __fadd_rn(__fadd_rn(__fmul_rn(c[0], c[0]), __fmul_rn(c[1], c[1])),
+                          __fadd_rn(__fmul_rn(c[2], c[2]), __fmul_rn(c[3], c[3])));
+      s = warp_sum_tree(s, LPG);
+      scale = __fdiv_rn(__fsqrt_rn(s), levels);
+    } else {
+      float m = fmaxf(fmaxf(fabsf(c[0]), fabsf(c[1])), fmaxf(fabsf(c[2]), fabsf(c[3])));
+#pragma unroll
+      for (int o2 = 1; o2 < LPG; o2 <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o2));
+      scale = m;
+    }
+    if (active && (lane % LPG) == 0) {
+      const int64_t g = i0 / G;
+      if (MODE == GC_MINMAX)
+        reinterpret_cast<float2*>(o.scales)[g] = make_float2(scale, offset);
+      else
+        o.scales[g] = scale;
+    }
+
+    float u[4] = {0.f, 0.f, 0.f, 0.f};
+    if (stochastic) uniform4((uint64_t)i0 >> 2, seed, step, u);
+    uint32_t q[4];
+    bool neg[4];
+    float r[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float gh;
+      q[j] = quantize_one<MODE>(c[j], scale, offset, stochastic != 0, u[j], top, &neg[j], &gh);
+      if (!valid[j]) { q[j] = 0u; neg[j] = false; }
+      r[j] = __fsub_rn(c[j], gh);
+    }
+    store_codes4<(MODE == GC_TERN) ? 2 : BITS>(o.codes, i0, active, code_bits4<MODE, BITS>(q, neg));
+    if (MODE == GC_QSGD) {
+      const bool s4[4] = {neg[0], neg[1], neg[2], neg[3]};
+      uint32_t sb[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sb[j] = s4[j] ? 1u : 0u;
+      store_codes4<1>(o.signs, i0, active, pack4<1>(sb));
+    }
+    if (IO == IO_EF) {
+      if (i0 + 3 < n) {
+        __stcs(reinterpret_cast<float4*>(err + i0), make_float4(r[0], r[1], r[2], r[3]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (valid[j]) err[i0 + j] = r[j];
+      }
+    } else if (IO == IO_SCATTER) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (!valid[j]) continue;
+        const int32_t t = scatter_idx[i0 + j];
+        if (t >= 0 && (int64_t)t < o.scatter_n) err[t] = r[j];
+        else atomicOr(o.status, kStatusScatterIndex);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Multi-pass path: statistics per chunk (one warp per chunk).
+// ---------------------------------------------------------------------------
+
+// Running adjacent-pair tree over equal-sized consecutive nodes: node j of
+// the stream enters as a leaf of the tree of nodes; carry[l] holds a pending
+// complete subtree of 2^l nodes (bit l of count).  Identical in all lanes.
+struct TreeAcc {
+  float carry[32];
+  uint32_t count;
+  __device__ __forceinline__ void init() { count = 0u; }
+  __device__ __forceinline__ void push(float v) {
+    int l = 0;
+    while (count & (1u << l)) {
+      v = __fadd_rn(carry[l], v);
+      ++l;
+    }
+    carry[l] = v;
+    count += 1u;
+  }
+  // Sum of the zero-padded tree: fold pending subtrees right to left.
+  __device__ __forceinline__ float finish() const {
+    float acc = 0.0f;
+    bool any = false;
+    for (int l = 0; l < 32; ++l) {
+      if (count & (1u << l)) {
+        acc = any ? __fadd_rn(carry[l], acc) : carry[l];
+        any = true;
+      }
+    }
+    return acc;
+  }
+};
+
+template <int MODE>
+__device__ __forceinline__ void finalize_group(float mn, float mx, float amax, float ss,
+                                               uint32_t top, float* scales, int64_t g) {
+  const float levels = (float)top;
+  if (MODE == GC_MINMAX) {
+    mn = __fadd_rn(mn, 0.0f);
+    mx = __fadd_rn(mx, 0.0f);
+    reinterpret_cast<float2*>(scales)[g] =
+        make_float2(__fdiv_rn(__fsub_rn(mx, mn), levels), mn);
+  } else if (MODE == GC_QSGD) {
+    scales[g] = __fdiv_rn(__fsqrt_rn(ss), levels);
+  } else {
+    scales[g] = amax;
+  }
+}
+
+template <int MODE, int IO>
+__global__ void __launch_bounds__(kQThreads) quant_stats_kernel(
+    const float* __restrict__ x, float* __restrict__ err, int64_t n, int64_t G,
+    int64_t chunk, int64_t cpg, int64_t nchunks, uint32_t top,
+    float4* __restrict__ partials, float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = ((int64_t)blockIdx.x * kQThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kQThreads) >> 5;
+  // 16-byte loads need every group to start on a 4-element boundary (or a
+  // single group starting at element 0)
+  const bool vec_ok = (G % 4) == 0 || G >= n;
+  for (int64_t ch = warp_id; ch < nchunks; ch += nwarps) {
+    const int64_t g = ch / cpg, cc = ch % cpg;
+    const int64_t g_begin = g * G;
+    const int64_t g_end = std::min<int64_t>(g_begin + G, n);
+    const int64_t begin = g_begin + cc * chunk;
+    const int64_t end = std::min<int64_t>(begin + chunk, g_end);
+    float mn = INFINITY, mx = -INFINITY, amax = 0.0f;
+    TreeAcc tree;
+    tree.init();
+    for (int64_t b = begin; b < end; b += 128) {
+      const int64_t i0 = b + 4 * lane;
+      float c[4];
+      if (vec_ok && i0 + 3 < end) {
+        float4 v = __ldcs(reinterpret_cast<const float4*>(x + i0));
+        if (IO == IO_EF) {
+          const float4 e = *reinterpret_cast<const float4*>(err + i0);
+          v.x = __fadd_rn(v.x, e.x);
+          v.y = __fadd_rn(v.y, e.y);
+          v.z = __fadd_rn(v.z, e.z);
+          v.w = __fadd_rn(v.w, e.w);
+          *reinterpret_cast<float4*>(err + i0) = v;
+        }
+        c[0] = v.x; c[1] = v.y; c[2] = v.z; c[3] = v.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          c[j] = 0.0f;
+          if (i0 + j < end) {
+            c[j] = x[i0 + j];
+            if (IO == IO_EF) {
+              c[j] = __fadd_rn(c[j], err[i0 + j]);
+              err[i0 + j] = c[j];
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (i0 + j < end) {
+          mn = fminf(mn, c[j]);
+          mx = fmaxf(mx, c[j]);
+          amax = fmaxf(amax, fabsf(c[j]));
+        }
+      }
+      if (MODE == GC_QSGD) {
+        float s = __fadd_rn(__fadd_rn(__fmul_rn(c[0], c[0]), __fmul_rn(c[1], c[1])),
+                            __fadd_rn(__fmul_rn(c[2], c[2]), __fmul_rn(c[3], c[3])));
+        tree.push(warp_sum_tree(s, 32));
+      }
+    }
+#pragma unroll
+    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o2));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+    }
+    const float ss = MODE == GC_QSGD ? tree.finish() : 0.0f;
+    if (lane == 0) {
+      if (cpg == 1)
+        finalize_group<MODE>(mn, mx, amax, ss, top, scales, g);
+      else
+        partials[ch] = make_float4(mn, mx, amax, ss);
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kQThreads) quant_combine_kernel(
+    const float4* __restrict__ partials, int64_t cpg, int64_t nchunks,
+    int64_t ngroups, uint32_t top, float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = ((int64_t)blockIdx.x * kQThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kQThreads) >> 5;
+  for (int64_t g = warp_id; g < ngroups; g += nwarps) {
+    const int64_t first = g * cpg;
+    const int64_t last = std::min<int64_t>(first + cpg, nchunks);
+    float mn = INFINITY, mx = -INFINITY, amax = 0.0f;
+    TreeAcc tree;
+    tree.init();
+    for (int64_t b = first; b < last; b += 32) {
+      float s = 0.0f;
+      if (b + lane < last) {
+        const float4 p = partials[b + lane];
+        mn = fminf(mn, p.x);
+        mx = fmaxf(mx, p.y);
+        amax = fmaxf(amax, p.z);
+        s = p.w;
+      }
+      if (MODE == GC_QSGD) tree.push(warp_sum_tree(s, 32));
+    }
+#pragma unroll
+    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o2));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+    }
+    const float ss = MODE == GC_QSGD ? tree.finish() : 0.0f;
+    if (lane == 0) finalize_group<MODE>(mn, mx, amax, ss, top, scales, g);
+  }
+}
+
+// Group of element i0 + j (0 <= j < 4) from one division per lane: with
+// G >= 4 at most one group boundary falls inside the 4 elements.
+struct GroupOf4 {
+  int64_t g0, r0, G;
+  __device__ __forceinline__ GroupOf4(int64_t i0, int64_t G_) : G(G_) {
+    g0 = i0 / G_;
+    r0 = i0 - g0 * G_;
+  }
+  __device__ __forceinline__ int64_t operator()(int j) const {
+    if (G >= 4) return g0 + ((r0 + j >= G) ? 1 : 0);
+    return (g0 * G + r0 + j) / G;
+  }
+};
+
+// Elementwise quantise + pack (+ residual), group parameters from scales.
+template <int MODE, int BITS, int IO>
+__global__ void __launch_bounds__(kQThreads) quant_apply_kernel(
+    const float* __restrict__ c_src, float* __restrict__ err, int64_t n, int64_t G,
+    QuantOut o, int stochastic, uint64_t seed, uint64_t step) {
+  constexpr uint32_t top = (MODE == GC_TERN) ? 1u : ((1u << BITS) - 1u);
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = ((int64_t)blockIdx.x * kQThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kQThreads) >> 5;
+  zero_padding(o);
+  for (int64_t base = warp_id * 128; base < n; base += nwarps * 128) {
+    const int64_t i0 = base + 4 * lane;
+    const bool active = i0 < n;
+    float c[4];
+    bool valid[4];
+    if (i0 + 3 < n) {
+      const float4 v = IO == IO_EF ? *reinterpret_cast<const float4*>(c_src + i0)
+                                   : __ldcs(reinterpret_cast<const float4*>(c_src + i0));
+      c[0] = v.x; c[1] = v.y; c[2] = v.z; c[3] = v.w;
+      valid[0] = valid[1] = valid[2] = valid[3] = true;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        valid[j] = i0 + j < n;
+        c[j] = valid[j] ? c_src[i0 + j] : 0.0f;
+      }
+    }
+    float u[4] = {0.f, 0.f, 0.f, 0.f};
+    if (stochastic) uniform4((uint64_t)i0 >> 2, seed, step, u);
+    uint32_t q[4];
+    bool neg[4];
+    float r[4];
+    const GroupOf4 group_of(i0, G);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      q[j] = 0u;
+      neg[j] = false;
+      r[j] = 0.0f;
+      if (valid[j]) {
+        const int64_t g = group_of(j);
+        float scale, offset = 0.0f;
+        if (MODE == GC_MINMAX) {
+          const float2 p = reinterpret_cast<const float2*>(o.scales)[g];
+          scale = p.x;
+          offset = p.y;
+        } else {
+          scale = o.scales[g];
+        }
+        float gh;
+        q[j] = quantize_one<MODE>(c[j], scale, offset, stochastic != 0, u[j], top, &neg[j], &gh);
+        r[j] = __fsub_rn(c[j], gh);
+      }
+    }
+    store_codes4<(MODE == GC_TERN) ? 2 : BITS>(o.codes, i0, active, code_bits4<MODE, BITS>(q, neg));
+    if (MODE == GC_QSGD) {
+      uint32_t sb[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sb[j] = neg[j] ? 1u : 0u;
+      store_codes4<1>(o.signs, i0, active, pack4<1>(sb));
+    }
+    if (IO == IO_EF) {
+      if (i0 + 3 < n) {
+        *reinterpret_cast<float4*>(err + i0) = make_float4(r[0], r[1], r[2], r[3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (valid[j]) err[i0 + j] = r[j];
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Dequantisation.
+// ---------------------------------------------------------------------------
+template <int MODE, int BITS>
+__global__ void __launch_bounds__(kQThreads) dequant_kernel(
+    const uint8_t* __restrict__ codes, const uint8_t* __restrict__ signs,
+    const float* __restrict__ scales, int64_t n, int64_t G, float* __restrict__ out) {
+  constexpr int CB = (MODE == GC_TERN) ? 2 : BITS;
+  const int64_t nvec = (n + 3) >> 2;
+  const int64_t stride = (int64_t)gridDim.x * kQThreads;
+  for (int64_t v = (int64_t)blockIdx.x * kQThreads + threadIdx.x; v < nvec; v += stride) {
+    const int64_t i0 = v << 2;
+    uint32_t bits4;
+    if (CB == 8) bits4 = *reinterpret_cast<const uint32_t*>(codes + i0);
+    else if (CB == 4) bits4 = *reinterpret_cast<const uint16_t*>(codes + (i0 >> 1));
+    else if (CB == 2) bits4 = codes[i0 >> 2];
+    else bits4 = (uint32_t)(codes[i0 >> 3] >> ((v & 1) * 4)) & 0xfu;
+    uint32_t sbits = 0u;
+    if (MODE == GC_QSGD) sbits = (uint32_t)(signs[i0 >> 3] >> ((v & 1) * 4)) & 0xfu;
+    float r[4];
+    const GroupOf4 group_of(i0, G);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      r[j] = 0.0f;
+      if (i0 + j < n) {
+        const uint32_t code = (bits4 >> (j * CB)) & ((1u << CB) - 1u);
+        const int64_t g = group_of(j);
+        if (MODE == GC_MINMAX) {
+          const float2 p = reinterpret_cast<const float2*>(scales)[g];
+          r[j] = __fadd_rn(__fmul_rn((float)code, p.x), p.y);
+        } else if (MODE == GC_QSGD) {
+          const float m = __fmul_rn((float)code, scales[g]);
+          r[j] = ((sbits >> j) & 1u) ? -m : m;
+        } else {
+          const float m = __fmul_rn((float)(code & 1u), scales[g]);
+          r[j] = (code >> 1) ? -m : m;
+        }
+      }
+    }
+    if (i0 + 3 < n) {
+      *reinterpret_cast<float4*>(out + i0) = make_float4(r[0], r[1], r[2], r[3]);
+    } else {
+      for (int j = 0; j < 4; ++j)
+        if (i0 + j < n) out[i0 + j] = r[j];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host dispatch.
+// ---------------------------------------------------------------------------
+QuantOut make_out(uint8_t* codes, float* scales, int64_t n, int bits, int mode) {
+  QuantOut o;
+  const int cb = mode == GC_TERN ? 2 : bits;
+  const int64_t mag = round_up((n * cb + 7) / 8, 16);
+  o.codes = codes;
+  o.scales = scales;
+  o.signs = mode == GC_QSGD ? codes + mag : nullptr;
+  // bytes written by the lanes cover ceil(n/4)*4 elements
+  const int64_t n4 = round_up(n, 4);
+  o.zero_begin = std::min<int64_t>((n4 * cb + 7) / 8, mag);
+  if (cb == 1) o.zero_begin = std::min<int64_t>(ceil_div(n4, 8), mag);
+  o.zero_end = mag;
+  const int64_t smag = round_up((n + 7) / 8, 16);
+  o.szero_begin = std::min<int64_t>(ceil_div(n4, 8), smag);
+  o.szero_end = smag;
+  o.scatter_n = 0;
+  o.status = nullptr;
+  return o;
+}
+
+int grid_for(gc_ctx* ctx, int64_t work_items, int per_block, int per_sm) {
+  const int64_t want = std::max<int64_t>(1, ceil_div(work_items, per_block));
+  return (int)std::min<int64_t>(want, (int64_t)ctx->num_sms * per_sm);
+}
+
+template <int MODE, int BITS, int IO>
+gc_status run_fused(gc_ctx* ctx, const float* x, float* err, const int32_t* idx,
+                    int64_t n, int64_t G, const QuantOut& o, int stoch, uint64_t seed,
+                    uint64_t step) {
+  const int grid = grid_for(ctx, ceil_div(n, 128), kQThreads / 32, 8);
+  cudaStream_t s = ctx->stream;
+  LaunchScope L(ctx, GC_PHASE_QUANT_FUSED);
+  switch (G) {
+    case 4: quant_fused_kernel<MODE, BITS, 1, IO><<<grid, kQThreads, 0, s>>>(x, err, idx, n, o, stoch, seed, step); break;
+    case 8: quant_fused_kernel<MODE, BITS, 2, IO><<<grid, kQThreads, 0, s>>>(x, err, idx, n, o, stoch, seed, step); break;
+    case 16: quant_fused_kernel<MODE, BITS, 4, IO><<<grid, kQThreads, 0, s>>>(x, err, idx, n, o, stoch, seed, step); break;
+    case 32: quant_fused_kernel<MODE, BITS, 8, IO><<<grid, kQThreads, 0, s>>>(x, err, idx, n, o, stoch, seed, step); break;
+    case 64: quant_fused_kernel<MODE, BITS, 16, IO><<<grid, kQThreads, 0, s>>>(x, err, idx, n, o, stoch, seed, step); break;
+    default: quant_fused_kernel<MODE, BITS, 32, IO><<<grid, kQThreads, 0, s>>>(x, err, idx, n, o, stoch, seed, step); break;
+  }
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+template <int MODE, int BITS, int IO>
+gc_status run_multipass(gc_ctx* ctx, const float* x, float* err, int64_t n,
+                        int64_t group, const QuantOut& o, int stoch, uint64_t seed,
+                        uint64_t step) {
+  const QuantPlan p = quant_plan(n, group);
+  if (p.chunks_per_group > 1 && p.nchunks > ctx->ws.max_partials) return GC_ERR_WORKSPACE;
+  constexpr uint32_t top = (MODE == GC_TERN) ? 1u : ((1u << BITS) - 1u);
+  cudaStream_t s = ctx->stream;
+  const int warps_per_block = kQThreads / 32;
+  {
+    LaunchScope L(ctx, GC_PHASE_QUANT_STATS);
+    quant_stats_kernel<MODE, IO><<<grid_for(ctx, p.nchunks, warps_per_block, 8), kQThreads, 0, s>>>(
+        x, err, n, p.G, p.chunk, p.chunks_per_group, p.nchunks, top, ctx->ws.partials, o.scales);
+  }
+  if (p.chunks_per_group > 1) {
+    LaunchScope L(ctx, GC_PHASE_QUANT_COMBINE);
+    quant_combine_kernel<MODE><<<grid_for(ctx, p.ngroups, warps_per_block, 8), kQThreads, 0, s>>>(
+        ctx->ws.partials, p.chunks_per_group, p.nchunks, p.ngroups, top, o.scales);
+  }
+  const float* c_src = IO == IO_EF ? err : x;
+  {
+    LaunchScope L(ctx, GC_PHASE_QUANT_APPLY);
+    quant_apply_kernel<MODE, BITS, IO><<<grid_for(ctx, ceil_div(n, 128), warps_per_block, 8), kQThreads, 0, s>>>(
+        c_src, err, n, p.G, o, stoch, seed, step);
+  }
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+template <int MODE, int BITS>
+gc_status dispatch_io(gc_ctx* ctx, const float* x, float* err, const int32_t* idx,
+                      int64_t n, int64_t group, const QuantOut& o, int stoch,
+                      uint64_t seed, uint64_t step) {
+  const int64_t G = group == 0 ? n : group;
+  if (quant_is_fused(n, group)) {
+    if (idx) return run_fused<MODE, BITS, IO_SCATTER>(ctx, x, err, idx, n, G, o, stoch, seed, step);
+    if (err) return run_fused<MODE, BITS, IO_EF>(ctx, x, err, idx, n, G, o, stoch, seed, step);
+    return run_fused<MODE, BITS, IO_PLAIN>(ctx, x, err, idx, n, G, o, stoch, seed, step);
+  }
+  if (idx) return GC_ERR_UNSUPPORTED;
+  if (n > ctx->ws.max_n) return GC_ERR_WORKSPACE;
+  if (err) return run_multipass<MODE, BITS, IO_EF>(ctx, x, err, n, group, o, stoch, seed, step);
+  return run_multipass<MODE, BITS, IO_PLAIN>(ctx, x, err, n, group, o, stoch, seed, step);
+}
+
+template <int MODE>
+gc_status dispatch_bits(gc_ctx* ctx, const float* x, float* err, const int32_t* idx,
+                        int64_t n, int bits, int64_t group, const QuantOut& o, int stoch,
+                        uint64_t seed, uint64_t step) {
+  switch (bits) {
+    case 1: return dispatch_io<MODE, 1>(ctx, x, err, idx, n, group, o, stoch, seed, step);
+    case 2: return dispatch_io<MODE, 2>(ctx, x, err, idx, n, group, o, stoch, seed, step);
+    case 4: return dispatch_io<MODE, 4>(ctx, x, err, idx, n, group, o, stoch, seed, step);
+    default: return dispatch_io<MODE, 8>(ctx, x, err, idx, n, group, o, stoch, seed, step);
+  }
+}
+
+}  // namespace
+
+gc_status launch_quant(gc_ctx* ctx, const float* x, float* err,
+                       const int32_t* scatter_idx, int64_t scatter_n, int64_t n,
+                       int bits, int64_t group, int mode, int rounding, uint64_t seed,
+                       uint64_t step, uint8_t* codes_out, float* scales_out) {
+  QuantOut o = make_out(codes_out, scales_out, n, bits, mode);
+  o.scatter_n = scatter_n;
+  o.status = ctx->ws.status;
+  if (n == 0) return GC_OK;
+  const int stoch = rounding == GC_STOCHASTIC;
+  if (mode == GC_MINMAX)
+    return dispatch_bits<GC_MINMAX>(ctx, x, err, scatter_idx, n, bits, group, o, stoch, seed, step);
+  if (mode == GC_QSGD)
+    return dispatch_bits<GC_QSGD>(ctx, x, err, scatter_idx, n, bits, group, o, stoch, seed, step);
+  return dispatch_io<GC_TERN, 2>(ctx, x, err, scatter_idx, n, group, o, stoch, seed, step);
+}
+
+gc_status launch_dequant(gc_ctx* ctx, const uint8_t* codes, const float* scales,
+                         int64_t n, int bits, int64_t group, int mode, float* x_out) {
+  if (n == 0) return GC_OK;
+  const int64_t G = group == 0 ? n : group;
+  const int cb = mode == GC_TERN ? 2 : bits;
+  const uint8_t* signs = mode == GC_QSGD ? codes + round_up((n * cb + 7) / 8, 16) : nullptr;
+  const int grid = grid_for(ctx, ceil_div(n, 4), kQThreads, 8);
+  cudaStream_t s = ctx->stream;
+  LaunchScope L(ctx, GC_PHASE_DEQUANT);
+#define GC_DQ(M, B) dequant_kernel<M, B><<<grid, kQThreads, 0, s>>>(codes, signs, scales, n, G, x_out)
+  if (mode == GC_TERN) {
+    GC_DQ(GC_TERN, 2);
+  } else if (mode == GC_MINMAX) {
+    switch (bits) {
+      case 1: GC_DQ(GC_MINMAX, 1); break;
+      case 2: GC_DQ(GC_MINMAX, 2); break;
+      case 4: GC_DQ(GC_MINMAX, 4); break;
+      default: GC_DQ(GC_MINMAX, 8); break;
+    }
+  } else {
+    switch (bits) {
+      case 1: GC_DQ(GC_QSGD, 1); break;
+      case 2: GC_DQ(GC_QSGD, 2); break;
+      case 4: GC_DQ(GC_QSGD, 4); break;
+      default: GC_DQ(GC_QSGD, 8); break;
+    }
+  }
+#undef GC_DQ
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+}  // namespace gc

@@ -1,0 +1,283 @@
+/*
+ * gc.h -- C ABI of the GB300 gradient compressor with error feedback.
+ *
+ * The compressor runs on a flat fp32 gradient before the gradient leaves GPU
+ * memory ("gradient-compression-quantization-sparsification" (hotdry blog),
+ * 3.2: compression finishes before the data leaves GPU memory and needs
+ * custom CUDA kernels).  It adds the error-feedback residual, selects the
+ * Top-K entries, quantises with per-group scales, packs the codes,
+ * dequantises and writes the new residual; PowerSGD is the low-rank variant.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Buffers are DEVICE pointers owned by the caller (plain C types, no
+ *    framework types).  Every buffer must start on a 16-byte boundary
+ *    (GC_ERR_ALIGNMENT otherwise); a pointer may be NULL only when the call
+ *    touches no element of it (n == 0, k == 0).
+ *  - Calls are asynchronous: they validate arguments on the host, enqueue
+ *    kernels on the context's CUDA stream and return.  The return value
+ *    reports host-side validation and launch errors only (a launch error is
+ *    GC_ERR_CUDA).  Device-side self checks set a status word in the
+ *    context; gc_ctx_check() synchronises the stream and reports it.
+ *  - No call allocates memory.  Scratch space lives in the context and is
+ *    reserved by gc_ctx_create / gc_ctx_reserve_powersgd.  Consecutive calls
+ *    on one context are ordered by its stream; calls that overlap in time
+ *    need one context each.
+ *  - n <= 2^31 - 1 (indices are int32) and, for calls that use the context's
+ *    scratch (Top-K, hybrid, quantisation with groups that do not fit the
+ *    single-pass kernel), n <= the context's max_n (GC_ERR_WORKSPACE).
+ *  - Finite inputs are a precondition.  Squares and ranges must not
+ *    overflow binary32 (|x| < 1.8e19 for QSGD).
+ *  - Arithmetic is IEEE-754 binary32 with one round-to-nearest-even per
+ *    operation and no fused multiply-add, so results are bit-identical to a
+ *    plain sequential evaluation of the same formulas; PowerSGD is the
+ *    exception (fp32 accumulation in an unspecified order).
+ *  - err is read and written in place; no other output may alias an input.
+ *
+ * Compressed formats
+ * ------------------
+ *  codes: the b-bit codes of elements 0..n-1 as one little-endian bit stream
+ *         (element i occupies bits i*b .. i*b+b-1, bit 0 being the least
+ *         significant bit of byte 0), zero-padded to a multiple of 16 bytes;
+ *         for GC_QSGD a sign plane (1 bit per element, set when the element
+ *         is negative and its code is not 0) follows, laid out the same way.
+ *         GC_TERN codes are 2 bits, (sign << 1) | q with q in {0, 1}.
+ *         gc_codes_bytes() gives the size.
+ *  scales: per group of `group` consecutive elements (group == 0: one group
+ *         of all n; the last group may be partial): GC_MINMAX stores
+ *         {scale, min} (two floats), GC_QSGD and GC_TERN store {scale}.
+ *         gc_scales_floats() gives the size in floats.
+ */
+#ifndef GC_H_
+#define GC_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GC_API __attribute__((visibility("default")))
+#else
+#define GC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gc_status {
+  GC_OK = 0,
+  GC_ERR_INVALID_ARG = -1,  /* NULL, negative size, k > n, group < 0 ... */
+  GC_ERR_UNSUPPORTED = -2,  /* bits not in {1,2,4,8}; TERN with bits != 2 */
+  GC_ERR_ALIGNMENT = -3,    /* a buffer is not 16-byte aligned */
+  GC_ERR_WORKSPACE = -4,    /* n above the context's reserved capacity */
+  GC_ERR_CUDA = -5,         /* a CUDA runtime call or launch failed */
+  GC_ERR_DEVICE_CHECK = -6, /* a device-side self check failed */
+  GC_ERR_NO_MEMORY = -7     /* gc_ctx_create could not reserve scratch */
+} gc_status;
+
+typedef enum gc_mode {
+  GC_MINMAX = 0, /* linear min-max quantisation */
+  GC_QSGD = 1,   /* s = 2^b - 1 levels of the group L2 norm, sign plane */
+  GC_TERN = 2    /* TernGrad: levels {-max|c|, 0, +max|c|} */
+} gc_mode;
+
+typedef enum gc_rounding {
+  GC_NEAREST_EVEN = 0, /* round half to even */
+  GC_STOCHASTIC = 1    /* unbiased, Philox-4x32-10 keyed by (seed, step, i) */
+} gc_rounding;
+
+typedef struct gc_ctx gc_ctx;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+GC_API int gc_version(void);
+
+/* Human-readable text for a gc_status value; never NULL. */
+GC_API const char* gc_status_string(int status);
+
+/*
+ * Creates a context bound to `cuda_stream` (a cudaStream_t; NULL selects the
+ * legacy default stream) on the current CUDA device and reserves its scratch
+ * for calls of up to `max_n` elements (about 12 bytes per element plus a
+ * few tens of KB).  The context owns the scratch; the caller owns every
+ * buffer passed to the compute calls.  Returns GC_ERR_NO_MEMORY when the
+ * device allocation fails, GC_ERR_CUDA on other CUDA errors.
+ */
+GC_API gc_status gc_ctx_create(gc_ctx** ctx, void* cuda_stream, int64_t max_n);
+
+/* Waits for the context's stream, then frees its scratch.  NULL is a no-op. */
+GC_API gc_status gc_ctx_destroy(gc_ctx* ctx);
+
+/* Rebinds the context to another stream of the same device. */
+GC_API gc_status gc_ctx_set_stream(gc_ctx* ctx, void* cuda_stream);
+
+/*
+ * Reserves the PowerSGD scratch for matrices up to max_m x max_n and rank
+ * up to max_r (1..16); a later call with larger limits grows it.  Must not
+ * be called while work is in flight on the context.
+ */
+GC_API gc_status gc_ctx_reserve_powersgd(gc_ctx* ctx, int64_t max_m, int64_t max_n,
+                                  int max_r);
+
+/*
+ * Synchronises the context's stream and reports the device status word:
+ * GC_OK, or GC_ERR_DEVICE_CHECK when a kernel's self check failed (the word
+ * is then cleared), or GC_ERR_CUDA for an asynchronous CUDA error.
+ */
+GC_API gc_status gc_ctx_check(gc_ctx* ctx);
+
+/*
+ * Kernel phases, for per-kernel timing.  Every kernel the library launches
+ * belongs to one phase.
+ */
+typedef enum gc_phase {
+  GC_PHASE_EF_HIST = 0,      /* Top-K pass 1: c = g + e, 12-bit histogram */
+  GC_PHASE_COLLECT = 1,      /* Top-K pass 2: candidates + exact threshold */
+  GC_PHASE_WRITE = 2,        /* Top-K pass 3: ordered compaction, e' = 0 */
+  GC_PHASE_EF_ADD = 3,       /* e = g + e (k == 0) */
+  GC_PHASE_QUANT_FUSED = 4,  /* single-pass group quantisation */
+  GC_PHASE_QUANT_STATS = 5,  /* multi-pass: chunk statistics */
+  GC_PHASE_QUANT_COMBINE = 6,/* multi-pass: group statistics */
+  GC_PHASE_QUANT_APPLY = 7,  /* multi-pass: quantise + pack + residual */
+  GC_PHASE_DEQUANT = 8,
+  GC_PHASE_PSGD_MQ = 9,      /* PowerSGD pass 1: M = G + E, P = M Q */
+  GC_PHASE_PSGD_MTP = 10,    /* PowerSGD pass 2: Q' = M^T P_hat */
+  GC_PHASE_PSGD_RESID = 11,  /* PowerSGD pass 3: E' = M - P_hat Q'^T */
+  GC_PHASE_COUNT = 12
+} gc_phase;
+
+/* Name of a phase ("ef_hist", ...); "?" when out of range. */
+GC_API const char* gc_phase_name(int phase);
+
+/*
+ * Per-kernel timing.  With max_launches > 0 every later kernel launch on the
+ * context is bracketed by two CUDA events recorded on the context's stream
+ * (up to max_launches launches between reads; further launches are not
+ * timed).  max_launches == 0 turns timing off.  The events are created here
+ * (not per call).
+ */
+GC_API gc_status gc_ctx_enable_timing(gc_ctx* ctx, int max_launches);
+
+/*
+ * Synchronises the stream, adds each timed launch's duration (ms) and count
+ * to ms_out[phase] and count_out[phase] (arrays of GC_PHASE_COUNT entries,
+ * caller-initialised), and starts a new timing window.
+ */
+GC_API gc_status gc_ctx_read_timing(gc_ctx* ctx, double* ms_out, int64_t* count_out);
+
+/* Number of kernels this context has launched since it was created. */
+GC_API int64_t gc_ctx_launch_count(gc_ctx* ctx);
+
+/* Bytes of the packed code buffer for n elements (see "Compressed
+ * formats"); -1 for invalid arguments. */
+GC_API int64_t gc_codes_bytes(int64_t n, int bits, int mode);
+
+/* Floats of the scale buffer for n elements; -1 for invalid arguments. */
+GC_API int64_t gc_scales_floats(int64_t n, int64_t group, int mode);
+
+/*
+ * Error feedback + Top-K sparsification.
+ * Pages: "分布式训练中的梯度压缩算法" 二.2 (Top-K keeps the K entries of
+ * largest |g|); "4、梯度累积与梯度压缩" 4.2.1 (exactly k entries, returned as
+ * (indices, values)); "梯度聚合通信优化实战方案" Python 演示
+ * error_feedback_compress (c = g + e; the entries not sent stay in the
+ * residual).
+ *   c = grad + err;  keep the k entries of largest |c|, ties broken by the
+ *   smaller index;  idx_out[0..k) = kept positions in ascending order;
+ *   val_out[j] = c[idx_out[j]];  err[i] = +0 at kept positions, c[i]
+ *   elsewhere.
+ * err == NULL selects from grad alone and writes no residual.
+ * grad: fp32[n] (read);  err: fp32[n] (read, then overwritten);
+ * idx_out: int32[k];  val_out: fp32[k].  0 <= k <= n <= max_n.
+ */
+GC_API gc_status gc_ef_topk(gc_ctx* ctx, const float* grad, float* err, int64_t n,
+                     int64_t k, int32_t* idx_out, float* val_out);
+
+/*
+ * Group-wise quantisation of x (no error feedback).
+ * Pages: "分布式训练中的梯度压缩算法" 二.1 线性量化 (q = round((g - min) /
+ * scale), scale = (max - min) / (2^b - 1)); "gradient-compression-
+ * quantization-sparsification" 1.1 (QSGD stochastic rounding, TernGrad
+ * {-1, 0, +1} with layer-wise scaling) and 1.2 (groups of e.g. 64;
+ * deterministic vs stochastic rounding).
+ *   GC_MINMAX: scale = (max - min) / (2^b - 1); t = (x - min) / scale.
+ *   GC_QSGD:   scale = ||x_group||_2 / (2^b - 1); t = |x| / scale; the sum of
+ *              squares is added as the perfect binary tree over the group
+ *              (zero-padded to a power of two, adjacent pairs first).
+ *   GC_TERN:   scale = max |x_group|; t = |x| / scale; bits must be 2.
+ *   q = round(t) (nearest-even) or floor(t) + [u < t - floor(t)]
+ *   (stochastic), clamped to [0, top]; scale == 0 gives q = 0.
+ *   The draw u of element i is word (i mod 4) of Philox-4x32-10 (Salmon et
+ *   al., SC'11) at counter {lo32(i/4), hi32(i/4), lo32(step), hi32(step)}
+ *   and key {lo32(seed), hi32(seed)}, taking its top 24 bits times 2^-24.
+ * x: fp32[n];  codes_out: gc_codes_bytes(n, bits, mode) bytes;
+ * scales_out: gc_scales_floats(n, group, mode) floats.  bits in {1,2,4,8}.
+ * Groups of 4..128 elements (a power of two) run in one fused pass and need
+ * no scratch; other group sizes need n <= max_n.
+ */
+GC_API gc_status gc_quant(gc_ctx* ctx, const float* x, int64_t n, int bits,
+                   int64_t group, int mode, int rounding, uint64_t seed,
+                   uint64_t step, uint8_t* codes_out, float* scales_out);
+
+/*
+ * Dequantisation: x_out[i] = q * scale + min (GC_MINMAX, two roundings) or
+ * +-(q * scale) (GC_QSGD / GC_TERN) -- "分布式训练中的梯度压缩算法" 二.1
+ * (g_hat = q * scale + min).  Arguments as written by gc_quant.
+ */
+GC_API gc_status gc_dequant(gc_ctx* ctx, const uint8_t* codes, const float* scales,
+                     int64_t n, int bits, int64_t group, int mode,
+                     float* x_out);
+
+/*
+ * Error feedback + quantisation.
+ * Pages: "分布式训练中的梯度压缩算法" 三 误差补偿代码示例 (compensate,
+ * quantise, keep the quantisation error for the next step).
+ *   c = grad + err;  (codes, scales) = gc_quant(c, ...);
+ *   err = c - dequant(codes, scales)   (one rounding).
+ * grad: fp32[n] (read);  err: fp32[n] (read, then overwritten).
+ */
+GC_API gc_status gc_ef_quant(gc_ctx* ctx, const float* grad, float* err, int64_t n,
+                      int bits, int64_t group, int mode, int rounding,
+                      uint64_t seed, uint64_t step, uint8_t* codes_out,
+                      float* scales_out);
+
+/*
+ * Hybrid: error feedback + Top-K, then QSGD on the kept values.
+ * Pages: "4、梯度累积与梯度压缩" 4.3 (TopK 1% + 8-bit QSGD);
+ * "gradient-compression-quantization-sparsification" 三 (hybrid
+ * compression).
+ *   c = grad + err;  (idx_out, val) = Top-K(c) as in gc_ef_topk;
+ *   (codes, scales) = QSGD(val[0..k), bits, group, rounding, seed, step),
+ *   element j of the quantised array being val[j];
+ *   err[idx_out[j]] = val[j] - g_hat[j];  err[i] = c[i] at every other i.
+ * idx_out: int32[k];  codes_out: gc_codes_bytes(k, bits, GC_QSGD) bytes;
+ * scales_out: gc_scales_floats(k, group, GC_QSGD) floats.  err must not be
+ * NULL.  The kept values live in the context's scratch (n <= max_n).
+ */
+GC_API gc_status gc_ef_topk_quant(gc_ctx* ctx, const float* grad, float* err,
+                           int64_t n, int64_t k, int bits, int64_t group,
+                           int rounding, uint64_t seed, uint64_t step,
+                           int32_t* idx_out, uint8_t* codes_out,
+                           float* scales_out);
+
+/*
+ * One rank-r PowerSGD step with error feedback.
+ * Pages: "gradient-compression-quantization-sparsification" 3.1 (low-rank
+ * approximation, send the two thin matrices, rebuild on the receiver);
+ * "梯度聚合通信优化实战方案" 梯度压缩原理 (error compensation is what makes
+ * PowerSGD work).  Steps (Vogels et al., NeurIPS 2019, Algorithm 1):
+ *   M = grad + err  (stored into err);  P = M Q;
+ *   P_hat = modified Gram-Schmidt(P);  Q' = M^T P_hat;
+ *   err = M - P_hat Q'^T.
+ * grad, err: fp32 m x n row-major;  P_out: fp32 m x r (receives P_hat);
+ * Q_inout: fp32 n x r (read as Q, overwritten with Q').  1 <= r <= 16;
+ * requires gc_ctx_reserve_powersgd with limits covering (m, n, r).
+ * Tolerance-based: fp32 CUDA-core accumulation.
+ */
+GC_API gc_status gc_powersgd_step(gc_ctx* ctx, const float* grad, float* err,
+                           int64_t m, int64_t n, int r, float* P_out,
+                           float* Q_inout);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GC_H_ */

@@ -1,0 +1,88 @@
+"""PowerSGD on the GPU against the oracle (binary64): the reconstruction
+P_hat Q'^T and the residual within 1e-3 relative Frobenius error at every one
+of several consecutive steps, plus orthonormality of P_hat."""
+import numpy as np
+import pytest
+
+import oracle
+from gradient_compression_ef_gb300 import inputs
+from tests.gpu_helpers import dev_f32, host, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = torch_cuda()
+    from gradient_compression_ef_gb300 import gc
+    ctx = gc.Context(1024)
+    ctx.reserve_powersgd(11008, 11008, 16)
+    yield torch, gc, ctx
+    ctx.close()
+
+
+def rel(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300)
+
+
+def run_steps(env, G, E, Q, r, steps):
+    torch, gc, ctx = env
+    m, n = G.shape
+    Gd, Ed, Qd = dev_f32(torch, G), dev_f32(torch, E), dev_f32(torch, Q)
+    Pd = torch.empty((m, r), dtype=torch.float32, device="cuda")
+    oE, oQ = E.copy(), Q.copy()
+    for s in range(steps):
+        gc.powersgd_step(ctx, Gd, Ed, m, n, r, Pd, Qd)
+        ctx.check()
+        oP, oQ, oE = oracle.powersgd_step(G, oE, oQ, r)
+        P, Qn, En = host(Pd), host(Qd), host(Ed)
+        approx = P.astype(np.float64) @ Qn.astype(np.float64).T
+        o_approx = oP.astype(np.float64) @ oQ.astype(np.float64).T
+        assert rel(approx, o_approx) <= TOL, "step %d reconstruction" % s
+        assert rel(En, oE) <= TOL * max(1.0, np.linalg.norm(o_approx) /
+                                        max(np.linalg.norm(oE), 1e-30)), "step %d residual" % s
+        assert np.abs(P.T.astype(np.float64) @ P - np.eye(r)).max() < 1e-4
+
+
+@pytest.mark.parametrize("m,n,r", [(300, 200, 4), (257, 131, 3), (64, 1000, 1), (1000, 64, 16),
+                                   (513, 515, 8)])
+def test_small_shapes(env, m, n, r):
+    M, _ = inputs.low_rank_matrix(m, n, r=r)
+    rg = np.random.default_rng(m + n)
+    E = (0.01 * rg.standard_normal((m, n))).astype(np.float32)
+    Q = rg.standard_normal((n, r)).astype(np.float32)
+    run_steps(env, M, E, Q, r, 3)
+
+
+@pytest.mark.parametrize("shape", inputs.POWERSGD_SHAPES)
+def test_workload_shapes_five_steps(env, shape):
+    """The rank-16 + noise workload at full size, rank 4, five steps reusing Q."""
+    m, n = shape
+    M, Q0 = inputs.low_rank_matrix(m, n, r=4)
+    run_steps(env, M, np.zeros_like(M), Q0, 4, 5)
+
+
+def test_zero_gradient(env):
+    G = np.zeros((40, 36), np.float32)
+    torch, gc, ctx = env
+    Gd, Ed = dev_f32(torch, G), dev_f32(torch, G)
+    Qd = torch.ones((36, 2), dtype=torch.float32, device="cuda")
+    Pd = torch.empty((40, 2), dtype=torch.float32, device="cuda")
+    gc.powersgd_step(ctx, Gd, Ed, 40, 36, 2, Pd, Qd)
+    ctx.check()
+    assert not host(Pd).any() and not host(Qd).any() and not host(Ed).any()
+
+
+def test_requires_reserved_scratch(env):
+    torch, gc, _ = env
+    c = gc.Context(16)
+    G = torch.zeros((8, 8), dtype=torch.float32, device="cuda")
+    with pytest.raises(gc.GCError) as ei:
+        gc.powersgd_step(c, G, G.clone(), 8, 8, 2, torch.zeros((8, 2), device="cuda"),
+                         torch.zeros((8, 2), device="cuda"))
+    assert ei.value.status == gc.ERR_WORKSPACE
+    c.close()
