@@ -230,6 +230,11 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Launchers implemented in the .cu files (return GC_OK or GC_ERR_CUDA).
 gc_status launch_ef_topk(gc_ctx* ctx, const float* grad, float* err, int64_t n,
                          int64_t k, int32_t* idx_out, float* val_out);
+// The same Top-K passes on an explicit workspace and stream (no context);
+// the workspace's hist, sel and status must be zero on entry.
+gc_status launch_ef_topk_on(const Workspace& ws, cudaStream_t s, int sms, const float* grad,
+                            float* err, int64_t n, int64_t k, int32_t* idx_out,
+                            float* val_out);
 // scatter_idx != NULL: x holds kept values and the residual of element j
 // goes to err[scatter_idx[j]] (err has scatter_n elements).
 gc_status launch_quant(gc_ctx* ctx, const float* x, float* err,

@@ -456,4 +456,36 @@ gc_status launch_ef_topk(gc_ctx* ctx, const float* grad, float* err, int64_t n,
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
 
+gc_status launch_ef_topk_on(const Workspace& ws, cudaStream_t s, int sms, const float* grad,
+                            float* err, int64_t n, int64_t k, int32_t* idx_out,
+                            float* val_out) {
+  if (n == 0) return GC_OK;
+  if (k == 0) {
+    if (err) {
+      const int64_t blocks = std::min<int64_t>(ceil_div(ceil_div(n, 4), 256), (int64_t)sms * 8);
+      ef_add_kernel<<<(int)blocks, 256, 0, s>>>(grad, err, n);
+    }
+    return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+  }
+  const int64_t tile_elems =
+      std::max<int64_t>(kTopkSub, round_up(ceil_div(n, kMaxTiles), kTopkSub));
+  const int ntiles = (int)ceil_div(n, tile_elems);
+  const int64_t hist_blocks =
+      std::max<int64_t>(1, std::min<int64_t>(ceil_div(ceil_div(n, 4), kThreads), (int64_t)sms * 4));
+  const int pass_blocks = (int)std::min<int64_t>(ntiles, (int64_t)sms * 4);
+  const float* c_src = err ? err : grad;
+  if (err)
+    ef_hist_kernel<true><<<(int)hist_blocks, kThreads, 0, s>>>(grad, err, n, (uint32_t)k, ws);
+  else
+    ef_hist_kernel<false><<<(int)hist_blocks, kThreads, 0, s>>>(grad, err, n, (uint32_t)k, ws);
+  collect_kernel<<<pass_blocks, kThreads, 0, s>>>(c_src, n, ntiles, tile_elems, ws);
+  if (err)
+    write_kernel<true><<<pass_blocks, kThreads, 0, s>>>(c_src, err, n, (uint32_t)k, ntiles,
+                                                        tile_elems, ws, idx_out, val_out);
+  else
+    write_kernel<false><<<pass_blocks, kThreads, 0, s>>>(c_src, err, n, (uint32_t)k, ntiles,
+                                                         tile_elems, ws, idx_out, val_out);
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
 }  // namespace gc

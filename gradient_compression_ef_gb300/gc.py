@@ -54,7 +54,11 @@ SIGNATURES = [
     ("gc_ef_topk_quant", _int, [_vp, _vp, _vp, _i64, _i64, _int, _i64, _int, _u64, _u64,
                                 _vp, _vp, _vp]),
     ("gc_powersgd_step", _int, [_vp, _vp, _vp, _i64, _i64, _int, _vp, _vp]),
+    ("gc_ef_topk_noalloc", _int, [_vp, _vp, _i64, _i64, _vp, _vp, _vp]),
 ]
+
+# largest n of gc_ef_topk_noalloc (GC_NOALLOC_MAX_N in include/gc.h)
+NOALLOC_MAX_N = 1048576
 
 
 def _load():
@@ -215,3 +219,15 @@ def ef_topk_quant(ctx, grad, err, k, bits, group, rounding, seed, step, idx_out,
 def powersgd_step(ctx, grad, err, m, n, r, P_out, Q_inout):
     _check(lib.gc_powersgd_step(ctx.handle, _ptr(grad), _ptr(err), m, n, r, _ptr(P_out),
                                 _ptr(Q_inout)), "gc_powersgd_step")
+
+
+def ef_topk_noalloc(grad, err, k, idx_out, val_out, stream=None, n=None):
+    """gc_ef_topk_noalloc: EF + Top-K with no context and no allocation, on
+    ``stream`` (default: torch's current stream); n <= NOALLOC_MAX_N."""
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    handle = stream if isinstance(stream, int) else stream.cuda_stream
+    n = grad.numel() if n is None else n
+    _check(lib.gc_ef_topk_noalloc(_ptr(grad), _ptr(err), n, k, _ptr(idx_out), _ptr(val_out),
+                                  handle), "gc_ef_topk_noalloc")

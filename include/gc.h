@@ -276,6 +276,41 @@ GC_API gc_status gc_powersgd_step(gc_ctx* ctx, const float* grad, float* err,
                            int64_t m, int64_t n, int r, float* P_out,
                            float* Q_inout);
 
+/*
+ * Largest n accepted by gc_ef_topk_noalloc: its scratch is a fixed device
+ * array of about 8 bytes per element up to this size (8.1 MiB in all).
+ */
+#define GC_NOALLOC_MAX_N 1048576
+
+/*
+ * gc_ef_topk without any allocation.  The pages have no counterpart: this
+ * entry exists for callers that must not allocate device memory -- code
+ * whose device memory all belongs to another allocator (a framework's
+ * caching pool, a fixed arena), code with a hard memory budget, or code on
+ * a latency-critical path where cudaMalloc's implicit device-wide
+ * synchronisation is unacceptable.  gc_ctx_create allocates; this call
+ * does not, and takes no context.
+ *
+ * Same arguments, results and error rules as gc_ef_topk (grad, err,
+ * idx_out and val_out are caller-owned device buffers; err may be NULL),
+ * plus the CUDA stream to run on, which must belong to the current device.
+ * n must be <= GC_NOALLOC_MAX_N, else GC_ERR_WORKSPACE before any device
+ * work.
+ *
+ * Scratch: one library-owned static device array per GPU, reserved when
+ * the library's module is loaded on that GPU and held until the process
+ * exits.  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  Every call on a device shares the one
+ * array, and each call first clears the part that must start at zero;
+ * calls that overlap on the GPU (other streams, other host threads) race on
+ * it and give wrong results, so serialise them.  Device self-check status
+ * is not reported (there is no context to hold it).  Calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ */
+GC_API gc_status gc_ef_topk_noalloc(const float* grad, float* err, int64_t n, int64_t k,
+                                    int32_t* idx_out, float* val_out, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif
