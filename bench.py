@@ -54,6 +54,8 @@ def parse_args():
     p.add_argument("--distinct", type=int, default=3, help="distinct correlated gradients")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--eager", action="store_true",
+                   help="time eager launches instead of CUDA-graph replay")
     return p.parse_args()
 
 
@@ -173,25 +175,58 @@ class BucketWorkload:
         kept = sum(self.ks)
         return 12 * self.n + kept * (4 + self.BITS / 8 + 1 / 8 + 4 / self.GROUP)
 
-    def launch_step(self, t, grad=None):
+    def launch_step(self, t, grad=None, main=None, ctxs=None):
         """Enqueues one step: every bucket on its context's stream, forked
         from and joined back into the main stream."""
         torch, gc = self.torch, self.gc
+        main = self.main if main is None else main
+        ctxs = self.ctxs if ctxs is None else ctxs
+        streams = [c._stream_ref for c in ctxs]
         g = self.grads[t % len(self.grads)] if grad is None else grad
         fork = torch.cuda.Event()
-        fork.record(self.main)
-        for s in self.streams:
+        fork.record(main)
+        for s in streams:
             s.wait_event(fork)
         for b, ((start, length), (oi, oc, os_, k, nb, ns)) in enumerate(zip(self.bounds, self.slices)):
-            ctx = self.ctxs[b % len(self.ctxs)]
+            ctx = ctxs[b % len(ctxs)]
             gc.ef_topk_quant(ctx, g[start:start + length], self.err[start:start + length], k,
                              self.BITS, self.GROUP, "stochastic", 1000 + b, t,
                              self.idx[oi:oi + k], self.codes[oc:oc + nb],
                              self.scales[os_:os_ + ns], n=length)
-        for s in self.streams:
+        for s in streams:
             j = torch.cuda.Event()
             j.record(s)
-            self.main.wait_event(j)
+            main.wait_event(j)
+
+    def capture(self):
+        """One CUDA graph per distinct gradient buffer, each holding a whole
+        step (all buckets, all streams).  Returns (graphs, launches/step)."""
+        torch = self.torch
+        graphs = []
+        cap = torch.cuda.Stream(device=self.dev)
+        before = self.launches()
+        for d in range(len(self.grads)):
+            g = torch.cuda.CUDAGraph()
+            cap.wait_stream(self.main)
+            with torch.cuda.graph(g, stream=cap):
+                self.launch_step(d, main=cap)
+            graphs.append(g)
+        self.main.wait_stream(cap)
+        return graphs, (self.launches() - before) // len(self.grads)
+
+    def algorithmic_bytes_per_launch(self):
+        """Average bytes each kernel must move per bucket: pass 1 reads g, e
+        and writes c (12 B/element); passes 2 and 4 read c (4 B/element; the
+        compaction also writes 8 B and zeroes 4 B per kept entry); pass 3
+        only touches the candidate list (no gradient bytes); the QSGD
+        kernel reads each kept value and index (8 B), writes its code, sign,
+        1/64 of a scale and its residual (4 B)."""
+        nb = len(self.bounds)
+        kept = sum(self.ks) / nb
+        n = self.n / nb
+        return {"ef_hist": 12.0 * n, "collect": 4.0 * n, "refine": 0.0,
+                "write": 4.0 * n + 12.0 * kept,
+                "quant_fused": kept * (8 + self.BITS / 8 + 1 / 8 + 4 / self.GROUP + 4)}
 
     def launches(self):
         return sum(c.launch_count() for c in self.ctxs)
@@ -202,19 +237,15 @@ class BucketWorkload:
 
 
 def kernel_timing(wl, steps, warmup_step):
-    """Per-phase CUDA-event durations over `steps` more steps."""
-    per_step = 8 * len(wl.bounds)
-    for c in wl.ctxs:
-        c.enable_timing(per_step * steps)
+    """Per-phase CUDA-event durations over `steps` more steps run with all
+    buckets on one context / stream, so that each kernel runs alone and its
+    events bracket its own execution."""
+    ctx = wl.ctxs[0]
+    ctx.enable_timing(8 * len(wl.bounds) * steps)
     for t in range(steps):
-        wl.launch_step(warmup_step + t)
-    phases = {}
-    for c in wl.ctxs:
-        for name, (ms, cnt) in c.read_timing().items():
-            a = phases.setdefault(name, [0.0, 0])
-            a[0] += ms
-            a[1] += cnt
-        c.enable_timing(0)
+        wl.launch_step(warmup_step + t, ctxs=[ctx])
+    phases = {name: [ms, cnt] for name, (ms, cnt) in ctx.read_timing().items()}
+    ctx.enable_timing(0)
     return phases
 
 
@@ -318,78 +349,104 @@ def main():
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
 
+    def timed(run_step, steps, side_streams=()):
+        barrier()
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        start.record(wl.main)
+        for s_ in side_streams:
+            s_.wait_event(start)
+        for t in range(steps):
+            run_step(t)
+        stop.record(wl.main)
+        torch.cuda.synchronize(dev)
+        barrier()
+        ms_ = start.elapsed_time(stop)
+        if world > 1:
+            tm = torch.tensor([ms_], device=dev)
+            torch.distributed.all_reduce(tm, op=torch.distributed.ReduceOp.MAX)
+            ms_ = float(tm.item())
+        return ms_ / steps
+
     props = torch.cuda.get_device_properties(dev)
     pci = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0),
                                  getattr(props, "pci_bus_id", 0),
                                  getattr(props, "pci_device_id", 0))
     sampler = ClockSampler(pci)
+
+    # eager launches through the C ABI
     launches0 = wl.launches()
-    barrier()
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with sampler:
-        start.record(wl.main)
-        for t in range(args.steps):
-            wl.launch_step(args.warmup + t)
-        stop.record(wl.main)
-        torch.cuda.synchronize(dev)
-    barrier()
-    ms = start.elapsed_time(stop)
-    launches = wl.launches() - launches0
+    eager_ms = timed(lambda t: wl.launch_step(args.warmup + t), args.steps)
+    eager_launches = wl.launches() - launches0
     wl.check()
-    if world > 1:
-        tmax = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tmax, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tmax.item())
-    ms_per_step = ms / args.steps
+    # CUDA-graph replay of whole steps (the same kernels, launched by the graph)
+    graphs, per_step_launches = wl.capture()
+    for t in range(args.warmup):
+        graphs[t % len(graphs)].replay()
+    wl.check()
+    with sampler:
+        graph_ms = timed(lambda t: graphs[t % len(graphs)].replay(), args.steps)
+    wl.check()
+    if args.eager:
+        ms_per_step, launches, launch_mode = eager_ms, eager_launches, "eager"
+    else:
+        ms_per_step, launches, launch_mode = graph_ms, per_step_launches * args.steps, "cuda_graph"
     value = world * 4.0 * wl.n / (ms_per_step * 1e-3) / 1e9
+    eager_value = world * 4.0 * wl.n / (eager_ms * 1e-3) / 1e9
 
     # per-kernel durations (second pass over the same kind of steps)
     phases = kernel_timing(wl, args.steps, args.warmup + args.steps)
     top = max(phases.items(), key=lambda kv: kv[1][0])
     peak, peak_src = measured_peaks()
-    per_launch_ms = {name: ms_ / cnt for name, (ms_, cnt) in phases.items()}
-    # algorithmic bytes per launch of each Top-K phase, per 6,553,600-element
-    # bucket: pass 1 reads g and e and writes c (12 B per element)
-    n_avg = wl.n / len(wl.bounds)
-    algo_per_launch = {"ef_hist": 12.0 * n_avg}
-    roofline = None
-    if top[0] in algo_per_launch:
-        achieved = algo_per_launch[top[0]] / (per_launch_ms[top[0]] * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "kernel": top[0], "achieved": achieved, "peak": peak,
-                    "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
-                    "traffic": None}
+    algo = wl.algorithmic_bytes_per_launch()
+    kernels = {}
+    for name, (ms_, cnt) in phases.items():
+        avg_s = ms_ / cnt * 1e-3
+        kernels[name] = {"launches": cnt, "total_ms": ms_, "avg_us": avg_s * 1e6,
+                         "algorithmic_bytes_per_launch": algo.get(name),
+                         "achieved_gbs": algo[name] / avg_s / 1e9 if algo.get(name) else None}
+    roofline = {"bound": "hbm", "kernel": top[0], "achieved": kernels[top[0]]["achieved_gbs"],
+                "peak": peak, "unit": "GB/s", "peak_source": peak_src,
+                "frac": kernels[top[0]]["achieved_gbs"] / peak, "traffic": None}
     step_achieved = wl.algorithmic_bytes() / (ms_per_step * 1e-3) / 1e9
 
-    # end to end through the C ABI with host buffers
+    # end to end through the C ABI with host buffers: every step copies its
+    # gradient from pinned host memory (overlapped with the previous step on a
+    # copy stream) and reads the compressed result back
     e2e = None
     if not args.no_e2e:
-        hosts = [g.cpu().pin_memory() for g in wl.grads[:2]]
-        dev_in = torch.empty(wl.n, dtype=torch.float32, device=dev)
+        T = len(wl.grads)
+        hosts = [g.cpu().pin_memory() for g in wl.grads]
         out_i = torch.empty(wl.idx.numel(), dtype=torch.int32).pin_memory()
         out_c = torch.empty(wl.codes.numel(), dtype=torch.uint8).pin_memory()
         out_s = torch.empty(wl.scales.numel(), dtype=torch.float32).pin_memory()
-        e2e_steps = max(3, min(args.steps, 20))
-        barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(wl.main)
-        with torch.cuda.stream(wl.main):
-            for t in range(e2e_steps):
-                dev_in.copy_(hosts[t % 2], non_blocking=True)
-                wl.launch_step(t, grad=dev_in)
-                out_i.copy_(wl.idx, non_blocking=True)
-                out_c.copy_(wl.codes, non_blocking=True)
-                out_s.copy_(wl.scales, non_blocking=True)
-        e1.record(wl.main)
-        torch.cuda.synchronize(dev)
-        barrier()
-        e_ms = e0.elapsed_time(e1) / e2e_steps
-        if world > 1:
-            tm = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(tm, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(tm.item())
+        copy_s = torch.cuda.Stream(device=dev)
+        ready = [torch.cuda.Event() for _ in range(T)]
+        done = [torch.cuda.Event() for _ in range(T)]
+        e2e_steps = max(3, min(args.steps, 30))
+
+        def e2e_step(t):
+            d = t % T
+            if t >= T:
+                copy_s.wait_event(done[d])
+            with torch.cuda.stream(copy_s):
+                wl.grads[d].copy_(hosts[d], non_blocking=True)
+            ready[d].record(copy_s)
+            wl.main.wait_event(ready[d])
+            if args.eager:
+                wl.launch_step(d)
+            else:
+                graphs[d].replay()
+            done[d].record(wl.main)
+            out_i.copy_(wl.idx, non_blocking=True)
+            out_c.copy_(wl.codes, non_blocking=True)
+            out_s.copy_(wl.scales, non_blocking=True)
+
+        e_ms = timed(e2e_step, e2e_steps, side_streams=(copy_s,))
         e2e = {"value": world * 4.0 * wl.n / (e_ms * 1e-3) / 1e9, "unit": UNIT,
                "h2d_bytes_per_step": 4 * wl.n, "d2h_bytes_per_step": wl.out_bytes(),
-               "ms_per_step": e_ms}
+               "ms_per_step": e_ms, "launch": launch_mode}
+        wl.check()
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -398,9 +455,9 @@ def main():
             "step_roofline": {"algorithmic_bytes_per_step": wl.algorithmic_bytes(),
                               "achieved": step_achieved, "peak": peak, "unit": "GB/s",
                               "frac": step_achieved / peak},
-            "kernels": {name: {"launches": cnt, "total_ms": ms_,
-                               "avg_us": 1e3 * ms_ / cnt} for name, (ms_, cnt) in phases.items()},
-            "e2e": e2e, "clocks": sampler.summary(), "gpu_launches": launches}
+            "kernels": kernels,
+            "e2e": e2e, "clocks": sampler.summary(), "gpu_launches": launches,
+            "launch": launch_mode, "eager": {"value": eager_value, "ms_per_step": eager_ms}}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:

@@ -54,7 +54,8 @@ struct DeviceGuard {
 
 // Layout of the per-context scratch (one allocation).
 struct WsLayout {
-  size_t hist, sel, status, tile_above, tile_out, tile_tie, cand, vals, partials, total;
+  size_t hist, mid, low, tile_kept, sel, status, tile_above, tile_out, tile_tie, cand, stash, vals,
+      partials, total;
 };
 
 WsLayout ws_layout(int64_t max_n, int64_t max_partials) {
@@ -62,12 +63,16 @@ WsLayout ws_layout(int64_t max_n, int64_t max_partials) {
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off += (bytes + 255) / 256 * 256; return o; };
   L.hist = take(sizeof(uint32_t) * gc::kHistBins);
+  L.mid = take(sizeof(uint32_t) * gc::kMidBins);
+  L.low = take(sizeof(uint32_t) * gc::kLowBins);
+  L.tile_kept = take(sizeof(uint32_t) * gc::kMaxTiles);
   L.sel = take(sizeof(gc::TopkSel));
   L.status = take(sizeof(uint32_t) * 4);
   L.tile_above = take(sizeof(uint32_t) * gc::kMaxTiles);
   L.tile_out = take(sizeof(uint32_t) * gc::kMaxTiles);
   L.tile_tie = take(sizeof(uint32_t) * gc::kMaxTiles);
   L.cand = take(sizeof(uint2) * std::max<int64_t>(max_n, 1));
+  L.stash = take(sizeof(uint2) * gc::kStashMax);
   L.vals = take(sizeof(float) * std::max<int64_t>(max_n, 1));
   L.partials = take(sizeof(float4) * std::max<int64_t>(max_partials, 1));
   L.total = off;
@@ -143,12 +148,16 @@ gc_status gc_ctx_create(gc_ctx** out, void* cuda_stream, int64_t max_n) {
   char* b = static_cast<char*>(base);
   ctx->ws_base = base;
   ctx->ws.hist = reinterpret_cast<uint32_t*>(b + L.hist);
+  ctx->ws.mid = reinterpret_cast<uint32_t*>(b + L.mid);
+  ctx->ws.low = reinterpret_cast<uint32_t*>(b + L.low);
+  ctx->ws.tile_kept = reinterpret_cast<uint32_t*>(b + L.tile_kept);
   ctx->ws.sel = reinterpret_cast<gc::TopkSel*>(b + L.sel);
   ctx->ws.status = reinterpret_cast<uint32_t*>(b + L.status);
   ctx->ws.tile_above = reinterpret_cast<uint32_t*>(b + L.tile_above);
   ctx->ws.tile_out = reinterpret_cast<uint32_t*>(b + L.tile_out);
   ctx->ws.tile_tie = reinterpret_cast<uint32_t*>(b + L.tile_tie);
   ctx->ws.cand = reinterpret_cast<uint2*>(b + L.cand);
+  ctx->ws.stash = reinterpret_cast<uint2*>(b + L.stash);
   ctx->ws.vals = reinterpret_cast<float*>(b + L.vals);
   ctx->ws.partials = reinterpret_cast<float4*>(b + L.partials);
   ctx->ws.max_n = max_n;
@@ -175,7 +184,8 @@ void free_timing(gc_ctx* ctx) {
 const char* gc_phase_name(int phase) {
   static const char* names[GC_PHASE_COUNT] = {
       "ef_hist", "collect", "write", "ef_add", "quant_fused", "quant_stats",
-      "quant_combine", "quant_apply", "dequant", "psgd_mq", "psgd_mtp", "psgd_resid"};
+      "quant_combine", "quant_apply", "dequant", "psgd_mq", "psgd_mtp", "psgd_resid",
+      "refine"};
   return (phase >= 0 && phase < GC_PHASE_COUNT) ? names[phase] : "?";
 }
 

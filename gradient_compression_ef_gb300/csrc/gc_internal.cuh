@@ -23,9 +23,9 @@ constexpr int kMidBits = 11;                     // bits 18..8
 constexpr int kMidBins = 1 << kMidBits;
 constexpr int kLowBits = 8;                      // bits 7..0
 constexpr int kLowBins = 1 << kLowBits;
-constexpr int kTopkThreads = 512;
-constexpr int kTopkSub = kTopkThreads * 4;       // elements per block step
-constexpr int kMaxTiles = 4096;                  // tiles of the ordered compaction
+constexpr int kMaxTiles = 2048;                  // tiles of the ordered compaction
+constexpr int kMinTileShift = 12;                // tiles of at least 4096 elements
+constexpr int kStashMax = 8192;                  // third-level candidates kept aside
 
 // Device status bits (OR-ed into the context's status word).
 constexpr uint32_t kStatusTopkCount = 1u << 0;   // candidate count mismatch
@@ -35,27 +35,36 @@ constexpr uint32_t kStatusScatterIndex = 1u << 3;  // residual index out of rang
 
 // Per-context Top-K selection state in device memory.
 struct TopkSel {
-  uint32_t bin;         // first-level threshold bin B
-  uint32_t above;       // elements whose bin is above B
-  uint32_t need1;       // k - above: how many of bin B are kept
-  uint32_t cand_total;  // elements in bin B
-  uint32_t T;           // exact threshold key
-  uint32_t need_T;      // entries with key == T to keep (smallest indices)
-  uint32_t ticket_hist; // last-block ticket of the histogram pass
-  uint32_t ticket_coll; // last-block ticket of the collection pass
-  uint32_t cand_count;  // fill counter of the candidate buffer
-  uint32_t pad[7];
+  uint32_t bin;           // first-level threshold bin B
+  uint32_t above;         // elements whose bin is above B
+  uint32_t need1;         // k - above: how many of bin B are kept
+  uint32_t cand_total;    // elements in bin B
+  uint32_t B2;            // second-level digit (bits 18..8)
+  uint32_t need2;         // how many of the (B, B2) entries are kept
+  uint32_t T;             // exact threshold key
+  uint32_t need_T;        // entries with key == T to keep (smallest indices)
+  uint32_t ticket_coll;   // last-block ticket of the collection pass
+  uint32_t ticket_refine; // last-block ticket of the refinement pass
+  uint32_t cand_count;    // fill counter of the candidate buffer
+  uint32_t stash_count;   // fill counter of the third-level stash
+  uint32_t pad[4];
 };
 
-// Device scratch of one context (all pointers into one allocation).
+// Device scratch of one context (all pointers into one allocation).  The
+// histograms, tile_kept, sel and status must be zero when a call starts;
+// every call leaves them zero again.
 struct Workspace {
-  uint32_t* hist;        // [kHistBins], zero between calls
+  uint32_t* hist;        // [kHistBins] first level
+  uint32_t* mid;         // [kMidBins] candidates' bits 18..8
+  uint32_t* low;         // [kLowBins] (B, B2) candidates' bits 7..0
+  uint32_t* tile_kept;   // [kMaxTiles] kept candidates per tile
   TopkSel* sel;          // one record
   uint32_t* status;      // device status word
   uint32_t* tile_above;  // [kMaxTiles]
   uint32_t* tile_out;    // [kMaxTiles] exclusive output offsets
   uint32_t* tile_tie;    // [kMaxTiles] exclusive tie offsets
   uint2* cand;           // [max_n] (key, index) candidates
+  uint2* stash;          // [kStashMax] third-level candidates
   float* vals;           // [max_n] kept values of the hybrid call
   float4* partials;      // [max_partials] chunk statistics of quantisation
   int64_t max_n;

@@ -18,11 +18,15 @@ constexpr int kMaxDevices = 128;
 // be zero when a call starts; the rest is fully written by every call.
 struct StaticScratch {
   uint32_t hist[kHistBins];
+  uint32_t mid[kMidBins];
+  uint32_t low[kLowBins];
+  uint32_t tile_kept[kMaxTiles];
   TopkSel sel;
   uint32_t status[4];
   uint32_t tile_above[kMaxTiles];
   uint32_t tile_out[kMaxTiles];
   uint32_t tile_tie[kMaxTiles];
+  uint2 stash[kStashMax];
   uint2 cand[kNoAllocMaxN];
 };
 
@@ -82,12 +86,16 @@ extern "C" gc_status gc_ef_topk_noalloc(const float* grad, float* err, int64_t n
   char* b = static_cast<char*>(base);
   gc::Workspace ws{};
   ws.hist = reinterpret_cast<uint32_t*>(b + offsetof(gc::StaticScratch, hist));
+  ws.mid = reinterpret_cast<uint32_t*>(b + offsetof(gc::StaticScratch, mid));
+  ws.low = reinterpret_cast<uint32_t*>(b + offsetof(gc::StaticScratch, low));
+  ws.tile_kept = reinterpret_cast<uint32_t*>(b + offsetof(gc::StaticScratch, tile_kept));
   ws.sel = reinterpret_cast<gc::TopkSel*>(b + offsetof(gc::StaticScratch, sel));
   ws.status = reinterpret_cast<uint32_t*>(b + offsetof(gc::StaticScratch, status));
   ws.tile_above = reinterpret_cast<uint32_t*>(b + offsetof(gc::StaticScratch, tile_above));
   ws.tile_out = reinterpret_cast<uint32_t*>(b + offsetof(gc::StaticScratch, tile_out));
   ws.tile_tie = reinterpret_cast<uint32_t*>(b + offsetof(gc::StaticScratch, tile_tie));
   ws.cand = reinterpret_cast<uint2*>(b + offsetof(gc::StaticScratch, cand));
+  ws.stash = reinterpret_cast<uint2*>(b + offsetof(gc::StaticScratch, stash));
   ws.vals = nullptr;
   ws.partials = nullptr;
   ws.max_n = gc::kNoAllocMaxN;

@@ -130,8 +130,8 @@ GC_API gc_status gc_ctx_check(gc_ctx* ctx);
  */
 typedef enum gc_phase {
   GC_PHASE_EF_HIST = 0,      /* Top-K pass 1: c = g + e, 12-bit histogram */
-  GC_PHASE_COLLECT = 1,      /* Top-K pass 2: candidates + exact threshold */
-  GC_PHASE_WRITE = 2,        /* Top-K pass 3: ordered compaction, e' = 0 */
+  GC_PHASE_COLLECT = 1,      /* Top-K pass 2: threshold bin, candidates */
+  GC_PHASE_WRITE = 2,        /* Top-K pass 4: ordered compaction, e' = 0 */
   GC_PHASE_EF_ADD = 3,       /* e = g + e (k == 0) */
   GC_PHASE_QUANT_FUSED = 4,  /* single-pass group quantisation */
   GC_PHASE_QUANT_STATS = 5,  /* multi-pass: chunk statistics */
@@ -141,7 +141,8 @@ typedef enum gc_phase {
   GC_PHASE_PSGD_MQ = 9,      /* PowerSGD pass 1: M = G + E, P = M Q */
   GC_PHASE_PSGD_MTP = 10,    /* PowerSGD pass 2: Q' = M^T P_hat */
   GC_PHASE_PSGD_RESID = 11,  /* PowerSGD pass 3: E' = M - P_hat Q'^T */
-  GC_PHASE_COUNT = 12
+  GC_PHASE_REFINE = 12,      /* Top-K pass 3: exact threshold, tile offsets */
+  GC_PHASE_COUNT = 13
 } gc_phase;
 
 /* Name of a phase ("ef_hist", ...); "?" when out of range. */
@@ -278,7 +279,7 @@ GC_API gc_status gc_powersgd_step(gc_ctx* ctx, const float* grad, float* err,
 
 /*
  * Largest n accepted by gc_ef_topk_noalloc: its scratch is a fixed device
- * array of about 8 bytes per element up to this size (8.1 MiB in all).
+ * array of about 8 bytes per element up to this size (8.2 MiB in all).
  */
 #define GC_NOALLOC_MAX_N 1048576
 
