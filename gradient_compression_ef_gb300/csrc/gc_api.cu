@@ -185,7 +185,7 @@ const char* gc_phase_name(int phase) {
   static const char* names[GC_PHASE_COUNT] = {
       "ef_hist", "collect", "write", "ef_add", "quant_fused", "quant_stats",
       "quant_combine", "quant_apply", "dequant", "psgd_mq", "psgd_mtp", "psgd_resid",
-      "refine"};
+      "refine", "bk_hist", "bk_collect", "bk_refine", "bk_write", "bk_quant"};
   return (phase >= 0 && phase < GC_PHASE_COUNT) ? names[phase] : "?";
 }
 
@@ -242,6 +242,7 @@ gc_status gc_ctx_destroy(gc_ctx* ctx) {
   free_timing(ctx);
   if (ctx->ws_base) cudaFree(ctx->ws_base);
   if (ctx->psgd_base) cudaFree(ctx->psgd_base);
+  gc::free_buckets(ctx);
   free(ctx);
   return st;
 }
@@ -394,6 +395,76 @@ gc_status gc_powersgd_step(gc_ctx* ctx, const float* grad, float* err, int64_t m
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return GC_ERR_CUDA;
   return gc::launch_powersgd(ctx, grad, err, m, n, r, P_out, Q_inout);
+}
+
+gc_status gc_ctx_set_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n,
+                             const int64_t* bucket_k) {
+  if (!ctx || nb < 1 || nb > gc::kMaxBuckets || !bucket_n || !bucket_k) return GC_ERR_INVALID_ARG;
+  for (int b = 0; b < nb; ++b) {
+    if (bucket_n[b] < 1 || bucket_n[b] > gc::kMaxBucketElems) return GC_ERR_INVALID_ARG;
+    if (bucket_k[b] < 0 || bucket_k[b] > bucket_n[b]) return GC_ERR_INVALID_ARG;
+  }
+  for (int b = 0; b + 1 < nb; ++b)
+    if (bucket_n[b] % 4 != 0) return GC_ERR_ALIGNMENT;
+  DeviceGuard guard(ctx->device);
+  if (!guard.ok) return GC_ERR_CUDA;
+  if (cudaStreamSynchronize(ctx->stream) != cudaSuccess) return GC_ERR_CUDA;
+  return gc::plan_buckets(ctx, nb, bucket_n, bucket_k);
+}
+
+gc_status gc_bucket_offsets(int nb, const int64_t* bucket_k, int bits, int64_t group,
+                            int64_t* idx_off, int64_t* codes_off, int64_t* scales_off) {
+  if (nb < 1 || nb > gc::kMaxBuckets || !bucket_k) return GC_ERR_INVALID_ARG;
+  for (int b = 0; b < nb; ++b)
+    if (bucket_k[b] < 0 || bucket_k[b] > INT32_MAX) return GC_ERR_INVALID_ARG;
+  if (codes_off && !valid_bits(bits)) return GC_ERR_UNSUPPORTED;
+  if (scales_off && group < 1) return GC_ERR_INVALID_ARG;
+  int64_t oi = 0, oc = 0, os = 0;
+  for (int b = 0; b <= nb; ++b) {
+    if (idx_off) idx_off[b] = oi;
+    if (codes_off) codes_off[b] = oc;
+    if (scales_off) scales_off[b] = os;
+    if (b == nb) break;
+    oi += round_up(bucket_k[b], 4);
+    if (codes_off) oc += gc_codes_bytes(bucket_k[b], bits, GC_QSGD);
+    if (scales_off) os += round_up(gc_scales_floats(bucket_k[b], group, GC_QSGD), 4);
+  }
+  return GC_OK;
+}
+
+gc_status gc_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int32_t* idx_out,
+                             float* val_out) {
+  if (!ctx) return GC_ERR_INVALID_ARG;
+  if (!ctx->bk_base) return GC_ERR_WORKSPACE;
+  const gc::BucketWs& w = ctx->bk;
+  GC_TRY(check_buf(grad, true));
+  if (err) GC_TRY(check_buf(err, true));
+  GC_TRY(check_buf(idx_out, w.vals_total > 0));
+  GC_TRY(check_buf(val_out, w.vals_total > 0));
+  DeviceGuard guard(ctx->device);
+  if (!guard.ok) return GC_ERR_CUDA;
+  return gc::launch_ef_topk_buckets(ctx, grad, err, idx_out, val_out, true, 0, 0);
+}
+
+gc_status gc_ef_topk_quant_buckets(gc_ctx* ctx, const float* grad, float* err, int bits,
+                                   int64_t group, int rounding, uint64_t seed, uint64_t step,
+                                   int32_t* idx_out, uint8_t* codes_out, float* scales_out) {
+  if (!ctx) return GC_ERR_INVALID_ARG;
+  if (!ctx->bk_base) return GC_ERR_WORKSPACE;
+  const gc::BucketWs& w = ctx->bk;
+  GC_TRY(check_quant(1, bits, group, GC_QSGD, rounding));
+  if (group < 4 || group > 128 || (group & (group - 1)) != 0) return GC_ERR_UNSUPPORTED;
+  GC_TRY(check_buf(grad, true));
+  if (!err) return GC_ERR_INVALID_ARG;
+  GC_TRY(check_buf(err, true));
+  GC_TRY(check_buf(idx_out, w.vals_total > 0));
+  GC_TRY(check_buf(codes_out, w.vals_total > 0));
+  GC_TRY(check_buf(scales_out, w.vals_total > 0));
+  DeviceGuard guard(ctx->device);
+  if (!guard.ok) return GC_ERR_CUDA;
+  GC_TRY(gc::launch_ef_topk_buckets(ctx, grad, err, idx_out, w.vals, false, bits, group));
+  return gc::launch_quant_buckets(ctx, err, idx_out, bits, group, rounding, seed, step,
+                                  codes_out, scales_out);
 }
 
 }  // extern "C"

@@ -71,6 +71,78 @@ struct Workspace {
   int64_t max_partials;
 };
 
+// ---------------------------------------------------------------------------
+// Bucketed calls: one launch per pass for every bucket of a flat gradient.
+// ---------------------------------------------------------------------------
+constexpr int kSegShift = 11;                    // segments of 2048 elements, one warp each
+constexpr int kSegElems = 1 << kSegShift;
+constexpr int kChunkVals = 128;                  // kept values per quantisation warp
+constexpr int kBkStash = 2048;                   // third-level entries set aside per bucket
+constexpr int kMaxBuckets = 65536;
+constexpr int64_t kMaxBucketElems = INT32_MAX - 65535;  // 32-bit offsets inside a bucket
+
+// One bucket of the plan (device copy written once by gc_ctx_set_buckets).
+struct BucketDesc {
+  int64_t start;        // first element in the flat gradient
+  int64_t idx_off;      // first slot of the bucket's idx / value outputs
+  int32_t n, k;
+  int32_t seg_first;    // first global segment
+  int32_t nseg;
+  int32_t chunk_first;  // first 128-value quantisation chunk
+  int32_t nchunk;
+  int32_t blk_hist;     // blocks of each pass that touch the bucket (last-block tickets)
+  int32_t blk_coll;
+  int32_t blk_ref;
+  int32_t pad;
+};
+
+// Per-bucket selection state.  Tickets and the stash counter are zero
+// between calls (each pass's last block resets its own).
+struct BucketSel {
+  uint32_t B, above1, need1, cntB;   // first level
+  uint32_t B2, need2;                // second level
+  uint32_t T, needT;                 // exact threshold key, ties kept at T
+  uint32_t ticket_hist, ticket_coll, ticket_ref;
+  uint32_t stash_count;
+  uint32_t pad[4];
+};
+
+// Device scratch of a bucket plan (pointers into one allocation).  hist,
+// mid, low, sel are zero between calls.
+struct BucketWs {
+  int nb;
+  int64_t total_n;      // elements of the flat gradient
+  int64_t nseg;         // segments over all buckets
+  int64_t nchunk;       // quantisation chunks over all buckets
+  int64_t vals_total;   // slots of the idx / value outputs (sum of k rounded up to 4)
+  int g_hist, g_coll, g_ref, g_write;  // grid sizes the tickets were counted for
+  BucketDesc* desc;     // [nb]
+  BucketSel* sel;       // [nb]
+  int32_t* seg_bucket;  // [nseg]
+  int32_t* chunk_bucket;  // [nchunk]
+  uint32_t* hist;       // [nb][kHistBins]
+  uint32_t* mid;        // [nb][kMidBins]
+  uint32_t* low;        // [nb][kLowBins]
+  uint32_t* seg_cnt;    // [nseg] list entries of the segment
+  uint32_t* seg_above;  // [nseg] entries above the first-level bin
+  uint32_t* seg_kept;   // [nseg] entries above the threshold key T
+  uint32_t* seg_tie;    // [nseg] entries equal to T
+  uint32_t* seg_out;    // [nseg] first output slot (bucket-relative)
+  uint32_t* seg_tieb;   // [nseg] ties at T in earlier segments of the bucket
+  uint2* list;          // [nseg * kSegElems] (bits of c, bucket index), per segment
+  uint2* stash;         // [nb][kBkStash] (key, segment)
+  int64_t* qoff;        // [nb][2] codes byte / scales float offset of each bucket
+  float* vals;          // [vals_total] kept values of the hybrid call
+  uint32_t* status;     // the context's device status word
+};
+
+// Segment range [lo, hi) of block i out of G over S segments.
+__host__ __device__ __forceinline__ void seg_range(int64_t S, int G, int i, int64_t* lo,
+                                                   int64_t* hi) {
+  *lo = S * i / G;
+  *hi = S * (i + 1) / G;
+}
+
 struct PsgdWorkspace {
   float* q_part;         // [splits][max_n][max_r] partial sums of M^T P
   uint32_t* tickets;     // [strips] last-block tickets
@@ -96,6 +168,9 @@ struct gc_ctx {
   cudaEvent_t* ev_stop;
   int* ev_phase;
   int64_t launches;         // kernels launched by this context
+  // bucket plan (gc_ctx_set_buckets)
+  void* bk_base;
+  gc::BucketWs bk;
 };
 
 namespace gc {
@@ -256,6 +331,21 @@ gc_status launch_dequant(gc_ctx* ctx, const uint8_t* codes,
 gc_status launch_powersgd(gc_ctx* ctx, const float* grad, float* err,
                           int64_t m, int64_t n, int r, float* P_out,
                           float* Q_inout);
+
+// Bucketed Top-K over every bucket of the context's plan; vals != NULL
+// receives the kept values at the bucket's idx_off (val_out otherwise);
+// zero_err writes e' = +0 at the kept positions.  qbits > 0 also lays out
+// the QSGD outputs of (qbits, qgroup) for launch_quant_buckets.
+gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int32_t* idx_out,
+                                 float* val_out, bool zero_err, int qbits, int64_t qgroup);
+// QSGD of every bucket's kept values (from launch_ef_topk_buckets) with the
+// residual scattered to err; bucket b uses seed + b.
+gc_status launch_quant_buckets(gc_ctx* ctx, float* err, const int32_t* idx_out, int bits,
+                               int64_t group, int rounding, uint64_t seed, uint64_t step,
+                               uint8_t* codes_out, float* scales_out);
+// Builds the device plan of nb buckets (synchronous; frees the previous).
+gc_status plan_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n, const int64_t* bucket_k);
+void free_buckets(gc_ctx* ctx);
 
 // Bytes of PowerSGD scratch for matrices up to max_m x max_n, rank max_r.
 int64_t psgd_workspace_bytes(int64_t max_m, int64_t max_n, int max_r, int num_sms);

@@ -68,12 +68,14 @@ struct QuantOut {
   uint32_t* status;                // device status word
 };
 
+__device__ __forceinline__ void zero_padding_bytes(const QuantOut& o) {
+  for (int64_t b = o.zero_begin; b < o.zero_end; ++b) o.codes[b] = 0;
+  if (o.signs)
+    for (int64_t b = o.szero_begin; b < o.szero_end; ++b) o.signs[b] = 0;
+}
+
 __device__ __forceinline__ void zero_padding(const QuantOut& o) {
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    for (int64_t b = o.zero_begin; b < o.zero_end; ++b) o.codes[b] = 0;
-    if (o.signs)
-      for (int64_t b = o.szero_begin; b < o.szero_end; ++b) o.signs[b] = 0;
-  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) zero_padding_bytes(o);
 }
 
 template <int MODE, int BITS>
@@ -90,118 +92,127 @@ __device__ __forceinline__ uint32_t code_bits4(const uint32_t q[4], const bool n
 // ---------------------------------------------------------------------------
 // Fused single-pass kernel for groups of G = 4 * LPG elements.
 // ---------------------------------------------------------------------------
+// One warp quantises elements base .. base+127 of x (groups of G = 4 * LPG
+// consecutive lanes, G dividing 128).  Every lane of the warp must call it.
+template <int MODE, int BITS, int LPG, int IO>
+__device__ __forceinline__ void quant_fused_chunk(
+    const float* __restrict__ x, float* __restrict__ err,
+    const int32_t* __restrict__ scatter_idx, int64_t n, const QuantOut& o,
+    int stochastic, uint64_t seed, uint64_t step, int64_t base, int lane) {
+  constexpr int G = 4 * LPG;
+  constexpr uint32_t top = (MODE == GC_TERN) ? 1u : ((1u << BITS) - 1u);
+  const float levels = (float)top;
+  const int64_t i0 = base + 4 * lane;
+  const bool active = i0 < n;
+  float c[4];
+  bool valid[4];
+  if (i0 + 3 < n) {
+    const float4 v = IO == IO_EF ? __ldcs(reinterpret_cast<const float4*>(x + i0))
+                                 : *reinterpret_cast<const float4*>(x + i0);
+    c[0] = v.x; c[1] = v.y; c[2] = v.z; c[3] = v.w;
+    valid[0] = valid[1] = valid[2] = valid[3] = true;
+    if (IO == IO_EF) {
+      const float4 e = *reinterpret_cast<const float4*>(err + i0);
+      c[0] = __fadd_rn(c[0], e.x);
+      c[1] = __fadd_rn(c[1], e.y);
+      c[2] = __fadd_rn(c[2], e.z);
+      c[3] = __fadd_rn(c[3], e.w);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      valid[j] = i0 + j < n;
+      c[j] = valid[j] ? x[i0 + j] : 0.0f;
+      if (IO == IO_EF && valid[j]) c[j] = __fadd_rn(c[j], err[i0 + j]);
+    }
+  }
+
+  // group statistics (lanes of a group are LPG consecutive lanes)
+  float scale, offset = 0.0f;
+  if (MODE == GC_MINMAX) {
+    float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (valid[j]) { mn = fminf(mn, c[j]); mx = fmaxf(mx, c[j]); }
+#pragma unroll
+    for (int o2 = 1; o2 < LPG; o2 <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o2));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+    }
+    mn = __fadd_rn(mn, 0.0f);
+    mx = __fadd_rn(mx, 0.0f);
+    scale = __fdiv_rn(__fsub_rn(mx, mn), levels);
+    offset = mn;
+  } else if (MODE == GC_QSGD) {
+    float s = __fadd_rn(__fadd_rn(__fmul_rn(c[0], c[0]), __fmul_rn(c[1], c[1])),
+                        __fadd_rn(__fmul_rn(c[2], c[2]), __fmul_rn(c[3], c[3])));
+    s = warp_sum_tree(s, LPG);
+    scale = __fdiv_rn(__fsqrt_rn(s), levels);
+  } else {
+    float m = fmaxf(fmaxf(fabsf(c[0]), fabsf(c[1])), fmaxf(fabsf(c[2]), fabsf(c[3])));
+#pragma unroll
+    for (int o2 = 1; o2 < LPG; o2 <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o2));
+    scale = m;
+  }
+  if (active && (lane % LPG) == 0) {
+    const int64_t g = i0 / G;
+    if (MODE == GC_MINMAX)
+      reinterpret_cast<float2*>(o.scales)[g] = make_float2(scale, offset);
+    else
+      o.scales[g] = scale;
+  }
+
+  float u[4] = {0.f, 0.f, 0.f, 0.f};
+  if (stochastic) uniform4((uint64_t)i0 >> 2, seed, step, u);
+  uint32_t q[4];
+  bool neg[4];
+  float r[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float gh;
+    q[j] = quantize_one<MODE>(c[j], scale, offset, stochastic != 0, u[j], top, &neg[j], &gh);
+    if (!valid[j]) { q[j] = 0u; neg[j] = false; }
+    r[j] = __fsub_rn(c[j], gh);
+  }
+  store_codes4<(MODE == GC_TERN) ? 2 : BITS>(o.codes, i0, active, code_bits4<MODE, BITS>(q, neg));
+  if (MODE == GC_QSGD) {
+    const bool s4[4] = {neg[0], neg[1], neg[2], neg[3]};
+    uint32_t sb[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) sb[j] = s4[j] ? 1u : 0u;
+    store_codes4<1>(o.signs, i0, active, pack4<1>(sb));
+  }
+  if (IO == IO_EF) {
+    if (i0 + 3 < n) {
+      __stcs(reinterpret_cast<float4*>(err + i0), make_float4(r[0], r[1], r[2], r[3]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (valid[j]) err[i0 + j] = r[j];
+    }
+  } else if (IO == IO_SCATTER) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (!valid[j]) continue;
+      const int32_t t = scatter_idx[i0 + j];
+      if (t >= 0 && (int64_t)t < o.scatter_n) err[t] = r[j];
+      else atomicOr(o.status, kStatusScatterIndex);
+    }
+  }
+}
+
 template <int MODE, int BITS, int LPG, int IO>
 __global__ void __launch_bounds__(kQThreads) quant_fused_kernel(
     const float* __restrict__ x, float* __restrict__ err,
     const int32_t* __restrict__ scatter_idx, int64_t n, QuantOut o,
     int stochastic, uint64_t seed, uint64_t step) {
-  constexpr int G = 4 * LPG;
-  constexpr uint32_t top = (MODE == GC_TERN) ? 1u : ((1u << BITS) - 1u);
-  const float levels = (float)top;
   const int lane = threadIdx.x & 31;
   const int64_t warp_id = ((int64_t)blockIdx.x * kQThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kQThreads) >> 5;
   zero_padding(o);
-
-  for (int64_t base = warp_id * 128; base < n; base += nwarps * 128) {
-    const int64_t i0 = base + 4 * lane;
-    const bool active = i0 < n;
-    float c[4];
-    bool valid[4];
-    if (i0 + 3 < n) {
-      const float4 v = IO == IO_EF ? __ldcs(reinterpret_cast<const float4*>(x + i0))
-                                   : *reinterpret_cast<const float4*>(x + i0);
-      c[0] = v.x; c[1] = v.y; c[2] = v.z; c[3] = v.w;
-      valid[0] = valid[1] = valid[2] = valid[3] = true;
-      if (IO == IO_EF) {
-        const float4 e = *reinterpret_cast<const float4*>(err + i0);
-        c[0] = __fadd_rn(c[0], e.x);
-        c[1] = __fadd_rn(c[1], e.y);
-        c[2] = __fadd_rn(c[2], e.z);
-        c[3] = __fadd_rn(c[3], e.w);
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        valid[j] = i0 + j < n;
-        c[j] = valid[j] ? x[i0 + j] : 0.0f;
-        if (IO == IO_EF && valid[j]) c[j] = __fadd_rn(c[j], err[i0 + j]);
-      }
-    }
-
-    // group statistics (lanes of a group are LPG consecutive lanes)
-    float scale, offset = 0.0f;
-    if (MODE == GC_MINMAX) {
-      float mn = INFINITY, mx = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (valid[j]) { mn = fminf(mn, c[j]); mx = fmaxf(mx, c[j]); }
-#pragma unroll
-      for (int o2 = 1; o2 < LPG; o2 <<= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o2));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
-      }
-      mn = __fadd_rn(mn, 0.0f);
-      mx = __fadd_rn(mx, 0.0f);
-      scale = __fdiv_rn(__fsub_rn(mx, mn), levels);
-      offset = mn;
-    } else if (MODE == GC_QSGD) {
-      float s = __fadd_rn(__fadd_rn(__fmul_rn(c[0], c[0]), __fmul_rn(c[1], c[1])),
-                          __fadd_rn(__fmul_rn(c[2], c[2]), __fmul_rn(c[3], c[3])));
-      s = warp_sum_tree(s, LPG);
-      scale = __fdiv_rn(__fsqrt_rn(s), levels);
-    } else {
-      float m = fmaxf(fmaxf(fabsf(c[0]), fabsf(c[1])), fmaxf(fabsf(c[2]), fabsf(c[3])));
-#pragma unroll
-      for (int o2 = 1; o2 < LPG; o2 <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o2));
-      scale = m;
-    }
-    if (active && (lane % LPG) == 0) {
-      const int64_t g = i0 / G;
-      if (MODE == GC_MINMAX)
-        reinterpret_cast<float2*>(o.scales)[g] = make_float2(scale, offset);
-      else
-        o.scales[g] = scale;
-    }
-
-    float u[4] = {0.f, 0.f, 0.f, 0.f};
-    if (stochastic) uniform4((uint64_t)i0 >> 2, seed, step, u);
-    uint32_t q[4];
-    bool neg[4];
-    float r[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float gh;
-      q[j] = quantize_one<MODE>(c[j], scale, offset, stochastic != 0, u[j], top, &neg[j], &gh);
-      if (!valid[j]) { q[j] = 0u; neg[j] = false; }
-      r[j] = __fsub_rn(c[j], gh);
-    }
-    store_codes4<(MODE == GC_TERN) ? 2 : BITS>(o.codes, i0, active, code_bits4<MODE, BITS>(q, neg));
-    if (MODE == GC_QSGD) {
-      const bool s4[4] = {neg[0], neg[1], neg[2], neg[3]};
-      uint32_t sb[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) sb[j] = s4[j] ? 1u : 0u;
-      store_codes4<1>(o.signs, i0, active, pack4<1>(sb));
-    }
-    if (IO == IO_EF) {
-      if (i0 + 3 < n) {
-        __stcs(reinterpret_cast<float4*>(err + i0), make_float4(r[0], r[1], r[2], r[3]));
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (valid[j]) err[i0 + j] = r[j];
-      }
-    } else if (IO == IO_SCATTER) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (!valid[j]) continue;
-        const int32_t t = scatter_idx[i0 + j];
-        if (t >= 0 && (int64_t)t < o.scatter_n) err[t] = r[j];
-        else atomicOr(o.status, kStatusScatterIndex);
-      }
-    }
-  }
+  for (int64_t base = warp_id * 128; base < n; base += nwarps * 128)
+    quant_fused_chunk<MODE, BITS, LPG, IO>(x, err, scatter_idx, n, o, stochastic, seed, step,
+                                           base, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -503,24 +514,55 @@ __global__ void __launch_bounds__(kQThreads) dequant_kernel(
 // ---------------------------------------------------------------------------
 // Host dispatch.
 // ---------------------------------------------------------------------------
-QuantOut make_out(uint8_t* codes, float* scales, int64_t n, int bits, int mode) {
+__host__ __device__ inline int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ inline int64_t up64(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+
+// Output pointers and padding ranges of n quantised elements.
+__host__ __device__ inline QuantOut make_out(uint8_t* codes, float* scales, int64_t n, int bits,
+                                             int mode) {
   QuantOut o;
   const int cb = mode == GC_TERN ? 2 : bits;
-  const int64_t mag = round_up((n * cb + 7) / 8, 16);
+  const int64_t mag = up64((n * cb + 7) / 8, 16);
   o.codes = codes;
   o.scales = scales;
   o.signs = mode == GC_QSGD ? codes + mag : nullptr;
   // bytes written by the lanes cover ceil(n/4)*4 elements
-  const int64_t n4 = round_up(n, 4);
-  o.zero_begin = std::min<int64_t>((n4 * cb + 7) / 8, mag);
-  if (cb == 1) o.zero_begin = std::min<int64_t>(ceil_div(n4, 8), mag);
+  const int64_t n4 = up64(n, 4);
+  o.zero_begin = min64((n4 * cb + 7) / 8, mag);
+  if (cb == 1) o.zero_begin = min64((n4 + 7) / 8, mag);
   o.zero_end = mag;
-  const int64_t smag = round_up((n + 7) / 8, 16);
-  o.szero_begin = std::min<int64_t>(ceil_div(n4, 8), smag);
+  const int64_t smag = up64((n + 7) / 8, 16);
+  o.szero_begin = min64((n4 + 7) / 8, smag);
   o.szero_end = smag;
   o.scatter_n = 0;
   o.status = nullptr;
   return o;
+}
+
+// QSGD of the kept values of every bucket of a plan: one warp per chunk of
+// 128 values of one bucket; bucket b's codes and scales start at the offsets
+// the hist pass laid out, its residuals go to err[start_b + idx].
+template <int BITS, int LPG>
+__global__ void __launch_bounds__(kQThreads) quant_buckets_kernel(
+    float* __restrict__ err, const int32_t* __restrict__ idx, BucketWs w,
+    uint8_t* __restrict__ codes_out, float* __restrict__ scales_out, int stochastic,
+    uint64_t seed, uint64_t step) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_id = ((int64_t)blockIdx.x * kQThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kQThreads) >> 5;
+  for (int64_t ch = warp_id; ch < w.nchunk; ch += nwarps) {
+    const int b = w.chunk_bucket[ch];
+    const BucketDesc d = w.desc[b];
+    const int64_t lc = ch - d.chunk_first;
+    QuantOut o = make_out(codes_out + w.qoff[2 * b], scales_out + w.qoff[2 * b + 1], d.k, BITS,
+                          GC_QSGD);
+    o.scatter_n = d.n;
+    o.status = w.status;
+    if (lc == 0 && lane == 0) zero_padding_bytes(o);
+    quant_fused_chunk<GC_QSGD, BITS, LPG, IO_SCATTER>(
+        w.vals + d.idx_off, err + d.start, idx + d.idx_off, d.k, o, stochastic,
+        seed + (uint64_t)b, step, lc * kChunkVals, lane);
+  }
 }
 
 int grid_for(gc_ctx* ctx, int64_t work_items, int per_block, int per_sm) {
@@ -648,6 +690,36 @@ gc_status launch_dequant(gc_ctx* ctx, const uint8_t* codes, const float* scales,
     }
   }
 #undef GC_DQ
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+gc_status launch_quant_buckets(gc_ctx* ctx, float* err, const int32_t* idx_out, int bits,
+                               int64_t group, int rounding, uint64_t seed, uint64_t step,
+                               uint8_t* codes_out, float* scales_out) {
+  const BucketWs& w = ctx->bk;
+  if (w.nchunk == 0) return GC_OK;
+  const int grid = grid_for(ctx, w.nchunk, kQThreads / 32, 8);
+  const int st = rounding == GC_STOCHASTIC;
+  cudaStream_t s = ctx->stream;
+  LaunchScope L(ctx, GC_PHASE_BK_QUANT);
+#define GC_BQ(B, LPG) quant_buckets_kernel<B, LPG><<<grid, kQThreads, 0, s>>>(err, idx_out, w, codes_out, scales_out, st, seed, step)
+#define GC_BQ_G(B)                 \
+  switch (group) {                 \
+    case 4: GC_BQ(B, 1); break;    \
+    case 8: GC_BQ(B, 2); break;    \
+    case 16: GC_BQ(B, 4); break;   \
+    case 32: GC_BQ(B, 8); break;   \
+    case 64: GC_BQ(B, 16); break;  \
+    default: GC_BQ(B, 32); break;  \
+  }
+  switch (bits) {
+    case 1: GC_BQ_G(1); break;
+    case 2: GC_BQ_G(2); break;
+    case 4: GC_BQ_G(4); break;
+    default: GC_BQ_G(8); break;
+  }
+#undef GC_BQ_G
+#undef GC_BQ
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
 

@@ -20,7 +20,7 @@ NEAREST_EVEN, STOCHASTIC = 0, 1
 MODES = {"minmax": MINMAX, "qsgd": QSGD, "tern": TERN}
 ROUNDINGS = {"nearest_even": NEAREST_EVEN, "stochastic": STOCHASTIC}
 
-PHASE_COUNT = 13
+PHASE_COUNT = 18
 
 OK = 0
 ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE = -1, -2, -3, -4
@@ -55,6 +55,12 @@ SIGNATURES = [
                                 _vp, _vp, _vp]),
     ("gc_powersgd_step", _int, [_vp, _vp, _vp, _i64, _i64, _int, _vp, _vp]),
     ("gc_ef_topk_noalloc", _int, [_vp, _vp, _i64, _i64, _vp, _vp, _vp]),
+    ("gc_ctx_set_buckets", _int, [_vp, _int, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
+    ("gc_bucket_offsets", _int, [_int, ctypes.POINTER(_i64), _int, _i64, ctypes.POINTER(_i64),
+                                 ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
+    ("gc_ef_topk_buckets", _int, [_vp, _vp, _vp, _vp, _vp]),
+    ("gc_ef_topk_quant_buckets", _int, [_vp, _vp, _vp, _int, _i64, _int, _u64, _u64, _vp, _vp,
+                                        _vp]),
 ]
 
 # largest n of gc_ef_topk_noalloc (GC_NOALLOC_MAX_N in include/gc.h)
@@ -163,6 +169,18 @@ class Context:
     def launch_count(self):
         return int(lib.gc_ctx_launch_count(self.handle))
 
+    def set_buckets(self, bucket_n, bucket_k):
+        """Bucket plan: consecutive slices of bucket_n[b] elements keeping
+        bucket_k[b] entries each (synchronous)."""
+        nb = len(bucket_n)
+        if len(bucket_k) != nb:
+            raise ValueError("bucket_n and bucket_k differ in length")
+        an = (_i64 * max(nb, 1))(*[int(v) for v in bucket_n])
+        ak = (_i64 * max(nb, 1))(*[int(v) for v in bucket_k])
+        _check(lib.gc_ctx_set_buckets(self.handle, nb, an, ak), "gc_ctx_set_buckets")
+        self.bucket_n = [int(v) for v in bucket_n]
+        self.bucket_k = [int(v) for v in bucket_k]
+
     def close(self):
         if getattr(self, "handle", None) is not None and self.handle.value:
             st = lib.gc_ctx_destroy(self.handle)
@@ -231,3 +249,32 @@ def ef_topk_noalloc(grad, err, k, idx_out, val_out, stream=None, n=None):
     n = grad.numel() if n is None else n
     _check(lib.gc_ef_topk_noalloc(_ptr(grad), _ptr(err), n, k, _ptr(idx_out), _ptr(val_out),
                                   handle), "gc_ef_topk_noalloc")
+
+
+def bucket_offsets(bucket_k, bits=None, group=None):
+    """gc_bucket_offsets: (idx_off, codes_off, scales_off), each a list of
+    nb + 1 starts (the last is the total); codes_off / scales_off are None
+    when bits / group are not given."""
+    nb = len(bucket_k)
+    ak = (_i64 * max(nb, 1))(*[int(v) for v in bucket_k])
+    oi = (_i64 * (nb + 1))()
+    oc = (_i64 * (nb + 1))() if bits is not None else None
+    os_ = (_i64 * (nb + 1))() if group is not None else None
+    _check(lib.gc_bucket_offsets(nb, ak, 0 if bits is None else bits,
+                                 0 if group is None else group, oi, oc, os_),
+           "gc_bucket_offsets")
+    return (list(oi), list(oc) if oc is not None else None,
+            list(os_) if os_ is not None else None)
+
+
+def ef_topk_buckets(ctx, grad, err, idx_out, val_out):
+    _check(lib.gc_ef_topk_buckets(ctx.handle, _ptr(grad), _ptr(err), _ptr(idx_out),
+                                  _ptr(val_out)), "gc_ef_topk_buckets")
+
+
+def ef_topk_quant_buckets(ctx, grad, err, bits, group, rounding, seed, step, idx_out,
+                          codes_out, scales_out):
+    _check(lib.gc_ef_topk_quant_buckets(ctx.handle, _ptr(grad), _ptr(err), bits, group,
+                                        _rounding(rounding), seed, step, _ptr(idx_out),
+                                        _ptr(codes_out), _ptr(scales_out)),
+           "gc_ef_topk_quant_buckets")

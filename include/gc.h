@@ -142,7 +142,12 @@ typedef enum gc_phase {
   GC_PHASE_PSGD_MTP = 10,    /* PowerSGD pass 2: Q' = M^T P_hat */
   GC_PHASE_PSGD_RESID = 11,  /* PowerSGD pass 3: E' = M - P_hat Q'^T */
   GC_PHASE_REFINE = 12,      /* Top-K pass 3: exact threshold, tile offsets */
-  GC_PHASE_COUNT = 13
+  GC_PHASE_BK_HIST = 13,     /* bucketed: c = g + e, first-level histograms */
+  GC_PHASE_BK_COLLECT = 14,  /* bucketed: per-segment lists of entries >= B */
+  GC_PHASE_BK_REFINE = 15,   /* bucketed: exact thresholds, segment offsets */
+  GC_PHASE_BK_WRITE = 16,    /* bucketed: ordered compaction */
+  GC_PHASE_BK_QUANT = 17,    /* bucketed: QSGD of the kept values */
+  GC_PHASE_COUNT = 18
 } gc_phase;
 
 /* Name of a phase ("ef_hist", ...); "?" when out of range. */
@@ -276,6 +281,75 @@ GC_API gc_status gc_ef_topk_quant(gc_ctx* ctx, const float* grad, float* err,
 GC_API gc_status gc_powersgd_step(gc_ctx* ctx, const float* grad, float* err,
                            int64_t m, int64_t n, int r, float* P_out,
                            float* Q_inout);
+
+/*
+ * Bucketed calls.
+ * A data-parallel step compresses a flat gradient bucket by bucket ("4、梯度
+ * 累积与梯度压缩" 4.3: a compression hook on the gradient buckets;
+ * "gradient-compression-quantization-sparsification" 3.2: compression
+ * happens before the data leaves GPU memory).  A bucket plan fixes the
+ * buckets once; each step then runs every bucket in one launch per pass
+ * (a few launches per step, whatever the number of buckets), so the
+ * passes stream the whole gradient at full memory bandwidth instead of
+ * one bucket at a time.
+ *
+ * Buckets are consecutive slices of one flat fp32 array: bucket b holds
+ * elements [start_b, start_b + bucket_n[b]) with start_b = sum of the
+ * earlier sizes, and keeps bucket_k[b] entries.  Per bucket the result is
+ * bit-identical to the single-bucket call on the slice (gc_ef_topk, or
+ * gc_ef_topk_quant with seed + b); indices are bucket-local.
+ */
+
+/*
+ * Sets the context's bucket plan: nb (1 .. 65536) buckets of bucket_n[b]
+ * elements (1 .. 2^31 - 2^16; a multiple of 4 for every bucket but the last,
+ * so that every bucket starts on a 16-byte boundary, else
+ * GC_ERR_ALIGNMENT) keeping bucket_k[b] (0 .. bucket_n[b]) entries each.
+ * bucket_n and bucket_k are HOST arrays, read during the call.  Reserves
+ * device scratch of about 8.1 bytes per element plus 40 KB per bucket
+ * (replacing any earlier plan) and uploads the plan; synchronises the
+ * context's stream first, so it must not be called while work is in flight
+ * or during stream capture.  GC_ERR_NO_MEMORY when the reservation fails.
+ */
+GC_API gc_status gc_ctx_set_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n,
+                                    const int64_t* bucket_k);
+
+/*
+ * Host-only layout of the bucketed outputs (no device work, no context).
+ * For b = 0 .. nb, writes the start of bucket b's outputs (entry nb = the
+ * total size):
+ *   idx_off[b]:    int32 / fp32 slots, sum of bucket_k rounded up to 4;
+ *   codes_off[b]:  bytes, sum of gc_codes_bytes(bucket_k, bits, GC_QSGD);
+ *   scales_off[b]: floats, sum of gc_scales_floats(bucket_k, group, GC_QSGD)
+ *                  rounded up to 4.
+ * Each output array may be NULL (not written); codes_off / scales_off need
+ * valid bits / group.  Every offset is a multiple of 16 bytes.
+ */
+GC_API gc_status gc_bucket_offsets(int nb, const int64_t* bucket_k, int bits, int64_t group,
+                                   int64_t* idx_off, int64_t* codes_off, int64_t* scales_off);
+
+/*
+ * gc_ef_topk on every bucket of the plan.
+ * grad, err: fp32[total] (err may be NULL: select from grad, no residual);
+ * idx_out: int32[idx_off[nb]], val_out: fp32[idx_off[nb]]; bucket b's
+ * entries start at idx_off[b] (slots between buckets are not written).
+ * GC_ERR_WORKSPACE when the context has no plan.
+ */
+GC_API gc_status gc_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err,
+                                    int32_t* idx_out, float* val_out);
+
+/*
+ * gc_ef_topk_quant on every bucket of the plan: bucket b is compressed as
+ * gc_ef_topk_quant(slice_b, bucket_k[b], bits, group, rounding, seed + b,
+ * step) with its indices at idx_out + idx_off[b], its codes at codes_out +
+ * codes_off[b] and its scales at scales_out + scales_off[b]
+ * (gc_bucket_offsets).  group must be a power of two in 4 .. 128
+ * (GC_ERR_UNSUPPORTED otherwise); err must not be NULL.
+ */
+GC_API gc_status gc_ef_topk_quant_buckets(gc_ctx* ctx, const float* grad, float* err,
+                                          int bits, int64_t group, int rounding,
+                                          uint64_t seed, uint64_t step, int32_t* idx_out,
+                                          uint8_t* codes_out, float* scales_out);
 
 /*
  * Largest n accepted by gc_ef_topk_noalloc: its scratch is a fixed device

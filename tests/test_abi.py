@@ -87,3 +87,39 @@ def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
     mod = importlib.util.module_from_spec(spec)
     with pytest.raises(ImportError):
         spec.loader.exec_module(mod)
+
+
+def test_bucket_offsets_agree_with_the_oracle_sizes(gc):
+    """gc_bucket_offsets is the running sum of the per-bucket output sizes
+    (indices rounded up to 4 slots, codes as gc_codes_bytes, scales rounded
+    up to 4 floats)."""
+    import oracle
+    ks = [0, 1, 5, 63, 64, 65, 1000, 12345, 65536]
+    for bits in (1, 2, 4, 8):
+        for group in (4, 64, 128):
+            oi, oc, os_ = gc.bucket_offsets(ks, bits, group)
+            assert len(oi) == len(oc) == len(os_) == len(ks) + 1
+            assert oi[0] == oc[0] == os_[0] == 0
+            for b, k in enumerate(ks):
+                assert oi[b + 1] - oi[b] == -(-k // 4) * 4
+                assert oc[b + 1] - oc[b] == oracle.codes_bytes(k, bits, "qsgd")
+                assert os_[b + 1] - os_[b] == -(-oracle.scales_floats(k, group, "qsgd") // 4) * 4
+                assert oc[b] % 16 == 0 and (4 * oi[b]) % 16 == 0 and (4 * os_[b]) % 16 == 0
+    oi, oc, os_ = gc.bucket_offsets(ks)
+    assert oc is None and os_ is None and oi[-1] == sum(-(-k // 4) * 4 for k in ks)
+
+
+def test_bucket_calls_validate_on_the_host(gc):
+    L = gc.lib
+    n = (ctypes.c_int64 * 2)(8, 8)
+    k = (ctypes.c_int64 * 2)(1, 1)
+    assert L.gc_ctx_set_buckets(None, 2, n, k) == gc.ERR_INVALID_ARG
+    assert L.gc_ef_topk_buckets(None, None, None, None, None) == gc.ERR_INVALID_ARG
+    assert L.gc_ef_topk_quant_buckets(None, None, None, 8, 64, 0, 0, 0, None, None, None) == \
+        gc.ERR_INVALID_ARG
+    out = (ctypes.c_int64 * 3)()
+    assert L.gc_bucket_offsets(0, k, 8, 64, out, None, None) == gc.ERR_INVALID_ARG
+    assert L.gc_bucket_offsets(2, None, 8, 64, out, None, None) == gc.ERR_INVALID_ARG
+    assert L.gc_bucket_offsets(2, k, 3, 64, out, out, None) == gc.ERR_UNSUPPORTED
+    bad = (ctypes.c_int64 * 2)(1, -1)
+    assert L.gc_bucket_offsets(2, bad, 8, 64, out, None, None) == gc.ERR_INVALID_ARG
