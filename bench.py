@@ -60,6 +60,9 @@ def parse_args():
                    help="time eager launches instead of CUDA-graph replay")
     p.add_argument("--path", choices=["buckets", "per-bucket"], default="buckets",
                    help="one bucketed call per step, or one call per bucket")
+    p.add_argument("--elems", type=int, default=inputs.FLAT_ELEMS,
+                   help="gradient elements (default: the 134,217,728-element workload; smaller "
+                        "values cut the same 25 MiB buckets from a shorter gradient, for profiling)")
     return p.parse_args()
 
 
@@ -150,9 +153,10 @@ class BucketWorkload:
 
     BITS, GROUP, SEED = 8, 64, 1000
 
-    def __init__(self, torch, gc, dev, ratio_per_mille, streams, distinct, seed, path):
+    def __init__(self, torch, gc, dev, ratio_per_mille, streams, distinct, seed, path,
+                 n=inputs.FLAT_ELEMS):
         self.torch, self.gc, self.dev, self.path = torch, gc, dev, path
-        self.n = inputs.FLAT_ELEMS
+        self.n = n
         self.bounds = inputs.bucket_bounds(self.n)
         self.ks = [inputs.ratio_k(length, ratio_per_mille, 1000) for _, length in self.bounds]
         self.grads = inputs.correlated_steps_device(self.n, distinct, dev, seed=seed)
@@ -293,15 +297,20 @@ def cpu_baseline(budget_s=12.0, seed=7):
 
 
 def config(args, wl=None):
-    cfg = {"workload": "flat fp32 gradient 134,217,728 elements in 25 MiB buckets "
-                       "(20 x 6,553,600 + 3,145,728), Student-t nu=3 x 1e-3, correlated steps; "
-                       "per bucket EF + Top-K %g%% + 8-bit QSGD (groups of 64, stochastic) on the "
-                       "kept values" % (args.ratio / 10),
-           "total_elems": inputs.FLAT_ELEMS, "bucket_elems": inputs.BUCKET_ELEMS,
-           "buckets": len(inputs.bucket_bounds()), "topk_per_mille": args.ratio,
+    n = args.elems
+    bounds = inputs.bucket_bounds(n)
+    sizes = "%d x %s" % (len([1 for _, l in bounds if l == inputs.BUCKET_ELEMS]), "6,553,600")
+    if bounds[-1][1] != inputs.BUCKET_ELEMS:
+        sizes += " + {:,}".format(bounds[-1][1])
+    cfg = {"workload": "flat fp32 gradient {:,} elements in 25 MiB buckets ({}), Student-t "
+                       "nu=3 x 1e-3, correlated steps; per bucket EF + Top-K {:g}% + 8-bit QSGD "
+                       "(groups of 64, stochastic) on the kept values".format(n, sizes,
+                                                                             args.ratio / 10),
+           "total_elems": n, "bucket_elems": inputs.BUCKET_ELEMS,
+           "buckets": len(bounds), "topk_per_mille": args.ratio,
            "quant": "qsgd 8-bit g64 stochastic",
-           "l2": "inputs larger than L2: each step reads a 512 MiB gradient and the 512 MiB "
-                 "residual, no flush", "parallelism": "dp%d" % args.gpus}
+           "l2": "inputs larger than L2: each step reads a {0} MiB gradient and the {0} MiB "
+                 "residual, no flush".format(4 * n >> 20), "parallelism": "dp%d" % args.gpus}
     cfg["path"] = args.path
     if wl is not None:
         cfg["streams"] = len(wl.streams)
@@ -360,7 +369,7 @@ def main():
     from gradient_compression_ef_gb300 import gc
 
     wl = BucketWorkload(torch, gc, dev, args.ratio, args.streams, args.distinct, seed=42 + rank,
-                        path=args.path)
+                        path=args.path, n=args.elems)
     torch.cuda.synchronize(dev)
     for t in range(args.warmup):
         wl.launch_step(t)

@@ -74,8 +74,28 @@ __device__ void layout_quant_outputs(const BucketWs& w, int bits, int64_t group,
   }
 }
 
+// Appends the entries flagged in ge[0..3] of this lane (elements base + 4 *
+// lane + j of one 128-element row, j = 0..3) to a segment list in index
+// order; every lane of the warp calls it.  Returns the new list length.
+__device__ __forceinline__ uint32_t append4(uint2* out, uint32_t cnt, const bool ge[4],
+                                            const float c[4], uint32_t base, int lane,
+                                            uint32_t lt) {
+  const uint32_t b0 = __ballot_sync(0xffffffffu, ge[0]);
+  const uint32_t b1 = __ballot_sync(0xffffffffu, ge[1]);
+  const uint32_t b2 = __ballot_sync(0xffffffffu, ge[2]);
+  const uint32_t b3 = __ballot_sync(0xffffffffu, ge[3]);
+  // index order is (lane, j): the lanes below come first
+  uint32_t pos = cnt + __popc(b0 & lt) + __popc(b1 & lt) + __popc(b2 & lt) + __popc(b3 & lt);
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (ge[j]) out[pos++] = make_uint2(__float_as_uint(c[j]), base + 4 * lane + j);
+  return cnt + __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
+}
+
 // ---------------------------------------------------------------------------
-// hist: c = g + e and the first-level histogram.
+// hist: c = g + e, the first-level histogram and, when the bucket has a
+// threshold guess, the per-segment lists of the entries whose key is at or
+// above the guess.
 // ---------------------------------------------------------------------------
 template <bool EF>
 __global__ void __launch_bounds__(kBkHistThreads, 1) bk_hist_kernel(
@@ -84,69 +104,98 @@ __global__ void __launch_bounds__(kBkHistThreads, 1) bk_hist_kernel(
   constexpr int NW = kBkHistThreads / 32;
   __shared__ uint32_t h[kHistBins];
   __shared__ uint32_t warp_sums[NW + 1];
-  __shared__ uint32_t digit, above;
+  __shared__ uint32_t digit, above, listed;
   __shared__ int last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t lt = lanemask_lt();
   if (blockIdx.x == 0 && warp == 0 && qbits > 0) layout_quant_outputs(w, qbits, qgroup, lane);
   for (int i = threadIdx.x; i < kHistBins; i += kBkHistThreads) h[i] = 0u;
+  if (threadIdx.x == 0) listed = 0u;
   __syncthreads();
-  int64_t s, s_hi;
-  seg_range(w.nseg, gridDim.x, blockIdx.x, &s, &s_hi);
+  int64_t s64, s_hi64;
+  seg_range(w.nseg, gridDim.x, blockIdx.x, &s64, &s_hi64);
+  // segment numbers fit 32 bits (the plan checks it)
+  int32_t s = (int32_t)s64;
+  const int32_t s_hi = (int32_t)s_hi64;
   while (s < s_hi) {
     const int b = w.seg_bucket[s];
     const BucketDesc* dp = w.desc + b;
     const int32_t seg_first = dp->seg_first, bn = dp->n, bk = dp->k;
-    const int64_t sub_hi = std::min<int64_t>(s_hi, (int64_t)seg_first + dp->nseg);
+    const int32_t sub_hi = min(s_hi, seg_first + dp->nseg);
     const bool select = bk > 0;
+    const uint32_t g1 = select ? __ldcg(&w.sel[b].guess1) : 0u;
+    const bool emit = g1 != 0u;
+    const uint32_t kg = g1 - 1u;
     const float* g = grad + dp->start;
     float* e = EF ? err + dp->start : nullptr;
-    for (int64_t seg = s + warp; seg < sub_hi; seg += NW) {
-      // bucket-local offsets fit 32 bits (n <= 2^31 - 1)
-      const int32_t l0 = (int32_t)(seg - seg_first) << kSegShift;
+    for (int32_t seg = s + warp; seg < sub_hi; seg += NW) {
+      // bucket-local offsets fit 32 bits (n <= 2^31 - 2^16)
+      const int32_t l0 = (seg - seg_first) << kSegShift;
       const int32_t l1 = min(l0 + kSegElems, bn);
+      uint32_t cnt = 0u;
       for (int32_t p = l0; p < l1; p += kPass) {
         const float4* gp = reinterpret_cast<const float4*>(g + p) + lane;
         float4* ep = reinterpret_cast<float4*>(e + p) + lane;
         const int32_t rem = l1 - p - 4 * lane;  // elements from this lane's first one on
-        float4 gv[4], ev[4];
+        float4 cv[4], ev[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           if (128 * u + 3 < rem) {
-            gv[u] = __ldcs(gp + 32 * u);
+            cv[u] = __ldcs(gp + 32 * u);
             if (EF) ev[u] = ep[32 * u];
           }
         }
+        // c = g + e over the four rows (into cv), written back, histogram
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           if (128 * u + 3 < rem) {
-            float4 c = gv[u];
             if (EF) {
-              c.x = __fadd_rn(c.x, ev[u].x);
-              c.y = __fadd_rn(c.y, ev[u].y);
-              c.z = __fadd_rn(c.z, ev[u].z);
-              c.w = __fadd_rn(c.w, ev[u].w);
-              ep[32 * u] = c;
+              cv[u].x = __fadd_rn(cv[u].x, ev[u].x);
+              cv[u].y = __fadd_rn(cv[u].y, ev[u].y);
+              cv[u].z = __fadd_rn(cv[u].z, ev[u].z);
+              cv[u].w = __fadd_rn(cv[u].w, ev[u].w);
+              ep[32 * u] = cv[u];
             }
             if (select) {
-              atomicAdd(&h[mag_key(c.x) >> kHistShift], 1u);
-              atomicAdd(&h[mag_key(c.y) >> kHistShift], 1u);
-              atomicAdd(&h[mag_key(c.z) >> kHistShift], 1u);
-              atomicAdd(&h[mag_key(c.w) >> kHistShift], 1u);
+              atomicAdd(&h[mag_key(cv[u].x) >> kHistShift], 1u);
+              atomicAdd(&h[mag_key(cv[u].y) >> kHistShift], 1u);
+              atomicAdd(&h[mag_key(cv[u].z) >> kHistShift], 1u);
+              atomicAdd(&h[mag_key(cv[u].w) >> kHistShift], 1u);
             }
           } else {
             const int32_t i = p + 128 * u + 4 * lane;
+            float c[4];
+#pragma unroll
             for (int j = 0; j < 4; ++j) {
+              c[j] = 0.0f;
               if (i + j < l1) {
-                float c = g[i + j];
+                c[j] = g[i + j];
                 if (EF) {
-                  c = __fadd_rn(c, e[i + j]);
-                  e[i + j] = c;
+                  c[j] = __fadd_rn(c[j], e[i + j]);
+                  e[i + j] = c[j];
                 }
-                if (select) atomicAdd(&h[mag_key(c) >> kHistShift], 1u);
+                if (select) atomicAdd(&h[mag_key(c[j]) >> kHistShift], 1u);
               }
             }
+            cv[u] = make_float4(c[0], c[1], c[2], c[3]);
           }
         }
+        if (emit) {
+          uint2* out = w.list + ((int64_t)seg << kSegShift);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int32_t i = p + 128 * u + 4 * lane;
+            const float c[4] = {cv[u].x, cv[u].y, cv[u].z, cv[u].w};
+            bool ge[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ge[j] = i + j < l1 && mag_key(c[j]) >= kg;
+            cnt = append4(out, cnt, ge, c, (uint32_t)(p + 128 * u), lane, lt);
+          }
+        }
+      }
+      if (emit && lane == 0) {
+        w.seg_cnt[seg] = cnt;
+        atomicAdd(&listed, cnt);
       }
     }
     __syncthreads();
@@ -155,6 +204,10 @@ __global__ void __launch_bounds__(kBkHistThreads, 1) bk_hist_kernel(
       for (int i = threadIdx.x; i < kHistBins; i += kBkHistThreads) {
         if (h[i]) atomicAdd(&hb[i], h[i]);
         h[i] = 0u;
+      }
+      if (threadIdx.x == 0 && emit) {
+        atomicAdd(&w.sel[b].list_total, listed);
+        listed = 0u;
       }
       __threadfence();
       __syncthreads();
@@ -176,12 +229,19 @@ __global__ void __launch_bounds__(kBkHistThreads, 1) bk_hist_kernel(
         find_digit<kBkHistThreads>(h, kHistBins, (uint32_t)bk, warp_sums, &digit, &above);
         if (threadIdx.x == 0) {
           BucketSel* q = &w.sel[b];
-          q->B = digit;
+          const uint32_t B = digit;
+          q->B = B;
           q->above1 = above;
           q->need1 = (uint32_t)bk - above;
-          q->cntB = digit != kNone ? h[digit] : 0u;
+          q->cntB = B != kNone ? h[B] : 0u;
           q->ticket_hist = 0u;
-          if (digit == kNone) atomicOr(w.status, kStatusTopkSelect);
+          // at least k entries with key >= guess: the threshold T is not
+          // below the guess, so the lists hold every entry with key >= T
+          const uint32_t L = emit ? __ldcg(&q->list_total) : 0u;
+          q->list_len = L;
+          q->list_total = 0u;
+          q->list_ok = (emit && L >= (uint32_t)bk) ? 1u : 0u;
+          if (B == kNone) atomicOr(w.status, kStatusTopkSelect);
         }
         __syncthreads();
         for (int i = threadIdx.x; i < kHistBins; i += kBkHistThreads) h[i] = 0u;
@@ -192,8 +252,42 @@ __global__ void __launch_bounds__(kBkHistThreads, 1) bk_hist_kernel(
   }
 }
 
+// List walkers take four consecutive segments per warp and load up to 128
+// entries of each per round (16 loads per lane in flight).
+constexpr int kWalkSegs = 4;
+constexpr int kWalkRows = 4;
+
+// List lengths of segments s0 .. s0+3 (0 past nq), to every lane.
+__device__ __forceinline__ void walk_counts(const BucketWs& w, int64_t s0, int nq, int lane,
+                                            uint32_t cnt[kWalkSegs]) {
+  const uint32_t c = lane < nq ? w.seg_cnt[s0 + lane] : 0u;
+#pragma unroll
+  for (int r = 0; r < kWalkSegs; ++r) cnt[r] = __shfl_sync(0xffffffffu, c, r);
+}
+
+// Entries j0 + 32 u + lane (u < 4) of the four lists; (0, 0) past the end.
+__device__ __forceinline__ void walk_load(const BucketWs& w, int64_t s0, uint32_t j0,
+                                          const uint32_t cnt[kWalkSegs], int lane,
+                                          uint2 e[kWalkSegs][kWalkRows]) {
+#pragma unroll
+  for (int r = 0; r < kWalkSegs; ++r) {
+#pragma unroll
+    for (int u = 0; u < kWalkRows; ++u) {
+      const uint32_t j = j0 + 32 * u + lane;
+      e[r][u] = j < cnt[r] ? w.list[((s0 + r) << kSegShift) + j] : make_uint2(0u, 0u);
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t max4(const uint32_t v[4]) {
+  return max(max(v[0], v[1]), max(v[2], v[3]));
+}
+
 // ---------------------------------------------------------------------------
-// collect: per-segment ordered lists of the entries with bin >= B.
+// collect: with usable lists, per segment the count above B, the histogram
+// of bits 18..8 of the bin-B entries, and the lists compacted in place to
+// the entries of bin >= B; otherwise c is read again and the lists of
+// bin >= B are built.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kBkThreads) bk_collect_kernel(const float* __restrict__ csrc,
                                                                 BucketWs w) {
@@ -217,63 +311,90 @@ __global__ void __launch_bounds__(kBkThreads) bk_collect_kernel(const float* __r
       continue;
     }
     const uint32_t B = __ldcg(&w.sel[b].B);
-    const float* c = csrc + d.start;
-    for (int64_t seg = s + warp; seg < sub_hi; seg += NW) {
-      const int64_t l0 = (seg - d.seg_first) << kSegShift;
-      const int64_t l1 = std::min<int64_t>(l0 + kSegElems, d.n);
-      uint2* out = w.list + (seg << kSegShift);
-      uint32_t cnt = 0u, above_l = 0u;
-      for (int64_t p = l0; p < l1; p += kPass) {
-        float v[16];
-        bool valid[16];
+    if (__ldcg(&w.sel[b].list_ok)) {
+      for (int64_t s0 = s + kWalkSegs * warp; s0 < sub_hi; s0 += kWalkSegs * NW) {
+        const int nq = (int)std::min<int64_t>(kWalkSegs, sub_hi - s0);
+        uint32_t cnt[kWalkSegs], abv[kWalkSegs], wpos[kWalkSegs];
+        walk_counts(w, s0, nq, lane, cnt);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int64_t i = p + 128 * u + 4 * lane;
-          if (i + 3 < l1) {
-            const float4 x = *reinterpret_cast<const float4*>(c + i);
-            v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
-            valid[4 * u] = valid[4 * u + 1] = valid[4 * u + 2] = valid[4 * u + 3] = true;
-          } else {
+        for (int r = 0; r < kWalkSegs; ++r) abv[r] = wpos[r] = 0u;
+        const uint32_t mx = max4(cnt);
+        for (uint32_t j0 = 0; j0 < mx; j0 += 32 * kWalkRows) {
+          uint2 e[kWalkSegs][kWalkRows];
+          walk_load(w, s0, j0, cnt, lane, e);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              valid[4 * u + j] = i + j < l1;
-              v[4 * u + j] = valid[4 * u + j] ? c[i + j] : 0.0f;
+          for (int r = 0; r < kWalkSegs; ++r) {
+            uint2* list = w.list + ((s0 + r) << kSegShift);
+#pragma unroll
+            for (int u = 0; u < kWalkRows; ++u) {
+              if (j0 + 32 * u >= cnt[r]) break;  // warp-uniform
+              const bool valid = j0 + 32 * u + lane < cnt[r];
+              const uint32_t key = e[r][u].x & 0x7fffffffu;
+              const uint32_t bin = key >> kHistShift;
+              const bool keep = valid && bin >= B;
+              abv[r] += (valid && bin > B) ? 1u : 0u;
+              if (valid && bin == B) atomicAdd(&mid[(key >> kLowBits) & (kMidBins - 1)], 1u);
+              // in place: the write position never passes the read position
+              const uint32_t kb = __ballot_sync(0xffffffffu, keep);
+              if (keep) list[wpos[r] + __popc(kb & lt)] = e[r][u];
+              wpos[r] += __popc(kb);
             }
           }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          bool ge[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t key = mag_key(v[4 * u + j]);
-            const uint32_t bin = key >> kHistShift;
-            ge[j] = valid[4 * u + j] && bin >= B;
-            above_l += (valid[4 * u + j] && bin > B) ? 1u : 0u;
-            if (valid[4 * u + j] && bin == B)
-              atomicAdd(&mid[(key >> kLowBits) & (kMidBins - 1)], 1u);
+        for (int r = 0; r < kWalkSegs; ++r) {
+          const uint32_t a = __reduce_add_sync(0xffffffffu, abv[r]);
+          if (lane == 0 && r < nq) {
+            w.seg_above[s0 + r] = a;
+            w.seg_cnt[s0 + r] = wpos[r];
           }
-          // index order is (u, lane, j): lanes below come first
-          const uint32_t b0 = __ballot_sync(0xffffffffu, ge[0]);
-          const uint32_t b1 = __ballot_sync(0xffffffffu, ge[1]);
-          const uint32_t b2 = __ballot_sync(0xffffffffu, ge[2]);
-          const uint32_t b3 = __ballot_sync(0xffffffffu, ge[3]);
-          uint32_t pos = cnt + __popc(b0 & lt) + __popc(b1 & lt) + __popc(b2 & lt) +
-                         __popc(b3 & lt);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (ge[j]) {
-              out[pos++] = make_uint2(__float_as_uint(v[4 * u + j]),
-                                      (uint32_t)(p + 128 * u + 4 * lane + j));
-            }
-          }
-          cnt += __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
         }
       }
-      above_l = __reduce_add_sync(0xffffffffu, above_l);
-      if (lane == 0) {
-        w.seg_cnt[seg] = cnt;
-        w.seg_above[seg] = above_l;
+    } else {
+      const float* c = csrc + d.start;
+      for (int64_t seg = s + warp; seg < sub_hi; seg += NW) {
+        const int64_t l0 = (seg - d.seg_first) << kSegShift;
+        const int64_t l1 = std::min<int64_t>(l0 + kSegElems, d.n);
+        uint2* out = w.list + (seg << kSegShift);
+        uint32_t cnt = 0u, above_l = 0u;
+        for (int64_t p = l0; p < l1; p += kPass) {
+          float v[16];
+          bool valid[16];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int64_t i = p + 128 * u + 4 * lane;
+            if (i + 3 < l1) {
+              const float4 x = *reinterpret_cast<const float4*>(c + i);
+              v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
+              valid[4 * u] = valid[4 * u + 1] = valid[4 * u + 2] = valid[4 * u + 3] = true;
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                valid[4 * u + j] = i + j < l1;
+                v[4 * u + j] = valid[4 * u + j] ? c[i + j] : 0.0f;
+              }
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            bool ge[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t key = mag_key(v[4 * u + j]);
+              const uint32_t bin = key >> kHistShift;
+              ge[j] = valid[4 * u + j] && bin >= B;
+              above_l += (valid[4 * u + j] && bin > B) ? 1u : 0u;
+              if (valid[4 * u + j] && bin == B)
+                atomicAdd(&mid[(key >> kLowBits) & (kMidBins - 1)], 1u);
+            }
+            cnt = append4(out, cnt, ge, &v[4 * u], (uint32_t)(p + 128 * u), lane, lt);
+          }
+        }
+        above_l = __reduce_add_sync(0xffffffffu, above_l);
+        if (lane == 0) {
+          w.seg_cnt[seg] = cnt;
+          w.seg_above[seg] = above_l;
+        }
       }
     }
     __syncthreads();
@@ -307,7 +428,10 @@ __global__ void __launch_bounds__(kBkThreads) bk_collect_kernel(const float* __r
         q->need2 = need1 - above;
         q->ticket_coll = 0u;
         if (digit == kNone) atomicOr(w.status, kStatusTopkSelect);
-        if (total != __ldcg(&q->cntB)) atomicOr(w.status, kStatusTopkCount);
+        // with lists that start inside bin B only part of the bin is seen
+        const uint32_t cntB = __ldcg(&q->cntB);
+        if (__ldcg(&q->list_ok) ? total > cntB : total != cntB)
+          atomicOr(w.status, kStatusTopkCount);
       }
       __syncthreads();
       for (int i = threadIdx.x; i < kMidBins; i += kBkThreads) mid[i] = 0u;
@@ -318,14 +442,16 @@ __global__ void __launch_bounds__(kBkThreads) bk_collect_kernel(const float* __r
 }
 
 // ---------------------------------------------------------------------------
-// refine: counts above (B, B2); the last block of a bucket finds T and the
-// segments' output offsets.
+// refine: counts above (B, B2); the last block of a bucket finds T, the
+// segments' output offsets and the next call's threshold guess.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void classify_at_T(const BucketWs& w, uint32_t key, uint32_t seg,
                                               uint32_t T) {
   if (key > T) atomicAdd(&w.seg_kept[seg], 1u);
   else if (key == T) atomicAdd(&w.seg_tie[seg], 1u);
 }
+
+constexpr int kScanPer = 8;  // segments per thread in the offset scan
 
 __global__ void __launch_bounds__(kBkThreads) bk_refine_kernel(BucketWs w) {
   constexpr int NW = kBkThreads / 32;
@@ -349,26 +475,45 @@ __global__ void __launch_bounds__(kBkThreads) bk_refine_kernel(BucketWs w) {
     BucketSel* q = &w.sel[b];
     const uint32_t B = __ldcg(&q->B), B2 = __ldcg(&q->B2);
     uint2* stash = w.stash + (int64_t)b * kBkStash;
-    for (int64_t seg = s + warp; seg < sub_hi; seg += NW) {
-      const uint32_t cnt = w.seg_cnt[seg];
-      const uint2* in = w.list + (seg << kSegShift);
-      uint32_t strict = 0u;
-      for (uint32_t j = lane; j < cnt; j += 32) {
-        const uint32_t key = in[j].x & 0x7fffffffu;
-        if ((key >> kHistShift) != B) continue;
-        const uint32_t m = (key >> kLowBits) & (kMidBins - 1);
-        if (m > B2) {
-          ++strict;
-        } else if (m == B2) {
-          atomicAdd(&low[key & (kLowBins - 1)], 1u);
-          const uint32_t slot = atomicAdd(&q->stash_count, 1u);
-          if (slot < (uint32_t)kBkStash) stash[slot] = make_uint2(key, (uint32_t)seg);
+    for (int64_t s0 = s + kWalkSegs * warp; s0 < sub_hi; s0 += kWalkSegs * NW) {
+      const int nq = (int)std::min<int64_t>(kWalkSegs, sub_hi - s0);
+      uint32_t cnt[kWalkSegs], strict[kWalkSegs];
+      walk_counts(w, s0, nq, lane, cnt);
+      const uint32_t aq = lane < nq ? w.seg_above[s0 + lane] : 0u;
+#pragma unroll
+      for (int r = 0; r < kWalkSegs; ++r) strict[r] = 0u;
+      const uint32_t mx = max4(cnt);
+      for (uint32_t j0 = 0; j0 < mx; j0 += 32 * kWalkRows) {
+        uint2 e[kWalkSegs][kWalkRows];
+        walk_load(w, s0, j0, cnt, lane, e);
+#pragma unroll
+        for (int r = 0; r < kWalkSegs; ++r) {
+#pragma unroll
+          for (int u = 0; u < kWalkRows; ++u) {
+            const uint32_t key = e[r][u].x & 0x7fffffffu;
+            if (j0 + 32 * u + lane < cnt[r] && (key >> kHistShift) == B) {
+              const uint32_t m = (key >> kLowBits) & (kMidBins - 1);
+              if (m > B2) {
+                ++strict[r];
+              } else if (m == B2) {
+                atomicAdd(&low[key & (kLowBins - 1)], 1u);
+                const uint32_t slot = atomicAdd(&q->stash_count, 1u);
+                if (slot < (uint32_t)kBkStash) stash[slot] = make_uint2(key, (uint32_t)(s0 + r));
+              }
+            }
+          }
         }
       }
-      strict = __reduce_add_sync(0xffffffffu, strict);
-      if (lane == 0) {
-        w.seg_kept[seg] = w.seg_above[seg] + strict;
-        w.seg_tie[seg] = 0u;
+      // lane r < nq writes segment r (entries above B come from collect)
+      uint32_t mine = 0u;
+#pragma unroll
+      for (int r = 0; r < kWalkSegs; ++r) {
+        const uint32_t t = __reduce_add_sync(0xffffffffu, strict[r]);
+        mine = lane == r ? t : mine;
+      }
+      if (lane < nq) {
+        w.seg_kept[s0 + lane] = aq + mine;
+        w.seg_tie[s0 + lane] = 0u;
       }
     }
     __syncthreads();
@@ -406,32 +551,52 @@ __global__ void __launch_bounds__(kBkThreads) bk_refine_kernel(BucketWs w) {
           classify_at_T(w, e.x, e.y, T);
         }
       } else {  // more (B, B2) entries than the stash holds: rescan the lists
+        const uint32_t prefix = (B << (kHistShift - kLowBits)) | B2;
         for (int64_t seg = d.seg_first + warp; seg < (int64_t)d.seg_first + d.nseg; seg += NW) {
           const uint32_t cnt = w.seg_cnt[seg];
           const uint2* in = w.list + (seg << kSegShift);
           for (uint32_t j = lane; j < cnt; j += 32) {
             const uint32_t key = in[j].x & 0x7fffffffu;
-            if ((key >> kLowBits) == ((B << (kHistShift - kLowBits)) | B2))
-              classify_at_T(w, key, (uint32_t)seg, T);
+            if ((key >> kLowBits) == prefix) classify_at_T(w, key, (uint32_t)seg, T);
           }
         }
       }
       __syncthreads();
-      // output offsets: the ties at T go to the segments in index order
+      // output offsets: the ties at T go to the segments in index order;
+      // each thread takes kScanPer consecutive segments per round
       uint32_t tie_carry = 0u, out_carry = 0u;
-      for (int64_t base = 0; base < d.nseg; base += kBkThreads) {
-        const int64_t sg = d.seg_first + base + threadIdx.x;
-        const bool valid = base + threadIdx.x < d.nseg;
-        const uint32_t tie = valid ? __ldcg(&w.seg_tie[sg]) : 0u;
-        const uint32_t kept = valid ? __ldcg(&w.seg_kept[sg]) : 0u;
+      for (int64_t base = 0; base < d.nseg; base += (int64_t)kBkThreads * kScanPer) {
+        const int64_t first = base + (int64_t)threadIdx.x * kScanPer;
+        uint32_t tie[kScanPer], kept[kScanPer];
+#pragma unroll
+        for (int r = 0; r < kScanPer; ++r) {
+          const bool valid = first + r < d.nseg;
+          tie[r] = valid ? __ldcg(&w.seg_tie[d.seg_first + first + r]) : 0u;
+          kept[r] = valid ? __ldcg(&w.seg_kept[d.seg_first + first + r]) : 0u;
+        }
+        uint32_t tsum = 0u;
+#pragma unroll
+        for (int r = 0; r < kScanPer; ++r) tsum += tie[r];
         uint32_t tt, ot;
-        const uint32_t tie_ex = tie_carry + block_scan<kBkThreads>(tie, warp_sums, &tt);
-        const uint32_t rem = needT > tie_ex ? needT - tie_ex : 0u;
-        const uint32_t kk = kept + (tie < rem ? tie : rem);
-        const uint32_t out_ex = out_carry + block_scan<kBkThreads>(kk, warp_sums, &ot);
-        if (valid) {
-          w.seg_out[sg] = out_ex;
-          w.seg_tieb[sg] = tie_ex;
+        const uint32_t tie0 = tie_carry + block_scan<kBkThreads>(tsum, warp_sums, &tt);
+        uint32_t run = tie0, ksum = 0u;
+#pragma unroll
+        for (int r = 0; r < kScanPer; ++r) {
+          const uint32_t rem = needT > run ? needT - run : 0u;
+          kept[r] += tie[r] < rem ? tie[r] : rem;  // kept + ties kept here
+          run += tie[r];
+          ksum += kept[r];
+        }
+        const uint32_t out0 = out_carry + block_scan<kBkThreads>(ksum, warp_sums, &ot);
+        uint32_t ro = out0, rt = tie0;
+#pragma unroll
+        for (int r = 0; r < kScanPer; ++r) {
+          if (first + r < d.nseg) {
+            w.seg_out[d.seg_first + first + r] = ro;
+            w.seg_tieb[d.seg_first + first + r] = rt;
+          }
+          ro += kept[r];
+          rt += tie[r];
         }
         tie_carry += tt;
         out_carry += ot;
@@ -443,6 +608,17 @@ __global__ void __launch_bounds__(kBkThreads) bk_refine_kernel(BucketWs w) {
         q->ticket_ref = 0u;
         if (B == kNone || B2 == kNone || B3 == kNone) atomicOr(w.status, kStatusTopkSelect);
         if (out_carry != (uint32_t)d.k) atomicOr(w.status, kStatusTopkOverflow);
+        // next call's guess: a margin below T, widened after a miss and
+        // tuned so that the lists hold about 1.5 to 3 times k entries
+        uint32_t m = __ldcg(&q->margin);
+        const uint32_t L = __ldcg(&q->list_len), k = (uint32_t)d.k;
+        if (m == 0u) m = kMarginInit;
+        else if (!__ldcg(&q->list_ok)) m = m <= kMarginMax / 2 ? 2u * m : kMarginMax;
+        else if (L > 3u * k) m -= m / 4u;
+        else if (L < k + k / 2u) m += m / 4u + 1u;
+        m = min(max(m, kMarginMin), kMarginMax);
+        q->margin = m;
+        q->guess1 = (T > m ? T - m : 0u) + 1u;
       }
       __syncthreads();
       for (int i = threadIdx.x; i < kLowBins; i += kBkThreads) low[i] = 0u;
@@ -453,7 +629,8 @@ __global__ void __launch_bounds__(kBkThreads) bk_refine_kernel(BucketWs w) {
 }
 
 // ---------------------------------------------------------------------------
-// write: ordered (index, value) of the kept entries.
+// write: ordered (index, value) of the kept entries, four segments per warp
+// (lane r < 4 holds segment r's bookkeeping).
 // ---------------------------------------------------------------------------
 template <bool ZERO>
 __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict__ err,
@@ -464,40 +641,72 @@ __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict_
   const uint32_t lt = lanemask_lt();
   const int64_t gwarp = ((int64_t)blockIdx.x * kBkThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kBkThreads) >> 5;
-  for (int64_t seg = gwarp; seg < w.nseg; seg += nwarps) {
-    const int b = w.seg_bucket[seg];
-    const BucketDesc* dp = w.desc + b;
-    const uint32_t bk = (uint32_t)dp->k, bn = (uint32_t)dp->n;
-    if (bk == 0u) continue;
-    const int64_t idx_off = dp->idx_off;
-    float* eb = err + dp->start;
-    const uint32_t T = w.sel[b].T, needT = w.sel[b].needT;
-    const uint32_t out = w.seg_out[seg], tieb = w.seg_tieb[seg], cnt = w.seg_cnt[seg];
-    const uint32_t rem = needT > tieb ? needT - tieb : 0u;
-    const uint2* in = w.list + (seg << kSegShift);
-    int32_t* io = idx_out + idx_off;
-    float* vo = val_out + idx_off;
-    uint32_t run = 0u, tie_run = 0u;
-    for (uint32_t j0 = 0; j0 < cnt; j0 += 32) {
-      const bool valid = j0 + lane < cnt;
-      const uint2 e = valid ? in[j0 + lane] : make_uint2(0u, 0u);
-      const uint32_t key = e.x & 0x7fffffffu;
-      const bool gt = valid && key > T, eq = valid && key == T;
-      const uint32_t eqb = __ballot_sync(0xffffffffu, eq);
-      const bool keep = gt || (eq && tie_run + __popc(eqb & lt) < rem);
-      const uint32_t kb = __ballot_sync(0xffffffffu, keep);
-      if (keep) {
-        const uint32_t pos = out + run + __popc(kb & lt);
-        if (pos < bk && e.y < bn) {
-          io[pos] = (int32_t)e.y;
-          vo[pos] = __uint_as_float(e.x);
-          if (ZERO) eb[e.y] = 0.0f;
-        } else {
-          atomicOr(w.status, kStatusTopkOverflow);
+  for (int64_t s0 = kWalkSegs * gwarp; s0 < w.nseg; s0 += kWalkSegs * nwarps) {
+    const int nq = (int)std::min<int64_t>(kWalkSegs, w.nseg - s0);
+    // lane r < nq: segment s0 + r
+    uint32_t cnt_l = 0u, out_l = 0u, rem_l = 0u, T_l = 0u, k_l = 0u, n_l = 0u;
+    int64_t off_l = 0, start_l = 0;
+    if (lane < nq) {
+      const int64_t sg = s0 + lane;
+      const int b = w.seg_bucket[sg];
+      const BucketDesc* dp = w.desc + b;
+      k_l = (uint32_t)dp->k;
+      n_l = (uint32_t)dp->n;
+      off_l = dp->idx_off;
+      start_l = dp->start;
+      if (k_l != 0u) {
+        cnt_l = w.seg_cnt[sg];
+        out_l = w.seg_out[sg];
+        const uint32_t tieb = w.seg_tieb[sg];
+        const uint32_t needT = w.sel[b].needT;
+        T_l = w.sel[b].T;
+        rem_l = needT > tieb ? needT - tieb : 0u;
+      }
+    }
+    uint32_t cnt[kWalkSegs], out[kWalkSegs], rem[kWalkSegs], T[kWalkSegs], bk[kWalkSegs],
+        bn[kWalkSegs];
+    int64_t off[kWalkSegs], start[kWalkSegs];
+#pragma unroll
+    for (int r = 0; r < kWalkSegs; ++r) {
+      cnt[r] = __shfl_sync(0xffffffffu, cnt_l, r);
+      out[r] = __shfl_sync(0xffffffffu, out_l, r);
+      rem[r] = __shfl_sync(0xffffffffu, rem_l, r);
+      T[r] = __shfl_sync(0xffffffffu, T_l, r);
+      bk[r] = __shfl_sync(0xffffffffu, k_l, r);
+      bn[r] = __shfl_sync(0xffffffffu, n_l, r);
+      off[r] = __shfl_sync(0xffffffffu, off_l, r);
+      start[r] = __shfl_sync(0xffffffffu, start_l, r);
+    }
+    const uint32_t mx = max4(cnt);
+    uint32_t run[kWalkSegs] = {0u, 0u, 0u, 0u}, tie_run[kWalkSegs] = {0u, 0u, 0u, 0u};
+    for (uint32_t j0 = 0; j0 < mx; j0 += 32 * kWalkRows) {
+      uint2 e[kWalkSegs][kWalkRows];
+      walk_load(w, s0, j0, cnt, lane, e);
+#pragma unroll
+      for (int r = 0; r < kWalkSegs; ++r) {
+#pragma unroll
+        for (int u = 0; u < kWalkRows; ++u) {
+          if (j0 + 32 * u >= cnt[r]) break;  // warp-uniform
+          const bool valid = j0 + 32 * u + lane < cnt[r];
+          const uint32_t key = e[r][u].x & 0x7fffffffu;
+          const bool gt = valid && key > T[r], eq = valid && key == T[r];
+          const uint32_t eqb = __ballot_sync(0xffffffffu, eq);
+          const bool keep = gt || (eq && tie_run[r] + __popc(eqb & lt) < rem[r]);
+          const uint32_t kb = __ballot_sync(0xffffffffu, keep);
+          if (keep) {
+            const uint32_t pos = out[r] + run[r] + __popc(kb & lt);
+            if (pos < bk[r] && e[r][u].y < bn[r]) {
+              idx_out[off[r] + pos] = (int32_t)e[r][u].y;
+              val_out[off[r] + pos] = __uint_as_float(e[r][u].x);
+              if (ZERO) err[start[r] + e[r][u].y] = 0.0f;
+            } else {
+              atomicOr(w.status, kStatusTopkOverflow);
+            }
+          }
+          run[r] += __popc(kb);
+          tie_run[r] += __popc(eqb);
         }
       }
-      run += __popc(kb);
-      tie_run += __popc(eqb);
     }
   }
 }

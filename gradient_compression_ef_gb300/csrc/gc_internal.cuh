@@ -78,6 +78,9 @@ constexpr int kSegShift = 11;                    // segments of 2048 elements, o
 constexpr int kSegElems = 1 << kSegShift;
 constexpr int kChunkVals = 128;                  // kept values per quantisation warp
 constexpr int kBkStash = 2048;                   // third-level entries set aside per bucket
+constexpr uint32_t kMarginInit = 1u << 19;       // first guess: one first-level bin below T
+constexpr uint32_t kMarginMin = 1u << 12;
+constexpr uint32_t kMarginMax = 1u << 23;        // one octave
 constexpr int kMaxBuckets = 65536;
 constexpr int64_t kMaxBucketElems = INT32_MAX - 65535;  // 32-bit offsets inside a bucket
 
@@ -104,7 +107,15 @@ struct BucketSel {
   uint32_t T, needT;                 // exact threshold key, ties kept at T
   uint32_t ticket_hist, ticket_coll, ticket_ref;
   uint32_t stash_count;
-  uint32_t pad[4];
+  // threshold reuse across calls: the hist pass lists the entries with
+  // key >= guess1 - 1 (guess1 == 0: no guess); when at least k are listed
+  // the lists hold every entry the selection needs
+  uint32_t guess1;
+  uint32_t list_ok;     // this call's lists are usable
+  uint32_t list_total;  // entries listed so far by the hist pass (reset by its last block)
+  uint32_t list_len;    // entries listed by this call's hist pass
+  uint32_t margin;      // key distance of the next guess below T
+  uint32_t pad[3];
 };
 
 // Device scratch of a bucket plan (pointers into one allocation).  hist,

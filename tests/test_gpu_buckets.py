@@ -344,3 +344,39 @@ def test_full_size_workload(env):
         assert_bits_equal(scales_h[os_[b]:os_[b] + o_scales.size], o_scales, "oracle scales %d" % b)
         assert_bits_equal(err_h[sl], o_err, "oracle err %d" % b)
     ctx.close()
+
+
+@pytest.mark.parametrize("scales", [(1.0, 1.0, 0.25, 4.0, 1.0), (1.0, 0.97, 1.03, 16.0, 0.01)])
+def test_threshold_guess_paths(env, scales):
+    """The hist pass lists entries from a little below the previous call's
+    threshold bin.  Calls whose magnitudes drop (the guess is too high: the
+    collect pass reads c again) or rise (long lists) give exactly the
+    oracle's result, as do steady calls that use the lists alone."""
+    torch, gc, ctx = env
+    ns, ks = [65_536, 131_072, 40_000], [655, 1_310, 400]
+    ctx.set_buckets(ns, ks)
+    oi, oc, os_ = gc.bucket_offsets(ks, 8, 64)
+    st = starts(ns)
+    r = np.random.default_rng(17)
+    base = inputs.student_t(r, sum(ns))
+    e = np.zeros(sum(ns), np.float32)
+    ed = dev_f32(torch, e)
+    idx = torch.empty(oi[-1], dtype=torch.int32, device="cuda")
+    codes = torch.empty(oc[-1], dtype=torch.uint8, device="cuda")
+    scl = torch.empty(os_[-1], dtype=torch.float32, device="cuda")
+    for step, f in enumerate(scales):
+        g = (base * np.float32(f)).astype(np.float32)
+        gc.ef_topk_quant_buckets(ctx, dev_f32(torch, g), ed, 8, 64, "stochastic", 3, step, idx,
+                                 codes, scl)
+        ctx.check()
+        e_new, i_h, c_h, s_h = host(ed), host(idx), host(codes), host(scl)
+        for b, (n, k) in enumerate(zip(ns, ks)):
+            sl = slice(st[b], st[b + 1])
+            o_idx, o_codes, o_scales, o_err = oracle.ef_topk_quant(
+                g[sl], e[sl], k, 8, 64, "stochastic", 3 + b, step)
+            w = "step %d bucket %d" % (step, b)
+            assert_bits_equal(i_h[oi[b]:oi[b] + k], o_idx, w + " idx")
+            assert_bits_equal(c_h[oc[b]:oc[b + 1]], o_codes, w + " codes")
+            assert_bits_equal(s_h[os_[b]:os_[b] + o_scales.size], o_scales, w + " scales")
+            assert_bits_equal(e_new[sl], o_err, w + " err")
+        e = e_new
