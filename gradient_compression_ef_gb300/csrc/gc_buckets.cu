@@ -42,6 +42,12 @@ constexpr uint32_t kNone = 0xffffffffu;
 
 __device__ __forceinline__ int64_t dev_round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 
+// Asks the L2 to fetch [p, p + bytes) (bytes a multiple of 16, p 16-byte
+// aligned); a hint with no completion to wait for.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Warp 0 of block 0: byte / float offsets of every bucket's QSGD codes and
 // scales for (bits, group), the running sums of gc_codes_bytes(k_b) and of
 // gc_scales_floats(k_b) rounded up to 4 floats.
@@ -134,6 +140,20 @@ __global__ void __launch_bounds__(kBkHistThreads, 1) bk_hist_kernel(
       const int32_t l1 = min(l0 + kSegElems, bn);
       uint32_t cnt = 0u;
       for (int32_t p = l0; p < l1; p += kPass) {
+        if (lane == 0) {
+          // the next pass of this warp (this segment's, else its next segment's
+          // first) is fetched into L2 while this one is processed
+          int32_t np = p + kPass, nl1 = l1;
+          if (np >= l1) {
+            np = seg + NW < sub_hi ? (seg + NW - seg_first) << kSegShift : bn;
+            nl1 = min(np + kSegElems, bn);
+          }
+          const uint32_t bytes = (uint32_t)(4 * min(kPass, nl1 - np)) & ~15u;
+          if (np < bn && bytes) {
+            prefetch_l2(g + np, bytes);
+            if (EF) prefetch_l2(e + np, bytes);
+          }
+        }
         const float4* gp = reinterpret_cast<const float4*>(g + p) + lane;
         float4* ep = reinterpret_cast<float4*>(e + p) + lane;
         const int32_t rem = l1 - p - 4 * lane;  // elements from this lane's first one on
@@ -663,20 +683,9 @@ __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict_
         rem_l = needT > tieb ? needT - tieb : 0u;
       }
     }
-    uint32_t cnt[kWalkSegs], out[kWalkSegs], rem[kWalkSegs], T[kWalkSegs], bk[kWalkSegs],
-        bn[kWalkSegs];
-    int64_t off[kWalkSegs], start[kWalkSegs];
+    uint32_t cnt[kWalkSegs];
 #pragma unroll
-    for (int r = 0; r < kWalkSegs; ++r) {
-      cnt[r] = __shfl_sync(0xffffffffu, cnt_l, r);
-      out[r] = __shfl_sync(0xffffffffu, out_l, r);
-      rem[r] = __shfl_sync(0xffffffffu, rem_l, r);
-      T[r] = __shfl_sync(0xffffffffu, T_l, r);
-      bk[r] = __shfl_sync(0xffffffffu, k_l, r);
-      bn[r] = __shfl_sync(0xffffffffu, n_l, r);
-      off[r] = __shfl_sync(0xffffffffu, off_l, r);
-      start[r] = __shfl_sync(0xffffffffu, start_l, r);
-    }
+    for (int r = 0; r < kWalkSegs; ++r) cnt[r] = __shfl_sync(0xffffffffu, cnt_l, r);
     const uint32_t mx = max4(cnt);
     uint32_t run[kWalkSegs] = {0u, 0u, 0u, 0u}, tie_run[kWalkSegs] = {0u, 0u, 0u, 0u};
     for (uint32_t j0 = 0; j0 < mx; j0 += 32 * kWalkRows) {
@@ -684,21 +693,29 @@ __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict_
       walk_load(w, s0, j0, cnt, lane, e);
 #pragma unroll
       for (int r = 0; r < kWalkSegs; ++r) {
+        if (j0 >= cnt[r]) continue;  // warp-uniform
+        const uint32_t T = __shfl_sync(0xffffffffu, T_l, r);
+        const uint32_t rem = __shfl_sync(0xffffffffu, rem_l, r);
+        const uint32_t out = __shfl_sync(0xffffffffu, out_l, r);
+        const uint32_t bk = __shfl_sync(0xffffffffu, k_l, r);
+        const uint32_t bn = __shfl_sync(0xffffffffu, n_l, r);
+        const int64_t off = __shfl_sync(0xffffffffu, off_l, r);
+        const int64_t start = __shfl_sync(0xffffffffu, start_l, r);
 #pragma unroll
         for (int u = 0; u < kWalkRows; ++u) {
           if (j0 + 32 * u >= cnt[r]) break;  // warp-uniform
           const bool valid = j0 + 32 * u + lane < cnt[r];
           const uint32_t key = e[r][u].x & 0x7fffffffu;
-          const bool gt = valid && key > T[r], eq = valid && key == T[r];
+          const bool gt = valid && key > T, eq = valid && key == T;
           const uint32_t eqb = __ballot_sync(0xffffffffu, eq);
-          const bool keep = gt || (eq && tie_run[r] + __popc(eqb & lt) < rem[r]);
+          const bool keep = gt || (eq && tie_run[r] + __popc(eqb & lt) < rem);
           const uint32_t kb = __ballot_sync(0xffffffffu, keep);
           if (keep) {
-            const uint32_t pos = out[r] + run[r] + __popc(kb & lt);
-            if (pos < bk[r] && e[r][u].y < bn[r]) {
-              idx_out[off[r] + pos] = (int32_t)e[r][u].y;
-              val_out[off[r] + pos] = __uint_as_float(e[r][u].x);
-              if (ZERO) err[start[r] + e[r][u].y] = 0.0f;
+            const uint32_t pos = out + run[r] + __popc(kb & lt);
+            if (pos < bk && e[r][u].y < bn) {
+              idx_out[off + pos] = (int32_t)e[r][u].y;
+              val_out[off + pos] = __uint_as_float(e[r][u].x);
+              if (ZERO) err[start + e[r][u].y] = 0.0f;
             } else {
               atomicOr(w.status, kStatusTopkOverflow);
             }
