@@ -35,18 +35,11 @@
 namespace gc {
 namespace {
 
-constexpr int kBkHistThreads = 1024;
 constexpr int kBkThreads = 256;
 constexpr int kPass = 512;            // elements a warp loads at once (4 x float4 per lane)
 constexpr uint32_t kNone = 0xffffffffu;
 
 __device__ __forceinline__ int64_t dev_round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
-
-// Asks the L2 to fetch [p, p + bytes) (bytes a multiple of 16, p 16-byte
-// aligned); a hint with no completion to wait for.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 
 // Warp 0 of block 0: byte / float offsets of every bucket's QSGD codes and
 // scales for (bits, group), the running sums of gc_codes_bytes(k_b) and of
@@ -102,21 +95,59 @@ __device__ __forceinline__ uint32_t append4(uint2* out, uint32_t cnt, const bool
 // hist: c = g + e, the first-level histogram and, when the bucket has a
 // threshold guess, the per-segment lists of the entries whose key is at or
 // above the guess.
+//
+// Each warp streams its segments in passes of 256 elements.  g and e of
+// the next kStages - 1 passes are in flight as asynchronous copies into the
+// warp's shared-memory stages (cp.async, completed with cp.async.wait_group)
+// while the current pass is processed, so the memory system always has
+// about 10 KB per warp outstanding without holding registers for it.  Each
+// lane copies and later reads back the same 16-byte chunks of a pass.
 // ---------------------------------------------------------------------------
+constexpr int kH1Threads = 512;
+constexpr int kH1Warps = kH1Threads / 32;
+constexpr int kH1Rows = 2;                 // rows of 128 elements per pass
+constexpr int kH1Pass = 128 * kH1Rows;     // elements per pass
+constexpr int kStages = 6;
+
+struct HistSmem {
+  float4 sg[kH1Warps][kStages][32 * kH1Rows];  // g of a pass
+  float4 se[kH1Warps][kStages][32 * kH1Rows];  // e of a pass
+  uint32_t h[kHistBins];
+  uint32_t warp_sums[kH1Warps + 1];
+  uint32_t digit, above, listed;
+  int last;
+};
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Position of a warp in its work: segment seg (bucket-local element offset
+// l0 .. l1) and pass p.
+struct PassCursor {
+  int32_t seg, l1, p;
+  __device__ __forceinline__ bool valid(int32_t sub_hi) const { return seg < sub_hi; }
+};
+
 template <bool EF>
-__global__ void __launch_bounds__(kBkHistThreads, 1) bk_hist_kernel(
+__global__ void __launch_bounds__(kH1Threads, 1) bk_hist_kernel(
     const float* __restrict__ grad, float* __restrict__ err, BucketWs w, int qbits,
     int64_t qgroup) {
-  constexpr int NW = kBkHistThreads / 32;
-  __shared__ uint32_t h[kHistBins];
-  __shared__ uint32_t warp_sums[NW + 1];
-  __shared__ uint32_t digit, above, listed;
-  __shared__ int last;
+  extern __shared__ __align__(16) unsigned char hist_smem_raw[];
+  HistSmem& sm = *reinterpret_cast<HistSmem*>(hist_smem_raw);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t lt = lanemask_lt();
   if (blockIdx.x == 0 && warp == 0 && qbits > 0) layout_quant_outputs(w, qbits, qgroup, lane);
-  for (int i = threadIdx.x; i < kHistBins; i += kBkHistThreads) h[i] = 0u;
-  if (threadIdx.x == 0) listed = 0u;
+  for (int i = threadIdx.x; i < kHistBins; i += kH1Threads) sm.h[i] = 0u;
+  if (threadIdx.x == 0) sm.listed = 0u;
   __syncthreads();
   int64_t s64, s_hi64;
   seg_range(w.nseg, gridDim.x, blockIdx.x, &s64, &s_hi64);
@@ -134,126 +165,148 @@ __global__ void __launch_bounds__(kBkHistThreads, 1) bk_hist_kernel(
     const uint32_t kg = g1 - 1u;
     const float* g = grad + dp->start;
     float* e = EF ? err + dp->start : nullptr;
-    for (int32_t seg = s + warp; seg < sub_hi; seg += NW) {
-      // bucket-local offsets fit 32 bits (n <= 2^31 - 2^16)
-      const int32_t l0 = (seg - seg_first) << kSegShift;
-      const int32_t l1 = min(l0 + kSegElems, bn);
-      uint32_t cnt = 0u;
-      for (int32_t p = l0; p < l1; p += kPass) {
-        if (lane == 0) {
-          // the next pass of this warp (this segment's, else its next segment's
-          // first) is fetched into L2 while this one is processed
-          int32_t np = p + kPass, nl1 = l1;
-          if (np >= l1) {
-            np = seg + NW < sub_hi ? (seg + NW - seg_first) << kSegShift : bn;
-            nl1 = min(np + kSegElems, bn);
-          }
-          const uint32_t bytes = (uint32_t)(4 * min(kPass, nl1 - np)) & ~15u;
-          if (np < bn && bytes) {
-            prefetch_l2(g + np, bytes);
-            if (EF) prefetch_l2(e + np, bytes);
-          }
-        }
-        const float4* gp = reinterpret_cast<const float4*>(g + p) + lane;
-        float4* ep = reinterpret_cast<float4*>(e + p) + lane;
-        const int32_t rem = l1 - p - 4 * lane;  // elements from this lane's first one on
-        float4 cv[4], ev[4];
+
+    // this warp's passes: segments s + warp, s + warp + NW, ...; 4 passes each
+    auto first = [&](int32_t seg) {
+      PassCursor c;
+      c.seg = seg;
+      const int32_t l0 = (seg - seg_first) << kSegShift;  // bucket-local (n <= 2^31 - 2^16)
+      c.p = l0;
+      c.l1 = min(l0 + kSegElems, bn);
+      return c;
+    };
+    auto advance = [&](PassCursor& c) {
+      c.p += kH1Pass;
+      if (c.p >= c.l1) c = first(c.seg + kH1Warps);
+    };
+    // copies of the whole 16-byte chunks of a pass; the ragged end of the
+    // last bucket is read directly when the pass is processed
+    auto issue = [&](const PassCursor& c, int st) {
+      if (c.valid(sub_hi)) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (128 * u + 3 < rem) {
-            cv[u] = __ldcs(gp + 32 * u);
-            if (EF) ev[u] = ep[32 * u];
-          }
-        }
-        // c = g + e over the four rows (into cv), written back, histogram
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (128 * u + 3 < rem) {
-            if (EF) {
-              cv[u].x = __fadd_rn(cv[u].x, ev[u].x);
-              cv[u].y = __fadd_rn(cv[u].y, ev[u].y);
-              cv[u].z = __fadd_rn(cv[u].z, ev[u].z);
-              cv[u].w = __fadd_rn(cv[u].w, ev[u].w);
-              ep[32 * u] = cv[u];
-            }
-            if (select) {
-              atomicAdd(&h[mag_key(cv[u].x) >> kHistShift], 1u);
-              atomicAdd(&h[mag_key(cv[u].y) >> kHistShift], 1u);
-              atomicAdd(&h[mag_key(cv[u].z) >> kHistShift], 1u);
-              atomicAdd(&h[mag_key(cv[u].w) >> kHistShift], 1u);
-            }
-          } else {
-            const int32_t i = p + 128 * u + 4 * lane;
-            float c[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              c[j] = 0.0f;
-              if (i + j < l1) {
-                c[j] = g[i + j];
-                if (EF) {
-                  c[j] = __fadd_rn(c[j], e[i + j]);
-                  e[i + j] = c[j];
-                }
-                if (select) atomicAdd(&h[mag_key(c[j]) >> kHistShift], 1u);
-              }
-            }
-            cv[u] = make_float4(c[0], c[1], c[2], c[3]);
-          }
-        }
-        if (emit) {
-          uint2* out = w.list + ((int64_t)seg << kSegShift);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int32_t i = p + 128 * u + 4 * lane;
-            const float c[4] = {cv[u].x, cv[u].y, cv[u].z, cv[u].w};
-            bool ge[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) ge[j] = i + j < l1 && mag_key(c[j]) >= kg;
-            cnt = append4(out, cnt, ge, c, (uint32_t)(p + 128 * u), lane, lt);
+        for (int u = 0; u < kH1Rows; ++u) {
+          const int32_t i = c.p + 128 * u + 4 * lane;
+          if (i + 3 < c.l1) {
+            cp_async16(&sm.sg[warp][st][32 * u + lane], g + i);
+            if (EF) cp_async16(&sm.se[warp][st][32 * u + lane], e + i);
           }
         }
       }
-      if (emit && lane == 0) {
-        w.seg_cnt[seg] = cnt;
-        atomicAdd(&listed, cnt);
+      cp_async_commit();  // one group per pass (possibly empty)
+    };
+
+    PassCursor ic = first(s + warp), uc = ic;
+#pragma unroll
+    for (int k = 0; k < kStages - 1; ++k) {
+      issue(ic, k);
+      if (ic.valid(sub_hi)) advance(ic);
+    }
+    int st_use = 0, st_issue = kStages - 1;
+    uint32_t cnt = 0u;
+    while (uc.valid(sub_hi)) {
+      cp_async_wait<kStages - 2>();  // the oldest pass has landed
+      const int32_t p = uc.p, l1 = uc.l1;
+      float4 cv[kH1Rows];
+#pragma unroll
+      for (int u = 0; u < kH1Rows; ++u) {
+        const int32_t i = p + 128 * u + 4 * lane;
+        if (i + 3 < l1) {
+          cv[u] = sm.sg[warp][st_use][32 * u + lane];
+          if (EF) {
+            const float4 ev = sm.se[warp][st_use][32 * u + lane];
+            cv[u].x = __fadd_rn(cv[u].x, ev.x);
+            cv[u].y = __fadd_rn(cv[u].y, ev.y);
+            cv[u].z = __fadd_rn(cv[u].z, ev.z);
+            cv[u].w = __fadd_rn(cv[u].w, ev.w);
+            *reinterpret_cast<float4*>(e + i) = cv[u];
+          }
+          if (select) {
+            atomicAdd(&sm.h[mag_key(cv[u].x) >> kHistShift], 1u);
+            atomicAdd(&sm.h[mag_key(cv[u].y) >> kHistShift], 1u);
+            atomicAdd(&sm.h[mag_key(cv[u].z) >> kHistShift], 1u);
+            atomicAdd(&sm.h[mag_key(cv[u].w) >> kHistShift], 1u);
+          }
+        } else {
+          float c[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            c[j] = 0.0f;
+            if (i + j < l1) {
+              c[j] = g[i + j];
+              if (EF) {
+                c[j] = __fadd_rn(c[j], e[i + j]);
+                e[i + j] = c[j];
+              }
+              if (select) atomicAdd(&sm.h[mag_key(c[j]) >> kHistShift], 1u);
+            }
+          }
+          cv[u] = make_float4(c[0], c[1], c[2], c[3]);
+        }
+      }
+      // this stage is free again: start the pass kStages - 1 ahead
+      issue(ic, st_issue);
+      if (ic.valid(sub_hi)) advance(ic);
+      st_issue = st_issue + 1 == kStages ? 0 : st_issue + 1;
+      st_use = st_use + 1 == kStages ? 0 : st_use + 1;
+      if (emit) {
+        uint2* out = w.list + ((int64_t)uc.seg << kSegShift);
+#pragma unroll
+        for (int u = 0; u < kH1Rows; ++u) {
+          const int32_t i = p + 128 * u + 4 * lane;
+          const float c[4] = {cv[u].x, cv[u].y, cv[u].z, cv[u].w};
+          bool ge[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) ge[j] = i + j < l1 && mag_key(c[j]) >= kg;
+          cnt = append4(out, cnt, ge, c, (uint32_t)(p + 128 * u), lane, lt);
+        }
+      }
+      const int32_t seg_done = uc.seg;
+      advance(uc);
+      if (uc.seg != seg_done) {  // last pass of the segment
+        if (emit && lane == 0) {
+          w.seg_cnt[seg_done] = cnt;
+          atomicAdd(&sm.listed, cnt);
+        }
+        cnt = 0u;
       }
     }
+    cp_async_wait<0>();
     __syncthreads();
     if (select) {
       uint32_t* hb = w.hist + (int64_t)b * kHistBins;
-      for (int i = threadIdx.x; i < kHistBins; i += kBkHistThreads) {
-        if (h[i]) atomicAdd(&hb[i], h[i]);
-        h[i] = 0u;
+      for (int i = threadIdx.x; i < kHistBins; i += kH1Threads) {
+        if (sm.h[i]) atomicAdd(&hb[i], sm.h[i]);
+        sm.h[i] = 0u;
       }
       if (threadIdx.x == 0 && emit) {
-        atomicAdd(&w.sel[b].list_total, listed);
-        listed = 0u;
+        atomicAdd(&w.sel[b].list_total, sm.listed);
+        sm.listed = 0u;
       }
       __threadfence();
       __syncthreads();
       if (threadIdx.x == 0)
-        last = atomicAdd(&w.sel[b].ticket_hist, 1u) == (uint32_t)dp->blk_hist - 1u;
+        sm.last = atomicAdd(&w.sel[b].ticket_hist, 1u) == (uint32_t)dp->blk_hist - 1u;
       __syncthreads();
-      if (last) {
+      if (sm.last) {
         // every block of the bucket has added its counts: first-level bin
         __threadfence();
-        for (int i = threadIdx.x; i < kHistBins; i += kBkHistThreads) {
-          h[i] = __ldcg(&hb[i]);
+        for (int i = threadIdx.x; i < kHistBins; i += kH1Threads) {
+          sm.h[i] = __ldcg(&hb[i]);
           hb[i] = 0u;
         }
         if (threadIdx.x == 0) {
-          digit = kNone;
-          above = 0u;
+          sm.digit = kNone;
+          sm.above = 0u;
         }
         __syncthreads();
-        find_digit<kBkHistThreads>(h, kHistBins, (uint32_t)bk, warp_sums, &digit, &above);
+        find_digit<kH1Threads>(sm.h, kHistBins, (uint32_t)bk, sm.warp_sums, &sm.digit, &sm.above);
         if (threadIdx.x == 0) {
           BucketSel* q = &w.sel[b];
-          const uint32_t B = digit;
+          const uint32_t B = sm.digit;
           q->B = B;
-          q->above1 = above;
-          q->need1 = (uint32_t)bk - above;
-          q->cntB = B != kNone ? h[B] : 0u;
+          q->above1 = sm.above;
+          q->need1 = (uint32_t)bk - sm.above;
+          q->cntB = B != kNone ? sm.h[B] : 0u;
           q->ticket_hist = 0u;
           // at least k entries with key >= guess: the threshold T is not
           // below the guess, so the lists hold every entry with key >= T
@@ -264,7 +317,7 @@ __global__ void __launch_bounds__(kBkHistThreads, 1) bk_hist_kernel(
           if (B == kNone) atomicOr(w.status, kStatusTopkSelect);
         }
         __syncthreads();
-        for (int i = threadIdx.x; i < kHistBins; i += kBkHistThreads) h[i] = 0u;
+        for (int i = threadIdx.x; i < kHistBins; i += kH1Threads) sm.h[i] = 0u;
         __syncthreads();
       }
     }
@@ -272,20 +325,24 @@ __global__ void __launch_bounds__(kBkHistThreads, 1) bk_hist_kernel(
   }
 }
 
-// List walkers take four consecutive segments per warp and load up to 128
-// entries of each per round (16 loads per lane in flight).
-constexpr int kWalkSegs = 4;
-constexpr int kWalkRows = 4;
+// List walkers take eight consecutive segments per warp and load up to 64
+// entries of each per round (16 loads per lane in flight).  Lane r < 8
+// keeps segment r's counters; every lane gets the list lengths.
+constexpr int kWalkSegs = 8;
+constexpr int kWalkRows = 2;
 
-// List lengths of segments s0 .. s0+3 (0 past nq), to every lane.
-__device__ __forceinline__ void walk_counts(const BucketWs& w, int64_t s0, int nq, int lane,
-                                            uint32_t cnt[kWalkSegs]) {
-  const uint32_t c = lane < nq ? w.seg_cnt[s0 + lane] : 0u;
+// List length of segment s0 + lane for lanes < nq (0 elsewhere); all
+// lengths to every lane in cnt[]; returns the largest.
+__device__ __forceinline__ uint32_t walk_counts(const BucketWs& w, int64_t s0, int nq, int lane,
+                                                uint32_t* c_l, uint32_t cnt[kWalkSegs]) {
+  *c_l = lane < nq ? __ldcg(&w.seg_cnt[s0 + lane]) : 0u;
 #pragma unroll
-  for (int r = 0; r < kWalkSegs; ++r) cnt[r] = __shfl_sync(0xffffffffu, c, r);
+  for (int r = 0; r < kWalkSegs; ++r) cnt[r] = __shfl_sync(0xffffffffu, *c_l, r);
+  return __reduce_max_sync(0xffffffffu, *c_l);
 }
 
-// Entries j0 + 32 u + lane (u < 4) of the four lists; (0, 0) past the end.
+// Entries j0 + 32 u + lane (u < kWalkRows) of the lists of segments s0 ..
+// s0 + 7; (0, 0) past each list's end.
 __device__ __forceinline__ void walk_load(const BucketWs& w, int64_t s0, uint32_t j0,
                                           const uint32_t cnt[kWalkSegs], int lane,
                                           uint2 e[kWalkSegs][kWalkRows]) {
@@ -294,13 +351,9 @@ __device__ __forceinline__ void walk_load(const BucketWs& w, int64_t s0, uint32_
 #pragma unroll
     for (int u = 0; u < kWalkRows; ++u) {
       const uint32_t j = j0 + 32 * u + lane;
-      e[r][u] = j < cnt[r] ? w.list[((s0 + r) << kSegShift) + j] : make_uint2(0u, 0u);
+      e[r][u] = j < cnt[r] ? __ldcg(&w.list[((s0 + r) << kSegShift) + j]) : make_uint2(0u, 0u);
     }
   }
-}
-
-__device__ __forceinline__ uint32_t max4(const uint32_t v[4]) {
-  return max(max(v[0], v[1]), max(v[2], v[3]));
 }
 
 // ---------------------------------------------------------------------------
@@ -334,17 +387,17 @@ __global__ void __launch_bounds__(kBkThreads) bk_collect_kernel(const float* __r
     if (__ldcg(&w.sel[b].list_ok)) {
       for (int64_t s0 = s + kWalkSegs * warp; s0 < sub_hi; s0 += kWalkSegs * NW) {
         const int nq = (int)std::min<int64_t>(kWalkSegs, sub_hi - s0);
-        uint32_t cnt[kWalkSegs], abv[kWalkSegs], wpos[kWalkSegs];
-        walk_counts(w, s0, nq, lane, cnt);
-#pragma unroll
-        for (int r = 0; r < kWalkSegs; ++r) abv[r] = wpos[r] = 0u;
-        const uint32_t mx = max4(cnt);
+        uint32_t c_l, cnt[kWalkSegs];
+        const uint32_t mx = walk_counts(w, s0, nq, lane, &c_l, cnt);
+        uint32_t abv_l = 0u, wpos_l = 0u;
         for (uint32_t j0 = 0; j0 < mx; j0 += 32 * kWalkRows) {
           uint2 e[kWalkSegs][kWalkRows];
           walk_load(w, s0, j0, cnt, lane, e);
 #pragma unroll
           for (int r = 0; r < kWalkSegs; ++r) {
+            if (j0 >= cnt[r]) continue;  // warp-uniform
             uint2* list = w.list + ((s0 + r) << kSegShift);
+            uint32_t wpos = __shfl_sync(0xffffffffu, wpos_l, r), abv = 0u;
 #pragma unroll
             for (int u = 0; u < kWalkRows; ++u) {
               if (j0 + 32 * u >= cnt[r]) break;  // warp-uniform
@@ -352,22 +405,23 @@ __global__ void __launch_bounds__(kBkThreads) bk_collect_kernel(const float* __r
               const uint32_t key = e[r][u].x & 0x7fffffffu;
               const uint32_t bin = key >> kHistShift;
               const bool keep = valid && bin >= B;
-              abv[r] += (valid && bin > B) ? 1u : 0u;
+              abv += (valid && bin > B) ? 1u : 0u;
               if (valid && bin == B) atomicAdd(&mid[(key >> kLowBits) & (kMidBins - 1)], 1u);
-              // in place: the write position never passes the read position
+              // in place: every position written was read by an earlier ballot
               const uint32_t kb = __ballot_sync(0xffffffffu, keep);
-              if (keep) list[wpos[r] + __popc(kb & lt)] = e[r][u];
-              wpos[r] += __popc(kb);
+              if (keep) list[wpos + __popc(kb & lt)] = e[r][u];
+              wpos += __popc(kb);
+            }
+            abv = __reduce_add_sync(0xffffffffu, abv);
+            if (lane == r) {
+              wpos_l = wpos;
+              abv_l += abv;
             }
           }
         }
-#pragma unroll
-        for (int r = 0; r < kWalkSegs; ++r) {
-          const uint32_t a = __reduce_add_sync(0xffffffffu, abv[r]);
-          if (lane == 0 && r < nq) {
-            w.seg_above[s0 + r] = a;
-            w.seg_cnt[s0 + r] = wpos[r];
-          }
+        if (lane < nq) {
+          w.seg_above[s0 + lane] = abv_l;
+          w.seg_cnt[s0 + lane] = wpos_l;
         }
       }
     } else {
@@ -497,24 +551,23 @@ __global__ void __launch_bounds__(kBkThreads) bk_refine_kernel(BucketWs w) {
     uint2* stash = w.stash + (int64_t)b * kBkStash;
     for (int64_t s0 = s + kWalkSegs * warp; s0 < sub_hi; s0 += kWalkSegs * NW) {
       const int nq = (int)std::min<int64_t>(kWalkSegs, sub_hi - s0);
-      uint32_t cnt[kWalkSegs], strict[kWalkSegs];
-      walk_counts(w, s0, nq, lane, cnt);
-      const uint32_t aq = lane < nq ? w.seg_above[s0 + lane] : 0u;
-#pragma unroll
-      for (int r = 0; r < kWalkSegs; ++r) strict[r] = 0u;
-      const uint32_t mx = max4(cnt);
+      uint32_t c_l, cnt[kWalkSegs];
+      const uint32_t mx = walk_counts(w, s0, nq, lane, &c_l, cnt);
+      uint32_t strict_l = 0u;
       for (uint32_t j0 = 0; j0 < mx; j0 += 32 * kWalkRows) {
         uint2 e[kWalkSegs][kWalkRows];
         walk_load(w, s0, j0, cnt, lane, e);
 #pragma unroll
         for (int r = 0; r < kWalkSegs; ++r) {
+          if (j0 >= cnt[r]) continue;  // warp-uniform
+          uint32_t strict = 0u;
 #pragma unroll
           for (int u = 0; u < kWalkRows; ++u) {
             const uint32_t key = e[r][u].x & 0x7fffffffu;
             if (j0 + 32 * u + lane < cnt[r] && (key >> kHistShift) == B) {
               const uint32_t m = (key >> kLowBits) & (kMidBins - 1);
               if (m > B2) {
-                ++strict[r];
+                ++strict;
               } else if (m == B2) {
                 atomicAdd(&low[key & (kLowBins - 1)], 1u);
                 const uint32_t slot = atomicAdd(&q->stash_count, 1u);
@@ -522,17 +575,13 @@ __global__ void __launch_bounds__(kBkThreads) bk_refine_kernel(BucketWs w) {
               }
             }
           }
+          strict = __reduce_add_sync(0xffffffffu, strict);
+          if (lane == r) strict_l += strict;
         }
       }
       // lane r < nq writes segment r (entries above B come from collect)
-      uint32_t mine = 0u;
-#pragma unroll
-      for (int r = 0; r < kWalkSegs; ++r) {
-        const uint32_t t = __reduce_add_sync(0xffffffffu, strict[r]);
-        mine = lane == r ? t : mine;
-      }
       if (lane < nq) {
-        w.seg_kept[s0 + lane] = aq + mine;
+        w.seg_kept[s0 + lane] = __ldcg(&w.seg_above[s0 + lane]) + strict_l;
         w.seg_tie[s0 + lane] = 0u;
       }
     }
@@ -686,8 +735,8 @@ __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict_
     uint32_t cnt[kWalkSegs];
 #pragma unroll
     for (int r = 0; r < kWalkSegs; ++r) cnt[r] = __shfl_sync(0xffffffffu, cnt_l, r);
-    const uint32_t mx = max4(cnt);
-    uint32_t run[kWalkSegs] = {0u, 0u, 0u, 0u}, tie_run[kWalkSegs] = {0u, 0u, 0u, 0u};
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, cnt_l);
+    uint32_t run_l = 0u, tr_l = 0u;
     for (uint32_t j0 = 0; j0 < mx; j0 += 32 * kWalkRows) {
       uint2 e[kWalkSegs][kWalkRows];
       walk_load(w, s0, j0, cnt, lane, e);
@@ -701,6 +750,8 @@ __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict_
         const uint32_t bn = __shfl_sync(0xffffffffu, n_l, r);
         const int64_t off = __shfl_sync(0xffffffffu, off_l, r);
         const int64_t start = __shfl_sync(0xffffffffu, start_l, r);
+        uint32_t run = __shfl_sync(0xffffffffu, run_l, r);
+        uint32_t tr = __shfl_sync(0xffffffffu, tr_l, r);
 #pragma unroll
         for (int u = 0; u < kWalkRows; ++u) {
           if (j0 + 32 * u >= cnt[r]) break;  // warp-uniform
@@ -708,10 +759,10 @@ __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict_
           const uint32_t key = e[r][u].x & 0x7fffffffu;
           const bool gt = valid && key > T, eq = valid && key == T;
           const uint32_t eqb = __ballot_sync(0xffffffffu, eq);
-          const bool keep = gt || (eq && tie_run[r] + __popc(eqb & lt) < rem);
+          const bool keep = gt || (eq && tr + __popc(eqb & lt) < rem);
           const uint32_t kb = __ballot_sync(0xffffffffu, keep);
           if (keep) {
-            const uint32_t pos = out + run[r] + __popc(kb & lt);
+            const uint32_t pos = out + run + __popc(kb & lt);
             if (pos < bk && e[r][u].y < bn) {
               idx_out[off + pos] = (int32_t)e[r][u].y;
               val_out[off + pos] = __uint_as_float(e[r][u].x);
@@ -720,8 +771,12 @@ __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict_
               atomicOr(w.status, kStatusTopkOverflow);
             }
           }
-          run[r] += __popc(kb);
-          tie_run[r] += __popc(eqb);
+          run += __popc(kb);
+          tr += __popc(eqb);
+        }
+        if (lane == r) {
+          run_l = run;
+          tr_l = tr;
         }
       }
     }
@@ -729,9 +784,9 @@ __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict_
 }
 
 template <class K>
-int blocks_per_sm(K kernel, int threads) {
+int blocks_per_sm(K kernel, int threads, size_t smem = 0) {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) {
     cudaGetLastError();
     n = 1;
   }
@@ -747,9 +802,11 @@ gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int
   {
     LaunchScope L(ctx, GC_PHASE_BK_HIST);
     if (err)
-      bk_hist_kernel<true><<<w.g_hist, kBkHistThreads, 0, s>>>(grad, err, w, qbits, qgroup);
+      bk_hist_kernel<true><<<w.g_hist, kH1Threads, sizeof(HistSmem), s>>>(grad, err, w, qbits,
+                                                                         qgroup);
     else
-      bk_hist_kernel<false><<<w.g_hist, kBkHistThreads, 0, s>>>(grad, err, w, qbits, qgroup);
+      bk_hist_kernel<false><<<w.g_hist, kH1Threads, sizeof(HistSmem), s>>>(grad, err, w, qbits,
+                                                                          qgroup);
   }
   {
     LaunchScope L(ctx, GC_PHASE_BK_COLLECT);
@@ -808,7 +865,12 @@ gc_status plan_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n, const int64
   w.nchunk = nchunk;
   w.vals_total = voff;
   auto grid = [&](int per_sm) { return (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * per_sm, nseg)); };
-  w.g_hist = grid(blocks_per_sm(bk_hist_kernel<true>, kBkHistThreads));
+  if (cudaFuncSetAttribute(bk_hist_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)sizeof(HistSmem)) != cudaSuccess ||
+      cudaFuncSetAttribute(bk_hist_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)sizeof(HistSmem)) != cudaSuccess)
+    return GC_ERR_CUDA;
+  w.g_hist = grid(blocks_per_sm(bk_hist_kernel<true>, kH1Threads, sizeof(HistSmem)));
   w.g_coll = grid(blocks_per_sm(bk_collect_kernel, kBkThreads));
   w.g_ref = grid(blocks_per_sm(bk_refine_kernel, kBkThreads));
   w.g_write = grid(blocks_per_sm(bk_write_kernel<true>, kBkThreads));
