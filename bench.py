@@ -48,7 +48,7 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args():
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["gc", "reference"], default="gc")
     p.add_argument("--streams", type=int, default=4, help="contexts/streams for the buckets")
@@ -128,6 +128,31 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples),
                 "source": "nvml"}
+
+
+# DRAM traffic of the dominant kernel from one ncu capture
+# (profiles/bucketed_kernels_65M_full.md: dram__bytes_read.sum + dram__bytes_write.sum
+# of bk_hist on 65,536,000 elements), per element; it scales with the elements.
+# Valid only for the kernel source it was taken on (first 16 hex digits of the
+# SHA-256 of the file), else the bench reports null.
+TRAFFIC = {"bk_hist": {"bytes_per_elem": 759.1e6 / 65536000,
+                       "source": "gradient_compression_ef_gb300/csrc/gc_buckets.cu",
+                       "sha256_16": "7c108dfa8d4803d8",
+                       "profile": "profiles/bucketed_kernels_65M_full.md"}}
+
+
+def kernel_traffic(name, elems):
+    import hashlib
+    t = TRAFFIC.get(name)
+    if t is None:
+        return None, "no ncu capture for this kernel"
+    try:
+        digest = hashlib.sha256(open(os.path.join(ROOT, t["source"]), "rb").read()).hexdigest()
+    except OSError:
+        return None, "kernel source missing"
+    if digest[:16] != t["sha256_16"]:
+        return None, "kernel changed since the ncu capture"
+    return t["bytes_per_elem"] * elems, "ncu capture scaled by elements: " + t["profile"]
 
 
 def measured_peaks():
@@ -438,9 +463,12 @@ def main():
         kernels[name] = {"launches": cnt, "total_ms": ms_, "avg_us": avg_s * 1e6,
                          "algorithmic_bytes_per_launch": algo.get(name),
                          "achieved_gbs": algo[name] / avg_s / 1e9 if algo.get(name) else None}
+    traffic, traffic_src = kernel_traffic(top[0], wl.n) if args.path == "buckets" else \
+        (None, "per-bucket path: no ncu capture")
     roofline = {"bound": "hbm", "kernel": top[0], "achieved": kernels[top[0]]["achieved_gbs"],
                 "peak": peak, "unit": "GB/s", "peak_source": peak_src,
-                "frac": kernels[top[0]]["achieved_gbs"] / peak, "traffic": None}
+                "frac": kernels[top[0]]["achieved_gbs"] / peak, "traffic": traffic,
+                "traffic_source": traffic_src}
     step_achieved = wl.algorithmic_bytes() / (ms_per_step * 1e-3) / 1e9
 
     # end to end through the C ABI with host buffers: every step copies its
