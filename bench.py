@@ -60,10 +60,24 @@ def parse_args():
                    help="time eager launches instead of CUDA-graph replay")
     p.add_argument("--path", choices=["buckets", "per-bucket"], default="buckets",
                    help="one bucketed call per step, or one call per bucket")
-    p.add_argument("--elems", type=int, default=inputs.FLAT_ELEMS,
-                   help="gradient elements (default: the 134,217,728-element workload; smaller "
-                        "values cut the same 25 MiB buckets from a shorter gradient, for profiling)")
-    return p.parse_args()
+    p.add_argument("--elems", type=int, default=None,
+                   help="gradient elements (default: the workload's own size; for buckets a "
+                        "smaller value cuts the same 25 MiB buckets from a shorter gradient)")
+    p.add_argument("--workload", choices=["buckets", "quant", "tern", "powersgd"],
+                   default="buckets",
+                   help="buckets: EF + Top-K + QSGD per 25 MiB bucket (the headline); quant: "
+                        "EF + group quantisation of 2^30 elements; tern: EF + TernGrad per "
+                        "tensor of one transformer layer; powersgd: rank-4 PowerSGD on one "
+                        "layer's matrix shapes")
+    p.add_argument("--mode", choices=["minmax", "qsgd"], default="qsgd",
+                   help="quant workload: quantisation rule")
+    p.add_argument("--bits", type=int, default=8, help="quant workload: bits per code")
+    p.add_argument("--rounding", choices=["nearest_even", "stochastic"], default="stochastic",
+                   help="quant workload: rounding")
+    args = p.parse_args()
+    if args.elems is None:
+        args.elems = inputs.GROUP_ELEMS if args.workload == "quant" else inputs.FLAT_ELEMS
+    return args
 
 
 # ---------------------------------------------------------------------------
@@ -202,7 +216,11 @@ class BucketWorkload:
                          for s in self.streams]
 
     def out_bytes(self):
-        return (self.idx.numel() * 4 + self.codes.numel() + self.scales.numel() * 4)
+        return sum(t.numel() * t.element_size() for t in self.outputs())
+
+    def outputs(self):
+        """Device tensors holding one step's compressed result."""
+        return [self.idx, self.codes, self.scales]
 
     def algorithmic_bytes(self):
         """Bytes the method must move per step: read g and e, write e' (12 B
@@ -285,12 +303,197 @@ class BucketWorkload:
             c.check()
 
 
+class _SimpleWorkload:
+    """Shared plumbing of the single-context workloads: one context on the
+    main stream, whole steps captured in CUDA graphs."""
+
+    def _init_common(self, torch, gc, dev, max_n):
+        self.torch, self.gc, self.dev = torch, gc, dev
+        self.main = torch.cuda.current_stream(dev)
+        self.streams = [self.main]
+        self.ctxs = [gc.Context(max_n, stream=self.main)]
+
+    def out_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.outputs())
+
+    def _ctx_on(self, main, ctxs):
+        ctx = self.ctxs[0] if ctxs is None else ctxs[0]
+        if ctx._stream_ref is not main:
+            ctx.set_stream(main)
+        return ctx
+
+    def capture(self):
+        torch = self.torch
+        graphs = []
+        cap = torch.cuda.Stream(device=self.dev)
+        before = self.launches()
+        for d in range(len(self.grads)):
+            g = torch.cuda.CUDAGraph()
+            cap.wait_stream(self.main)
+            with torch.cuda.graph(g, stream=cap):
+                self.launch_step(d, main=cap)
+            graphs.append(g)
+        self.main.wait_stream(cap)
+        self.ctxs[0].set_stream(self.main)
+        return graphs, (self.launches() - before) // len(self.grads)
+
+    def launches(self):
+        return sum(c.launch_count() for c in self.ctxs)
+
+    def check(self):
+        for c in self.ctxs:
+            c.check()
+
+
+class QuantWorkload(_SimpleWorkload):
+    """Group-wise quantisation with error feedback: 2^30 fp32 N(0, 0.01^2)
+    with 0.1 % distinct positions x 100, groups of 64; one step is one
+    gc_ef_quant call over the whole array (the fused single-pass kernel)."""
+
+    GROUP, SEED = 64, 77
+
+    def __init__(self, torch, gc, dev, args, seed):
+        self.n = args.elems
+        self.bits, self.mode, self.rounding = args.bits, args.mode, args.rounding
+        self._init_common(torch, gc, dev, 0)
+        self.grads = [inputs.outlier_gradient_device(self.n, dev, seed + d)
+                      for d in range(args.distinct)]
+        self.err = torch.zeros(self.n, dtype=torch.float32, device=dev)
+        self.codes = torch.empty(gc.codes_bytes(self.n, self.bits, self.mode),
+                                 dtype=torch.uint8, device=dev)
+        self.scales = torch.empty(gc.scales_floats(self.n, self.GROUP, self.mode),
+                                  dtype=torch.float32, device=dev)
+
+    def outputs(self):
+        return [self.codes, self.scales]
+
+    def launch_step(self, t, grad=None, main=None, ctxs=None):
+        main = self.main if main is None else main
+        ctx = self._ctx_on(main, ctxs)
+        g = self.grads[t % len(self.grads)] if grad is None else grad
+        self.gc.ef_quant(ctx, g, self.err, self.bits, self.GROUP, self.mode, self.rounding,
+                         self.SEED, t, self.codes, self.scales)
+
+    def algorithmic_bytes(self):
+        """Read g and e, write e' (12 B per element), the packed codes and
+        the scales."""
+        return 12 * self.n + self.codes.numel() + 4 * self.scales.numel()
+
+    def algorithmic_bytes_per_launch(self):
+        return {"quant_fused": float(self.algorithmic_bytes())}
+
+
+class TernWorkload(_SimpleWorkload):
+    """TernGrad with error feedback on the tensors of one transformer layer
+    (4 x 4096^2, 2 x 4096 x 11008, 11008 x 4096, 4096), one scale per tensor
+    (max |c|), stochastic rounding: one gc_ef_quant call per tensor."""
+
+    SEED = 91
+
+    def __init__(self, torch, gc, dev, args, seed):
+        sizes = [int(np.prod(s)) for s in inputs.TRANSFORMER_SHAPES]
+        self.sizes = sizes
+        self.n = sum(sizes)
+        self._init_common(torch, gc, dev, max(sizes))
+        self.starts = np.concatenate([[0], np.cumsum(sizes)]).tolist()
+        self.grads = []
+        for d in range(args.distinct):
+            flat = torch.empty(self.n, dtype=torch.float32, device=dev)
+            for w_, (a, b) in enumerate(zip(self.starts, self.starts[1:])):
+                flat[a:b] = inputs.transformer_tensor_device(d, w_, dev, seed=seed)
+            self.grads.append(flat)
+        self.err = torch.zeros(self.n, dtype=torch.float32, device=dev)
+        self.cb = [gc.codes_bytes(n_, 2, "tern") for n_ in sizes]
+        self.coff = np.concatenate([[0], np.cumsum(self.cb)]).tolist()
+        self.codes = torch.empty(self.coff[-1], dtype=torch.uint8, device=dev)
+        self.scales = torch.empty(4 * len(sizes), dtype=torch.float32, device=dev)
+
+    def outputs(self):
+        return [self.codes, self.scales]
+
+    def launch_step(self, t, grad=None, main=None, ctxs=None):
+        main = self.main if main is None else main
+        ctx = self._ctx_on(main, ctxs)
+        g = self.grads[t % len(self.grads)] if grad is None else grad
+        for w_, (a, b) in enumerate(zip(self.starts, self.starts[1:])):
+            self.gc.ef_quant(ctx, g[a:b], self.err[a:b], 2, 0, "tern", "stochastic",
+                             self.SEED + w_, t, self.codes[self.coff[w_]:self.coff[w_ + 1]],
+                             self.scales[4 * w_:4 * w_ + 4])
+
+    def algorithmic_bytes(self):
+        """Read g and e, write e' (12 B per element) and 2-bit codes; the
+        per-tensor max needs the whole tensor before any element can be
+        coded, so the kernels read c once more (16 B per element)."""
+        return 12 * self.n + self.codes.numel() + 4 * len(self.sizes)
+
+    def algorithmic_bytes_per_launch(self):
+        """quant_stats reads g, e and writes c (12 B per element); quant_apply
+        reads c, writes e' and the codes (8.25 B per element); averaged over
+        the layer's 8 tensors."""
+        k = len(self.sizes)
+        return {"quant_stats": 12.0 * self.n / k,
+                "quant_apply": (8.0 * self.n + self.codes.numel()) / k}
+
+
+class PowerSGDWorkload(_SimpleWorkload):
+    """Rank-4 PowerSGD with error feedback on one layer's three matrix shapes
+    (4096 x 4096, 4096 x 11008, 11008 x 4096), each a low-rank signal plus
+    noise: one gc_powersgd_step per matrix, Q carried between steps."""
+
+    R = 4
+
+    def __init__(self, torch, gc, dev, args, seed):
+        shapes = inputs.POWERSGD_SHAPES
+        self.shapes = shapes
+        self.n = sum(m * n_ for m, n_ in shapes)
+        self._init_common(torch, gc, dev, 0)
+        self.ctxs[0].reserve_powersgd(max(m for m, _ in shapes), max(n_ for _, n_ in shapes),
+                                      self.R)
+        self.starts = np.concatenate([[0], np.cumsum([m * n_ for m, n_ in shapes])]).tolist()
+        flat = torch.empty(self.n, dtype=torch.float32, device=dev)
+        self.Q = []
+        for i, (m, n_) in enumerate(shapes):
+            M, Q0 = inputs.low_rank_matrix(m, n_, seed=seed, r=self.R)
+            flat[self.starts[i]:self.starts[i + 1]] = torch.from_numpy(M.ravel()).to(dev)
+            self.Q.append(torch.from_numpy(Q0).to(dev).contiguous())
+        self.grads = [flat]
+        self.err = torch.zeros(self.n, dtype=torch.float32, device=dev)
+        self.P = [torch.empty(m * self.R, dtype=torch.float32, device=dev) for m, _ in shapes]
+
+    def outputs(self):
+        return self.P + self.Q
+
+    def launch_step(self, t, grad=None, main=None, ctxs=None):
+        main = self.main if main is None else main
+        ctx = self._ctx_on(main, ctxs)
+        g = self.grads[t % len(self.grads)] if grad is None else grad
+        for i, (m, n_) in enumerate(self.shapes):
+            a, b = self.starts[i], self.starts[i + 1]
+            self.gc.powersgd_step(ctx, g[a:b], self.err[a:b], m, n_, self.R, self.P[i],
+                                  self.Q[i])
+
+    def algorithmic_bytes(self):
+        """The minimum: read G and E, write E' (12 B per element)."""
+        return 12 * self.n
+
+    def algorithmic_bytes_per_launch(self):
+        """Per matrix: pass 1 reads G, E and writes M into E (12 B per
+        element), pass 2 reads M (4 B), pass 3 reads M and writes E' (8 B);
+        averaged over the three matrices."""
+        k = len(self.shapes)
+        return {"psgd_mq": 12.0 * self.n / k, "psgd_mtp": 4.0 * self.n / k,
+                "psgd_resid": 8.0 * self.n / k}
+
+
+WORKLOADS = {"quant": QuantWorkload, "tern": TernWorkload, "powersgd": PowerSGDWorkload}
+
+
 def kernel_timing(wl, steps, warmup_step):
     """Per-phase CUDA-event durations over `steps` more steps run with all
     buckets on one context / stream, so that each kernel runs alone and its
     events bracket its own execution."""
     ctx = wl.ctxs[0]
-    ctx.enable_timing(8 * len(wl.bounds) * steps)
+    ctx.enable_timing(64 * steps)
     for t in range(steps):
         wl.launch_step(warmup_step + t, ctxs=[ctx])
     phases = {name: [ms, cnt] for name, (ms, cnt) in ctx.read_timing().items()}
@@ -298,45 +501,89 @@ def kernel_timing(wl, steps, warmup_step):
     return phases
 
 
-def cpu_baseline(budget_s=12.0, seed=7):
-    """The oracle (single-threaded C) on whole buckets of the workload until
-    about budget_s seconds of CPU work; GB/s of fp32 gradient."""
+def cpu_sample(args, seed=7):
+    """One bounded sample of the workload for the oracle: returns
+    (callable running the oracle on it once, fp32 gradient elements it
+    covers, description)."""
     import oracle
     r = inputs.rng(seed)
+    if args.workload == "quant":
+        n = 1 << 22
+        g = r.standard_normal(n).astype(np.float32) * np.float32(0.01)
+        e = np.zeros(n, np.float32)
+        return (lambda: oracle.ef_quant(g, e, args.bits, 64, args.mode, args.rounding, 77, 0),
+                n, "4,194,304 elements of the 2^30-element gradient, EF + %s %d-bit g64 %s"
+                % (args.mode, args.bits, args.rounding))
+    if args.workload == "tern":
+        g = inputs.transformer_tensor(0, 0)
+        e = np.zeros_like(g)
+        return (lambda: oracle.ef_quant(g, e, 2, 0, "tern", "stochastic", 91, 0), g.size,
+                "one 4096 x 4096 tensor of the layer, EF + TernGrad per tensor")
+    if args.workload == "powersgd":
+        M, Q0 = inputs.low_rank_matrix(4096, 4096, seed=seed, r=4)
+        E = np.zeros_like(M)
+        return (lambda: oracle.powersgd_step(M, E, Q0, 4), M.size,
+                "one 4096 x 4096 matrix of the layer, rank-4 PowerSGD step (fp64)")
     length = inputs.BUCKET_ELEMS
-    k = inputs.ratio_k(length, 10, 1000)
-    done, elapsed, buckets = 0, 0.0, 0
-    while buckets == 0 or elapsed < budget_s:
-        g = inputs.student_t(r, length)
-        e = (0.1 * inputs.student_t(r, length)).astype(np.float32)
+    k = inputs.ratio_k(length, args.ratio, 1000)
+    g = inputs.student_t(r, length)
+    e = (0.1 * inputs.student_t(r, length)).astype(np.float32)
+    return (lambda: oracle.ef_topk_quant(g, e, k, 8, 64, "stochastic", 1000, 0), length,
+            "one 6,553,600-element bucket, EF + Top-K %g%% + 8-bit QSGD" % (args.ratio / 10))
+
+
+def cpu_baseline(args, budget_s=12.0):
+    """The oracle (single-threaded C) on a bounded sample of the workload,
+    repeated until about budget_s seconds (at most 8 runs); GB/s of fp32
+    gradient."""
+    run, n, what = cpu_sample(args)
+    elapsed, runs = 0.0, 0
+    while runs == 0 or (elapsed < budget_s and runs < 8):
         t0 = time.perf_counter()
-        oracle.ef_topk_quant(g, e, k, 8, 64, "stochastic", 1000 + buckets, 0)
+        run()
         elapsed += time.perf_counter() - t0
-        done += length
-        buckets += 1
-        if buckets >= 8:
-            break
-    return {"value": 4.0 * done / elapsed / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "%d bucket(s) of 6,553,600 elements, EF + Top-K 1%% + 8-bit QSGD, "
-                      "%.1f s single-threaded" % (buckets, elapsed)}
+        runs += 1
+    return {"value": 4.0 * n * runs / elapsed / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "%s, %d run(s), %.1f s single-threaded" % (what, runs, elapsed)}
 
 
 def config(args, wl=None):
     n = args.elems
-    bounds = inputs.bucket_bounds(n)
-    sizes = "%d x %s" % (len([1 for _, l in bounds if l == inputs.BUCKET_ELEMS]), "6,553,600")
-    if bounds[-1][1] != inputs.BUCKET_ELEMS:
-        sizes += " + {:,}".format(bounds[-1][1])
-    cfg = {"workload": "flat fp32 gradient {:,} elements in 25 MiB buckets ({}), Student-t "
-                       "nu=3 x 1e-3, correlated steps; per bucket EF + Top-K {:g}% + 8-bit QSGD "
-                       "(groups of 64, stochastic) on the kept values".format(n, sizes,
-                                                                             args.ratio / 10),
-           "total_elems": n, "bucket_elems": inputs.BUCKET_ELEMS,
-           "buckets": len(bounds), "topk_per_mille": args.ratio,
-           "quant": "qsgd 8-bit g64 stochastic",
-           "l2": "inputs larger than L2: each step reads a {0} MiB gradient and the {0} MiB "
-                 "residual, no flush".format(4 * n >> 20), "parallelism": "dp%d" % args.gpus}
-    cfg["path"] = args.path
+    l2 = {"l2": "inputs larger than L2: each step reads a {0} MiB gradient and the {0} MiB "
+                "residual, no flush", "parallelism": "dp%d" % args.gpus}
+    if args.workload == "quant":
+        cfg = {"workload": "flat fp32 gradient {:,} elements N(0, 0.01^2) with 0.1% distinct "
+                           "positions x 100; EF + {} {}-bit quantisation, groups of 64, {} "
+                           "rounding".format(n, args.mode, args.bits, args.rounding),
+               "total_elems": n, "group": 64, "mode": args.mode, "bits": args.bits,
+               "rounding": args.rounding}
+    elif args.workload == "tern":
+        n = sum(int(np.prod(s_)) for s_ in inputs.TRANSFORMER_SHAPES)
+        cfg = {"workload": "one transformer layer's gradient tensors (4 x 4096^2, 2 x 4096 x "
+                           "11008, 11008 x 4096, 4096; N(0, (1e-3/sqrt(fan_in))^2)), EF + "
+                           "TernGrad per tensor (scale = max|c| of the tensor), stochastic",
+               "total_elems": n, "tensors": len(inputs.TRANSFORMER_SHAPES)}
+    elif args.workload == "powersgd":
+        n = sum(m * n_ for m, n_ in inputs.POWERSGD_SHAPES)
+        cfg = {"workload": "one transformer layer's matrix shapes (4096 x 4096, 4096 x 11008, "
+                           "11008 x 4096) as rank-16 signal + N(0, 1e-4^2) noise; rank-4 "
+                           "PowerSGD step with error feedback per matrix",
+               "total_elems": n, "rank": 4}
+    else:
+        bounds = inputs.bucket_bounds(n)
+        sizes = "%d x %s" % (len([1 for _, l in bounds if l == inputs.BUCKET_ELEMS]),
+                             "6,553,600")
+        if bounds[-1][1] != inputs.BUCKET_ELEMS:
+            sizes += " + {:,}".format(bounds[-1][1])
+        cfg = {"workload": "flat fp32 gradient {:,} elements in 25 MiB buckets ({}), Student-t "
+                           "nu=3 x 1e-3, correlated steps; per bucket EF + Top-K {:g}% + 8-bit "
+                           "QSGD (groups of 64, stochastic) on the kept values".format(
+                               n, sizes, args.ratio / 10),
+               "total_elems": n, "bucket_elems": inputs.BUCKET_ELEMS,
+               "buckets": len(bounds), "topk_per_mille": args.ratio,
+               "quant": "qsgd 8-bit g64 stochastic", "path": args.path}
+    cfg["l2"] = l2["l2"].format(4 * n >> 20)
+    cfg["parallelism"] = l2["parallelism"]
     if wl is not None:
         cfg["streams"] = len(wl.streams)
         cfg["distinct_gradients"] = len(wl.grads)
@@ -345,26 +592,22 @@ def config(args, wl=None):
 
 # ---------------------------------------------------------------------------
 def run_reference(args):
+    """The reference arm: the oracle (single-threaded C, the pages'
+    definitions), each step one bounded sample of the workload."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    import oracle
-    r = inputs.rng(11)
-    length = inputs.BUCKET_ELEMS
-    k = inputs.ratio_k(length, args.ratio, 1000)
-    g = inputs.student_t(r, length)
-    e = np.zeros(length, np.float32)
+    run, n, what = cpu_sample(args, seed=11)
     times = []
     for t in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        _, _, _, e = oracle.ef_topk_quant(g, e, k, 8, 64, "stochastic", 1000, t)
+        run()
         dt = time.perf_counter() - t0
         if t >= args.warmup:
             times.append(dt)
     sec = sum(times) / len(times)
-    value = 4.0 * length / sec / 1e9
-    sample = ("one 6,553,600-element bucket (1/21 of the 134,217,728-element step) per step, "
-              "EF + Top-K %g%% + 8-bit QSGD, single-threaded C oracle" % (args.ratio / 10))
+    value = 4.0 * n / sec / 1e9
+    sample = what + ", single-threaded C oracle, one sample per step"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -393,8 +636,11 @@ def main():
     torch.cuda.set_device(dev)
     from gradient_compression_ef_gb300 import gc
 
-    wl = BucketWorkload(torch, gc, dev, args.ratio, args.streams, args.distinct, seed=42 + rank,
-                        path=args.path, n=args.elems)
+    if args.workload == "buckets":
+        wl = BucketWorkload(torch, gc, dev, args.ratio, args.streams, args.distinct,
+                            seed=42 + rank, path=args.path, n=args.elems)
+    else:
+        wl = WORKLOADS[args.workload](torch, gc, dev, args, seed=42 + rank)
     torch.cuda.synchronize(dev)
     for t in range(args.warmup):
         wl.launch_step(t)
@@ -463,8 +709,8 @@ def main():
         kernels[name] = {"launches": cnt, "total_ms": ms_, "avg_us": avg_s * 1e6,
                          "algorithmic_bytes_per_launch": algo.get(name),
                          "achieved_gbs": algo[name] / avg_s / 1e9 if algo.get(name) else None}
-    traffic, traffic_src = kernel_traffic(top[0], wl.n) if args.path == "buckets" else \
-        (None, "per-bucket path: no ncu capture")
+    traffic, traffic_src = kernel_traffic(top[0], wl.n) \
+        if args.workload == "buckets" and args.path == "buckets" else (None, "no ncu capture")
     roofline = {"bound": "hbm", "kernel": top[0], "achieved": kernels[top[0]]["achieved_gbs"],
                 "peak": peak, "unit": "GB/s", "peak_source": peak_src,
                 "frac": kernels[top[0]]["achieved_gbs"] / peak, "traffic": traffic,
@@ -478,9 +724,7 @@ def main():
     if not args.no_e2e:
         T = len(wl.grads)
         hosts = [g.cpu().pin_memory() for g in wl.grads]
-        out_i = torch.empty(wl.idx.numel(), dtype=torch.int32).pin_memory()
-        out_c = torch.empty(wl.codes.numel(), dtype=torch.uint8).pin_memory()
-        out_s = torch.empty(wl.scales.numel(), dtype=torch.float32).pin_memory()
+        outs_h = [torch.empty(t.numel(), dtype=t.dtype).pin_memory() for t in wl.outputs()]
         copy_s = torch.cuda.Stream(device=dev)
         ready = [torch.cuda.Event() for _ in range(T)]
         done = [torch.cuda.Event() for _ in range(T)]
@@ -499,9 +743,8 @@ def main():
             else:
                 graphs[d].replay()
             done[d].record(wl.main)
-            out_i.copy_(wl.idx, non_blocking=True)
-            out_c.copy_(wl.codes, non_blocking=True)
-            out_s.copy_(wl.scales, non_blocking=True)
+            for h_, t_ in zip(outs_h, wl.outputs()):
+                h_.copy_(t_.view(-1), non_blocking=True)
 
         e_ms = timed(e2e_step, e2e_steps, side_streams=(copy_s,))
         e2e = {"value": world * 4.0 * wl.n / (e_ms * 1e-3) / 1e9, "unit": UNIT,
@@ -520,7 +763,7 @@ def main():
             "e2e": e2e, "clocks": sampler.summary(), "gpu_launches": launches,
             "launch": launch_mode, "eager": {"value": eager_value, "ms_per_step": eager_ms}}
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline()
+        line["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -126,6 +126,33 @@ def outlier_gradient(n=GROUP_ELEMS, seed=42, std=0.01, frac=0.001, mult=100.0):
     return x
 
 
+def outlier_gradient_device(n, device, seed, std=0.01, frac=0.001, mult=100.0):
+    """The outlier recipe drawn by torch on ``device`` (seeded): N(0, std^2)
+    with round(frac * n) distinct positions (a random permutation's prefix)
+    multiplied by mult."""
+    import torch
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    x = torch.randn(n, generator=gen, device=device, dtype=torch.float32).mul_(std)
+    m = int(round(frac * n))
+    if m > 0:
+        pos = torch.randperm(n, generator=gen, device=device)[:m]
+        x[pos] *= mult
+    return x
+
+
+def transformer_tensor_device(layer, which, device, seed=42, scale=1e-3):
+    """Tensor ``which`` of ``layer`` with the same distribution as
+    transformer_tensor, drawn by torch on ``device`` (seeded)."""
+    import torch
+    shape = TRANSFORMER_SHAPES[which]
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed) * 1_000_003 + int(layer) * 1009 + int(which))
+    n = int(np.prod(shape))
+    return torch.randn(n, generator=gen, device=device,
+                       dtype=torch.float32).mul_(scale / float(np.sqrt(shape[0])))
+
+
 def transformer_tensor(layer, which, seed=42, scale=1e-3):
     """Tensor ``which`` (0..7) of ``layer`` as a flat float32 array."""
     shape = TRANSFORMER_SHAPES[which]
