@@ -92,20 +92,12 @@ __device__ __forceinline__ uint32_t code_bits4(const uint32_t q[4], const bool n
 // ---------------------------------------------------------------------------
 // Fused single-pass kernel for groups of G = 4 * LPG elements.
 // ---------------------------------------------------------------------------
-// One warp quantises elements base .. base+127 of x (groups of G = 4 * LPG
-// consecutive lanes, G dividing 128).  Every lane of the warp must call it.
-template <int MODE, int BITS, int LPG, int IO>
-__device__ __forceinline__ void quant_fused_chunk(
-    const float* __restrict__ x, float* __restrict__ err,
-    const int32_t* __restrict__ scatter_idx, int64_t n, const QuantOut& o,
-    int stochastic, uint64_t seed, uint64_t step, int64_t base, int lane) {
-  constexpr int G = 4 * LPG;
-  constexpr uint32_t top = (MODE == GC_TERN) ? 1u : ((1u << BITS) - 1u);
-  const float levels = (float)top;
-  const int64_t i0 = base + 4 * lane;
-  const bool active = i0 < n;
-  float c[4];
-  bool valid[4];
+// Values of elements i0 .. i0+3 of a chunk: c = x (+ e with error
+// feedback); lanes past n get zeros and valid = false.
+template <int IO>
+__device__ __forceinline__ void quant_load4(const float* __restrict__ x,
+                                            const float* __restrict__ err, int64_t n,
+                                            int64_t i0, float c[4], bool valid[4]) {
   if (i0 + 3 < n) {
     const float4 v = IO == IO_EF ? __ldcs(reinterpret_cast<const float4*>(x + i0))
                                  : *reinterpret_cast<const float4*>(x + i0);
@@ -126,6 +118,22 @@ __device__ __forceinline__ void quant_fused_chunk(
       if (IO == IO_EF && valid[j]) c[j] = __fadd_rn(c[j], err[i0 + j]);
     }
   }
+}
+
+// One warp quantises elements base .. base+127 of x (groups of G = 4 * LPG
+// consecutive lanes, G dividing 128), lane l holding elements base + 4l ..
+// base + 4l + 3 with values c[] (from quant_load4).  Every lane of the warp
+// must call it.
+template <int MODE, int BITS, int LPG, int IO>
+__device__ __forceinline__ void quant_fused_apply(
+    float c[4], const bool valid[4], float* __restrict__ err,
+    const int32_t* __restrict__ scatter_idx, int64_t n, const QuantOut& o,
+    int stochastic, uint64_t seed, uint64_t step, int64_t base, int lane) {
+  constexpr int G = 4 * LPG;
+  constexpr uint32_t top = (MODE == GC_TERN) ? 1u : ((1u << BITS) - 1u);
+  const float levels = (float)top;
+  const int64_t i0 = base + 4 * lane;
+  const bool active = i0 < n;
 
   // group statistics (lanes of a group are LPG consecutive lanes)
   float scale, offset = 0.0f;
@@ -199,6 +207,19 @@ __device__ __forceinline__ void quant_fused_chunk(
       else atomicOr(o.status, kStatusScatterIndex);
     }
   }
+}
+
+// Load + quantise of one 128-element chunk (the bucketed kernel's unit).
+template <int MODE, int BITS, int LPG, int IO>
+__device__ __forceinline__ void quant_fused_chunk(
+    const float* __restrict__ x, float* __restrict__ err,
+    const int32_t* __restrict__ scatter_idx, int64_t n, const QuantOut& o,
+    int stochastic, uint64_t seed, uint64_t step, int64_t base, int lane) {
+  float c[4];
+  bool valid[4];
+  quant_load4<IO>(x, err, n, base + 4 * lane, c, valid);
+  quant_fused_apply<MODE, BITS, LPG, IO>(c, valid, err, scatter_idx, n, o, stochastic, seed,
+                                         step, base, lane);
 }
 
 template <int MODE, int BITS, int LPG, int IO>
@@ -570,20 +591,26 @@ int grid_for(gc_ctx* ctx, int64_t work_items, int per_block, int per_sm) {
   return (int)std::min<int64_t>(want, (int64_t)ctx->num_sms * per_sm);
 }
 
+template <int MODE, int BITS, int LPG, int IO>
+void launch_fused(gc_ctx* ctx, const float* x, float* err, const int32_t* idx, int64_t n,
+                  const QuantOut& o, int stoch, uint64_t seed, uint64_t step) {
+  const int grid = grid_for(ctx, ceil_div(n, 128), kQThreads / 32, 8);
+  quant_fused_kernel<MODE, BITS, LPG, IO><<<grid, kQThreads, 0, ctx->stream>>>(
+      x, err, idx, n, o, stoch, seed, step);
+}
+
 template <int MODE, int BITS, int IO>
 gc_status run_fused(gc_ctx* ctx, const float* x, float* err, const int32_t* idx,
                     int64_t n, int64_t G, const QuantOut& o, int stoch, uint64_t seed,
                     uint64_t step) {
-  const int grid = grid_for(ctx, ceil_div(n, 128), kQThreads / 32, 8);
-  cudaStream_t s = ctx->stream;
   LaunchScope L(ctx, GC_PHASE_QUANT_FUSED);
   switch (G) {
-    case 4: quant_fused_kernel<MODE, BITS, 1, IO><<<grid, kQThreads, 0, s>>>(x, err, idx, n, o, stoch, seed, step); break;
-    case 8: quant_fused_kernel<MODE, BITS, 2, IO><<<grid, kQThreads, 0, s>>>(x, err, idx, n, o, stoch, seed, step); break;
-    case 16: quant_fused_kernel<MODE, BITS, 4, IO><<<grid, kQThreads, 0, s>>>(x, err, idx, n, o, stoch, seed, step); break;
-    case 32: quant_fused_kernel<MODE, BITS, 8, IO><<<grid, kQThreads, 0, s>>>(x, err, idx, n, o, stoch, seed, step); break;
-    case 64: quant_fused_kernel<MODE, BITS, 16, IO><<<grid, kQThreads, 0, s>>>(x, err, idx, n, o, stoch, seed, step); break;
-    default: quant_fused_kernel<MODE, BITS, 32, IO><<<grid, kQThreads, 0, s>>>(x, err, idx, n, o, stoch, seed, step); break;
+    case 4: launch_fused<MODE, BITS, 1, IO>(ctx, x, err, idx, n, o, stoch, seed, step); break;
+    case 8: launch_fused<MODE, BITS, 2, IO>(ctx, x, err, idx, n, o, stoch, seed, step); break;
+    case 16: launch_fused<MODE, BITS, 4, IO>(ctx, x, err, idx, n, o, stoch, seed, step); break;
+    case 32: launch_fused<MODE, BITS, 8, IO>(ctx, x, err, idx, n, o, stoch, seed, step); break;
+    case 64: launch_fused<MODE, BITS, 16, IO>(ctx, x, err, idx, n, o, stoch, seed, step); break;
+    default: launch_fused<MODE, BITS, 32, IO>(ctx, x, err, idx, n, o, stoch, seed, step); break;
   }
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
