@@ -70,6 +70,11 @@ def lib():
         L.orc_powersgd_step.argtypes = [_f32p, _f32p, _i64, _i64, _int, _f32p,
                                         _f32p]
         L.orc_powersgd_step.restype = _int
+        L.orc_topk_aggregate.argtypes = [_int, _i64, _i32p, _f32p, _i64, _f32p]
+        L.orc_topk_aggregate.restype = _int
+        L.orc_topk_quant_aggregate.argtypes = [_int, _i64, _i32p, _u8p, _f32p, _int, _i64,
+                                               _i64, _f32p]
+        L.orc_topk_quant_aggregate.restype = _int
         _lib = L
     return _lib
 
@@ -213,6 +218,44 @@ def ef_topk_quant(grad, err, k, bits, group, rounding="nearest_even", seed=0,
                                    _p(idx, _i32p), _p(codes, _u8p),
                                    _p(scales, _f32p)), "orc_ef_topk_quant")
     return idx[:k], codes[:cb], scales[:sf], e
+
+
+def _aggregate_idx(idx, W, k):
+    ix = np.ascontiguousarray(idx, dtype=np.int32).reshape(-1)
+    if ix.size != W * k:
+        raise OracleError("idx must hold W * k indices")
+    return ix if ix.size else np.zeros(1, np.int32)
+
+
+def topk_aggregate(idx, val, W, k, n):
+    """Sum of W ranks' sparse vectors in rank order.  idx, val: W * k
+    entries, rank w's at [w*k, (w+1)*k).  Returns float32[n]."""
+    ix = _aggregate_idx(idx, W, k)
+    v = np.ascontiguousarray(val, dtype=np.float32).reshape(-1)
+    if v.size != W * k:
+        raise OracleError("val must hold W * k values")
+    v = v if v.size else np.zeros(1, np.float32)
+    out = np.zeros(max(n, 1), dtype=np.float32)
+    _check(lib().orc_topk_aggregate(W, k, _p(ix, _i32p), _p(v, _f32p), n, _p(out, _f32p)),
+           "orc_topk_aggregate")
+    return out[:n]
+
+
+def topk_quant_aggregate(idx, codes, scales, W, k, bits, group, n):
+    """Sum of W ranks' QSGD-compressed sparse vectors in rank order; rank w's
+    codes and scales at w * codes_bytes(k) and w * scales_floats(k)."""
+    ix = _aggregate_idx(idx, W, k)
+    c = np.ascontiguousarray(codes, dtype=np.uint8).reshape(-1)
+    s = np.ascontiguousarray(scales, dtype=np.float32).reshape(-1)
+    if c.size != W * codes_bytes(k, bits, QSGD) or s.size != W * scales_floats(k, group, QSGD):
+        raise OracleError("codes / scales do not hold W ranks")
+    c = c if c.size else np.zeros(1, np.uint8)
+    s = s if s.size else np.zeros(1, np.float32)
+    out = np.zeros(max(n, 1), dtype=np.float32)
+    _check(lib().orc_topk_quant_aggregate(W, k, _p(ix, _i32p), _p(c, _u8p), _p(s, _f32p),
+                                          bits, group, n, _p(out, _f32p)),
+           "orc_topk_quant_aggregate")
+    return out[:n]
 
 
 def powersgd_step(grad, err, Q, r):

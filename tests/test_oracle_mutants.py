@@ -11,6 +11,7 @@ import pytest
 import oracle.build as obuild
 import oracle.oracle as ofront
 
+from tests import test_oracle_aggregate as tagg
 from tests import test_oracle_philox as tphilox
 from tests import test_oracle_powersgd as tpsgd
 from tests import test_oracle_quant as tquant
@@ -47,6 +48,9 @@ MUTANTS = {
                                "err[i * n + j] = (float)(a - M[i * n + j]);"),
     "powersgd_q_transposed": ("for (int64_t i = 0; i < m; ++i) s += M[i * n + j] * P[i * r + c];",
                               "for (int64_t i = 0; i < m && i < n; ++i) s += M[j * n + i] * P[i * r + c];"),
+    "aggregate_reverse_rank_order": ("  for (int w = 0; w < W; ++w)\n    for (int64_t j = 0; j < k; ++j) {\n      int64_t at",
+                                     "  for (int w = W - 1; w >= 0; --w)\n    for (int64_t j = 0; j < k; ++j) {\n      int64_t at"),
+    "aggregate_assign_not_add": ("out[idx[at]] = out[idx[at]] + val[at];", "out[idx[at]] = val[at];"),
 }
 
 
@@ -69,6 +73,8 @@ def _pins(golden_dir):
     yield lambda: tphilox.test_uniform_distribution()
     yield lambda: tpsgd.test_exact_low_rank_is_reconstructed()
     yield lambda: tpsgd.test_orthonormal_and_matches_numpy_qr()
+    yield lambda: tagg.test_hand_cases(golden_dir)
+    yield lambda: tagg.test_quant_hand_case(golden_dir)
 
 
 @pytest.fixture(scope="module")
