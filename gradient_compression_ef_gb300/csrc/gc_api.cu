@@ -162,6 +162,11 @@ gc_status gc_ctx_create(gc_ctx** out, void* cuda_stream, int64_t max_n) {
   ctx->ws.partials = reinterpret_cast<float4*>(b + L.partials);
   ctx->ws.max_n = max_n;
   ctx->ws.max_partials = max_partials;
+  if (gc::prepare_aggregate_kernels() != GC_OK) {
+    cudaFree(base);
+    free(ctx);
+    return GC_ERR_CUDA;
+  }
   *out = ctx;
   return GC_OK;
 }
@@ -185,7 +190,8 @@ const char* gc_phase_name(int phase) {
   static const char* names[GC_PHASE_COUNT] = {
       "ef_hist", "collect", "write", "ef_add", "quant_fused", "quant_stats",
       "quant_combine", "quant_apply", "dequant", "psgd_mq", "psgd_mtp", "psgd_resid",
-      "refine", "bk_hist", "bk_collect", "bk_refine", "bk_write", "bk_quant"};
+      "refine", "bk_hist", "bk_collect", "bk_refine", "bk_write", "bk_quant", "agg_bounds",
+      "agg_accumulate"};
   return (phase >= 0 && phase < GC_PHASE_COUNT) ? names[phase] : "?";
 }
 
@@ -465,6 +471,41 @@ gc_status gc_ef_topk_quant_buckets(gc_ctx* ctx, const float* grad, float* err, i
   GC_TRY(gc::launch_ef_topk_buckets(ctx, grad, err, idx_out, w.vals, false, bits, group));
   return gc::launch_quant_buckets(ctx, err, idx_out, bits, group, rounding, seed, step,
                                   codes_out, scales_out);
+}
+
+namespace {
+gc_status check_aggregate(gc_ctx* ctx, int W, int64_t k, int64_t n, const void* idx,
+                          const void* out) {
+  if (!ctx || W < 1 || W > gc::aggregate_max_ranks() || k < 0 || n < 0 || k > n ||
+      n > INT32_MAX)
+    return GC_ERR_INVALID_ARG;
+  GC_TRY(check_buf(idx, k > 0));
+  GC_TRY(check_buf(out, n > 0));
+  if (n > 0 && gc::aggregate_scratch_ints(W, n) > 2 * std::max<int64_t>(ctx->ws.max_n, 1))
+    return GC_ERR_WORKSPACE;
+  return GC_OK;
+}
+}  // namespace
+
+gc_status gc_topk_aggregate(gc_ctx* ctx, int W, int64_t k, const int32_t* idx,
+                            const float* val, int64_t n, float* out) {
+  GC_TRY(check_aggregate(ctx, W, k, n, idx, out));
+  GC_TRY(check_buf(val, k > 0));
+  DeviceGuard guard(ctx->device);
+  if (!guard.ok) return GC_ERR_CUDA;
+  return gc::launch_aggregate(ctx, W, k, idx, val, nullptr, nullptr, 0, 0, n, out);
+}
+
+gc_status gc_topk_quant_aggregate(gc_ctx* ctx, int W, int64_t k, const int32_t* idx,
+                                  const uint8_t* codes, const float* scales, int bits,
+                                  int64_t group, int64_t n, float* out) {
+  GC_TRY(check_aggregate(ctx, W, k, n, idx, out));
+  GC_TRY(check_quant(k, bits, group, GC_QSGD, GC_NEAREST_EVEN));
+  GC_TRY(check_buf(codes, k > 0));
+  GC_TRY(check_buf(scales, k > 0));
+  DeviceGuard guard(ctx->device);
+  if (!guard.ok) return GC_ERR_CUDA;
+  return gc::launch_aggregate(ctx, W, k, idx, nullptr, codes, scales, bits, group, n, out);
 }
 
 }  // extern "C"

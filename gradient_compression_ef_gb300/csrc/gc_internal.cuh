@@ -354,6 +354,18 @@ gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int
 gc_status launch_quant_buckets(gc_ctx* ctx, float* err, const int32_t* idx_out, int bits,
                                int64_t group, int rounding, uint64_t seed, uint64_t step,
                                uint8_t* codes_out, float* scales_out);
+// Sum of W ranks' sparse vectors into out[n] in rank order; bits == 0: fp32
+// values val[W*k], else QSGD codes / scales laid out per rank (see gc.h).
+gc_status launch_aggregate(gc_ctx* ctx, int W, int64_t k, const int32_t* idx, const float* val,
+                           const uint8_t* codes, const float* scales, int bits, int64_t group,
+                           int64_t n, float* out);
+// int32 scratch the aggregation needs for W ranks over n elements, and the
+// largest W.
+int64_t aggregate_scratch_ints(int W, int64_t n);
+int aggregate_max_ranks();
+// Opts the aggregation kernels into their shared memory (once per device).
+gc_status prepare_aggregate_kernels();
+
 // Builds the device plan of nb buckets (synchronous; frees the previous).
 gc_status plan_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n, const int64_t* bucket_k);
 void free_buckets(gc_ctx* ctx);

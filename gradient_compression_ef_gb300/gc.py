@@ -20,7 +20,7 @@ NEAREST_EVEN, STOCHASTIC = 0, 1
 MODES = {"minmax": MINMAX, "qsgd": QSGD, "tern": TERN}
 ROUNDINGS = {"nearest_even": NEAREST_EVEN, "stochastic": STOCHASTIC}
 
-PHASE_COUNT = 18
+PHASE_COUNT = 20
 
 OK = 0
 ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE = -1, -2, -3, -4
@@ -61,6 +61,8 @@ SIGNATURES = [
     ("gc_ef_topk_buckets", _int, [_vp, _vp, _vp, _vp, _vp]),
     ("gc_ef_topk_quant_buckets", _int, [_vp, _vp, _vp, _int, _i64, _int, _u64, _u64, _vp, _vp,
                                         _vp]),
+    ("gc_topk_aggregate", _int, [_vp, _int, _i64, _vp, _vp, _i64, _vp]),
+    ("gc_topk_quant_aggregate", _int, [_vp, _int, _i64, _vp, _vp, _vp, _int, _i64, _i64, _vp]),
 ]
 
 # largest n of gc_ef_topk_noalloc (GC_NOALLOC_MAX_N in include/gc.h)
@@ -278,3 +280,15 @@ def ef_topk_quant_buckets(ctx, grad, err, bits, group, rounding, seed, step, idx
                                         _rounding(rounding), seed, step, _ptr(idx_out),
                                         _ptr(codes_out), _ptr(scales_out)),
            "gc_ef_topk_quant_buckets")
+
+
+def topk_aggregate(ctx, W, k, idx, val, n, out):
+    """gc_topk_aggregate: out[n] = rank-ordered sum of W ranks' (idx, val)."""
+    _check(lib.gc_topk_aggregate(ctx.handle, W, k, _ptr(idx), _ptr(val), n, _ptr(out)),
+           "gc_topk_aggregate")
+
+
+def topk_quant_aggregate(ctx, W, k, idx, codes, scales, bits, group, n, out):
+    """gc_topk_quant_aggregate: the same with QSGD-coded values per rank."""
+    _check(lib.gc_topk_quant_aggregate(ctx.handle, W, k, _ptr(idx), _ptr(codes), _ptr(scales),
+                                       bits, group, n, _ptr(out)), "gc_topk_quant_aggregate")

@@ -147,7 +147,9 @@ typedef enum gc_phase {
   GC_PHASE_BK_REFINE = 15,   /* bucketed: exact thresholds, segment offsets */
   GC_PHASE_BK_WRITE = 16,    /* bucketed: ordered compaction */
   GC_PHASE_BK_QUANT = 17,    /* bucketed: QSGD of the kept values */
-  GC_PHASE_COUNT = 18
+  GC_PHASE_AGG_BOUNDS = 18,  /* aggregation: each rank's entries per output range */
+  GC_PHASE_AGG_ACCUMULATE = 19, /* aggregation: rank-ordered sum into the dense output */
+  GC_PHASE_COUNT = 20
 } gc_phase;
 
 /* Name of a phase ("ef_hist", ...); "?" when out of range. */
@@ -281,6 +283,39 @@ GC_API gc_status gc_ef_topk_quant(gc_ctx* ctx, const float* grad, float* err,
 GC_API gc_status gc_powersgd_step(gc_ctx* ctx, const float* grad, float* err,
                            int64_t m, int64_t n, int r, float* P_out,
                            float* Q_inout);
+
+/*
+ * Aggregation of several ranks' compressed gradients.
+ * Page: "分布式训练中的梯度压缩算法" 四 (gradient compression with All-Reduce:
+ * every worker compresses its local gradient, the compressed gradients are
+ * aggregated and decompressed, every worker applies the result).  With
+ * Top-K each rank keeps its own positions (and, quantised, its own scales),
+ * so the aggregate is the sum of the ranks' decompressed sparse vectors:
+ *   out[i] = 0;  for w = 0 .. W-1 in order:  out[idx_w[j]] += v_w[j]
+ * one binary32 addition per present entry (deterministic).
+ * idx: int32[W*K] with K = k rounded up to a multiple of 4: rank w's k
+ * indices at idx + w*K (16-byte aligned, as gc_ef_topk writes them),
+ * strictly increasing in [0, n) (a violation sets the device status:
+ * GC_ERR_DEVICE_CHECK from gc_ctx_check, with the offending entries left
+ * out).  val: fp32[W*K], laid out the same way.  out: fp32[n], fully
+ * written.  1 <= W <= 1024;
+ * 0 <= k <= n <= 2^31 - 1.  Scratch: W * (ceil(n / 8192) + 1) int32 of the
+ * context's Top-K scratch, i.e. at most 2 * max_n (GC_ERR_WORKSPACE).
+ */
+GC_API gc_status gc_topk_aggregate(gc_ctx* ctx, int W, int64_t k, const int32_t* idx,
+                                   const float* val, int64_t n, float* out);
+
+/*
+ * The same for the hybrid's output: rank w's values are its QSGD codes
+ * decompressed, v_w[j] = +-fl(q * scale) (gc_dequant), with rank w's codes
+ * at codes + w * gc_codes_bytes(k, bits, GC_QSGD) and its scales at
+ * scales + w * S, S = gc_scales_floats(k, group, GC_QSGD) rounded up to a
+ * multiple of 4 (so every rank's scales start on a 16-byte boundary and
+ * gc_ef_topk_quant can write them in place).
+ */
+GC_API gc_status gc_topk_quant_aggregate(gc_ctx* ctx, int W, int64_t k, const int32_t* idx,
+                                         const uint8_t* codes, const float* scales, int bits,
+                                         int64_t group, int64_t n, float* out);
 
 /*
  * Bucketed calls.

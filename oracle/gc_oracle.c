@@ -553,13 +553,17 @@ int orc_ef_topk_quant(const float* grad, float* err, int64_t n, int64_t k,
  * the ranks' decompressed sparse vectors.  Reading: the ranks are added in
  * rank order, one binary32 addition per present entry:
  *   out[i] = 0;  for w = 0 .. W-1:  out[idx_w[j]] += v_w[j]  (j ascending)
- * Inputs follow the compressor's output: rank w's k indices idx[w*k ..]
- * strictly increasing in [0, n) (ORC_EINVAL otherwise).
+ * Inputs follow the compressor's output: rank w's k indices at
+ * idx[w*K ..], K = k rounded up to a multiple of 4 (every rank's entries
+ * start on a 16-byte boundary), strictly increasing in [0, n) (ORC_EINVAL
+ * otherwise); values at the same positions.
  */
+static int64_t rank_stride(int64_t k) { return (k + 3) / 4 * 4; }
+
 static int check_aggregate_idx(int W, int64_t k, const int32_t* idx, int64_t n) {
   if (W < 1 || k < 0 || n < 0 || k > n) return ORC_EINVAL;
   for (int w = 0; w < W; ++w) {
-    const int32_t* iw = idx + (int64_t)w * k;
+    const int32_t* iw = idx + (int64_t)w * rank_stride(k);
     for (int64_t j = 0; j < k; ++j) {
       if (iw[j] < 0 || (int64_t)iw[j] >= n) return ORC_EINVAL;
       if (j > 0 && iw[j] <= iw[j - 1]) return ORC_EINVAL;
@@ -568,7 +572,7 @@ static int check_aggregate_idx(int W, int64_t k, const int32_t* idx, int64_t n) 
   return ORC_OK;
 }
 
-/* Rank w's values are val[w*k .. w*k + k). */
+/* Rank w's values are val[w*K .. w*K + k). */
 int orc_topk_aggregate(int W, int64_t k, const int32_t* idx, const float* val, int64_t n,
                        float* out) {
   int st = check_aggregate_idx(W, k, idx, n);
@@ -576,7 +580,7 @@ int orc_topk_aggregate(int W, int64_t k, const int32_t* idx, const float* val, i
   for (int64_t i = 0; i < n; ++i) out[i] = 0.0f;
   for (int w = 0; w < W; ++w)
     for (int64_t j = 0; j < k; ++j) {
-      int64_t at = (int64_t)w * k + j;
+      int64_t at = (int64_t)w * rank_stride(k) + j;
       out[idx[at]] = out[idx[at]] + val[at];
     }
   return ORC_OK;
@@ -586,7 +590,9 @@ int orc_topk_aggregate(int W, int64_t k, const int32_t* idx, const float* val, i
  * QSGD-compressed ranks (the hybrid's output): rank w's values are
  * dequant(codes_w, scales_w, k, bits, group, QSGD) with codes_w at
  * codes + w * orc_codes_bytes(k, bits, QSGD) and scales_w at
- * scales + w * orc_scales_floats(k, group, QSGD).
+ * scales + w * S, S = orc_scales_floats(k, group, QSGD) rounded up to a
+ * multiple of 4 (each rank's scales start on a 16-byte boundary, as the
+ * compressor writes them).
  */
 int orc_topk_quant_aggregate(int W, int64_t k, const int32_t* idx, const uint8_t* codes,
                              const float* scales, int bits, int64_t group, int64_t n,
@@ -596,14 +602,14 @@ int orc_topk_quant_aggregate(int W, int64_t k, const int32_t* idx, const uint8_t
   st = check_quant_args(k, bits, group, ORC_QSGD, ORC_NEAREST_EVEN);
   if (st != ORC_OK) return st;
   int64_t cb = orc_codes_bytes(k, bits, ORC_QSGD);
-  int64_t sf = orc_scales_floats(k, group, ORC_QSGD);
+  int64_t sf = (orc_scales_floats(k, group, ORC_QSGD) + 3) / 4 * 4;
   float* val = (float*)malloc((size_t)(k > 0 ? k : 1) * sizeof(float));
   if (!val) return ORC_ENOMEM;
   for (int64_t i = 0; i < n; ++i) out[i] = 0.0f;
   for (int w = 0; w < W && st == ORC_OK; ++w) {
     st = orc_dequant(codes + (int64_t)w * cb, scales + (int64_t)w * sf, k, bits, group,
                      ORC_QSGD, val);
-    const int32_t* iw = idx + (int64_t)w * k;
+    const int32_t* iw = idx + (int64_t)w * rank_stride(k);
     for (int64_t j = 0; st == ORC_OK && j < k; ++j) out[iw[j]] = out[iw[j]] + val[j];
   }
   free(val);

@@ -220,21 +220,22 @@ def ef_topk_quant(grad, err, k, bits, group, rounding="nearest_even", seed=0,
     return idx[:k], codes[:cb], scales[:sf], e
 
 
-def _aggregate_idx(idx, W, k):
-    ix = np.ascontiguousarray(idx, dtype=np.int32).reshape(-1)
-    if ix.size != W * k:
-        raise OracleError("idx must hold W * k indices")
-    return ix if ix.size else np.zeros(1, np.int32)
+def _rank_rows(a, W, k, dtype):
+    """(W, k) per-rank rows in the layout the aggregation takes: rank w at
+    w * K, K = k rounded up to a multiple of 4 (the padding is zero)."""
+    a = np.asarray(a, dtype=dtype).reshape(W, k)
+    K = -(-k // 4) * 4
+    out = np.zeros((W, K), dtype=dtype)
+    out[:, :k] = a
+    out = out.reshape(-1)
+    return out if out.size else np.zeros(1, dtype)
 
 
 def topk_aggregate(idx, val, W, k, n):
-    """Sum of W ranks' sparse vectors in rank order.  idx, val: W * k
-    entries, rank w's at [w*k, (w+1)*k).  Returns float32[n]."""
-    ix = _aggregate_idx(idx, W, k)
-    v = np.ascontiguousarray(val, dtype=np.float32).reshape(-1)
-    if v.size != W * k:
-        raise OracleError("val must hold W * k values")
-    v = v if v.size else np.zeros(1, np.float32)
+    """Sum of W ranks' sparse vectors in rank order.  idx, val: (W, k)
+    per-rank rows (any shape of W * k entries).  Returns float32[n]."""
+    ix = _rank_rows(idx, W, k, np.int32)
+    v = _rank_rows(val, W, k, np.float32)
     out = np.zeros(max(n, 1), dtype=np.float32)
     _check(lib().orc_topk_aggregate(W, k, _p(ix, _i32p), _p(v, _f32p), n, _p(out, _f32p)),
            "orc_topk_aggregate")
@@ -242,12 +243,14 @@ def topk_aggregate(idx, val, W, k, n):
 
 
 def topk_quant_aggregate(idx, codes, scales, W, k, bits, group, n):
-    """Sum of W ranks' QSGD-compressed sparse vectors in rank order; rank w's
-    codes and scales at w * codes_bytes(k) and w * scales_floats(k)."""
-    ix = _aggregate_idx(idx, W, k)
+    """Sum of W ranks' QSGD-compressed sparse vectors in rank order; idx as
+    (W, k) rows, rank w's codes at w * codes_bytes(k), its scales at
+    w * (scales_floats(k) rounded up to a multiple of 4)."""
+    ix = _rank_rows(idx, W, k, np.int32)
     c = np.ascontiguousarray(codes, dtype=np.uint8).reshape(-1)
     s = np.ascontiguousarray(scales, dtype=np.float32).reshape(-1)
-    if c.size != W * codes_bytes(k, bits, QSGD) or s.size != W * scales_floats(k, group, QSGD):
+    sf = -(-scales_floats(k, group, QSGD) // 4) * 4
+    if c.size != W * codes_bytes(k, bits, QSGD) or s.size != W * sf:
         raise OracleError("codes / scales do not hold W ranks")
     c = c if c.size else np.zeros(1, np.uint8)
     s = s if s.size else np.zeros(1, np.float32)

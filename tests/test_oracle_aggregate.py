@@ -43,9 +43,9 @@ def test_quant_hand_case(golden_dir):
         W, k, n, bits, group = case["W"], case["k"], case["n"], case["bits"], case["group"]
         codes = np.concatenate([_pack(c, s, bits, k) for c, s in zip(case["codes"], case["signs"])])
         assert codes.size == W * oracle.codes_bytes(k, bits, "qsgd")
-        out = oracle.topk_quant_aggregate(np.array(case["idx"], np.int32), codes,
-                                          np.array(case["scales"], np.float32), W, k, bits,
-                                          group, n)
+        scales = np.array([sc + [0.0] * (-len(sc) % 4) for sc in case["scales"]], np.float32)
+        out = oracle.topk_quant_aggregate(np.array(case["idx"], np.int32), codes, scales, W, k,
+                                          bits, group, n)
         assert out.tolist() == case["out"], case["name"]
 
 
@@ -81,7 +81,7 @@ def test_quant_equals_numpy_decode_then_scatter(bits, group):
     q = r.integers(0, top + 1, size=(W, k))
     sg = (r.random((W, k)) < 0.5) & (q != 0)
     ng = -(-k // group)
-    scales = (r.random((W, ng)) + 0.1).astype(np.float32)
+    scales = (r.random((W, -(-ng // 4) * 4)) + 0.1).astype(np.float32)  # 16-byte rank stride
     codes = np.concatenate([_pack(q[w], sg[w], bits, k) for w in range(W)])
     vals = np.zeros((W, k), np.float32)
     for w in range(W):
