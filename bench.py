@@ -63,12 +63,13 @@ def parse_args():
     p.add_argument("--elems", type=int, default=None,
                    help="gradient elements (default: the workload's own size; for buckets a "
                         "smaller value cuts the same 25 MiB buckets from a shorter gradient)")
-    p.add_argument("--workload", choices=["buckets", "quant", "tern", "powersgd"],
+    p.add_argument("--workload", choices=["buckets", "quant", "tern", "powersgd", "aggregate"],
                    default="buckets",
                    help="buckets: EF + Top-K + QSGD per 25 MiB bucket (the headline); quant: "
                         "EF + group quantisation of 2^30 elements; tern: EF + TernGrad per "
                         "tensor of one transformer layer; powersgd: rank-4 PowerSGD on one "
-                        "layer's matrix shapes")
+                        "layer's matrix shapes; aggregate: 8 ranks' Top-K + QSGD outputs summed "
+                        "into one dense gradient")
     p.add_argument("--mode", choices=["minmax", "qsgd"], default="qsgd",
                    help="quant workload: quantisation rule")
     p.add_argument("--bits", type=int, default=8, help="quant workload: bits per code")
@@ -485,7 +486,81 @@ class PowerSGDWorkload(_SimpleWorkload):
                 "psgd_resid": 8.0 * self.n / k}
 
 
-WORKLOADS = {"quant": QuantWorkload, "tern": TernWorkload, "powersgd": PowerSGDWorkload}
+class AggregateWorkload(_SimpleWorkload):
+    """The step after compression: W = 8 simulated ranks' Top-K 1 % + 8-bit
+    QSGD outputs (groups of 64) over the 134,217,728-element gradient,
+    aggregated into one dense fp32 gradient in rank order by one
+    gc_topk_quant_aggregate call.  Each rank's outputs come from the hybrid
+    compressor on its own Student-t gradient; all of a step's compressed
+    inputs sit in one byte buffer (indices, codes, scales)."""
+
+    W, BITS, GROUP = 8, 8, 64
+
+    def __init__(self, torch, gc, dev, args, seed):
+        self.n = args.elems
+        n, W = self.n, self.W
+        self.k = k = inputs.ratio_k(n, 1, 100)
+        K = -(-k // 4) * 4
+        self.cb = gc.codes_bytes(k, self.BITS, "qsgd")
+        self.sf = -(-gc.scales_floats(k, self.GROUP, "qsgd") // 4) * 4
+        self._init_common(torch, gc, dev, n)
+        # byte offsets of the three arrays inside one step's input buffer
+        self.o_idx, self.o_codes = 0, 4 * W * K
+        self.o_scales = self.o_codes + -(-(W * self.cb) // 16) * 16
+        total = self.o_scales + 4 * W * self.sf
+        self.grads = []
+        ctx = self.ctxs[0]
+        e = torch.zeros(n, dtype=torch.float32, device=dev)
+        for d in range(args.distinct):
+            buf = torch.zeros(total, dtype=torch.uint8, device=dev)
+            idx, codes, scales = self._views(buf)
+            for w in range(W):
+                g = inputs.student_t_device(n, dev, seed=seed * 100 + d * W + w)
+                e.zero_()
+                gc.ef_topk_quant(ctx, g, e, k, self.BITS, self.GROUP, "stochastic", 5 + w, d,
+                                 idx[w * K:w * K + k], codes[w * self.cb:(w + 1) * self.cb],
+                                 scales[w * self.sf:w * self.sf +
+                                        gc.scales_floats(k, self.GROUP, "qsgd")])
+            self.grads.append(buf)
+        ctx.check()
+        del e
+        self.out = torch.empty(n, dtype=torch.float32, device=dev)
+
+    def _views(self, buf):
+        W, K = self.W, -(-self.k // 4) * 4
+        idx = buf[self.o_idx:self.o_idx + 4 * W * K].view(self.torch.int32)
+        codes = buf[self.o_codes:self.o_codes + W * self.cb]
+        scales = buf[self.o_scales:self.o_scales + 4 * W * self.sf].view(self.torch.float32)
+        return idx, codes, scales
+
+    def outputs(self):
+        return [self.out]
+
+    def launch_step(self, t, grad=None, main=None, ctxs=None):
+        main = self.main if main is None else main
+        ctx = self._ctx_on(main, ctxs)
+        buf = self.grads[t % len(self.grads)] if grad is None else grad
+        idx, codes, scales = self._views(buf)
+        self.gc.topk_quant_aggregate(ctx, self.W, self.k, idx, codes, scales, self.BITS,
+                                     self.GROUP, self.n, self.out)
+
+    def input_bytes(self):
+        return self.grads[0].numel()
+
+    def algorithmic_bytes(self):
+        """Write the dense gradient (4 B per element) and read every rank's
+        indices, codes, signs and scales once."""
+        return 4 * self.n + self.W * (4 * self.k + self.cb + 4 * self.sf)
+
+    def algorithmic_bytes_per_launch(self):
+        """bounds reads the indices (4 B per entry); accumulate reads indices,
+        codes and scales and writes the dense output."""
+        return {"agg_bounds": 4.0 * self.W * self.k,
+                "agg_accumulate": float(self.algorithmic_bytes())}
+
+
+WORKLOADS = {"quant": QuantWorkload, "tern": TernWorkload, "powersgd": PowerSGDWorkload,
+             "aggregate": AggregateWorkload}
 
 
 def kernel_timing(wl, steps, warmup_step):
@@ -519,6 +594,22 @@ def cpu_sample(args, seed=7):
         e = np.zeros_like(g)
         return (lambda: oracle.ef_quant(g, e, 2, 0, "tern", "stochastic", 91, 0), g.size,
                 "one 4096 x 4096 tensor of the layer, EF + TernGrad per tensor")
+    if args.workload == "aggregate":
+        n, W = 1 << 22, 8
+        k = inputs.ratio_k(n, 1, 100)
+        idx, codes, scales = [], [], []
+        for w in range(W):
+            g = inputs.student_t(inputs.rng(seed + w), n)
+            i_, c_, s_, _ = oracle.ef_topk_quant(g, np.zeros(n, np.float32), k, 8, 64,
+                                                 "stochastic", 5 + w, 0)
+            idx.append(i_)
+            codes.append(c_)
+            s4 = np.zeros(-(-s_.size // 4) * 4, np.float32)
+            s4[:s_.size] = s_
+            scales.append(s4)
+        idx, codes, scales = np.stack(idx), np.concatenate(codes), np.concatenate(scales)
+        return (lambda: oracle.topk_quant_aggregate(idx, codes, scales, W, k, 8, 64, n), n,
+                "8 ranks' Top-K 1%% + 8-bit QSGD outputs over 4,194,304 elements, aggregated")
     if args.workload == "powersgd":
         M, Q0 = inputs.low_rank_matrix(4096, 4096, seed=seed, r=4)
         E = np.zeros_like(M)
@@ -563,6 +654,11 @@ def config(args, wl=None):
                            "11008, 11008 x 4096, 4096; N(0, (1e-3/sqrt(fan_in))^2)), EF + "
                            "TernGrad per tensor (scale = max|c| of the tensor), stochastic",
                "total_elems": n, "tensors": len(inputs.TRANSFORMER_SHAPES)}
+    elif args.workload == "aggregate":
+        cfg = {"workload": "8 simulated ranks' Top-K 1% + 8-bit QSGD (groups of 64) outputs over "
+                           "a {:,}-element Student-t gradient, summed in rank order into one "
+                           "dense fp32 gradient".format(n),
+               "total_elems": n, "ranks": 8, "topk_percent": 1, "quant": "qsgd 8-bit g64"}
     elif args.workload == "powersgd":
         n = sum(m * n_ for m, n_ in inputs.POWERSGD_SHAPES)
         cfg = {"workload": "one transformer layer's matrix shapes (4096 x 4096, 4096 x 11008, "
@@ -747,8 +843,9 @@ def main():
                 h_.copy_(t_.view(-1), non_blocking=True)
 
         e_ms = timed(e2e_step, e2e_steps, side_streams=(copy_s,))
+        h2d = wl.input_bytes() if hasattr(wl, "input_bytes") else 4 * wl.n
         e2e = {"value": world * 4.0 * wl.n / (e_ms * 1e-3) / 1e9, "unit": UNIT,
-               "h2d_bytes_per_step": 4 * wl.n, "d2h_bytes_per_step": wl.out_bytes(),
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": wl.out_bytes(),
                "ms_per_step": e_ms, "launch": launch_mode}
         wl.check()
 

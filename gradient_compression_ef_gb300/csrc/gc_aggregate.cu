@@ -11,8 +11,8 @@
 // Rank w's indices are strictly increasing, so no two of its entries touch
 // the same element and the rank order is the only order that matters.  The
 // output is cut into ranges of kAggRange elements, one block each:
-//   bounds     : for every rank, the first entry of each range (one thread
-//                per entry boundary; each range is written exactly once).
+//   bounds     : for every rank, the first entry of each range (four entry
+//                boundaries per thread; each range is written exactly once).
 //   accumulate : a block gathers the entries of its range, rank by rank, in
 //                chunks into shared memory (all loads of a chunk in flight at
 //                once), adds them to its shared accumulator in rank order
@@ -26,8 +26,9 @@ namespace {
 
 constexpr int kAggShift = 13;
 constexpr int kAggRange = 1 << kAggShift;   // output elements per block
-constexpr int kAggThreads = 512;
-constexpr int kAggSlots = 4096;             // gathered entries per chunk
+constexpr int kAggThreads = 256;
+constexpr int kAggSlots = 2048;             // gathered entries per chunk
+constexpr int kAggGather = 4;               // entries per thread per gathering round
 constexpr int kAggMaxRanks = 1024;
 
 // Per-rank stride of the index and value arrays: k rounded up to 4 entries,
@@ -35,41 +36,68 @@ constexpr int kAggMaxRanks = 1024;
 __host__ __device__ __forceinline__ int64_t round_up4(int64_t k) { return (k + 3) / 4 * 4; }
 
 // start[w * (nblk + 1) + b] = first entry of rank w whose index is in range
-// b or later (k when none).
-__global__ void agg_bounds_kernel(const int32_t* __restrict__ idx, int W, int64_t k, int64_t n,
-                                  int64_t nblk, int32_t* __restrict__ start,
-                                  uint32_t* __restrict__ status) {
-  const int64_t per = k + 1;  // boundary positions j = 0 .. k of one rank
-  const int64_t total = (int64_t)W * per;
-  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
-       t += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t w = t / per, j = t - w * per;
-    const int32_t* iw = idx + w * round_up4(k);
-    auto blk = [&](int64_t jj) -> int64_t {
-      const int64_t v = iw[jj];
-      if (v < 0 || v >= n) {
-        atomicOr(status, kStatusScatterIndex);
-        return v < 0 ? 0 : nblk - 1;
-      }
-      return v >> kAggShift;
-    };
-    int64_t lo = j == 0 ? 0 : blk(j - 1) + 1;
-    int64_t hi = j == k ? nblk : blk(j);
-    if (j > 0 && j < k && iw[j] <= iw[j - 1]) atomicOr(status, kStatusScatterIndex);
-    lo = std::min<int64_t>(std::max<int64_t>(lo, 0), nblk);
-    hi = std::min<int64_t>(hi, nblk);
-    int32_t* sw = start + w * (nblk + 1);
-    for (int64_t b = lo; b <= hi; ++b) sw[b] = (int32_t)j;
+// b or later (k when none).  Boundary position j (0 .. k) of rank w owns the
+// ranges (range(idx[j-1]), range(idx[j])], so every range is written by
+// exactly one position.
+constexpr int kBoundsPer = 16;  // boundary positions per thread (four 16-byte loads)
+
+__global__ void __launch_bounds__(256) agg_bounds_kernel(const int32_t* __restrict__ idx, int W,
+                                                         int64_t k, int64_t n, int64_t nblk,
+                                                         int32_t* __restrict__ start,
+                                                         uint32_t* __restrict__ status) {
+  // rank w = blockIdx.y; positions 0 .. k fit 32 bits
+  const int32_t j0 = (int32_t)(blockIdx.x * blockDim.x + threadIdx.x) * kBoundsPer;
+  if ((int64_t)j0 > k) return;
+  const int64_t w = blockIdx.y;
+  const int32_t* iw = idx + w * round_up4(k);
+  int32_t* sw = start + w * (nblk + 1);
+  // indices of positions j0 - 1 .. j0 + 15, all loads issued first
+  int32_t v[kBoundsPer + 1];
+  v[0] = j0 > 0 ? iw[j0 - 1] : 0;
+#pragma unroll
+  for (int q = 0; q < kBoundsPer / 4; ++q) {
+    const int64_t jq = j0 + 4 * q;
+    if (jq + 3 < k) {
+      const int4 x = *reinterpret_cast<const int4*>(iw + jq);
+      v[4 * q + 1] = x.x; v[4 * q + 2] = x.y; v[4 * q + 3] = x.z; v[4 * q + 4] = x.w;
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[4 * q + 1 + u] = jq + u < k ? iw[jq + u] : 0;
+    }
+  }
+  auto range_of = [&](int32_t x) -> int64_t {
+    if (x < 0 || (int64_t)x >= n) {
+      atomicOr(status, kStatusScatterIndex);
+      return x < 0 ? 0 : nblk - 1;
+    }
+    return (int64_t)x >> kAggShift;
+  };
+  const int32_t nb = (int32_t)nblk, kk = (int32_t)k;  // ranges < 2^18, k < 2^31
+  int32_t prev = j0 > 0 ? (int32_t)range_of(v[0]) : -1;
+#pragma unroll
+  for (int u = 1; u <= kBoundsPer; ++u) {
+    const int32_t j = j0 + u - 1;
+    if (j > kk) break;
+    const int32_t cur = j < kk ? (int32_t)range_of(v[u]) : nb;
+    if (j > 0 && j < kk && v[u] <= v[u - 1]) atomicOr(status, kStatusScatterIndex);
+    const int32_t hi = min(cur, nb);
+    for (int32_t b = max(prev + 1, 0); b <= hi; ++b) sw[b] = j;
+    prev = cur;
   }
 }
 
+// Shared memory of a block: the accumulator of its range, one gathered
+// chunk, and two int32[W + 1] arrays sized by the launch (rank w's entries of
+// this range are [first[w], first[w] + pre[w+1] - pre[w])).
 struct AggSmem {
   float acc[kAggRange];
   float val[kAggSlots];
   uint16_t loc[kAggSlots];
-  int32_t first[kAggMaxRanks + 1];  // rank w's entries of this range: [first, first + cnt)
-  int32_t pre[kAggMaxRanks + 1];    // exclusive prefix of the counts
 };
+
+__host__ __device__ inline size_t agg_smem_bytes(int W) {
+  return sizeof(AggSmem) + 2 * sizeof(int32_t) * (size_t)(W + 1);
+}
 
 // Value of entry j of rank w: val[w*K + j] (K = k rounded up to 4), or for QSGD codes
 // +-fl(q * scale) with rank w's codes at w * cb and scales at w * sf (sf a
@@ -97,6 +125,8 @@ __global__ void __launch_bounds__(kAggThreads) agg_accumulate_kernel(
     const int32_t* __restrict__ start, float* __restrict__ out, uint32_t* __restrict__ status) {
   extern __shared__ __align__(16) unsigned char agg_smem_raw[];
   AggSmem& sm = *reinterpret_cast<AggSmem*>(agg_smem_raw);
+  int32_t* first = reinterpret_cast<int32_t*>(agg_smem_raw + sizeof(AggSmem));
+  int32_t* pre = first + (W + 1);
   const int64_t b = blockIdx.x;
   const int64_t a = b << kAggShift;
   const int len = (int)std::min<int64_t>(kAggRange, n - a);
@@ -106,47 +136,69 @@ __global__ void __launch_bounds__(kAggThreads) agg_accumulate_kernel(
     const int32_t* sw = start + (int64_t)w * (nblk + 1);
     const int64_t f = std::min<int64_t>(std::max<int32_t>(sw[b], 0), k);
     const int64_t l = std::min<int64_t>(std::max<int32_t>(sw[b + 1], 0), k);
-    sm.first[w] = (int32_t)f;
+    first[w] = (int32_t)f;
     // a range holds at most kAggRange entries of one rank (distinct indices)
-    sm.pre[w] = (int32_t)std::min<int64_t>(l > f ? l - f : 0, kAggRange);  // scanned below
+    pre[w] = (int32_t)std::min<int64_t>(l > f ? l - f : 0, kAggRange);  // scanned below
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     int32_t run = 0;
     for (int w = 0; w < W; ++w) {
-      const int32_t c = sm.pre[w];
-      sm.pre[w] = run;
+      const int32_t c = pre[w];
+      pre[w] = run;
       run += c;
     }
-    sm.pre[W] = run;
+    pre[W] = run;
   }
   __syncthreads();
-  const int32_t total = sm.pre[W];
+  const int32_t total = pre[W];
   // chunks of the block's entries in rank-major order
   for (int32_t c0 = 0; c0 < total; c0 += kAggSlots) {
     const int32_t c1 = min(c0 + kAggSlots, total);
-    for (int32_t e = c0 + threadIdx.x; e < c1; e += kAggThreads) {
-      int w = 0;  // rank of flat entry e: the last w with pre[w] <= e
-      int lo = 0, hi = W - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (sm.pre[mid] <= e) lo = mid;
-        else hi = mid - 1;
+    for (int32_t e0 = c0 + threadIdx.x; e0 < c1; e0 += kAggThreads * kAggGather) {
+      // rank and entry of each of this thread's flat entries, then all their
+      // global loads, then the shared-memory stores
+      int wq[kAggGather];
+      int64_t jq[kAggGather];
+#pragma unroll
+      for (int u = 0; u < kAggGather; ++u) {
+        const int32_t e = e0 + u * kAggThreads;
+        int lo = 0, hi = W - 1;  // the last rank w with pre[w] <= e
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (pre[mid] <= e) lo = mid;
+          else hi = mid - 1;
+        }
+        wq[u] = lo;
+        jq[u] = (int64_t)first[lo] + (e - pre[lo]);
       }
-      w = lo;
-      const int64_t j = (int64_t)sm.first[w] + (e - sm.pre[w]);
-      const int64_t i = (int64_t)idx[(int64_t)w * round_up4(k) + j] - a;
-      const bool ok = i >= 0 && i < len;
-      if (!ok) atomicOr(status, kStatusScatterIndex);
-      sm.loc[e - c0] = ok ? (uint16_t)i : (uint16_t)0xffffu;
-      sm.val[e - c0] = agg_value<BITS>(val, codes, scales, k, cb, mag, sf, G, w, j);
+      int32_t iq[kAggGather];
+      float vq[kAggGather];
+#pragma unroll
+      for (int u = 0; u < kAggGather; ++u) {
+        if (e0 + u * kAggThreads < c1) {
+          iq[u] = idx[(int64_t)wq[u] * round_up4(k) + jq[u]];
+          vq[u] = agg_value<BITS>(val, codes, scales, k, cb, mag, sf, G, wq[u], jq[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kAggGather; ++u) {
+        const int32_t e = e0 + u * kAggThreads;
+        if (e < c1) {
+          const int64_t i = (int64_t)iq[u] - a;
+          const bool ok = i >= 0 && i < len;
+          if (!ok) atomicOr(status, kStatusScatterIndex);
+          sm.loc[e - c0] = ok ? (uint16_t)i : (uint16_t)0xffffu;
+          sm.val[e - c0] = vq[u];
+        }
+      }
     }
     __syncthreads();
     // rank by rank: within a rank the locations are distinct
     int w0 = 0;
-    while (w0 < W && sm.pre[w0 + 1] <= c0) ++w0;
-    for (int w = w0; w < W && sm.pre[w] < c1; ++w) {
-      const int32_t e0 = max(sm.pre[w], c0), e1 = min(sm.pre[w + 1], c1);
+    while (w0 < W && pre[w0 + 1] <= c0) ++w0;
+    for (int w = w0; w < W && pre[w] < c1; ++w) {
+      const int32_t e0 = max(pre[w], c0), e1 = min(pre[w + 1], c1);
       for (int32_t e = e0 + threadIdx.x; e < e1; e += kAggThreads) {
         const uint16_t l = sm.loc[e - c0];
         if (l != 0xffffu) sm.acc[l] = __fadd_rn(sm.acc[l], sm.val[e - c0]);
@@ -170,7 +222,7 @@ gc_status run_accumulate(gc_ctx* ctx, const int32_t* idx, const float* val, cons
                          int64_t sf, int64_t G, int64_t n, int64_t nblk, const int32_t* start,
                          float* out) {
   LaunchScope L(ctx, GC_PHASE_AGG_ACCUMULATE);
-  agg_accumulate_kernel<BITS><<<(unsigned)nblk, kAggThreads, sizeof(AggSmem), ctx->stream>>>(
+  agg_accumulate_kernel<BITS><<<(unsigned)nblk, kAggThreads, agg_smem_bytes(W), ctx->stream>>>(
       idx, val, codes, scales, W, k, cb, mag, sf, G, n, nblk, start, out, ctx->ws.status);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
@@ -178,7 +230,7 @@ gc_status run_accumulate(gc_ctx* ctx, const int32_t* idx, const float* val, cons
 }  // namespace
 
 gc_status prepare_aggregate_kernels() {
-  const int bytes = (int)sizeof(AggSmem);
+  const int bytes = (int)agg_smem_bytes(kAggMaxRanks);
   const bool ok =
       cudaFuncSetAttribute(agg_accumulate_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
       cudaFuncSetAttribute(agg_accumulate_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
@@ -202,10 +254,9 @@ gc_status launch_aggregate(gc_ctx* ctx, int W, int64_t k, const int32_t* idx, co
   int32_t* start = reinterpret_cast<int32_t*>(ctx->ws.cand);
   {
     LaunchScope L(ctx, GC_PHASE_AGG_BOUNDS);
-    const int64_t total = (int64_t)W * (k + 1);
-    const int grid = (int)std::max<int64_t>(
-        1, std::min<int64_t>(ceil_div(total, 256), (int64_t)ctx->num_sms * 8));
-    agg_bounds_kernel<<<grid, 256, 0, ctx->stream>>>(idx, W, k, n, nblk, start, ctx->ws.status);
+    const dim3 grid((unsigned)ceil_div(ceil_div(k + 1, kBoundsPer), 256), (unsigned)W);
+    agg_bounds_kernel<<<grid, 256, 0, ctx->stream>>>(idx, W, k, n, nblk, start,
+                                                      ctx->ws.status);
   }
   if (cudaGetLastError() != cudaSuccess) return GC_ERR_CUDA;
   if (bits == 0)
