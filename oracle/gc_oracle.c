@@ -542,6 +542,44 @@ int orc_ef_topk_quant(const float* grad, float* err, int64_t n, int64_t k,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Random sparsification with error feedback.                                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [P2 二.2 随机稀疏化]: every element is kept with probability p (the page's
+ * mask = rand(n) < p); [P1 2.2]: random sparsification keeps the traffic
+ * steady.  With error feedback ([P4 梯度压缩原理]) the unsent entries stay in
+ * the residual, as for Top-K:
+ *   c = g + e;  keep i when u_i < p, u_i = orc_uniform(seed, step, i)
+ *   (reading: the same Philox-4x32-10 draw as stochastic rounding);
+ *   emit (i, c_i) of the kept entries in ascending index order;
+ *   e'_i = +0 when kept, c_i otherwise.
+ * At most `capacity` entries are written; *count receives how many were kept
+ * (ORC_EINVAL when that exceeds the capacity, the first `capacity` written).
+ * err == NULL selects from grad alone and writes no residual.
+ */
+int orc_ef_randk(const float* grad, float* err, int64_t n, float p, uint64_t seed,
+                 uint64_t step, int32_t* idx_out, float* val_out, int64_t capacity,
+                 int64_t* count) {
+  if (n < 0 || n > INT32_MAX || capacity < 0 || !count) return ORC_EINVAL;
+  int64_t kept = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    float c = err ? grad[i] + err[i] : grad[i];
+    int keep = orc_uniform(seed, step, (uint64_t)i) < p;
+    if (keep) {
+      if (kept < capacity) {
+        idx_out[kept] = (int32_t)i;
+        val_out[kept] = c;
+      }
+      ++kept;
+    }
+    if (err) err[i] = keep ? 0.0f : c;
+  }
+  *count = kept;
+  return kept <= capacity ? ORC_OK : ORC_EINVAL;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Aggregation of several ranks' compressed gradients.                       */
 /* ------------------------------------------------------------------------ */
 

@@ -70,6 +70,9 @@ def lib():
         L.orc_powersgd_step.argtypes = [_f32p, _f32p, _i64, _i64, _int, _f32p,
                                         _f32p]
         L.orc_powersgd_step.restype = _int
+        L.orc_ef_randk.argtypes = [_f32p, _f32p, _i64, ctypes.c_float, _u64, _u64, _i32p,
+                                   _f32p, _i64, ctypes.POINTER(_i64)]
+        L.orc_ef_randk.restype = _int
         L.orc_topk_aggregate.argtypes = [_int, _i64, _i32p, _f32p, _i64, _f32p]
         L.orc_topk_aggregate.restype = _int
         L.orc_topk_quant_aggregate.argtypes = [_int, _i64, _i32p, _u8p, _f32p, _int, _i64,
@@ -218,6 +221,22 @@ def ef_topk_quant(grad, err, k, bits, group, rounding="nearest_even", seed=0,
                                    _p(idx, _i32p), _p(codes, _u8p),
                                    _p(scales, _f32p)), "orc_ef_topk_quant")
     return idx[:k], codes[:cb], scales[:sf], e
+
+
+def ef_randk(grad, err, p, seed=0, step=0):
+    """EF + random sparsification: keep i when uniform(seed, step, i) < p.
+    Returns (idx int32[kept], val float32[kept], err' or None)."""
+    g = _f32(grad)
+    n = g.size
+    e = _f32(err) if err is not None else None
+    idx = np.zeros(max(n, 1), dtype=np.int32)
+    val = np.zeros(max(n, 1), dtype=np.float32)
+    count = _i64(0)
+    _check(lib().orc_ef_randk(_p(g, _f32p), _p(e, _f32p) if e is not None else None, n,
+                              float(p), seed, step, _p(idx, _i32p), _p(val, _f32p), n,
+                              ctypes.byref(count)), "orc_ef_randk")
+    k = count.value
+    return idx[:k], val[:k], e
 
 
 def _rank_rows(a, W, k, dtype):

@@ -15,6 +15,7 @@ from tests import test_oracle_aggregate as tagg
 from tests import test_oracle_philox as tphilox
 from tests import test_oracle_powersgd as tpsgd
 from tests import test_oracle_quant as tquant
+from tests import test_oracle_randk as trandk
 from tests import test_oracle_topk as ttopk
 
 MUTANTS = {
@@ -51,6 +52,9 @@ MUTANTS = {
     "aggregate_reverse_rank_order": ("  for (int w = 0; w < W; ++w)\n    for (int64_t j = 0; j < k; ++j) {\n      int64_t at",
                                      "  for (int w = W - 1; w >= 0; --w)\n    for (int64_t j = 0; j < k; ++j) {\n      int64_t at"),
     "aggregate_assign_not_add": ("out[idx[at]] = out[idx[at]] + val[at];", "out[idx[at]] = val[at];"),
+    "randk_compare_flipped": ("int keep = orc_uniform(seed, step, (uint64_t)i) < p;",
+                              "int keep = orc_uniform(seed, step, (uint64_t)i) >= p;"),
+    "randk_residual_not_zeroed": ("if (err) err[i] = keep ? 0.0f : c;", "if (err) err[i] = c;"),
 }
 
 
@@ -75,6 +79,8 @@ def _pins(golden_dir):
     yield lambda: tpsgd.test_orthonormal_and_matches_numpy_qr()
     yield lambda: tagg.test_hand_cases(golden_dir)
     yield lambda: tagg.test_quant_hand_case(golden_dir)
+    yield lambda: trandk.test_keep_set_is_the_philox_draw_below_p(1000, 0.1, 3, 0)
+    yield lambda: trandk.test_limits()
 
 
 @pytest.fixture(scope="module")
