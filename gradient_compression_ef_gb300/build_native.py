@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libgc.so")
 SOURCES = ["gc_api.cu", "gc_topk.cu", "gc_buckets.cu", "gc_quant.cu", "gc_powersgd.cu",
-           "gc_noalloc.cu", "gc_aggregate.cu"]
+           "gc_noalloc.cu", "gc_aggregate.cu", "gc_randk.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]

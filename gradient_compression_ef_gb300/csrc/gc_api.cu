@@ -191,7 +191,7 @@ const char* gc_phase_name(int phase) {
       "ef_hist", "collect", "write", "ef_add", "quant_fused", "quant_stats",
       "quant_combine", "quant_apply", "dequant", "psgd_mq", "psgd_mtp", "psgd_resid",
       "refine", "bk_hist", "bk_collect", "bk_refine", "bk_write", "bk_quant", "agg_bounds",
-      "agg_accumulate"};
+      "agg_accumulate", "randk_mark", "randk_write"};
   return (phase >= 0 && phase < GC_PHASE_COUNT) ? names[phase] : "?";
 }
 
@@ -506,6 +506,23 @@ gc_status gc_topk_quant_aggregate(gc_ctx* ctx, int W, int64_t k, const int32_t* 
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return GC_ERR_CUDA;
   return gc::launch_aggregate(ctx, W, k, idx, nullptr, codes, scales, bits, group, n, out);
+}
+
+gc_status gc_ef_randk(gc_ctx* ctx, const float* grad, float* err, int64_t n, float p,
+                      uint64_t seed, uint64_t step, int32_t* idx_out, float* val_out,
+                      int64_t capacity, int64_t* count_out) {
+  if (!ctx || n < 0 || n > INT32_MAX || capacity < 0 || !count_out || !(p >= 0.0f) ||
+      !(p <= 1.0f))
+    return GC_ERR_INVALID_ARG;
+  GC_TRY(check_buf(grad, n > 0));
+  if (err) GC_TRY(check_buf(err, n > 0));
+  GC_TRY(check_buf(idx_out, capacity > 0));
+  GC_TRY(check_buf(val_out, capacity > 0));
+  if (n > ctx->ws.max_n) return GC_ERR_WORKSPACE;
+  DeviceGuard guard(ctx->device);
+  if (!guard.ok) return GC_ERR_CUDA;
+  return gc::launch_ef_randk(ctx, grad, err, n, p, seed, step, idx_out, val_out, capacity,
+                             count_out);
 }
 
 }  // extern "C"

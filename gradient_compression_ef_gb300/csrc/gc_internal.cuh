@@ -354,6 +354,12 @@ gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int
 gc_status launch_quant_buckets(gc_ctx* ctx, float* err, const int32_t* idx_out, int bits,
                                int64_t group, int rounding, uint64_t seed, uint64_t step,
                                uint8_t* codes_out, float* scales_out);
+// EF + random sparsification over n <= max_n elements (list scratch in the
+// context); writes at most `capacity` entries and the kept count.
+gc_status launch_ef_randk(gc_ctx* ctx, const float* grad, float* err, int64_t n, float p,
+                          uint64_t seed, uint64_t step, int32_t* idx_out, float* val_out,
+                          int64_t capacity, int64_t* count_out);
+
 // Sum of W ranks' sparse vectors into out[n] in rank order; bits == 0: fp32
 // values val[W*k], else QSGD codes / scales laid out per rank (see gc.h).
 gc_status launch_aggregate(gc_ctx* ctx, int W, int64_t k, const int32_t* idx, const float* val,

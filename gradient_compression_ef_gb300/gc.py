@@ -20,7 +20,7 @@ NEAREST_EVEN, STOCHASTIC = 0, 1
 MODES = {"minmax": MINMAX, "qsgd": QSGD, "tern": TERN}
 ROUNDINGS = {"nearest_even": NEAREST_EVEN, "stochastic": STOCHASTIC}
 
-PHASE_COUNT = 20
+PHASE_COUNT = 22
 
 OK = 0
 ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE = -1, -2, -3, -4
@@ -61,6 +61,8 @@ SIGNATURES = [
     ("gc_ef_topk_buckets", _int, [_vp, _vp, _vp, _vp, _vp]),
     ("gc_ef_topk_quant_buckets", _int, [_vp, _vp, _vp, _int, _i64, _int, _u64, _u64, _vp, _vp,
                                         _vp]),
+    ("gc_ef_randk", _int, [_vp, _vp, _vp, _i64, ctypes.c_float, _u64, _u64, _vp, _vp, _i64,
+                           _vp]),
     ("gc_topk_aggregate", _int, [_vp, _int, _i64, _vp, _vp, _i64, _vp]),
     ("gc_topk_quant_aggregate", _int, [_vp, _int, _i64, _vp, _vp, _vp, _int, _i64, _i64, _vp]),
 ]
@@ -292,3 +294,13 @@ def topk_quant_aggregate(ctx, W, k, idx, codes, scales, bits, group, n, out):
     """gc_topk_quant_aggregate: the same with QSGD-coded values per rank."""
     _check(lib.gc_topk_quant_aggregate(ctx.handle, W, k, _ptr(idx), _ptr(codes), _ptr(scales),
                                        bits, group, n, _ptr(out)), "gc_topk_quant_aggregate")
+
+
+def ef_randk(ctx, grad, err, p, seed, step, idx_out, val_out, count_out, n=None, capacity=None):
+    """gc_ef_randk: EF + random sparsification; count_out is a device int64
+    tensor receiving the kept count."""
+    n = grad.numel() if n is None else n
+    capacity = idx_out.numel() if capacity is None else capacity
+    _check(lib.gc_ef_randk(ctx.handle, _ptr(grad), _ptr(err), n, float(p), seed, step,
+                           _ptr(idx_out), _ptr(val_out), capacity, _ptr(count_out)),
+           "gc_ef_randk")

@@ -149,7 +149,9 @@ typedef enum gc_phase {
   GC_PHASE_BK_QUANT = 17,    /* bucketed: QSGD of the kept values */
   GC_PHASE_AGG_BOUNDS = 18,  /* aggregation: each rank's entries per output range */
   GC_PHASE_AGG_ACCUMULATE = 19, /* aggregation: rank-ordered sum into the dense output */
-  GC_PHASE_COUNT = 20
+  GC_PHASE_RANDK_MARK = 20,  /* random sparsification: draws, residual, kept lists */
+  GC_PHASE_RANDK_WRITE = 21, /* random sparsification: ordered output */
+  GC_PHASE_COUNT = 22
 } gc_phase;
 
 /* Name of a phase ("ef_hist", ...); "?" when out of range. */
@@ -283,6 +285,26 @@ GC_API gc_status gc_ef_topk_quant(gc_ctx* ctx, const float* grad, float* err,
 GC_API gc_status gc_powersgd_step(gc_ctx* ctx, const float* grad, float* err,
                            int64_t m, int64_t n, int r, float* P_out,
                            float* Q_inout);
+
+/*
+ * Error feedback + random sparsification.
+ * Pages: "分布式训练中的梯度压缩算法" 二.2 随机稀疏化 (keep each element with
+ * probability p: mask = rand(n) < p); "gradient-compression-quantization-
+ * sparsification" 2.2 (random sparsification keeps the traffic steady);
+ * "梯度聚合通信优化实战方案" 梯度压缩原理 (unsent entries stay in the residual).
+ *   c = grad + err;  element i is kept when u_i < p, u_i being the draw of
+ *   stochastic rounding (word i mod 4 of Philox-4x32-10 at counter {i/4,
+ *   step}, key seed, top 24 bits * 2^-24);  the kept (i, c_i) are written in
+ *   ascending index order;  err[i] = +0 when kept, c_i otherwise.
+ * The number kept is random: *count_out (a DEVICE int64) receives it.  At
+ * most `capacity` entries are written to idx_out / val_out; a larger count
+ * sets the device status (GC_ERR_DEVICE_CHECK from gc_ctx_check).
+ * err == NULL selects from grad alone and writes no residual.  0 <= n <=
+ * max_n (the context's scratch holds the candidate lists).
+ */
+GC_API gc_status gc_ef_randk(gc_ctx* ctx, const float* grad, float* err, int64_t n, float p,
+                             uint64_t seed, uint64_t step, int32_t* idx_out, float* val_out,
+                             int64_t capacity, int64_t* count_out);
 
 /*
  * Aggregation of several ranks' compressed gradients.
