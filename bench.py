@@ -63,13 +63,14 @@ def parse_args():
     p.add_argument("--elems", type=int, default=None,
                    help="gradient elements (default: the workload's own size; for buckets a "
                         "smaller value cuts the same 25 MiB buckets from a shorter gradient)")
-    p.add_argument("--workload", choices=["buckets", "quant", "tern", "powersgd", "aggregate"],
+    p.add_argument("--workload", choices=["buckets", "quant", "tern", "powersgd", "aggregate",
+                                          "randk"],
                    default="buckets",
                    help="buckets: EF + Top-K + QSGD per 25 MiB bucket (the headline); quant: "
                         "EF + group quantisation of 2^30 elements; tern: EF + TernGrad per "
                         "tensor of one transformer layer; powersgd: rank-4 PowerSGD on one "
                         "layer's matrix shapes; aggregate: 8 ranks' Top-K + QSGD outputs summed "
-                        "into one dense gradient")
+                        "into one dense gradient; randk: EF + random sparsification at 1%%")
     p.add_argument("--mode", choices=["minmax", "qsgd"], default="qsgd",
                    help="quant workload: quantisation rule")
     p.add_argument("--bits", type=int, default=8, help="quant workload: bits per code")
@@ -559,8 +560,45 @@ class AggregateWorkload(_SimpleWorkload):
                 "agg_accumulate": float(self.algorithmic_bytes())}
 
 
+class RandKWorkload(_SimpleWorkload):
+    """Error feedback + random sparsification (keep each element with
+    probability 1 %) over the 134,217,728-element gradient: one gc_ef_randk
+    call per step."""
+
+    P, SEED = 0.01, 31
+
+    def __init__(self, torch, gc, dev, args, seed):
+        self.n = args.elems
+        self._init_common(torch, gc, dev, self.n)
+        self.grads = inputs.correlated_steps_device(self.n, args.distinct, dev, seed=seed)
+        self.err = torch.zeros(self.n, dtype=torch.float32, device=dev)
+        self.cap = -(-int(self.n * self.P * 1.1 + 1024) // 4) * 4
+        self.idx = torch.empty(self.cap, dtype=torch.int32, device=dev)
+        self.val = torch.empty(self.cap, dtype=torch.float32, device=dev)
+        self.count = torch.zeros(2, dtype=torch.int64, device=dev)
+
+    def outputs(self):
+        return [self.idx, self.val, self.count]
+
+    def launch_step(self, t, grad=None, main=None, ctxs=None):
+        main = self.main if main is None else main
+        ctx = self._ctx_on(main, ctxs)
+        g = self.grads[t % len(self.grads)] if grad is None else grad
+        self.gc.ef_randk(ctx, g, self.err, self.P, self.SEED, t, self.idx, self.val, self.count)
+
+    def algorithmic_bytes(self):
+        """Read g and e, write e' (12 B per element) and the kept (index,
+        value) pairs (8 B per kept entry)."""
+        return 12 * self.n + 8 * self.n * self.P
+
+    def algorithmic_bytes_per_launch(self):
+        """mark reads g, e and writes e' (12 B per element); write stores the
+        kept pairs (8 B each)."""
+        return {"randk_mark": 12.0 * self.n, "randk_write": 8.0 * self.n * self.P}
+
+
 WORKLOADS = {"quant": QuantWorkload, "tern": TernWorkload, "powersgd": PowerSGDWorkload,
-             "aggregate": AggregateWorkload}
+             "aggregate": AggregateWorkload, "randk": RandKWorkload}
 
 
 def kernel_timing(wl, steps, warmup_step):
@@ -594,6 +632,12 @@ def cpu_sample(args, seed=7):
         e = np.zeros_like(g)
         return (lambda: oracle.ef_quant(g, e, 2, 0, "tern", "stochastic", 91, 0), g.size,
                 "one 4096 x 4096 tensor of the layer, EF + TernGrad per tensor")
+    if args.workload == "randk":
+        n = 1 << 22
+        g = inputs.student_t(r, n)
+        e = (0.1 * inputs.student_t(r, n)).astype(np.float32)
+        return (lambda: oracle.ef_randk(g, e.copy(), 0.01, 31, 0), n,
+                "4,194,304 elements, EF + random sparsification at 1%")
     if args.workload == "aggregate":
         n, W = 1 << 22, 8
         k = inputs.ratio_k(n, 1, 100)
@@ -654,6 +698,11 @@ def config(args, wl=None):
                            "11008, 11008 x 4096, 4096; N(0, (1e-3/sqrt(fan_in))^2)), EF + "
                            "TernGrad per tensor (scale = max|c| of the tensor), stochastic",
                "total_elems": n, "tensors": len(inputs.TRANSFORMER_SHAPES)}
+    elif args.workload == "randk":
+        cfg = {"workload": "flat fp32 gradient {:,} elements, Student-t nu=3 x 1e-3, correlated "
+                           "steps; EF + random sparsification keeping each element with "
+                           "probability 1% (Philox draws)".format(n),
+               "total_elems": n, "keep_probability": 0.01}
     elif args.workload == "aggregate":
         cfg = {"workload": "8 simulated ranks' Top-K 1% + 8-bit QSGD (groups of 64) outputs over "
                            "a {:,}-element Student-t gradient, summed in rank order into one "
