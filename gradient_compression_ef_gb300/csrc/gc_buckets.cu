@@ -118,18 +118,6 @@ struct HistSmem {
   int last;
 };
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // Position of a warp in its work: segment seg (bucket-local element offset
 // l0 .. l1) and pass p.
 struct PassCursor {
@@ -781,16 +769,6 @@ __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict_
       }
     }
   }
-}
-
-template <class K>
-int blocks_per_sm(K kernel, int threads, size_t smem = 0) {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) {
-    cudaGetLastError();
-    n = 1;
-  }
-  return std::max(n, 1);
 }
 
 }  // namespace

@@ -229,18 +229,18 @@ __device__ __forceinline__ void uniform4(uint64_t block, uint64_t seed,
 // Level of one element: t >= 0 is its position on the level grid.
 // Nearest-even: rint(t).  Stochastic: floor(t) + [u < t - floor(t)].
 // Clamped to [0, top].
+// The conversions saturate and take NaN to 0, so a NaN t gives level 0 and
+// a t beyond the grid gives top.
 __device__ __forceinline__ uint32_t round_level(float t, bool stochastic,
                                                 float u, uint32_t top) {
-  float q;
+  int q;
   if (stochastic) {
     const float fl = floorf(t);
-    q = __fadd_rn(fl, (u < __fsub_rn(t, fl)) ? 1.0f : 0.0f);
+    q = __float2int_rz(fl) + ((u < __fsub_rn(t, fl)) ? 1 : 0);
   } else {
-    q = rintf(t);
+    q = __float2int_rn(t);  // half to even
   }
-  if (!(q > 0.0f)) return 0u;
-  if (q >= (float)top) return top;
-  return (uint32_t)q;
+  return (uint32_t)min(max(q, 0), (int)top);
 }
 
 // Quantise one value c against its group parameters; returns the code
@@ -291,6 +291,21 @@ __device__ __forceinline__ void store_codes4(uint8_t* codes, int64_t i0,
   }
 }
 
+// Asynchronous 16-byte global -> shared copies (cp.async.cg: cached in L2
+// only), grouped per commit and completed with cp.async.wait_group, which
+// makes a thread's own copies visible to that thread.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ float warp_sum_tree(float s, int lanes) {
   // Butterfly over `lanes` consecutive lanes: with offsets 1, 2, 4 ... the
   // value after offset o is the sum of an aligned block of 2o lanes, formed
@@ -321,6 +336,17 @@ struct LaunchScope {
 // Host helpers.
 inline int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Resident blocks per SM of a kernel at `threads` threads (at least 1).
+template <class K>
+int blocks_per_sm(K kernel, int threads, size_t smem = 0) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    n = 1;
+  }
+  return n > 1 ? n : 1;
+}
 
 // Launchers implemented in the .cu files (return GC_OK or GC_ERR_CUDA).
 gc_status launch_ef_topk(gc_ctx* ctx, const float* grad, float* err, int64_t n,

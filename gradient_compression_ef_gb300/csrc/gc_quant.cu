@@ -222,18 +222,73 @@ __device__ __forceinline__ void quant_fused_chunk(
                                          step, base, lane);
 }
 
+// The fused kernel gives every warp a contiguous run of 128-element chunks
+// and keeps the next kQStages - 1 chunks of x (and e) in flight as
+// asynchronous copies into the warp's shared-memory stages while it
+// quantises the current one; each lane copies and later reads back its own
+// 16-byte pieces, so no barrier is involved.  The grid is one wave of
+// resident blocks.
+constexpr int kQStages = 4;
+
 template <int MODE, int BITS, int LPG, int IO>
-__global__ void __launch_bounds__(kQThreads) quant_fused_kernel(
+__global__ void __launch_bounds__(kQThreads, 5) quant_fused_kernel(
     const float* __restrict__ x, float* __restrict__ err,
     const int32_t* __restrict__ scatter_idx, int64_t n, QuantOut o,
     int stochastic, uint64_t seed, uint64_t step) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warp_id = ((int64_t)blockIdx.x * kQThreads + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * kQThreads) >> 5;
+  constexpr int NW = kQThreads / 32;
+  constexpr int NA = IO == IO_EF ? 2 : 1;  // staged arrays: x (and e)
+  __shared__ float4 stage[NW][kQStages][NA][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   zero_padding(o);
-  for (int64_t base = warp_id * 128; base < n; base += nwarps * 128)
-    quant_fused_chunk<MODE, BITS, LPG, IO>(x, err, scatter_idx, n, o, stochastic, seed, step,
-                                           base, lane);
+  const int64_t nch = (n + 127) >> 7;
+  const int64_t gw = (int64_t)blockIdx.x * NW + warp, nw = (int64_t)gridDim.x * NW;
+  const int64_t c_lo = nch * gw / nw;
+  const int cnt = (int)(nch * (gw + 1) / nw - c_lo);  // chunks of this warp
+  // lane's piece of the warp's first chunk; whole pieces are copied, the
+  // ragged end of x is read directly when its chunk is processed
+  const int64_t i_first = (c_lo << 7) + 4 * lane;
+  auto issue = [&](int j, int st) {
+    const int64_t i0 = i_first + ((int64_t)j << 7);
+    if (j < cnt && i0 + 3 < n) {
+      cp_async16(&stage[warp][st][0][lane], x + i0);
+      if (IO == IO_EF) cp_async16(&stage[warp][st][NA - 1][lane], err + i0);
+    }
+    cp_async_commit();  // one group per chunk (possibly empty)
+  };
+#pragma unroll
+  for (int k = 0; k < kQStages - 1; ++k) issue(k, k);
+  int st = 0;
+  for (int j = 0; j < cnt; ++j) {
+    cp_async_wait<kQStages - 2>();  // chunk j has landed
+    const int64_t i0 = i_first + ((int64_t)j << 7);
+    float c[4];
+    bool valid[4];
+    if (i0 + 3 < n) {
+      const float4 v = stage[warp][st][0][lane];
+      c[0] = v.x; c[1] = v.y; c[2] = v.z; c[3] = v.w;
+      valid[0] = valid[1] = valid[2] = valid[3] = true;
+      if (IO == IO_EF) {
+        const float4 e = stage[warp][st][NA - 1][lane];
+        c[0] = __fadd_rn(c[0], e.x);
+        c[1] = __fadd_rn(c[1], e.y);
+        c[2] = __fadd_rn(c[2], e.z);
+        c[3] = __fadd_rn(c[3], e.w);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        valid[q] = i0 + q < n;
+        c[q] = valid[q] ? x[i0 + q] : 0.0f;
+        if (IO == IO_EF && valid[q]) c[q] = __fadd_rn(c[q], err[i0 + q]);
+      }
+    }
+    // the stage read one chunk ago is free: refill it kQStages - 1 ahead
+    issue(j + kQStages - 1, st == 0 ? kQStages - 1 : st - 1);
+    quant_fused_apply<MODE, BITS, LPG, IO>(c, valid, err, scatter_idx, n, o, stochastic, seed,
+                                           step, i0 - 4 * lane, lane);
+    st = st + 1 == kQStages ? 0 : st + 1;
+  }
+  cp_async_wait<0>();
 }
 
 // ---------------------------------------------------------------------------
@@ -594,9 +649,16 @@ int grid_for(gc_ctx* ctx, int64_t work_items, int per_block, int per_sm) {
 template <int MODE, int BITS, int LPG, int IO>
 void launch_fused(gc_ctx* ctx, const float* x, float* err, const int32_t* idx, int64_t n,
                   const QuantOut& o, int stoch, uint64_t seed, uint64_t step) {
-  const int grid = grid_for(ctx, ceil_div(n, 128), kQThreads / 32, 8);
-  quant_fused_kernel<MODE, BITS, LPG, IO><<<grid, kQThreads, 0, ctx->stream>>>(
-      x, err, idx, n, o, stoch, seed, step);
+  auto kernel = quant_fused_kernel<MODE, BITS, LPG, IO>;
+  // resident blocks per SM of this instantiation, with shared memory
+  // preferred over L1 (the stages bypass L1)
+  static const int per_sm = [&] {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaGetLastError();
+    return blocks_per_sm(kernel, kQThreads);
+  }();
+  const int grid = grid_for(ctx, ceil_div(n, 128), kQThreads / 32, per_sm);
+  kernel<<<grid, kQThreads, 0, ctx->stream>>>(x, err, idx, n, o, stoch, seed, step);
 }
 
 template <int MODE, int BITS, int IO>
