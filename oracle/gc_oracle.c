@@ -580,6 +580,49 @@ int orc_ef_randk(const float* grad, float* err, int64_t n, float p, uint64_t see
 }
 
 /* ------------------------------------------------------------------------ */
+/* Diagnostics of one compressed bucket.                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [P1 3.2]: production systems watch the ratio of the gradient norm after
+ * compression to the norm before it; [P4 Python 演示] prints the error
+ * energy, the sum of the squared residual, after each compression.  For one
+ * compressed bucket, from the call's inputs and its transmitted values:
+ *   c_i = g_i + e_i (binary32; g_i when e is NULL);
+ *   g_hat_j, j < k: the value the receiver reconstructs for kept index
+ *   idx[j] (strictly increasing);
+ *   e'_i = c_i - g_hat_j (binary32) where i = idx[j], c_i elsewhere
+ *   (for Top-K g_hat_j = c_i, so e'_i = +0: the residual the call stores);
+ *   out[0] = sum_i c_i^2,  out[1] = sum_j g_hat_j^2,  out[2] = sum_i e'_i^2.
+ * Reading: "before compression" is the gradient the compressor sees, c
+ * (with error feedback the corrected gradient), so the norm ratio is
+ * sqrt(out[1] / out[0]).  Every square of a binary32 value is exact in
+ * binary64; the sums run in binary64 in index order.
+ */
+int orc_diagnostics(const float* grad, const float* err, int64_t n, const int32_t* idx,
+                    const float* g_hat, int64_t k, double* out) {
+  if (n < 0 || k < 0 || k > n || !out) return ORC_EINVAL;
+  double s_c = 0.0, s_g = 0.0, s_e = 0.0;
+  int64_t j = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    float c = err ? grad[i] + err[i] : grad[i];
+    float r = c;
+    if (j < k && idx[j] == i) {
+      r = c - g_hat[j];
+      s_g += (double)g_hat[j] * (double)g_hat[j];
+      ++j;
+    }
+    s_c += (double)c * (double)c;
+    s_e += (double)r * (double)r;
+  }
+  if (j != k) return ORC_EINVAL; /* indices not increasing or out of range */
+  out[0] = s_c;
+  out[1] = s_g;
+  out[2] = s_e;
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Aggregation of several ranks' compressed gradients.                       */
 /* ------------------------------------------------------------------------ */
 

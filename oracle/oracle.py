@@ -73,6 +73,9 @@ def lib():
         L.orc_ef_randk.argtypes = [_f32p, _f32p, _i64, ctypes.c_float, _u64, _u64, _i32p,
                                    _f32p, _i64, ctypes.POINTER(_i64)]
         L.orc_ef_randk.restype = _int
+        L.orc_diagnostics.argtypes = [_f32p, _f32p, _i64, _i32p, _f32p, _i64,
+                                      ctypes.POINTER(ctypes.c_double)]
+        L.orc_diagnostics.restype = _int
         L.orc_topk_aggregate.argtypes = [_int, _i64, _i32p, _f32p, _i64, _f32p]
         L.orc_topk_aggregate.restype = _int
         L.orc_topk_quant_aggregate.argtypes = [_int, _i64, _i32p, _u8p, _f32p, _int, _i64,
@@ -237,6 +240,22 @@ def ef_randk(grad, err, p, seed=0, step=0):
                               ctypes.byref(count)), "orc_ef_randk")
     k = count.value
     return idx[:k], val[:k], e
+
+
+def diagnostics(grad, err, idx, g_hat):
+    """(sum c^2, sum g_hat^2, sum e'^2) of one compressed bucket as float64
+    [3]: c = grad + err (or grad), g_hat the reconstructed kept values at
+    the increasing indices idx, e' = c - g_hat there and c elsewhere."""
+    g = _f32(grad)
+    e = _f32(err) if err is not None else None
+    ix = np.ascontiguousarray(idx, dtype=np.int32)
+    gh = _f32(g_hat)
+    out = np.zeros(3, dtype=np.float64)
+    _check(lib().orc_diagnostics(_p(g, _f32p), _p(e, _f32p) if e is not None else None, g.size,
+                                 _p(ix, _i32p), _p(gh, _f32p), ix.size,
+                                 out.ctypes.data_as(ctypes.POINTER(ctypes.c_double))),
+           "orc_diagnostics")
+    return out
 
 
 def _rank_rows(a, W, k, dtype):

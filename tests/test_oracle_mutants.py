@@ -12,6 +12,7 @@ import oracle.build as obuild
 import oracle.oracle as ofront
 
 from tests import test_oracle_aggregate as tagg
+from tests import test_oracle_diag as tdiag
 from tests import test_oracle_philox as tphilox
 from tests import test_oracle_powersgd as tpsgd
 from tests import test_oracle_quant as tquant
@@ -55,6 +56,10 @@ MUTANTS = {
     "randk_compare_flipped": ("int keep = orc_uniform(seed, step, (uint64_t)i) < p;",
                               "int keep = orc_uniform(seed, step, (uint64_t)i) >= p;"),
     "randk_residual_not_zeroed": ("if (err) err[i] = keep ? 0.0f : c;", "if (err) err[i] = c;"),
+    "diag_energy_of_c_not_residual": ("s_e += (double)r * (double)r;",
+                                      "s_e += (double)c * (double)c;"),
+    "diag_sent_norm_from_c": ("s_g += (double)g_hat[j] * (double)g_hat[j];",
+                              "s_g += (double)c * (double)c;"),
 }
 
 
@@ -81,6 +86,8 @@ def _pins(golden_dir):
     yield lambda: tagg.test_quant_hand_case(golden_dir)
     yield lambda: trandk.test_keep_set_is_the_philox_draw_below_p(1000, 0.1, 3, 0)
     yield lambda: trandk.test_limits()
+    yield lambda: tdiag.test_hand_case()
+    yield lambda: tdiag.test_hybrid_matches_the_stored_residual(8, 64)
 
 
 @pytest.fixture(scope="module")
