@@ -55,6 +55,8 @@ def parse_args():
     p.add_argument("--ratio", type=int, default=10, help="Top-K ratio in per mille")
     p.add_argument("--distinct", type=int, default=3, help="distinct correlated gradients")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--diag", action="store_true",
+                   help="buckets workload: also compute the fused per-bucket diagnostics")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--eager", action="store_true",
                    help="time eager launches instead of CUDA-graph replay")
@@ -195,7 +197,7 @@ class BucketWorkload:
     BITS, GROUP, SEED = 8, 64, 1000
 
     def __init__(self, torch, gc, dev, ratio_per_mille, streams, distinct, seed, path,
-                 n=inputs.FLAT_ELEMS):
+                 n=inputs.FLAT_ELEMS, diag=False):
         self.torch, self.gc, self.dev, self.path = torch, gc, dev, path
         self.n = n
         self.bounds = inputs.bucket_bounds(self.n)
@@ -207,6 +209,9 @@ class BucketWorkload:
         self.idx = torch.empty(self.oi[-1], dtype=torch.int32, device=dev)
         self.codes = torch.empty(self.oc[-1], dtype=torch.uint8, device=dev)
         self.scales = torch.empty(self.os[-1], dtype=torch.float32, device=dev)
+        # per-bucket diagnostics (sum c^2, sum g_hat^2, sum e'^2), bucketed path only
+        self.diag = (torch.zeros(3 * len(self.bounds), dtype=torch.float64, device=dev)
+                     if diag and path == "buckets" else None)
         self.main = torch.cuda.current_stream(dev)
         if path == "buckets":
             self.streams = [self.main]
@@ -222,7 +227,8 @@ class BucketWorkload:
 
     def outputs(self):
         """Device tensors holding one step's compressed result."""
-        return [self.idx, self.codes, self.scales]
+        return [self.idx, self.codes, self.scales] + ([self.diag] if self.diag is not None
+                                                      else [])
 
     def algorithmic_bytes(self):
         """Bytes the method must move per step: read g and e, write e' (12 B
@@ -241,7 +247,8 @@ class BucketWorkload:
             if ctx._stream_ref is not main:
                 ctx.set_stream(main)
             gc.ef_topk_quant_buckets(ctx, g, self.err, self.BITS, self.GROUP, "stochastic",
-                                     self.SEED, t, self.idx, self.codes, self.scales)
+                                     self.SEED, t, self.idx, self.codes, self.scales,
+                                     diag=self.diag)
             return
         ctxs = self.ctxs if ctxs is None else ctxs
         streams = [c._stream_ref for c in ctxs]
@@ -727,6 +734,8 @@ def config(args, wl=None):
                "total_elems": n, "bucket_elems": inputs.BUCKET_ELEMS,
                "buckets": len(bounds), "topk_per_mille": args.ratio,
                "quant": "qsgd 8-bit g64 stochastic", "path": args.path}
+        if args.diag:
+            cfg["diagnostics"] = "per-bucket sum c^2, sum g_hat^2, sum e'^2 fused into the passes"
     cfg["l2"] = l2["l2"].format(4 * n >> 20)
     cfg["parallelism"] = l2["parallelism"]
     if wl is not None:
@@ -783,7 +792,7 @@ def main():
 
     if args.workload == "buckets":
         wl = BucketWorkload(torch, gc, dev, args.ratio, args.streams, args.distinct,
-                            seed=42 + rank, path=args.path, n=args.elems)
+                            seed=42 + rank, path=args.path, n=args.elems, diag=args.diag)
     else:
         wl = WORKLOADS[args.workload](torch, gc, dev, args, seed=42 + rank)
     torch.cuda.synchronize(dev)

@@ -191,7 +191,7 @@ const char* gc_phase_name(int phase) {
       "ef_hist", "collect", "write", "ef_add", "quant_fused", "quant_stats",
       "quant_combine", "quant_apply", "dequant", "psgd_mq", "psgd_mtp", "psgd_resid",
       "refine", "bk_hist", "bk_collect", "bk_refine", "bk_write", "bk_quant", "agg_bounds",
-      "agg_accumulate", "randk_mark", "randk_write"};
+      "agg_accumulate", "randk_mark", "randk_write", "bk_diag"};
   return (phase >= 0 && phase < GC_PHASE_COUNT) ? names[phase] : "?";
 }
 
@@ -439,7 +439,7 @@ gc_status gc_bucket_offsets(int nb, const int64_t* bucket_k, int bits, int64_t g
 }
 
 gc_status gc_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int32_t* idx_out,
-                             float* val_out) {
+                             float* val_out, double* diag_out) {
   if (!ctx) return GC_ERR_INVALID_ARG;
   if (!ctx->bk_base) return GC_ERR_WORKSPACE;
   const gc::BucketWs& w = ctx->bk;
@@ -447,14 +447,18 @@ gc_status gc_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int32_t
   if (err) GC_TRY(check_buf(err, true));
   GC_TRY(check_buf(idx_out, w.vals_total > 0));
   GC_TRY(check_buf(val_out, w.vals_total > 0));
+  if (diag_out) GC_TRY(check_buf(diag_out, true));
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return GC_ERR_CUDA;
-  return gc::launch_ef_topk_buckets(ctx, grad, err, idx_out, val_out, true, 0, 0);
+  GC_TRY(gc::launch_ef_topk_buckets(ctx, grad, err, idx_out, val_out, true, 0, 0,
+                                    diag_out != nullptr));
+  return diag_out ? gc::launch_bucket_diag(ctx, false, diag_out) : GC_OK;
 }
 
 gc_status gc_ef_topk_quant_buckets(gc_ctx* ctx, const float* grad, float* err, int bits,
                                    int64_t group, int rounding, uint64_t seed, uint64_t step,
-                                   int32_t* idx_out, uint8_t* codes_out, float* scales_out) {
+                                   int32_t* idx_out, uint8_t* codes_out, float* scales_out,
+                                   double* diag_out) {
   if (!ctx) return GC_ERR_INVALID_ARG;
   if (!ctx->bk_base) return GC_ERR_WORKSPACE;
   const gc::BucketWs& w = ctx->bk;
@@ -466,11 +470,14 @@ gc_status gc_ef_topk_quant_buckets(gc_ctx* ctx, const float* grad, float* err, i
   GC_TRY(check_buf(idx_out, w.vals_total > 0));
   GC_TRY(check_buf(codes_out, w.vals_total > 0));
   GC_TRY(check_buf(scales_out, w.vals_total > 0));
+  if (diag_out) GC_TRY(check_buf(diag_out, true));
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return GC_ERR_CUDA;
-  GC_TRY(gc::launch_ef_topk_buckets(ctx, grad, err, idx_out, w.vals, false, bits, group));
-  return gc::launch_quant_buckets(ctx, err, idx_out, bits, group, rounding, seed, step,
-                                  codes_out, scales_out);
+  const bool diag = diag_out != nullptr;
+  GC_TRY(gc::launch_ef_topk_buckets(ctx, grad, err, idx_out, w.vals, false, bits, group, diag));
+  GC_TRY(gc::launch_quant_buckets(ctx, err, idx_out, bits, group, rounding, seed, step,
+                                  codes_out, scales_out, diag));
+  return diag ? gc::launch_bucket_diag(ctx, true, diag_out) : GC_OK;
 }
 
 namespace {

@@ -125,7 +125,7 @@ struct PassCursor {
   __device__ __forceinline__ bool valid(int32_t sub_hi) const { return seg < sub_hi; }
 };
 
-template <bool EF>
+template <bool EF, bool DIAG>
 __global__ void __launch_bounds__(kH1Threads, 1) bk_hist_kernel(
     const float* __restrict__ grad, float* __restrict__ err, BucketWs w, int qbits,
     int64_t qgroup) {
@@ -191,6 +191,7 @@ __global__ void __launch_bounds__(kH1Threads, 1) bk_hist_kernel(
     }
     int st_use = 0, st_issue = kStages - 1;
     uint32_t cnt = 0u;
+    float d_all = 0.0f, d_unl = 0.0f;  // sums of c^2: all, key below the guess
     while (uc.valid(sub_hi)) {
       cp_async_wait<kStages - 2>();  // the oldest pass has landed
       const int32_t p = uc.p, l1 = uc.l1;
@@ -231,6 +232,18 @@ __global__ void __launch_bounds__(kH1Threads, 1) bk_hist_kernel(
           cv[u] = make_float4(c[0], c[1], c[2], c[3]);
         }
       }
+      if (DIAG) {
+        // entries past the end hold 0 and add nothing
+#pragma unroll
+        for (int u = 0; u < kH1Rows; ++u) {
+          const float c[4] = {cv[u].x, cv[u].y, cv[u].z, cv[u].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            d_all = __fmaf_rn(c[j], c[j], d_all);
+            if (mag_key(c[j]) < kg) d_unl = __fmaf_rn(c[j], c[j], d_unl);
+          }
+        }
+      }
       // this stage is free again: start the pass kStages - 1 ahead
       issue(ic, st_issue);
       if (ic.valid(sub_hi)) advance(ic);
@@ -256,6 +269,13 @@ __global__ void __launch_bounds__(kH1Threads, 1) bk_hist_kernel(
           atomicAdd(&sm.listed, cnt);
         }
         cnt = 0u;
+        if (DIAG) {
+          float v2[2] = {d_all, d_unl};
+          const float t = warp_sum_many<2>(v2, lane);  // lane 0: all, lane 16: unlisted
+          if (lane == 0) w.seg_c2[seg_done] = t;
+          if (lane == 16 && emit) w.seg_drop[seg_done] = t;
+          d_all = d_unl = 0.0f;
+        }
       }
     }
     cp_async_wait<0>();
@@ -350,8 +370,10 @@ __device__ __forceinline__ void walk_load(const BucketWs& w, int64_t s0, uint32_
 // the entries of bin >= B; otherwise c is read again and the lists of
 // bin >= B are built.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kBkThreads) bk_collect_kernel(const float* __restrict__ csrc,
-                                                                BucketWs w) {
+template <bool DIAG>
+__global__ void __launch_bounds__(kBkThreads, 4) bk_collect_kernel(const float* __restrict__ csrc,
+                                                                   BucketWs w) {
+  constexpr bool diag = DIAG;
   constexpr int NW = kBkThreads / 32;
   __shared__ uint32_t mid[kMidBins];
   __shared__ uint32_t warp_sums[NW + 1];
@@ -378,6 +400,11 @@ __global__ void __launch_bounds__(kBkThreads) bk_collect_kernel(const float* __r
         uint32_t c_l, cnt[kWalkSegs];
         const uint32_t mx = walk_counts(w, s0, nq, lane, &c_l, cnt);
         uint32_t abv_l = 0u, wpos_l = 0u;
+        float drop[kWalkSegs];  // this lane's sums of c^2 of the dropped entries
+#pragma unroll
+        for (int r = 0; r < kWalkSegs; ++r) drop[r] = 0.0f;
+        // lane r < nq: segment s0 + r's sum of the entries the hist pass left out
+        const float drop0 = (diag && lane < nq) ? w.seg_drop[s0 + lane] : 0.0f;
         for (uint32_t j0 = 0; j0 < mx; j0 += 32 * kWalkRows) {
           uint2 e[kWalkSegs][kWalkRows];
           walk_load(w, s0, j0, cnt, lane, e);
@@ -393,6 +420,10 @@ __global__ void __launch_bounds__(kBkThreads) bk_collect_kernel(const float* __r
               const uint32_t key = e[r][u].x & 0x7fffffffu;
               const uint32_t bin = key >> kHistShift;
               const bool keep = valid && bin >= B;
+              if (diag && valid && bin < B) {
+                const float v = __uint_as_float(e[r][u].x);
+                drop[r] = __fmaf_rn(v, v, drop[r]);
+              }
               abv += (valid && bin > B) ? 1u : 0u;
               if (valid && bin == B) atomicAdd(&mid[(key >> kLowBits) & (kMidBins - 1)], 1u);
               // in place: every position written was read by an earlier ballot
@@ -411,6 +442,12 @@ __global__ void __launch_bounds__(kBkThreads) bk_collect_kernel(const float* __r
           w.seg_above[s0 + lane] = abv_l;
           w.seg_cnt[s0 + lane] = wpos_l;
         }
+        if (diag) {
+          // segment r's total lands on lanes 4r .. 4r + 3
+          const float t = warp_sum_many<kWalkSegs>(drop, lane);
+          const float mine = __shfl_sync(0xffffffffu, t, (4 * lane) & 31);
+          if (lane < nq) w.seg_drop[s0 + lane] = __fadd_rn(drop0, mine);
+        }
       }
     } else {
       const float* c = csrc + d.start;
@@ -419,6 +456,7 @@ __global__ void __launch_bounds__(kBkThreads) bk_collect_kernel(const float* __r
         const int64_t l1 = std::min<int64_t>(l0 + kSegElems, d.n);
         uint2* out = w.list + (seg << kSegShift);
         uint32_t cnt = 0u, above_l = 0u;
+        float drop = 0.0f;  // this lane's sum of c^2 below bin B
         for (int64_t p = l0; p < l1; p += kPass) {
           float v[16];
           bool valid[16];
@@ -445,6 +483,8 @@ __global__ void __launch_bounds__(kBkThreads) bk_collect_kernel(const float* __r
               const uint32_t key = mag_key(v[4 * u + j]);
               const uint32_t bin = key >> kHistShift;
               ge[j] = valid[4 * u + j] && bin >= B;
+              if (diag && valid[4 * u + j] && bin < B)
+                drop = __fmaf_rn(v[4 * u + j], v[4 * u + j], drop);
               above_l += (valid[4 * u + j] && bin > B) ? 1u : 0u;
               if (valid[4 * u + j] && bin == B)
                 atomicAdd(&mid[(key >> kLowBits) & (kMidBins - 1)], 1u);
@@ -453,9 +493,11 @@ __global__ void __launch_bounds__(kBkThreads) bk_collect_kernel(const float* __r
           }
         }
         above_l = __reduce_add_sync(0xffffffffu, above_l);
+        if (diag) drop = warp_allsum(drop);
         if (lane == 0) {
           w.seg_cnt[seg] = cnt;
           w.seg_above[seg] = above_l;
+          if (diag) w.seg_drop[seg] = drop;
         }
       }
     }
@@ -689,7 +731,7 @@ __global__ void __launch_bounds__(kBkThreads) bk_refine_kernel(BucketWs w) {
 // write: ordered (index, value) of the kept entries, four segments per warp
 // (lane r < 4 holds segment r's bookkeeping).
 // ---------------------------------------------------------------------------
-template <bool ZERO>
+template <bool ZERO, bool DIAG>
 __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict__ err,
                                                               BucketWs w,
                                                               int32_t* __restrict__ idx_out,
@@ -725,6 +767,12 @@ __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict_
     for (int r = 0; r < kWalkSegs; ++r) cnt[r] = __shfl_sync(0xffffffffu, cnt_l, r);
     const uint32_t mx = __reduce_max_sync(0xffffffffu, cnt_l);
     uint32_t run_l = 0u, tr_l = 0u;
+    // this lane's sums of c^2: [r] dropped, [kWalkSegs + r] kept, of segment r
+    float dk[2 * kWalkSegs];
+#pragma unroll
+    for (int r = 0; r < 2 * kWalkSegs; ++r) dk[r] = 0.0f;
+    // lane r < nq: segment s0 + r's sum of the entries dropped before
+    const float drop0 = (DIAG && k_l != 0u) ? w.seg_drop[s0 + lane] : 0.0f;
     for (uint32_t j0 = 0; j0 < mx; j0 += 32 * kWalkRows) {
       uint2 e[kWalkSegs][kWalkRows];
       walk_load(w, s0, j0, cnt, lane, e);
@@ -749,6 +797,11 @@ __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict_
           const uint32_t eqb = __ballot_sync(0xffffffffu, eq);
           const bool keep = gt || (eq && tr + __popc(eqb & lt) < rem);
           const uint32_t kb = __ballot_sync(0xffffffffu, keep);
+          if (DIAG && valid) {
+            const float v = __uint_as_float(e[r][u].x);
+            if (keep) dk[kWalkSegs + r] = __fmaf_rn(v, v, dk[kWalkSegs + r]);
+            else dk[r] = __fmaf_rn(v, v, dk[r]);
+          }
           if (keep) {
             const uint32_t pos = out + run + __popc(kb & lt);
             if (pos < bk && e[r][u].y < bn) {
@@ -768,27 +821,132 @@ __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict_
         }
       }
     }
+    if (DIAG) {
+      // value j's total lands on lanes 2j, 2j + 1
+      const float t = warp_sum_many<2 * kWalkSegs>(dk, lane);
+      const float dt = __shfl_sync(0xffffffffu, t, (2 * lane) & 31);
+      const float kt = __shfl_sync(0xffffffffu, t, (2 * lane + 2 * kWalkSegs) & 31);
+      if (k_l != 0u) {  // lanes < nq only
+        w.seg_drop[s0 + lane] = __fadd_rn(drop0, dt);
+        w.seg_keep[s0 + lane] = kt;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// diag: per bucket, the sums of the per-segment (and, for the hybrid,
+// per-chunk) partials in a fixed order: each thread adds a strided run in
+// index order, then a fixed tree over the threads.
+// ---------------------------------------------------------------------------
+constexpr int kDiagThreads = 512;
+
+// Compensated binary32 accumulation (Neumaier's variant of Kahan summation,
+// with Knuth's TwoSum for the rounding error of each addition): hi + lo
+// carries the sum with a relative error of about 2u + n u^2 (u = 2^-24) for
+// non-negative terms, without binary64 arithmetic.
+struct Acc {
+  float hi, lo;
+};
+
+__device__ __forceinline__ void acc_add(Acc& a, float x) {
+  const float s = __fadd_rn(a.hi, x);
+  const float bb = __fsub_rn(s, a.hi);
+  const float err = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(x, bb));
+  a.hi = s;
+  a.lo = __fadd_rn(a.lo, err);
+}
+
+__device__ __forceinline__ void acc_merge(Acc& a, const Acc& b) {
+  acc_add(a, b.hi);
+  a.lo = __fadd_rn(a.lo, b.lo);
+}
+
+__global__ void __launch_bounds__(kDiagThreads) bk_diag_kernel(BucketWs w, int quant,
+                                                               double* __restrict__ out) {
+  __shared__ Acc red[3][kDiagThreads];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.x;
+  const BucketDesc d = w.desc[b];
+  const bool kept = d.k != 0;
+  // a[0] sum c^2, a[1] sum g_hat^2, a[2] sum e'^2: each thread adds a
+  // strided run of the partials in index order
+  Acc a[3] = {{0.0f, 0.0f}, {0.0f, 0.0f}, {0.0f, 0.0f}};
+  for (int i = threadIdx.x; i < d.nseg; i += kDiagThreads) {
+    const int64_t sg = (int64_t)d.seg_first + i;
+    acc_add(a[0], w.seg_c2[sg]);
+    if (kept) {
+      acc_add(a[2], w.seg_drop[sg]);
+      if (!quant) acc_add(a[1], w.seg_keep[sg]);
+    }
+  }
+  if (quant && kept) {
+    for (int i = threadIdx.x; i < d.nchunk; i += kDiagThreads) {
+      const int64_t ch = (int64_t)d.chunk_first + i;
+      acc_add(a[1], w.chunk_g2[ch]);
+      acc_add(a[2], w.chunk_r2[ch]);
+    }
+  }
+  // fixed order: warp 0 merges the threads' sums in thread order (16 per
+  // lane), then a butterfly
+#pragma unroll
+  for (int q = 0; q < 3; ++q) red[q][threadIdx.x] = a[q];
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int per = kDiagThreads / 32;
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      Acc t = red[q][lane * per];
+      for (int i = 1; i < per; ++i) acc_merge(t, red[q][lane * per + i]);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        Acc u;
+        u.hi = __shfl_xor_sync(0xffffffffu, t.hi, o);
+        u.lo = __shfl_xor_sync(0xffffffffu, t.lo, o);
+        // the lower lane's sum first, so both lanes get the same result
+        if (lane & o) {
+          acc_merge(u, t);
+          t = u;
+        } else {
+          acc_merge(t, u);
+        }
+      }
+      a[q] = t;
+    }
+    if (lane == 0) {
+      const double s0 = (double)a[0].hi + (double)a[0].lo;
+      out[3 * (int64_t)b] = s0;
+      out[3 * (int64_t)b + 1] = kept ? (double)a[1].hi + (double)a[1].lo : 0.0;
+      out[3 * (int64_t)b + 2] = kept ? (double)a[2].hi + (double)a[2].lo : s0;  // e' = c
+    }
   }
 }
 
 }  // namespace
 
 gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int32_t* idx_out,
-                                 float* val_out, bool zero_err, int qbits, int64_t qgroup) {
+                                 float* val_out, bool zero_err, int qbits, int64_t qgroup,
+                                 bool diag) {
   const BucketWs& w = ctx->bk;
   cudaStream_t s = ctx->stream;
   {
     LaunchScope L(ctx, GC_PHASE_BK_HIST);
-    if (err)
-      bk_hist_kernel<true><<<w.g_hist, kH1Threads, sizeof(HistSmem), s>>>(grad, err, w, qbits,
-                                                                         qgroup);
+    const size_t sm = sizeof(HistSmem);
+    if (err && diag)
+      bk_hist_kernel<true, true><<<w.g_hist, kH1Threads, sm, s>>>(grad, err, w, qbits, qgroup);
+    else if (err)
+      bk_hist_kernel<true, false><<<w.g_hist, kH1Threads, sm, s>>>(grad, err, w, qbits, qgroup);
+    else if (diag)
+      bk_hist_kernel<false, true><<<w.g_hist, kH1Threads, sm, s>>>(grad, err, w, qbits, qgroup);
     else
-      bk_hist_kernel<false><<<w.g_hist, kH1Threads, sizeof(HistSmem), s>>>(grad, err, w, qbits,
-                                                                          qgroup);
+      bk_hist_kernel<false, false><<<w.g_hist, kH1Threads, sm, s>>>(grad, err, w, qbits, qgroup);
   }
   {
     LaunchScope L(ctx, GC_PHASE_BK_COLLECT);
-    bk_collect_kernel<<<w.g_coll, kBkThreads, 0, s>>>(err ? err : grad, w);
+    if (diag)
+      bk_collect_kernel<true><<<w.g_coll, kBkThreads, 0, s>>>(err ? err : grad, w);
+    else
+      bk_collect_kernel<false><<<w.g_coll, kBkThreads, 0, s>>>(err ? err : grad, w);
   }
   {
     LaunchScope L(ctx, GC_PHASE_BK_REFINE);
@@ -796,11 +954,24 @@ gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int
   }
   {
     LaunchScope L(ctx, GC_PHASE_BK_WRITE);
-    if (zero_err && err)
-      bk_write_kernel<true><<<w.g_write, kBkThreads, 0, s>>>(err, w, idx_out, val_out);
+    const bool z = zero_err && err;
+    const int gd = w.g_write_diag;
+    if (z && diag)
+      bk_write_kernel<true, true><<<gd, kBkThreads, 0, s>>>(err, w, idx_out, val_out);
+    else if (z)
+      bk_write_kernel<true, false><<<w.g_write, kBkThreads, 0, s>>>(err, w, idx_out, val_out);
+    else if (diag)
+      bk_write_kernel<false, true><<<gd, kBkThreads, 0, s>>>(err, w, idx_out, val_out);
     else
-      bk_write_kernel<false><<<w.g_write, kBkThreads, 0, s>>>(err, w, idx_out, val_out);
+      bk_write_kernel<false, false><<<w.g_write, kBkThreads, 0, s>>>(err, w, idx_out, val_out);
   }
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+gc_status launch_bucket_diag(gc_ctx* ctx, bool quant, double* out) {
+  const BucketWs& w = ctx->bk;
+  LaunchScope L(ctx, GC_PHASE_BK_DIAG);
+  bk_diag_kernel<<<w.nb, kDiagThreads, 0, ctx->stream>>>(w, quant ? 1 : 0, out);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
 
@@ -843,15 +1014,26 @@ gc_status plan_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n, const int64
   w.nchunk = nchunk;
   w.vals_total = voff;
   auto grid = [&](int per_sm) { return (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * per_sm, nseg)); };
-  if (cudaFuncSetAttribute(bk_hist_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)sizeof(HistSmem)) != cudaSuccess ||
-      cudaFuncSetAttribute(bk_hist_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)sizeof(HistSmem)) != cudaSuccess)
+  const int hsm = (int)sizeof(HistSmem);
+  if (cudaFuncSetAttribute(bk_hist_kernel<true, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, hsm) != cudaSuccess ||
+      cudaFuncSetAttribute(bk_hist_kernel<false, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, hsm) != cudaSuccess ||
+      cudaFuncSetAttribute(bk_hist_kernel<true, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, hsm) != cudaSuccess ||
+      cudaFuncSetAttribute(bk_hist_kernel<false, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, hsm) != cudaSuccess)
     return GC_ERR_CUDA;
-  w.g_hist = grid(blocks_per_sm(bk_hist_kernel<true>, kH1Threads, sizeof(HistSmem)));
-  w.g_coll = grid(blocks_per_sm(bk_collect_kernel, kBkThreads));
+  // every instantiation of a pass runs on the same grid (the tickets count
+  // its blocks): the smallest resident count of them
+  w.g_hist = grid(std::min(blocks_per_sm(bk_hist_kernel<true, false>, kH1Threads, hsm),
+                           blocks_per_sm(bk_hist_kernel<true, true>, kH1Threads, hsm)));
+  w.g_coll = grid(std::min(blocks_per_sm(bk_collect_kernel<false>, kBkThreads),
+                           blocks_per_sm(bk_collect_kernel<true>, kBkThreads)));
   w.g_ref = grid(blocks_per_sm(bk_refine_kernel, kBkThreads));
-  w.g_write = grid(blocks_per_sm(bk_write_kernel<true>, kBkThreads));
+  // the write pass takes no tickets: each variant gets its own grid
+  w.g_write = grid(blocks_per_sm(bk_write_kernel<true, false>, kBkThreads));
+  w.g_write_diag = grid(blocks_per_sm(bk_write_kernel<true, true>, kBkThreads));
   // blocks of each ticketed pass that touch each bucket
   auto count_blocks = [&](int G, int32_t BucketDesc::*field) {
     for (int i = 0; i < G; ++i) {
@@ -880,6 +1062,9 @@ gc_status plan_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n, const int64
   const size_t o_stash = take(sizeof(uint2) * kBkStash * (size_t)nb);
   const size_t o_qoff = take(sizeof(int64_t) * 2 * (size_t)nb);
   const size_t o_vals = take(sizeof(float) * (size_t)std::max<int64_t>(voff, 1));
+  size_t o_dseg[3];
+  for (int i = 0; i < 3; ++i) o_dseg[i] = take(sizeof(float) * nseg);
+  const size_t o_dch = take(sizeof(float) * 2 * chunk_bucket.size());
 
   free_buckets(ctx);
   void* base = nullptr;
@@ -906,6 +1091,11 @@ gc_status plan_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n, const int64
   w.stash = reinterpret_cast<uint2*>(p + o_stash);
   w.qoff = reinterpret_cast<int64_t*>(p + o_qoff);
   w.vals = reinterpret_cast<float*>(p + o_vals);
+  w.seg_c2 = reinterpret_cast<float*>(p + o_dseg[0]);
+  w.seg_drop = reinterpret_cast<float*>(p + o_dseg[1]);
+  w.seg_keep = reinterpret_cast<float*>(p + o_dseg[2]);
+  w.chunk_g2 = reinterpret_cast<float*>(p + o_dch);
+  w.chunk_r2 = w.chunk_g2 + chunk_bucket.size();
   w.status = ctx->ws.status;
   // zero the state that must start at zero; the list, segment arrays and
   // outputs are written before they are read

@@ -127,6 +127,7 @@ struct BucketWs {
   int64_t nchunk;       // quantisation chunks over all buckets
   int64_t vals_total;   // slots of the idx / value outputs (sum of k rounded up to 4)
   int g_hist, g_coll, g_ref, g_write;  // grid sizes the tickets were counted for
+  int g_write_diag;     // grid of the write pass with diagnostics
   BucketDesc* desc;     // [nb]
   BucketSel* sel;       // [nb]
   int32_t* seg_bucket;  // [nseg]
@@ -144,6 +145,12 @@ struct BucketWs {
   uint2* stash;         // [nb][kBkStash] (key, segment)
   int64_t* qoff;        // [nb][2] codes byte / scales float offset of each bucket
   float* vals;          // [vals_total] kept values of the hybrid call
+  // per-segment / per-chunk partial sums of the diagnostics
+  float* seg_c2;        // [nseg] sum of c^2
+  float* seg_drop;      // [nseg] sum of c^2 over the entries not kept
+  float* seg_keep;      // [nseg] sum of c^2 over the kept entries
+  float* chunk_g2;      // [nchunk] sum of g_hat^2 of a chunk of kept values
+  float* chunk_r2;      // [nchunk] sum of e'^2 of a chunk of kept values
   uint32_t* status;     // the context's device status word
 };
 
@@ -306,6 +313,39 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Sums each of v[0 .. N-1] (N a power of two <= 32) over the 32 lanes by a
+// transposed butterfly: at the exchange across lane bit 4, 3, ... a lane
+// keeps the half of its values picked by that bit and receives the
+// partner's copy of the same half, so N values take N + 5 - log2(N)
+// shuffles instead of 5 N.  Value j ends on the lanes l with
+// l >> (5 - log2 N) == j and is returned there.  Fixed order of additions.
+template <int N>
+__device__ __forceinline__ float warp_sum_many(float (&v)[N], int lane) {
+  int off = 16;
+#pragma unroll
+  for (int half = N / 2; half >= 1; half >>= 1, off >>= 1) {
+    const bool hi = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float keep = hi ? v[i + half] : v[i];
+      const float send = hi ? v[i] : v[i + half];
+      v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, off));
+    }
+  }
+  float t = v[0];
+#pragma unroll
+  for (; off >= 1; off >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, off));
+  return t;
+}
+
+// Sum over the 32 lanes by the butterfly (the same value on every lane, the
+// same order of additions on every call).
+__device__ __forceinline__ float warp_allsum(float s) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, o));
+  return s;
+}
+
 __device__ __forceinline__ float warp_sum_tree(float s, int lanes) {
   // Butterfly over `lanes` consecutive lanes: with offsets 1, 2, 4 ... the
   // value after offset o is the sum of an aligned block of 2o lanes, formed
@@ -373,13 +413,19 @@ gc_status launch_powersgd(gc_ctx* ctx, const float* grad, float* err,
 // receives the kept values at the bucket's idx_off (val_out otherwise);
 // zero_err writes e' = +0 at the kept positions.  qbits > 0 also lays out
 // the QSGD outputs of (qbits, qgroup) for launch_quant_buckets.
+// diag also leaves the per-segment diagnostic partial sums.
 gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int32_t* idx_out,
-                                 float* val_out, bool zero_err, int qbits, int64_t qgroup);
+                                 float* val_out, bool zero_err, int qbits, int64_t qgroup,
+                                 bool diag);
 // QSGD of every bucket's kept values (from launch_ef_topk_buckets) with the
-// residual scattered to err; bucket b uses seed + b.
+// residual scattered to err; bucket b uses seed + b.  diag also leaves the
+// per-chunk diagnostic partial sums.
 gc_status launch_quant_buckets(gc_ctx* ctx, float* err, const int32_t* idx_out, int bits,
                                int64_t group, int rounding, uint64_t seed, uint64_t step,
-                               uint8_t* codes_out, float* scales_out);
+                               uint8_t* codes_out, float* scales_out, bool diag);
+// Per-bucket diagnostics {sum c^2, sum g_hat^2, sum e'^2} into out[nb][3]
+// from the partial sums of the last bucketed call (quant: the hybrid's).
+gc_status launch_bucket_diag(gc_ctx* ctx, bool quant, double* out);
 // EF + random sparsification over n <= max_n elements (list scratch in the
 // context); writes at most `capacity` entries and the kept count.
 gc_status launch_ef_randk(gc_ctx* ctx, const float* grad, float* err, int64_t n, float p,

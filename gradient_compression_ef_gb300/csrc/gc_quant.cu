@@ -124,11 +124,13 @@ __device__ __forceinline__ void quant_load4(const float* __restrict__ x,
 // consecutive lanes, G dividing 128), lane l holding elements base + 4l ..
 // base + 4l + 3 with values c[] (from quant_load4).  Every lane of the warp
 // must call it.
-template <int MODE, int BITS, int LPG, int IO>
+// With DIAG, dsum[0] and dsum[1] accumulate this lane's g_hat^2 and e'^2.
+template <int MODE, int BITS, int LPG, int IO, bool DIAG = false>
 __device__ __forceinline__ void quant_fused_apply(
     float c[4], const bool valid[4], float* __restrict__ err,
     const int32_t* __restrict__ scatter_idx, int64_t n, const QuantOut& o,
-    int stochastic, uint64_t seed, uint64_t step, int64_t base, int lane) {
+    int stochastic, uint64_t seed, uint64_t step, int64_t base, int lane,
+    float* dsum = nullptr) {
   constexpr int G = 4 * LPG;
   constexpr uint32_t top = (MODE == GC_TERN) ? 1u : ((1u << BITS) - 1u);
   const float levels = (float)top;
@@ -181,6 +183,10 @@ __device__ __forceinline__ void quant_fused_apply(
     q[j] = quantize_one<MODE>(c[j], scale, offset, stochastic != 0, u[j], top, &neg[j], &gh);
     if (!valid[j]) { q[j] = 0u; neg[j] = false; }
     r[j] = __fsub_rn(c[j], gh);
+    if (DIAG && valid[j]) {
+      dsum[0] = __fmaf_rn(gh, gh, dsum[0]);
+      dsum[1] = __fmaf_rn(r[j], r[j], dsum[1]);
+    }
   }
   store_codes4<(MODE == GC_TERN) ? 2 : BITS>(o.codes, i0, active, code_bits4<MODE, BITS>(q, neg));
   if (MODE == GC_QSGD) {
@@ -210,16 +216,17 @@ __device__ __forceinline__ void quant_fused_apply(
 }
 
 // Load + quantise of one 128-element chunk (the bucketed kernel's unit).
-template <int MODE, int BITS, int LPG, int IO>
+template <int MODE, int BITS, int LPG, int IO, bool DIAG = false>
 __device__ __forceinline__ void quant_fused_chunk(
     const float* __restrict__ x, float* __restrict__ err,
     const int32_t* __restrict__ scatter_idx, int64_t n, const QuantOut& o,
-    int stochastic, uint64_t seed, uint64_t step, int64_t base, int lane) {
+    int stochastic, uint64_t seed, uint64_t step, int64_t base, int lane,
+    float* dsum = nullptr) {
   float c[4];
   bool valid[4];
   quant_load4<IO>(x, err, n, base + 4 * lane, c, valid);
-  quant_fused_apply<MODE, BITS, LPG, IO>(c, valid, err, scatter_idx, n, o, stochastic, seed,
-                                         step, base, lane);
+  quant_fused_apply<MODE, BITS, LPG, IO, DIAG>(c, valid, err, scatter_idx, n, o, stochastic,
+                                               seed, step, base, lane, dsum);
 }
 
 // The fused kernel gives every warp a contiguous run of 128-element chunks
@@ -618,7 +625,7 @@ __host__ __device__ inline QuantOut make_out(uint8_t* codes, float* scales, int6
 // QSGD of the kept values of every bucket of a plan: one warp per chunk of
 // 128 values of one bucket; bucket b's codes and scales start at the offsets
 // the hist pass laid out, its residuals go to err[start_b + idx].
-template <int BITS, int LPG>
+template <int BITS, int LPG, bool DIAG>
 __global__ void __launch_bounds__(kQThreads) quant_buckets_kernel(
     float* __restrict__ err, const int32_t* __restrict__ idx, BucketWs w,
     uint8_t* __restrict__ codes_out, float* __restrict__ scales_out, int stochastic,
@@ -635,9 +642,17 @@ __global__ void __launch_bounds__(kQThreads) quant_buckets_kernel(
     o.scatter_n = d.n;
     o.status = w.status;
     if (lc == 0 && lane == 0) zero_padding_bytes(o);
-    quant_fused_chunk<GC_QSGD, BITS, LPG, IO_SCATTER>(
+    float dsum[2] = {0.0f, 0.0f};
+    quant_fused_chunk<GC_QSGD, BITS, LPG, IO_SCATTER, DIAG>(
         w.vals + d.idx_off, err + d.start, idx + d.idx_off, d.k, o, stochastic,
-        seed + (uint64_t)b, step, lc * kChunkVals, lane);
+        seed + (uint64_t)b, step, lc * kChunkVals, lane, dsum);
+    if (DIAG) {
+      const float g2 = warp_allsum(dsum[0]), r2 = warp_allsum(dsum[1]);
+      if (lane == 0) {
+        w.chunk_g2[ch] = g2;
+        w.chunk_r2[ch] = r2;
+      }
+    }
   }
 }
 
@@ -784,14 +799,22 @@ gc_status launch_dequant(gc_ctx* ctx, const uint8_t* codes, const float* scales,
 
 gc_status launch_quant_buckets(gc_ctx* ctx, float* err, const int32_t* idx_out, int bits,
                                int64_t group, int rounding, uint64_t seed, uint64_t step,
-                               uint8_t* codes_out, float* scales_out) {
+                               uint8_t* codes_out, float* scales_out, bool diag) {
   const BucketWs& w = ctx->bk;
   if (w.nchunk == 0) return GC_OK;
   const int grid = grid_for(ctx, w.nchunk, kQThreads / 32, 8);
   const int st = rounding == GC_STOCHASTIC;
   cudaStream_t s = ctx->stream;
   LaunchScope L(ctx, GC_PHASE_BK_QUANT);
-#define GC_BQ(B, LPG) quant_buckets_kernel<B, LPG><<<grid, kQThreads, 0, s>>>(err, idx_out, w, codes_out, scales_out, st, seed, step)
+#define GC_BQ(B, LPG)                                                                    \
+  do {                                                                                   \
+    if (diag)                                                                            \
+      quant_buckets_kernel<B, LPG, true><<<grid, kQThreads, 0, s>>>(                     \
+          err, idx_out, w, codes_out, scales_out, st, seed, step);                       \
+    else                                                                                 \
+      quant_buckets_kernel<B, LPG, false><<<grid, kQThreads, 0, s>>>(                    \
+          err, idx_out, w, codes_out, scales_out, st, seed, step);                       \
+  } while (0)
 #define GC_BQ_G(B)                 \
   switch (group) {                 \
     case 4: GC_BQ(B, 1); break;    \

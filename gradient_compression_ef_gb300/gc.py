@@ -20,7 +20,7 @@ NEAREST_EVEN, STOCHASTIC = 0, 1
 MODES = {"minmax": MINMAX, "qsgd": QSGD, "tern": TERN}
 ROUNDINGS = {"nearest_even": NEAREST_EVEN, "stochastic": STOCHASTIC}
 
-PHASE_COUNT = 22
+PHASE_COUNT = 23
 
 OK = 0
 ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE = -1, -2, -3, -4
@@ -58,9 +58,9 @@ SIGNATURES = [
     ("gc_ctx_set_buckets", _int, [_vp, _int, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
     ("gc_bucket_offsets", _int, [_int, ctypes.POINTER(_i64), _int, _i64, ctypes.POINTER(_i64),
                                  ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
-    ("gc_ef_topk_buckets", _int, [_vp, _vp, _vp, _vp, _vp]),
+    ("gc_ef_topk_buckets", _int, [_vp, _vp, _vp, _vp, _vp, _vp]),
     ("gc_ef_topk_quant_buckets", _int, [_vp, _vp, _vp, _int, _i64, _int, _u64, _u64, _vp, _vp,
-                                        _vp]),
+                                        _vp, _vp]),
     ("gc_ef_randk", _int, [_vp, _vp, _vp, _i64, ctypes.c_float, _u64, _u64, _vp, _vp, _i64,
                            _vp]),
     ("gc_topk_aggregate", _int, [_vp, _int, _i64, _vp, _vp, _i64, _vp]),
@@ -271,17 +271,28 @@ def bucket_offsets(bucket_k, bits=None, group=None):
             list(os_) if os_ is not None else None)
 
 
-def ef_topk_buckets(ctx, grad, err, idx_out, val_out):
+def ef_topk_buckets(ctx, grad, err, idx_out, val_out, diag=None):
+    """diag: None, or a device float64 tensor of 3 * nb values receiving per
+    bucket (sum c^2, sum g_hat^2, sum e'^2)."""
     _check(lib.gc_ef_topk_buckets(ctx.handle, _ptr(grad), _ptr(err), _ptr(idx_out),
-                                  _ptr(val_out)), "gc_ef_topk_buckets")
+                                  _ptr(val_out), _ptr(diag)), "gc_ef_topk_buckets")
 
 
 def ef_topk_quant_buckets(ctx, grad, err, bits, group, rounding, seed, step, idx_out,
-                          codes_out, scales_out):
+                          codes_out, scales_out, diag=None):
     _check(lib.gc_ef_topk_quant_buckets(ctx.handle, _ptr(grad), _ptr(err), bits, group,
                                         _rounding(rounding), seed, step, _ptr(idx_out),
-                                        _ptr(codes_out), _ptr(scales_out)),
+                                        _ptr(codes_out), _ptr(scales_out), _ptr(diag)),
            "gc_ef_topk_quant_buckets")
+
+
+def norm_ratio(diag):
+    """Per-bucket gradient norm ratio ||g_hat|| / ||c|| from the diagnostics
+    (a host computation on the 3 * nb values)."""
+    import math
+    d = [float(x) for x in diag]
+    return [math.sqrt(d[3 * b + 1] / d[3 * b]) if d[3 * b] > 0 else 0.0
+            for b in range(len(d) // 3)]
 
 
 def topk_aggregate(ctx, W, k, idx, val, n, out):

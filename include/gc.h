@@ -151,7 +151,8 @@ typedef enum gc_phase {
   GC_PHASE_AGG_ACCUMULATE = 19, /* aggregation: rank-ordered sum into the dense output */
   GC_PHASE_RANDK_MARK = 20,  /* random sparsification: draws, residual, kept lists */
   GC_PHASE_RANDK_WRITE = 21, /* random sparsification: ordered output */
-  GC_PHASE_COUNT = 22
+  GC_PHASE_BK_DIAG = 22,     /* bucketed: per-bucket diagnostics */
+  GC_PHASE_COUNT = 23
 } gc_phase;
 
 /* Name of a phase ("ef_hist", ...); "?" when out of range. */
@@ -386,14 +387,38 @@ GC_API gc_status gc_bucket_offsets(int nb, const int64_t* bucket_k, int bits, in
                                    int64_t* idx_off, int64_t* codes_off, int64_t* scales_off);
 
 /*
+ * Diagnostics of the bucketed calls ("gradient-compression-quantization-
+ * sparsification" 3.2: watch the ratio of the gradient norm after and before
+ * compression; "梯度聚合通信优化实战方案" Python 演示: the error energy, the
+ * sum of the squared residual).  When diag_out is not NULL the call also
+ * writes, for every bucket b, three fp64 values at diag_out[3b ..]:
+ *   [0] sum over the bucket of c_i^2             (c = g + e, or g)
+ *   [1] sum over the kept entries of g_hat_j^2   (what the receiver
+ *       reconstructs: the kept c for Top-K, the dequantised value for the
+ *       hybrid), so the norm ratio is sqrt([1] / [0]);
+ *   [2] sum over the bucket of e'_i^2            (the new residual; kept
+ *       Top-K entries contribute 0; with err == NULL the residual the call
+ *       would have stored)
+ * diag_out is a DEVICE fp64[3 * nb], 16-byte aligned.  The sums are
+ * computed inside the passes that already touch each value: fp32 squares
+ * accumulated by fused multiply-add in runs of at most 64 per lane, added
+ * over the warp into one fp32 partial per 2048-element segment (or 128 kept
+ * values), then per bucket by compensated (TwoSum) fp32 summation, all in a
+ * fixed order (deterministic); the relative error of each value is below
+ * 5e-6 (73 roundings of 2^-24 at most).  One more small launch per call.
+ * Requires finite c with |c| < 2^63 (no overflow of c^2 in fp32).
+ */
+
+/*
  * gc_ef_topk on every bucket of the plan.
  * grad, err: fp32[total] (err may be NULL: select from grad, no residual);
  * idx_out: int32[idx_off[nb]], val_out: fp32[idx_off[nb]]; bucket b's
- * entries start at idx_off[b] (slots between buckets are not written).
+ * entries start at idx_off[b] (slots between buckets are not written);
+ * diag_out: NULL, or the diagnostics above.
  * GC_ERR_WORKSPACE when the context has no plan.
  */
 GC_API gc_status gc_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err,
-                                    int32_t* idx_out, float* val_out);
+                                    int32_t* idx_out, float* val_out, double* diag_out);
 
 /*
  * gc_ef_topk_quant on every bucket of the plan: bucket b is compressed as
@@ -401,12 +426,14 @@ GC_API gc_status gc_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err,
  * step) with its indices at idx_out + idx_off[b], its codes at codes_out +
  * codes_off[b] and its scales at scales_out + scales_off[b]
  * (gc_bucket_offsets).  group must be a power of two in 4 .. 128
- * (GC_ERR_UNSUPPORTED otherwise); err must not be NULL.
+ * (GC_ERR_UNSUPPORTED otherwise); err must not be NULL.  diag_out: NULL, or
+ * the diagnostics above (g_hat = the dequantised kept values).
  */
 GC_API gc_status gc_ef_topk_quant_buckets(gc_ctx* ctx, const float* grad, float* err,
                                           int bits, int64_t group, int rounding,
                                           uint64_t seed, uint64_t step, int32_t* idx_out,
-                                          uint8_t* codes_out, float* scales_out);
+                                          uint8_t* codes_out, float* scales_out,
+                                          double* diag_out);
 
 /*
  * Largest n accepted by gc_ef_topk_noalloc: its scratch is a fixed device

@@ -114,9 +114,9 @@ def test_bucket_calls_validate_on_the_host(gc):
     n = (ctypes.c_int64 * 2)(8, 8)
     k = (ctypes.c_int64 * 2)(1, 1)
     assert L.gc_ctx_set_buckets(None, 2, n, k) == gc.ERR_INVALID_ARG
-    assert L.gc_ef_topk_buckets(None, None, None, None, None) == gc.ERR_INVALID_ARG
-    assert L.gc_ef_topk_quant_buckets(None, None, None, 8, 64, 0, 0, 0, None, None, None) == \
-        gc.ERR_INVALID_ARG
+    assert L.gc_ef_topk_buckets(None, None, None, None, None, None) == gc.ERR_INVALID_ARG
+    assert L.gc_ef_topk_quant_buckets(None, None, None, 8, 64, 0, 0, 0, None, None, None,
+                                      None) == gc.ERR_INVALID_ARG
     out = (ctypes.c_int64 * 3)()
     assert L.gc_bucket_offsets(0, k, 8, 64, out, None, None) == gc.ERR_INVALID_ARG
     assert L.gc_bucket_offsets(2, None, 8, 64, out, None, None) == gc.ERR_INVALID_ARG
