@@ -30,6 +30,10 @@
  *   TernGrad: W. Wen et al., "TernGrad: Ternary Gradients to Reduce
  *        Communication in Distributed Deep Learning", NeurIPS 2017, eq. 2
  *        (s = max|g|, Bernoulli(|g|/s) times sign times s).
+ *   Cody-Waite: W. J. Cody, W. Waite, "Software Manual for the Elementary
+ *        Functions", Prentice-Hall 1980, the ALOG and EXP chapters (argument
+ *        reduction by ln 2 split in two parts, a series in s = (m-1)/(m+1)
+ *        for the logarithm, a polynomial for exp on [-ln2/2, ln2/2]).
  *   PowerSGD: T. Vogels, S. P. Karimireddy, M. Jaggi, "PowerSGD: Practical
  *        Low-Rank Gradient Compression for Distributed Optimization",
  *        NeurIPS 2019, Algorithm 1 (P = MQ, orthogonalise, Q = M^T P,
@@ -57,6 +61,7 @@
 #define ORC_MINMAX 0
 #define ORC_QSGD 1
 #define ORC_TERN 2
+#define ORC_LOG 3
 
 #define ORC_NEAREST_EVEN 0
 #define ORC_STOCHASTIC 1
@@ -262,6 +267,86 @@ static float tree_sum_squares(const float* x, int64_t len, float* scratch) {
   return scratch[0];
 }
 
+/* ------------------------------------------------------------------------ */
+/* Natural logarithm and exponential in binary32 (logarithmic quantisation). */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [P2 二.1 对数量化] needs log and exp, and its level q = round(log(|g|+1) /
+ * scale) is an integer that a one-ulp difference in log can change.
+ * Reading: the pages do not fix the functions to the bit, so log and exp are
+ * defined here by the Cody-Waite method, every step one binary32 operation
+ * (the CUDA library implements the same definition independently); their
+ * accuracy against the true functions is checked by the tests.
+ *
+ * ln 2 = LN2_HI + LN2_LO: LN2_HI = 45426 / 2^16 (16 significant bits, so
+ * k * LN2_HI is exact for |k| < 2^8) and LN2_LO = ln 2 - LN2_HI rounded to
+ * binary32.  The series coefficients are 1/(2j+1) and 1/j! rounded to
+ * binary32.
+ */
+#define LN2_HI 0x1.62e4p-1f
+#define LN2_LO 0x1.7f7d1cp-20f
+#define INV_LN2 0x1.715476p+0f
+#define SQRT2_F 0x1.6a09e6p+0f
+
+/*
+ * log(x) for finite x >= 1: x = 2^k m with m in [sqrt(2)/2, sqrt(2)],
+ * s = (m - 1) / (m + 1), log m = 2 atanh(s) = 2s (1 + z/3 + z^2/5 + ...
+ * + z^5/11), z = s^2 (|s| <= 0.1716, the first omitted term is below
+ * 2^-36 of 2s); log x = k LN2_HI + (k LN2_LO + log m).
+ */
+float orc_logf(float x) {
+  uint32_t u;
+  memcpy(&u, &x, 4);
+  int k = (int)(u >> 23) - 127;
+  u = (u & 0x007fffffu) | 0x3f800000u;
+  float m;
+  memcpy(&m, &u, 4);
+  if (m > SQRT2_F) {
+    m = m * 0.5f;
+    k += 1;
+  }
+  float f = m - 1.0f;
+  float s = f / (f + 2.0f);
+  float z = s * s;
+  float r = 0x1.745d18p-4f;             /* 1/11 */
+  r = 0x1.c71c72p-4f + z * r;           /* 1/9 */
+  r = 0x1.24924ap-3f + z * r;           /* 1/7 */
+  r = 0x1.99999ap-3f + z * r;           /* 1/5 */
+  r = 0x1.555556p-2f + z * r;           /* 1/3 */
+  r = z * r;
+  float w = s + s;
+  float logm = w + w * r;
+  float kf = (float)k;
+  return kf * LN2_HI + (kf * LN2_LO + logm);
+}
+
+/*
+ * exp(y) for 0 <= y < 89: k = rint(y / ln 2), r = (y - k LN2_HI) - k LN2_LO
+ * (|r| <= ln2 / 2), exp r = 1 + r + r^2/2! + ... + r^8/8! (Horner; the first
+ * omitted term is below 2^-31), exp y = 2^k exp r (an exact scaling; k = 128
+ * overflows to +inf).
+ */
+float orc_expf(float y) {
+  float kf = rintf(y * INV_LN2);
+  float r = (y - kf * LN2_HI) - kf * LN2_LO;
+  float p = 0x1.a01a02p-16f;            /* 1/8! */
+  p = 0x1.a01a02p-13f + r * p;          /* 1/7! */
+  p = 0x1.6c16c2p-10f + r * p;          /* 1/6! */
+  p = 0x1.111112p-7f + r * p;           /* 1/5! */
+  p = 0x1.555556p-5f + r * p;           /* 1/4! */
+  p = 0x1.555556p-3f + r * p;           /* 1/3! */
+  p = 0.5f + r * p;                     /* 1/2! */
+  p = 1.0f + r * p;
+  p = 1.0f + r * p;
+  int k = (int)kf;
+  if (k >= 128) return INFINITY;
+  uint32_t bits = (uint32_t)(k + 127) << 23;
+  float two_k;
+  memcpy(&two_k, &bits, 4);
+  return p * two_k;
+}
+
 typedef struct {
   float scale;  /* step between levels (0 means every code is 0) */
   float offset; /* min-max: the group minimum; otherwise unused */
@@ -277,6 +362,9 @@ typedef struct {
  *           square root of tree_sum_squares.
  *  TernGrad [P1 1.1 "逐层归一化"; Wen et al. eq. 2]: scale = max |c| over the
  *           group (the group is the whole tensor for layer-wise scaling).
+ *  log      [P2 二.1 对数量化]: scale = log(max |c| + 1) / (2^(b-1) - 1), one
+ *           bit being the sign; max over the group (the page's example takes
+ *           the whole tensor: group 0).
  */
 static group_param group_stats(const float* x, int64_t len, int bits, int mode,
                                float* scratch) {
@@ -297,13 +385,18 @@ static group_param group_stats(const float* x, int64_t len, int bits, int mode,
     float norm = sqrtf(ss);
     float levels = (float)((1 << bits) - 1);
     p.scale = norm / levels;
-  } else { /* ORC_TERN */
+  } else { /* ORC_TERN, ORC_LOG */
     float mx = 0.0f;
     for (int64_t i = 0; i < len; ++i) {
       float a = fabsf(x[i]);
       if (a > mx) mx = a;
     }
-    p.scale = mx;
+    if (mode == ORC_TERN) {
+      p.scale = mx;
+    } else {
+      float levels = (float)((1 << (bits - 1)) - 1);
+      p.scale = orc_logf(mx + 1.0f) / levels;
+    }
   }
   return p;
 }
@@ -355,19 +448,22 @@ static int check_quant_args(int64_t n, int bits, int64_t group, int mode,
                             int rounding) {
   if (n < 0 || n > INT32_MAX || group < 0) return ORC_EINVAL;
   if (!valid_bits(bits)) return ORC_EUNSUP;
-  if (mode != ORC_MINMAX && mode != ORC_QSGD && mode != ORC_TERN)
+  if (mode != ORC_MINMAX && mode != ORC_QSGD && mode != ORC_TERN && mode != ORC_LOG)
     return ORC_EINVAL;
   if (mode == ORC_TERN && bits != 2) return ORC_EUNSUP;
+  if (mode == ORC_LOG && bits == 1) return ORC_EUNSUP; /* no magnitude bit */
   if (rounding != ORC_NEAREST_EVEN && rounding != ORC_STOCHASTIC)
     return ORC_EINVAL;
   return ORC_OK;
 }
 
 /* Dequantised value of one element ([P2 二.1]: g_hat = q*scale + min, two
- * separate roundings; QSGD / TernGrad: sign times q*scale). */
+ * separate roundings; QSGD / TernGrad: sign times q*scale; log: sign times
+ * exp(q*scale) - 1). */
 static float dequant_one(uint32_t q, int negative, group_param p, int mode) {
   float mag = (float)q * p.scale;
   if (mode == ORC_MINMAX) return mag + p.offset;
+  if (mode == ORC_LOG) mag = orc_expf(mag) - 1.0f;
   return negative ? -mag : mag;
 }
 
@@ -377,6 +473,8 @@ static float dequant_one(uint32_t q, int negative, group_param p, int mode) {
  *  min-max:  t = (x - min) / scale, q in [0, 2^b - 1].
  *  QSGD:     t = |x| / scale, q in [0, 2^b - 1], sign in the sign plane.
  *  TernGrad: t = |x| / scale, q in {0, 1}, 2-bit code (sign << 1) | q.
+ *  log:      t = log(|x| + 1) / scale, q in [0, 2^(b-1) - 1], b-bit
+ *            sign-magnitude code (sign << (b-1)) | q.
  * scale == 0 (a constant group for min-max, an all-zero group otherwise)
  * gives q = 0 without dividing.  A sign is recorded only when q != 0, so a
  * zero code always dequantises to +0.
@@ -396,7 +494,9 @@ static int quant_core(const float* x, int64_t n, int64_t base, int bits,
   int64_t ng = num_groups(n, group);
   float* scratch = (float*)malloc((size_t)G * sizeof(float));
   if (!scratch) return ORC_ENOMEM;
-  uint32_t top = (mode == ORC_TERN) ? 1u : ((1u << bits) - 1u);
+  uint32_t top = (mode == ORC_TERN)  ? 1u
+                 : (mode == ORC_LOG) ? ((1u << (bits - 1)) - 1u)
+                                     : ((1u << bits) - 1u);
   for (int64_t g = 0; g < ng; ++g) {
     int64_t start = g * G;
     int64_t len = (n - start < G) ? (n - start) : G;
@@ -411,6 +511,8 @@ static int quant_core(const float* x, int64_t n, int64_t base, int bits,
       float t;
       if (mode == ORC_MINMAX)
         t = p.scale == 0.0f ? 0.0f : (x[i] - p.offset) / p.scale;
+      else if (mode == ORC_LOG)
+        t = p.scale == 0.0f ? 0.0f : orc_logf(fabsf(x[i]) + 1.0f) / p.scale;
       else
         t = p.scale == 0.0f ? 0.0f : fabsf(x[i]) / p.scale;
       uint32_t q = p.scale == 0.0f
@@ -420,6 +522,8 @@ static int quant_core(const float* x, int64_t n, int64_t base, int bits,
       int negative = (mode != ORC_MINMAX) && q != 0 && x[i] < 0.0f;
       if (mode == ORC_TERN) {
         put_bits(codes_out, i, 2, ((uint32_t)negative << 1) | q);
+      } else if (mode == ORC_LOG) {
+        put_bits(codes_out, i, bits, ((uint32_t)negative << (bits - 1)) | q);
       } else {
         put_bits(codes_out, i, bits, q);
         if (mode == ORC_QSGD && negative) put_bits(sign_plane, i, 1, 1u);
@@ -478,6 +582,9 @@ int orc_dequant(const uint8_t* codes, const float* scales, int64_t n, int bits,
     if (mode == ORC_TERN) {
       q = code & 1u;
       negative = (int)(code >> 1);
+    } else if (mode == ORC_LOG) {
+      q = code & ((1u << (bits - 1)) - 1u);
+      negative = (int)(code >> (bits - 1));
     } else {
       q = code;
       negative = mode == ORC_QSGD ? (int)get_bits(sign_plane, i, 1) : 0;
@@ -509,6 +616,63 @@ int orc_ef_quant(const float* grad, float* err, int64_t n, int bits,
     for (int64_t i = 0; i < n; ++i) err[i] = c[i] - g_hat[i];
   free(c);
   free(g_hat);
+  return st;
+}
+
+/*
+ * Differential quantisation ([P2 二.4 差分量化]): only the difference between
+ * the gradient and the previous one is sent, quantised with few bits; the
+ * page notes that both sides keep a gradient history and that errors pile up
+ * over the steps unless corrected from time to time.  Reading: the history
+ * ref is the gradient the receiver reconstructed last (closed loop, the
+ * same on both sides, so quantisation errors do not pile up in it), and a
+ * refresh step (the periodic correction) sends the full gradient, as if ref
+ * were 0.  With error feedback ([P4 梯度压缩原理]):
+ *   c = g + e (or g);  r = refresh ? 0 : ref;  d = c - r;
+ *   (codes, scales) = quant(d);  d_hat = dequant(codes, scales);
+ *   g_hat = r + d_hat;  e' = c - g_hat (when e is given);  ref' = g_hat.
+ * Every step is one binary32 operation.
+ */
+int orc_ef_diff_quant(const float* grad, float* err, float* ref, int64_t n, int bits,
+                      int64_t group, int mode, int rounding, uint64_t seed, uint64_t step,
+                      int refresh, uint8_t* codes_out, float* scales_out) {
+  int st = check_quant_args(n, bits, group, mode, rounding);
+  if (st != ORC_OK) return st;
+  if (!ref && n > 0) return ORC_EINVAL;
+  float* c = (float*)malloc((size_t)(n > 0 ? n : 1) * sizeof(float));
+  float* d = (float*)malloc((size_t)(n > 0 ? n : 1) * sizeof(float));
+  float* d_hat = (float*)malloc((size_t)(n > 0 ? n : 1) * sizeof(float));
+  if (!c || !d || !d_hat) { free(c); free(d); free(d_hat); return ORC_ENOMEM; }
+  for (int64_t i = 0; i < n; ++i) {
+    c[i] = err ? grad[i] + err[i] : grad[i];
+    float r = refresh ? 0.0f : ref[i];
+    d[i] = c[i] - r;
+  }
+  st = quant_core(d, n, 0, bits, group, mode, rounding, seed, step, codes_out, scales_out,
+                  d_hat);
+  if (st == ORC_OK) {
+    for (int64_t i = 0; i < n; ++i) {
+      float r = refresh ? 0.0f : ref[i];
+      float g_hat = r + d_hat[i];
+      if (err) err[i] = c[i] - g_hat;
+      ref[i] = g_hat;
+    }
+  }
+  free(c);
+  free(d);
+  free(d_hat);
+  return st;
+}
+
+/* The receiving side: ref' = (refresh ? 0 : ref) + dequant(codes, scales). */
+int orc_diff_dequant(const uint8_t* codes, const float* scales, int64_t n, int bits,
+                     int64_t group, int mode, int refresh, float* ref) {
+  float* d_hat = (float*)malloc((size_t)(n > 0 ? n : 1) * sizeof(float));
+  if (!d_hat) return ORC_ENOMEM;
+  int st = orc_dequant(codes, scales, n, bits, group, mode, d_hat);
+  if (st == ORC_OK)
+    for (int64_t i = 0; i < n; ++i) ref[i] = (refresh ? 0.0f : ref[i]) + d_hat[i];
+  free(d_hat);
   return st;
 }
 

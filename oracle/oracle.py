@@ -14,9 +14,9 @@ import numpy as np
 
 from . import build as _build
 
-MINMAX, QSGD, TERN = 0, 1, 2
+MINMAX, QSGD, TERN, LOG = 0, 1, 2, 3
 NEAREST_EVEN, STOCHASTIC = 0, 1
-MODES = {"minmax": MINMAX, "qsgd": QSGD, "tern": TERN}
+MODES = {"minmax": MINMAX, "qsgd": QSGD, "tern": TERN, "log": LOG}
 ROUNDINGS = {"nearest_even": NEAREST_EVEN, "stochastic": STOCHASTIC}
 
 _lib = None
@@ -73,6 +73,15 @@ def lib():
         L.orc_ef_randk.argtypes = [_f32p, _f32p, _i64, ctypes.c_float, _u64, _u64, _i32p,
                                    _f32p, _i64, ctypes.POINTER(_i64)]
         L.orc_ef_randk.restype = _int
+        L.orc_logf.argtypes = [ctypes.c_float]
+        L.orc_logf.restype = ctypes.c_float
+        L.orc_expf.argtypes = [ctypes.c_float]
+        L.orc_expf.restype = ctypes.c_float
+        L.orc_ef_diff_quant.argtypes = [_f32p, _f32p, _f32p, _i64, _int, _i64, _int, _int,
+                                        _u64, _u64, _int, _u8p, _f32p]
+        L.orc_ef_diff_quant.restype = _int
+        L.orc_diff_dequant.argtypes = [_u8p, _f32p, _i64, _int, _i64, _int, _int, _f32p]
+        L.orc_diff_dequant.restype = _int
         L.orc_diagnostics.argtypes = [_f32p, _f32p, _i64, _i32p, _f32p, _i64,
                                       ctypes.POINTER(ctypes.c_double)]
         L.orc_diagnostics.restype = _int
@@ -204,6 +213,50 @@ def ef_quant(grad, err, bits, group, mode, rounding="nearest_even", seed=0,
                               _p(codes, _u8p), _p(scales, _f32p)),
            "orc_ef_quant")
     return codes[:cb], scales[:sf], e
+
+
+def logf(x):
+    """The oracle's binary32 natural logarithm (x >= 1)."""
+    return np.float32(lib().orc_logf(float(x)))
+
+
+def expf(y):
+    """The oracle's binary32 exponential (0 <= y < 89)."""
+    return np.float32(lib().orc_expf(float(y)))
+
+
+def ef_diff_quant(grad, err, ref, bits, group, mode, rounding="nearest_even", seed=0, step=0,
+                  refresh=False):
+    """EF + differential quantisation against the history ref.  Returns
+    (codes, scales, err' or None, ref')."""
+    g = _f32(grad)
+    e = _f32(err) if err is not None else None
+    r = _f32(ref)
+    n = g.size
+    m = _mode(mode)
+    cb = codes_bytes(n, bits, m)
+    sf = scales_floats(n, group, m)
+    codes = np.zeros(max(cb, 1), dtype=np.uint8)
+    scales = np.zeros(max(sf, 1), dtype=np.float32)
+    _check(lib().orc_ef_diff_quant(_p(g, _f32p), _p(e, _f32p) if e is not None else None,
+                                   _p(r, _f32p), n, bits, group, m, _rounding(rounding), seed,
+                                   step, 1 if refresh else 0, _p(codes, _u8p),
+                                   _p(scales, _f32p)), "orc_ef_diff_quant")
+    return codes[:cb], scales[:sf], e, r
+
+
+def diff_dequant(codes, scales, ref, n, bits, group, mode, refresh=False):
+    """The receiving side of differential quantisation: returns ref'."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8).copy()
+    s = _f32(scales)
+    r = _f32(ref)
+    if c.size == 0:
+        c = np.zeros(1, dtype=np.uint8)
+    if s.size == 0:
+        s = np.zeros(1, dtype=np.float32)
+    _check(lib().orc_diff_dequant(_p(c, _u8p), _p(s, _f32p), n, bits, group, _mode(mode),
+                                  1 if refresh else 0, _p(r, _f32p)), "orc_diff_dequant")
+    return r
 
 
 def ef_topk_quant(grad, err, k, bits, group, rounding="nearest_even", seed=0,

@@ -13,6 +13,7 @@ import oracle.oracle as ofront
 
 from tests import test_oracle_aggregate as tagg
 from tests import test_oracle_diag as tdiag
+from tests import test_oracle_logdiff as tlog
 from tests import test_oracle_philox as tphilox
 from tests import test_oracle_powersgd as tpsgd
 from tests import test_oracle_quant as tquant
@@ -56,6 +57,16 @@ MUTANTS = {
     "randk_compare_flipped": ("int keep = orc_uniform(seed, step, (uint64_t)i) < p;",
                               "int keep = orc_uniform(seed, step, (uint64_t)i) >= p;"),
     "randk_residual_not_zeroed": ("if (err) err[i] = keep ? 0.0f : c;", "if (err) err[i] = c;"),
+    "log_plus_one_dropped": ("t = p.scale == 0.0f ? 0.0f : orc_logf(fabsf(x[i]) + 1.0f) / p.scale;",
+                             "t = p.scale == 0.0f ? 0.0f : orc_logf(fabsf(x[i]) + 0.0f) / p.scale;"),
+    "log_levels_ignore_sign_bit": ("float levels = (float)((1 << (bits - 1)) - 1);\n      p.scale = orc_logf",
+                                   "float levels = (float)((1 << bits) - 1);\n      p.scale = orc_logf"),
+    "log_series_term_dropped": ("r = 0x1.555556p-2f + z * r;", "r = 0x1.555556p-2f + 0.0f * r;"),
+    "exp_range_reduction_lo_dropped": ("float r = (y - kf * LN2_HI) - kf * LN2_LO;",
+                                       "float r = (y - kf * LN2_HI);"),
+    "diff_open_loop_history": ("      ref[i] = g_hat;\n", "      ref[i] = c[i];\n"),
+    "diff_refresh_ignored": ("    float r = refresh ? 0.0f : ref[i];\n    d[i] = c[i] - r;",
+                             "    float r = ref[i];\n    d[i] = c[i] - r;"),
     "diag_energy_of_c_not_residual": ("s_e += (double)r * (double)r;",
                                       "s_e += (double)c * (double)c;"),
     "diag_sent_norm_from_c": ("s_g += (double)g_hat[j] * (double)g_hat[j];",
@@ -86,6 +97,11 @@ def _pins(golden_dir):
     yield lambda: tagg.test_quant_hand_case(golden_dir)
     yield lambda: trandk.test_keep_set_is_the_philox_draw_below_p(1000, 0.1, 3, 0)
     yield lambda: trandk.test_limits()
+    yield lambda: tlog.test_log_exp_accuracy()
+    yield lambda: tlog.test_log_hand_case()
+    yield lambda: tlog.test_diff_hand_case()
+    yield lambda: tlog.test_refresh_is_plain_quantisation("minmax", 4)
+    yield lambda: tlog.test_closed_loop_over_steps("qsgd", 4)
     yield lambda: tdiag.test_hand_case()
     yield lambda: tdiag.test_hybrid_matches_the_stored_residual(8, 64)
 
