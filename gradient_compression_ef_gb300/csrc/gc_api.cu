@@ -18,10 +18,12 @@ bool valid_bits(int bits) { return bits == 1 || bits == 2 || bits == 4 || bits =
 
 gc_status check_quant(int64_t n, int bits, int64_t group, int mode, int rounding) {
   if (n < 0 || n > INT32_MAX || group < 0) return GC_ERR_INVALID_ARG;
-  if (mode != GC_MINMAX && mode != GC_QSGD && mode != GC_TERN) return GC_ERR_INVALID_ARG;
+  if (mode != GC_MINMAX && mode != GC_QSGD && mode != GC_TERN && mode != GC_LOG)
+    return GC_ERR_INVALID_ARG;
   if (rounding != GC_NEAREST_EVEN && rounding != GC_STOCHASTIC) return GC_ERR_INVALID_ARG;
   if (!valid_bits(bits)) return GC_ERR_UNSUPPORTED;
   if (mode == GC_TERN && bits != 2) return GC_ERR_UNSUPPORTED;
+  if (mode == GC_LOG && bits == 1) return GC_ERR_UNSUPPORTED;  // no magnitude bit
   return GC_OK;
 }
 
@@ -101,7 +103,7 @@ const char* gc_status_string(int status) {
 
 int64_t gc_codes_bytes(int64_t n, int bits, int mode) {
   if (n < 0 || !valid_bits(bits)) return -1;
-  if (mode != GC_MINMAX && mode != GC_QSGD && mode != GC_TERN) return -1;
+  if (mode != GC_MINMAX && mode != GC_QSGD && mode != GC_TERN && mode != GC_LOG) return -1;
   const int cb = mode == GC_TERN ? 2 : bits;
   int64_t bytes = round_up((n * cb + 7) / 8, 16);
   if (mode == GC_QSGD) bytes += round_up((n + 7) / 8, 16);
@@ -110,7 +112,7 @@ int64_t gc_codes_bytes(int64_t n, int bits, int mode) {
 
 int64_t gc_scales_floats(int64_t n, int64_t group, int mode) {
   if (n < 0 || group < 0) return -1;
-  if (mode != GC_MINMAX && mode != GC_QSGD && mode != GC_TERN) return -1;
+  if (mode != GC_MINMAX && mode != GC_QSGD && mode != GC_TERN && mode != GC_LOG) return -1;
   if (n == 0) return 0;
   const int64_t G = group == 0 ? n : group;
   return ceil_div(n, G) * (mode == GC_MINMAX ? 2 : 1);
@@ -361,6 +363,35 @@ gc_status gc_ef_quant(gc_ctx* ctx, const float* grad, float* err, int64_t n, int
   if (!guard.ok) return GC_ERR_CUDA;
   return gc::launch_quant(ctx, grad, err, nullptr, 0, n, bits, group, mode, rounding, seed,
                           step, codes_out, scales_out);
+}
+
+gc_status gc_ef_diff_quant(gc_ctx* ctx, const float* grad, float* err, float* ref, int64_t n,
+                           int bits, int64_t group, int mode, int rounding, uint64_t seed,
+                           uint64_t step, int refresh, uint8_t* codes_out, float* scales_out) {
+  if (!ctx) return GC_ERR_INVALID_ARG;
+  GC_TRY(check_quant(n, bits, group, mode, rounding));
+  GC_TRY(check_buf(grad, n > 0));
+  if (err) GC_TRY(check_buf(err, n > 0));
+  GC_TRY(check_buf(ref, n > 0));
+  GC_TRY(check_buf(codes_out, n > 0));
+  GC_TRY(check_buf(scales_out, n > 0));
+  if (n > 0 && !gc::quant_is_fused(n, group)) return GC_ERR_UNSUPPORTED;
+  DeviceGuard guard(ctx->device);
+  if (!guard.ok) return GC_ERR_CUDA;
+  return gc::launch_diff_quant(ctx, grad, err, ref, n, bits, group, mode, rounding, seed, step,
+                               refresh, codes_out, scales_out);
+}
+
+gc_status gc_diff_dequant(gc_ctx* ctx, const uint8_t* codes, const float* scales, int64_t n,
+                          int bits, int64_t group, int mode, int refresh, float* ref) {
+  if (!ctx) return GC_ERR_INVALID_ARG;
+  GC_TRY(check_quant(n, bits, group, mode, GC_NEAREST_EVEN));
+  GC_TRY(check_buf(codes, n > 0));
+  GC_TRY(check_buf(scales, n > 0));
+  GC_TRY(check_buf(ref, n > 0));
+  DeviceGuard guard(ctx->device);
+  if (!guard.ok) return GC_ERR_CUDA;
+  return gc::launch_diff_dequant(ctx, codes, scales, n, bits, group, mode, refresh, ref);
 }
 
 gc_status gc_ef_topk_quant(gc_ctx* ctx, const float* grad, float* err, int64_t n, int64_t k,

@@ -233,6 +233,72 @@ __device__ __forceinline__ void uniform4(uint64_t block, uint64_t seed,
   u[3] = __fmul_rn(__uint2float_rn(r.w >> 8), 0x1p-24f);
 }
 
+// Natural logarithm and exponential of the logarithmic quantiser, by the
+// Cody-Waite method (W. J. Cody, W. Waite, "Software Manual for the
+// Elementary Functions", 1980, ALOG and EXP), every step one rounded
+// binary32 operation so that any IEEE-754 evaluation of the same steps gives
+// the same bits.  ln 2 = kLn2Hi + kLn2Lo with kLn2Hi = 45426 * 2^-16 (16
+// significant bits: k * kLn2Hi is exact for |k| < 256) and kLn2Lo the rest
+// rounded to binary32; the series coefficients are 1/(2j+1) and 1/j!
+// rounded to binary32.
+constexpr float kLn2Hi = 0x1.62e4p-1f;
+constexpr float kLn2Lo = 0x1.7f7d1cp-20f;
+constexpr float kInvLn2 = 0x1.715476p+0f;
+constexpr float kSqrt2 = 0x1.6a09e6p+0f;
+
+// log x for finite x >= 1: x = 2^k m with m in [sqrt(2)/2, sqrt(2)],
+// s = (m - 1) / (m + 1), log m = 2 atanh s = 2s (1 + z/3 + ... + z^5/11),
+// z = s^2; log x = k kLn2Hi + (k kLn2Lo + log m).
+__device__ __forceinline__ float cw_logf(float x) {
+  uint32_t u = __float_as_uint(x);
+  int k = (int)(u >> 23) - 127;
+  float m = __uint_as_float((u & 0x007fffffu) | 0x3f800000u);
+  if (m > kSqrt2) {
+    m = __fmul_rn(m, 0.5f);
+    k += 1;
+  }
+  const float f = __fsub_rn(m, 1.0f);
+  const float s = __fdiv_rn(f, __fadd_rn(f, 2.0f));
+  const float z = __fmul_rn(s, s);
+  float r = 0x1.745d18p-4f;                    // 1/11
+  r = __fadd_rn(0x1.c71c72p-4f, __fmul_rn(z, r));  // 1/9
+  r = __fadd_rn(0x1.24924ap-3f, __fmul_rn(z, r));  // 1/7
+  r = __fadd_rn(0x1.99999ap-3f, __fmul_rn(z, r));  // 1/5
+  r = __fadd_rn(0x1.555556p-2f, __fmul_rn(z, r));  // 1/3
+  r = __fmul_rn(z, r);
+  const float w = __fadd_rn(s, s);
+  const float logm = __fadd_rn(w, __fmul_rn(w, r));
+  const float kf = (float)k;
+  return __fadd_rn(__fmul_rn(kf, kLn2Hi), __fadd_rn(__fmul_rn(kf, kLn2Lo), logm));
+}
+
+// exp y for 0 <= y < 89: k = rint(y / ln 2), r = (y - k kLn2Hi) - k kLn2Lo,
+// exp r by the Taylor polynomial to r^8/8! (Horner), times 2^k exactly;
+// k >= 128 overflows to +inf.
+__device__ __forceinline__ float cw_expf(float y) {
+  const float kf = rintf(__fmul_rn(y, kInvLn2));
+  const float r = __fsub_rn(__fsub_rn(y, __fmul_rn(kf, kLn2Hi)), __fmul_rn(kf, kLn2Lo));
+  float p = 0x1.a01a02p-16f;                       // 1/8!
+  p = __fadd_rn(0x1.a01a02p-13f, __fmul_rn(r, p));  // 1/7!
+  p = __fadd_rn(0x1.6c16c2p-10f, __fmul_rn(r, p));  // 1/6!
+  p = __fadd_rn(0x1.111112p-7f, __fmul_rn(r, p));   // 1/5!
+  p = __fadd_rn(0x1.555556p-5f, __fmul_rn(r, p));   // 1/4!
+  p = __fadd_rn(0x1.555556p-3f, __fmul_rn(r, p));   // 1/3!
+  p = __fadd_rn(0.5f, __fmul_rn(r, p));             // 1/2!
+  p = __fadd_rn(1.0f, __fmul_rn(r, p));
+  p = __fadd_rn(1.0f, __fmul_rn(r, p));
+  const int k = (int)kf;
+  if (k >= 128) return __int_as_float(0x7f800000);
+  return __fmul_rn(p, __uint_as_float((uint32_t)(k + 127) << 23));
+}
+
+// Top level of a mode's code: TernGrad 1, logarithmic 2^(b-1) - 1 (one bit
+// is the sign), otherwise 2^b - 1.
+template <int MODE, int BITS>
+__host__ __device__ constexpr uint32_t mode_top() {
+  return MODE == GC_TERN ? 1u : MODE == GC_LOG ? ((1u << (BITS - 1)) - 1u) : ((1u << BITS) - 1u);
+}
+
 // Level of one element: t >= 0 is its position on the level grid.
 // Nearest-even: rint(t).  Stochastic: floor(t) + [u < t - floor(t)].
 // Clamped to [0, top].
@@ -260,10 +326,12 @@ __device__ __forceinline__ uint32_t quantize_one(float c, float scale,
   uint32_t q = 0u;
   if (scale != 0.0f) {
     const float t = (MODE == GC_MINMAX) ? __fdiv_rn(__fsub_rn(c, offset), scale)
+                    : (MODE == GC_LOG)  ? __fdiv_rn(cw_logf(__fadd_rn(fabsf(c), 1.0f)), scale)
                                         : __fdiv_rn(fabsf(c), scale);
     q = round_level(t, stochastic, u, top);
   }
-  const float mag = __fmul_rn((float)q, scale);
+  float mag = __fmul_rn((float)q, scale);
+  if (MODE == GC_LOG) mag = __fsub_rn(cw_expf(mag), 1.0f);
   if (MODE == GC_MINMAX) {
     *negative = false;
     *ghat = __fadd_rn(mag, offset);
@@ -426,6 +494,15 @@ gc_status launch_quant_buckets(gc_ctx* ctx, float* err, const int32_t* idx_out, 
 // Per-bucket diagnostics {sum c^2, sum g_hat^2, sum e'^2} into out[nb][3]
 // from the partial sums of the last bucketed call (quant: the hybrid's).
 gc_status launch_bucket_diag(gc_ctx* ctx, bool quant, double* out);
+// EF + differential quantisation (group 4..128, a power of two) against the
+// history ref; refresh treats ref as 0.
+gc_status launch_diff_quant(gc_ctx* ctx, const float* grad, float* err, float* ref, int64_t n,
+                            int bits, int64_t group, int mode, int rounding, uint64_t seed,
+                            uint64_t step, int refresh, uint8_t* codes_out, float* scales_out);
+// ref = (refresh ? 0 : ref) + dequant(codes, scales).
+gc_status launch_diff_dequant(gc_ctx* ctx, const uint8_t* codes, const float* scales,
+                              int64_t n, int bits, int64_t group, int mode, int refresh,
+                              float* ref);
 // EF + random sparsification over n <= max_n elements (list scratch in the
 // context); writes at most `capacity` entries and the kept count.
 gc_status launch_ef_randk(gc_ctx* ctx, const float* grad, float* err, int64_t n, float p,

@@ -56,7 +56,7 @@ namespace {
 
 constexpr int kQThreads = 256;
 
-enum IoKind { IO_PLAIN = 0, IO_EF = 1, IO_SCATTER = 2 };
+enum IoKind { IO_PLAIN = 0, IO_EF = 1, IO_SCATTER = 2, IO_DIFF = 3 };
 
 struct QuantOut {
   uint8_t* codes;
@@ -66,6 +66,8 @@ struct QuantOut {
   int64_t szero_begin, szero_end;  // padding bytes of the sign plane
   int64_t scatter_n;               // length of err for the scattered residual
   uint32_t* status;                // device status word
+  float* ref;                      // differential quantisation: the history
+  int refresh;                     // differential quantisation: ref taken as 0
 };
 
 __device__ __forceinline__ void zero_padding_bytes(const QuantOut& o) {
@@ -80,11 +82,12 @@ __device__ __forceinline__ void zero_padding(const QuantOut& o) {
 
 template <int MODE, int BITS>
 __device__ __forceinline__ uint32_t code_bits4(const uint32_t q[4], const bool neg[4]) {
-  if (MODE == GC_TERN) {
+  if (MODE == GC_TERN || MODE == GC_LOG) {  // sign-magnitude
+    constexpr int SB = MODE == GC_TERN ? 1 : BITS - 1;
     uint32_t t[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) t[j] = q[j] | ((uint32_t)neg[j] << 1);
-    return pack4<2>(t);
+    for (int j = 0; j < 4; ++j) t[j] = q[j] | ((uint32_t)neg[j] << SB);
+    return pack4<(MODE == GC_TERN) ? 2 : BITS>(t);
   }
   return pack4<BITS>(q);
 }
@@ -125,14 +128,15 @@ __device__ __forceinline__ void quant_load4(const float* __restrict__ x,
 // base + 4l + 3 with values c[] (from quant_load4).  Every lane of the warp
 // must call it.
 // With DIAG, dsum[0] and dsum[1] accumulate this lane's g_hat^2 and e'^2.
+// IO_DIFF writes no residual: the dequantised values go to ghat_out[4].
 template <int MODE, int BITS, int LPG, int IO, bool DIAG = false>
 __device__ __forceinline__ void quant_fused_apply(
     float c[4], const bool valid[4], float* __restrict__ err,
     const int32_t* __restrict__ scatter_idx, int64_t n, const QuantOut& o,
     int stochastic, uint64_t seed, uint64_t step, int64_t base, int lane,
-    float* dsum = nullptr) {
+    float* dsum = nullptr, float* ghat_out = nullptr) {
   constexpr int G = 4 * LPG;
-  constexpr uint32_t top = (MODE == GC_TERN) ? 1u : ((1u << BITS) - 1u);
+  constexpr uint32_t top = mode_top<MODE, BITS>();
   const float levels = (float)top;
   const int64_t i0 = base + 4 * lane;
   const bool active = i0 < n;
@@ -158,11 +162,11 @@ __device__ __forceinline__ void quant_fused_apply(
                         __fadd_rn(__fmul_rn(c[2], c[2]), __fmul_rn(c[3], c[3])));
     s = warp_sum_tree(s, LPG);
     scale = __fdiv_rn(__fsqrt_rn(s), levels);
-  } else {
+  } else {  // TernGrad, logarithmic: max |c|
     float m = fmaxf(fmaxf(fabsf(c[0]), fabsf(c[1])), fmaxf(fabsf(c[2]), fabsf(c[3])));
 #pragma unroll
     for (int o2 = 1; o2 < LPG; o2 <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o2));
-    scale = m;
+    scale = MODE == GC_LOG ? __fdiv_rn(cw_logf(__fadd_rn(m, 1.0f)), levels) : m;
   }
   if (active && (lane % LPG) == 0) {
     const int64_t g = i0 / G;
@@ -182,6 +186,7 @@ __device__ __forceinline__ void quant_fused_apply(
     float gh;
     q[j] = quantize_one<MODE>(c[j], scale, offset, stochastic != 0, u[j], top, &neg[j], &gh);
     if (!valid[j]) { q[j] = 0u; neg[j] = false; }
+    if (IO == IO_DIFF) ghat_out[j] = gh;
     r[j] = __fsub_rn(c[j], gh);
     if (DIAG && valid[j]) {
       dsum[0] = __fmaf_rn(gh, gh, dsum[0]);
@@ -243,8 +248,10 @@ __global__ void __launch_bounds__(kQThreads, 5) quant_fused_kernel(
     const int32_t* __restrict__ scatter_idx, int64_t n, QuantOut o,
     int stochastic, uint64_t seed, uint64_t step) {
   constexpr int NW = kQThreads / 32;
-  constexpr int NA = IO == IO_EF ? 2 : 1;  // staged arrays: x (and e)
-  __shared__ float4 stage[NW][kQStages][NA][32];
+  constexpr int S = IO == IO_DIFF ? kQStages - 1 : kQStages;  // 36 KB at most
+  // staged arrays: x (and e; and the history for differential quantisation)
+  constexpr int NA = IO == IO_DIFF ? 3 : IO == IO_EF ? 2 : 1;
+  __shared__ float4 stage[NW][S][NA][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   zero_padding(o);
   const int64_t nch = (n + 127) >> 7;
@@ -254,46 +261,81 @@ __global__ void __launch_bounds__(kQThreads, 5) quant_fused_kernel(
   // lane's piece of the warp's first chunk; whole pieces are copied, the
   // ragged end of x is read directly when its chunk is processed
   const int64_t i_first = (c_lo << 7) + 4 * lane;
+  const bool has_err = IO == IO_EF || (IO == IO_DIFF && err != nullptr);
+  const bool use_ref = IO == IO_DIFF && !o.refresh;
   auto issue = [&](int j, int st) {
     const int64_t i0 = i_first + ((int64_t)j << 7);
     if (j < cnt && i0 + 3 < n) {
       cp_async16(&stage[warp][st][0][lane], x + i0);
-      if (IO == IO_EF) cp_async16(&stage[warp][st][NA - 1][lane], err + i0);
+      if (has_err) cp_async16(&stage[warp][st][1][lane], err + i0);
+      if (use_ref) cp_async16(&stage[warp][st][NA - 1][lane], o.ref + i0);
     }
     cp_async_commit();  // one group per chunk (possibly empty)
   };
 #pragma unroll
-  for (int k = 0; k < kQStages - 1; ++k) issue(k, k);
+  for (int k = 0; k < S - 1; ++k) issue(k, k);
   int st = 0;
   for (int j = 0; j < cnt; ++j) {
-    cp_async_wait<kQStages - 2>();  // chunk j has landed
+    cp_async_wait<S - 2>();  // chunk j has landed
     const int64_t i0 = i_first + ((int64_t)j << 7);
-    float c[4];
+    float c[4], rf[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     bool valid[4];
     if (i0 + 3 < n) {
       const float4 v = stage[warp][st][0][lane];
       c[0] = v.x; c[1] = v.y; c[2] = v.z; c[3] = v.w;
       valid[0] = valid[1] = valid[2] = valid[3] = true;
-      if (IO == IO_EF) {
-        const float4 e = stage[warp][st][NA - 1][lane];
+      if (has_err) {
+        const float4 e = stage[warp][st][1][lane];
         c[0] = __fadd_rn(c[0], e.x);
         c[1] = __fadd_rn(c[1], e.y);
         c[2] = __fadd_rn(c[2], e.z);
         c[3] = __fadd_rn(c[3], e.w);
+      }
+      if (use_ref) {
+        const float4 h = stage[warp][st][NA - 1][lane];
+        rf[0] = h.x; rf[1] = h.y; rf[2] = h.z; rf[3] = h.w;
       }
     } else {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         valid[q] = i0 + q < n;
         c[q] = valid[q] ? x[i0 + q] : 0.0f;
-        if (IO == IO_EF && valid[q]) c[q] = __fadd_rn(c[q], err[i0 + q]);
+        if (has_err && valid[q]) c[q] = __fadd_rn(c[q], err[i0 + q]);
+        if (use_ref && valid[q]) rf[q] = o.ref[i0 + q];
       }
     }
-    // the stage read one chunk ago is free: refill it kQStages - 1 ahead
-    issue(j + kQStages - 1, st == 0 ? kQStages - 1 : st - 1);
-    quant_fused_apply<MODE, BITS, LPG, IO>(c, valid, err, scatter_idx, n, o, stochastic, seed,
-                                           step, i0 - 4 * lane, lane);
-    st = st + 1 == kQStages ? 0 : st + 1;
+    // the stage read one chunk ago is free: refill it S - 1 ahead
+    issue(j + S - 1, st == 0 ? S - 1 : st - 1);
+    if (IO == IO_DIFF) {
+      // quantise d = c - r; g_hat = r + d_hat; e' = c - g_hat; ref' = g_hat
+      float d[4], dh[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) d[q] = valid[q] ? __fsub_rn(c[q], rf[q]) : 0.0f;
+      quant_fused_apply<MODE, BITS, LPG, IO>(d, valid, err, scatter_idx, n, o, stochastic,
+                                             seed, step, i0 - 4 * lane, lane, nullptr, dh);
+      float gh[4], e2[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        gh[q] = __fadd_rn(rf[q], dh[q]);
+        e2[q] = __fsub_rn(c[q], gh[q]);
+      }
+      if (i0 + 3 < n) {
+        __stcs(reinterpret_cast<float4*>(o.ref + i0), make_float4(gh[0], gh[1], gh[2], gh[3]));
+        if (has_err)
+          __stcs(reinterpret_cast<float4*>(err + i0), make_float4(e2[0], e2[1], e2[2], e2[3]));
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (!valid[q]) continue;
+          o.ref[i0 + q] = gh[q];
+          if (has_err) err[i0 + q] = e2[q];
+        }
+      }
+    } else {
+      quant_fused_apply<MODE, BITS, LPG, IO>(c, valid, err, scatter_idx, n, o, stochastic,
+                                             seed, step, i0 - 4 * lane, lane);
+    }
+    st = st + 1 == S ? 0 : st + 1;
   }
   cp_async_wait<0>();
 }
@@ -343,6 +385,8 @@ __device__ __forceinline__ void finalize_group(float mn, float mx, float amax, f
         make_float2(__fdiv_rn(__fsub_rn(mx, mn), levels), mn);
   } else if (MODE == GC_QSGD) {
     scales[g] = __fdiv_rn(__fsqrt_rn(ss), levels);
+  } else if (MODE == GC_LOG) {
+    scales[g] = __fdiv_rn(cw_logf(__fadd_rn(amax, 1.0f)), levels);
   } else {
     scales[g] = amax;
   }
@@ -479,7 +523,7 @@ template <int MODE, int BITS, int IO>
 __global__ void __launch_bounds__(kQThreads) quant_apply_kernel(
     const float* __restrict__ c_src, float* __restrict__ err, int64_t n, int64_t G,
     QuantOut o, int stochastic, uint64_t seed, uint64_t step) {
-  constexpr uint32_t top = (MODE == GC_TERN) ? 1u : ((1u << BITS) - 1u);
+  constexpr uint32_t top = mode_top<MODE, BITS>();
   const int lane = threadIdx.x & 31;
   const int64_t warp_id = ((int64_t)blockIdx.x * kQThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kQThreads) >> 5;
@@ -549,10 +593,12 @@ __global__ void __launch_bounds__(kQThreads) quant_apply_kernel(
 // ---------------------------------------------------------------------------
 // Dequantisation.
 // ---------------------------------------------------------------------------
+// acc: 0 writes g_hat; 1 adds it to out (out + g_hat); 2 writes 0 + g_hat
+// (the receiving side of differential quantisation, without / with refresh).
 template <int MODE, int BITS>
 __global__ void __launch_bounds__(kQThreads) dequant_kernel(
     const uint8_t* __restrict__ codes, const uint8_t* __restrict__ signs,
-    const float* __restrict__ scales, int64_t n, int64_t G, float* __restrict__ out) {
+    const float* __restrict__ scales, int64_t n, int64_t G, float* __restrict__ out, int acc) {
   constexpr int CB = (MODE == GC_TERN) ? 2 : BITS;
   const int64_t nvec = (n + 3) >> 2;
   const int64_t stride = (int64_t)gridDim.x * kQThreads;
@@ -579,11 +625,21 @@ __global__ void __launch_bounds__(kQThreads) dequant_kernel(
         } else if (MODE == GC_QSGD) {
           const float m = __fmul_rn((float)code, scales[g]);
           r[j] = ((sbits >> j) & 1u) ? -m : m;
+        } else if (MODE == GC_LOG) {
+          constexpr uint32_t mask = (1u << (BITS - 1)) - 1u;
+          const float m =
+              __fsub_rn(cw_expf(__fmul_rn((float)(code & mask), scales[g])), 1.0f);
+          r[j] = (code >> (BITS - 1)) ? -m : m;
         } else {
           const float m = __fmul_rn((float)(code & 1u), scales[g]);
           r[j] = (code >> 1) ? -m : m;
         }
       }
+    }
+    if (acc != 0) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (i0 + j < n) r[j] = __fadd_rn(acc == 1 ? out[i0 + j] : 0.0f, r[j]);
     }
     if (i0 + 3 < n) {
       *reinterpret_cast<float4*>(out + i0) = make_float4(r[0], r[1], r[2], r[3]);
@@ -619,6 +675,8 @@ __host__ __device__ inline QuantOut make_out(uint8_t* codes, float* scales, int6
   o.szero_end = smag;
   o.scatter_n = 0;
   o.status = nullptr;
+  o.ref = nullptr;
+  o.refresh = 0;
   return o;
 }
 
@@ -698,7 +756,7 @@ gc_status run_multipass(gc_ctx* ctx, const float* x, float* err, int64_t n,
                         uint64_t step) {
   const QuantPlan p = quant_plan(n, group);
   if (p.chunks_per_group > 1 && p.nchunks > ctx->ws.max_partials) return GC_ERR_WORKSPACE;
-  constexpr uint32_t top = (MODE == GC_TERN) ? 1u : ((1u << BITS) - 1u);
+  constexpr uint32_t top = mode_top<MODE, BITS>();
   cudaStream_t s = ctx->stream;
   const int warps_per_block = kQThreads / 32;
   {
@@ -740,12 +798,76 @@ template <int MODE>
 gc_status dispatch_bits(gc_ctx* ctx, const float* x, float* err, const int32_t* idx,
                         int64_t n, int bits, int64_t group, const QuantOut& o, int stoch,
                         uint64_t seed, uint64_t step) {
+  // bits as validated by the API: TernGrad 2; logarithmic 2, 4, 8
+  if constexpr (MODE == GC_TERN) {
+    return dispatch_io<GC_TERN, 2>(ctx, x, err, idx, n, group, o, stoch, seed, step);
+  } else {
   switch (bits) {
-    case 1: return dispatch_io<MODE, 1>(ctx, x, err, idx, n, group, o, stoch, seed, step);
+    case 1:
+      if (MODE == GC_LOG) return GC_ERR_UNSUPPORTED;
+      return dispatch_io<MODE, (MODE == GC_LOG ? 2 : 1)>(ctx, x, err, idx, n, group, o, stoch,
+                                                         seed, step);
     case 2: return dispatch_io<MODE, 2>(ctx, x, err, idx, n, group, o, stoch, seed, step);
     case 4: return dispatch_io<MODE, 4>(ctx, x, err, idx, n, group, o, stoch, seed, step);
     default: return dispatch_io<MODE, 8>(ctx, x, err, idx, n, group, o, stoch, seed, step);
   }
+  }
+}
+
+// Differential quantisation: the fused pass only.
+template <int MODE>
+gc_status diff_bits(gc_ctx* ctx, const float* grad, float* err, int64_t n, int bits, int64_t G,
+                    const QuantOut& o, int stoch, uint64_t seed, uint64_t step) {
+  if constexpr (MODE == GC_TERN) {
+    return run_fused<GC_TERN, 2, IO_DIFF>(ctx, grad, err, nullptr, n, G, o, stoch, seed, step);
+  } else {
+  switch (bits) {
+    case 1:
+      if (MODE == GC_LOG) return GC_ERR_UNSUPPORTED;
+      return run_fused<MODE, (MODE == GC_LOG ? 2 : 1), IO_DIFF>(ctx, grad, err, nullptr, n, G,
+                                                                o, stoch, seed, step);
+    case 2: return run_fused<MODE, 2, IO_DIFF>(ctx, grad, err, nullptr, n, G, o, stoch, seed, step);
+    case 4: return run_fused<MODE, 4, IO_DIFF>(ctx, grad, err, nullptr, n, G, o, stoch, seed, step);
+    default: return run_fused<MODE, 8, IO_DIFF>(ctx, grad, err, nullptr, n, G, o, stoch, seed, step);
+  }
+  }
+}
+
+// Dequantisation into out (acc 0), added to out (1) or to 0 (2).
+gc_status dequant_into(gc_ctx* ctx, const uint8_t* codes, const float* scales, int64_t n,
+                       int bits, int64_t group, int mode, float* out, int acc) {
+  if (n == 0) return GC_OK;
+  const int64_t G = group == 0 ? n : group;
+  const int cb = mode == GC_TERN ? 2 : bits;
+  const uint8_t* signs = mode == GC_QSGD ? codes + round_up((n * cb + 7) / 8, 16) : nullptr;
+  const int grid = grid_for(ctx, ceil_div(n, 4), kQThreads, 8);
+  cudaStream_t s = ctx->stream;
+  LaunchScope L(ctx, GC_PHASE_DEQUANT);
+#define GC_DQ(M, B) \
+  dequant_kernel<M, B><<<grid, kQThreads, 0, s>>>(codes, signs, scales, n, G, out, acc)
+#define GC_DQ_BITS(M)               \
+  switch (bits) {                   \
+    case 1: GC_DQ(M, 1); break;     \
+    case 2: GC_DQ(M, 2); break;     \
+    case 4: GC_DQ(M, 4); break;     \
+    default: GC_DQ(M, 8); break;    \
+  }
+  if (mode == GC_TERN) {
+    GC_DQ(GC_TERN, 2);
+  } else if (mode == GC_LOG) {
+    switch (bits) {
+      case 2: GC_DQ(GC_LOG, 2); break;
+      case 4: GC_DQ(GC_LOG, 4); break;
+      default: GC_DQ(GC_LOG, 8); break;
+    }
+  } else if (mode == GC_MINMAX) {
+    GC_DQ_BITS(GC_MINMAX)
+  } else {
+    GC_DQ_BITS(GC_QSGD)
+  }
+#undef GC_DQ_BITS
+#undef GC_DQ
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
 
 }  // namespace
@@ -763,38 +885,36 @@ gc_status launch_quant(gc_ctx* ctx, const float* x, float* err,
     return dispatch_bits<GC_MINMAX>(ctx, x, err, scatter_idx, n, bits, group, o, stoch, seed, step);
   if (mode == GC_QSGD)
     return dispatch_bits<GC_QSGD>(ctx, x, err, scatter_idx, n, bits, group, o, stoch, seed, step);
-  return dispatch_io<GC_TERN, 2>(ctx, x, err, scatter_idx, n, group, o, stoch, seed, step);
+  if (mode == GC_LOG)
+    return dispatch_bits<GC_LOG>(ctx, x, err, scatter_idx, n, bits, group, o, stoch, seed, step);
+  return dispatch_bits<GC_TERN>(ctx, x, err, scatter_idx, n, bits, group, o, stoch, seed, step);
 }
 
 gc_status launch_dequant(gc_ctx* ctx, const uint8_t* codes, const float* scales,
                          int64_t n, int bits, int64_t group, int mode, float* x_out) {
+  return dequant_into(ctx, codes, scales, n, bits, group, mode, x_out, 0);
+}
+
+gc_status launch_diff_quant(gc_ctx* ctx, const float* grad, float* err, float* ref, int64_t n,
+                            int bits, int64_t group, int mode, int rounding, uint64_t seed,
+                            uint64_t step, int refresh, uint8_t* codes_out, float* scales_out) {
+  QuantOut o = make_out(codes_out, scales_out, n, bits, mode);
+  o.status = ctx->ws.status;
+  o.ref = ref;
+  o.refresh = refresh ? 1 : 0;
   if (n == 0) return GC_OK;
+  const int stoch = rounding == GC_STOCHASTIC;
   const int64_t G = group == 0 ? n : group;
-  const int cb = mode == GC_TERN ? 2 : bits;
-  const uint8_t* signs = mode == GC_QSGD ? codes + round_up((n * cb + 7) / 8, 16) : nullptr;
-  const int grid = grid_for(ctx, ceil_div(n, 4), kQThreads, 8);
-  cudaStream_t s = ctx->stream;
-  LaunchScope L(ctx, GC_PHASE_DEQUANT);
-#define GC_DQ(M, B) dequant_kernel<M, B><<<grid, kQThreads, 0, s>>>(codes, signs, scales, n, G, x_out)
-  if (mode == GC_TERN) {
-    GC_DQ(GC_TERN, 2);
-  } else if (mode == GC_MINMAX) {
-    switch (bits) {
-      case 1: GC_DQ(GC_MINMAX, 1); break;
-      case 2: GC_DQ(GC_MINMAX, 2); break;
-      case 4: GC_DQ(GC_MINMAX, 4); break;
-      default: GC_DQ(GC_MINMAX, 8); break;
-    }
-  } else {
-    switch (bits) {
-      case 1: GC_DQ(GC_QSGD, 1); break;
-      case 2: GC_DQ(GC_QSGD, 2); break;
-      case 4: GC_DQ(GC_QSGD, 4); break;
-      default: GC_DQ(GC_QSGD, 8); break;
-    }
-  }
-#undef GC_DQ
-  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+  if (mode == GC_MINMAX) return diff_bits<GC_MINMAX>(ctx, grad, err, n, bits, G, o, stoch, seed, step);
+  if (mode == GC_QSGD) return diff_bits<GC_QSGD>(ctx, grad, err, n, bits, G, o, stoch, seed, step);
+  if (mode == GC_LOG) return diff_bits<GC_LOG>(ctx, grad, err, n, bits, G, o, stoch, seed, step);
+  return diff_bits<GC_TERN>(ctx, grad, err, n, bits, G, o, stoch, seed, step);
+}
+
+gc_status launch_diff_dequant(gc_ctx* ctx, const uint8_t* codes, const float* scales,
+                              int64_t n, int bits, int64_t group, int mode, int refresh,
+                              float* ref) {
+  return dequant_into(ctx, codes, scales, n, bits, group, mode, ref, refresh ? 2 : 1);
 }
 
 gc_status launch_quant_buckets(gc_ctx* ctx, float* err, const int32_t* idx_out, int bits,

@@ -15,9 +15,9 @@ import os
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libgc.so")
 
-MINMAX, QSGD, TERN = 0, 1, 2
+MINMAX, QSGD, TERN, LOG = 0, 1, 2, 3
 NEAREST_EVEN, STOCHASTIC = 0, 1
-MODES = {"minmax": MINMAX, "qsgd": QSGD, "tern": TERN}
+MODES = {"minmax": MINMAX, "qsgd": QSGD, "tern": TERN, "log": LOG}
 ROUNDINGS = {"nearest_even": NEAREST_EVEN, "stochastic": STOCHASTIC}
 
 PHASE_COUNT = 23
@@ -53,6 +53,9 @@ SIGNATURES = [
     ("gc_ef_quant", _int, [_vp, _vp, _vp, _i64, _int, _i64, _int, _int, _u64, _u64, _vp, _vp]),
     ("gc_ef_topk_quant", _int, [_vp, _vp, _vp, _i64, _i64, _int, _i64, _int, _u64, _u64,
                                 _vp, _vp, _vp]),
+    ("gc_ef_diff_quant", _int, [_vp, _vp, _vp, _vp, _i64, _int, _i64, _int, _int, _u64, _u64,
+                                _int, _vp, _vp]),
+    ("gc_diff_dequant", _int, [_vp, _vp, _vp, _i64, _int, _i64, _int, _int, _vp]),
     ("gc_powersgd_step", _int, [_vp, _vp, _vp, _i64, _i64, _int, _vp, _vp]),
     ("gc_ef_topk_noalloc", _int, [_vp, _vp, _i64, _i64, _vp, _vp, _vp]),
     ("gc_ctx_set_buckets", _int, [_vp, _int, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
@@ -228,6 +231,22 @@ def ef_quant(ctx, grad, err, bits, group, mode, rounding, seed, step, codes_out,
     _check(lib.gc_ef_quant(ctx.handle, _ptr(grad), _ptr(err), n, bits, group, _mode(mode),
                            _rounding(rounding), seed, step, _ptr(codes_out),
                            _ptr(scales_out)), "gc_ef_quant")
+
+
+def ef_diff_quant(ctx, grad, err, ref, bits, group, mode, rounding, seed, step, refresh,
+                  codes_out, scales_out, n=None):
+    """Differential quantisation against the history ref (updated in place);
+    err may be None."""
+    n = grad.numel() if n is None else n
+    _check(lib.gc_ef_diff_quant(ctx.handle, _ptr(grad), _ptr(err), _ptr(ref), n, bits, group,
+                                _mode(mode), _rounding(rounding), seed, step,
+                                1 if refresh else 0, _ptr(codes_out), _ptr(scales_out)),
+           "gc_ef_diff_quant")
+
+
+def diff_dequant(ctx, codes, scales, n, bits, group, mode, refresh, ref):
+    _check(lib.gc_diff_dequant(ctx.handle, _ptr(codes), _ptr(scales), n, bits, group,
+                               _mode(mode), 1 if refresh else 0, _ptr(ref)), "gc_diff_dequant")
 
 
 def ef_topk_quant(ctx, grad, err, k, bits, group, rounding, seed, step, idx_out, codes_out,

@@ -41,11 +41,13 @@
  *         significant bit of byte 0), zero-padded to a multiple of 16 bytes;
  *         for GC_QSGD a sign plane (1 bit per element, set when the element
  *         is negative and its code is not 0) follows, laid out the same way.
- *         GC_TERN codes are 2 bits, (sign << 1) | q with q in {0, 1}.
+ *         GC_TERN codes are 2 bits, (sign << 1) | q with q in {0, 1};
+ *         GC_LOG codes are b-bit sign-magnitude, (sign << (b-1)) | q.
  *         gc_codes_bytes() gives the size.
  *  scales: per group of `group` consecutive elements (group == 0: one group
  *         of all n; the last group may be partial): GC_MINMAX stores
- *         {scale, min} (two floats), GC_QSGD and GC_TERN store {scale}.
+ *         {scale, min} (two floats), GC_QSGD, GC_TERN and GC_LOG store
+ *         {scale}.
  *         gc_scales_floats() gives the size in floats.
  */
 #ifndef GC_H_
@@ -66,7 +68,8 @@ extern "C" {
 typedef enum gc_status {
   GC_OK = 0,
   GC_ERR_INVALID_ARG = -1,  /* NULL, negative size, k > n, group < 0 ... */
-  GC_ERR_UNSUPPORTED = -2,  /* bits not in {1,2,4,8}; TERN with bits != 2 */
+  GC_ERR_UNSUPPORTED = -2,  /* bits not in {1,2,4,8}; TERN with bits != 2;
+                               LOG with bits == 1 */
   GC_ERR_ALIGNMENT = -3,    /* a buffer is not 16-byte aligned */
   GC_ERR_WORKSPACE = -4,    /* n above the context's reserved capacity */
   GC_ERR_CUDA = -5,         /* a CUDA runtime call or launch failed */
@@ -77,7 +80,8 @@ typedef enum gc_status {
 typedef enum gc_mode {
   GC_MINMAX = 0, /* linear min-max quantisation */
   GC_QSGD = 1,   /* s = 2^b - 1 levels of the group L2 norm, sign plane */
-  GC_TERN = 2    /* TernGrad: levels {-max|c|, 0, +max|c|} */
+  GC_TERN = 2,   /* TernGrad: levels {-max|c|, 0, +max|c|} */
+  GC_LOG = 3     /* logarithmic: levels exp(q * scale) - 1, sign bit */
 } gc_mode;
 
 typedef enum gc_rounding {
@@ -214,6 +218,17 @@ GC_API gc_status gc_ef_topk(gc_ctx* ctx, const float* grad, float* err, int64_t 
  *              squares is added as the perfect binary tree over the group
  *              (zero-padded to a power of two, adjacent pairs first).
  *   GC_TERN:   scale = max |x_group|; t = |x| / scale; bits must be 2.
+ *   GC_LOG:    ("分布式训练中的梯度压缩算法" 二.1 对数量化)
+ *              scale = log(max |x_group| + 1) / (2^(b-1) - 1);
+ *              t = log(|x| + 1) / scale; levels 0 .. 2^(b-1) - 1 plus a sign
+ *              bit, so bits must be 2, 4 or 8.  log and exp are the
+ *              Cody-Waite binary32 functions (W. J. Cody, W. Waite,
+ *              "Software Manual for the Elementary Functions", 1980: ln 2
+ *              split as 45426 * 2^-16 + rest, the atanh series in
+ *              s = (m-1)/(m+1) up to s^11/11 for log, the Taylor polynomial
+ *              to r^8/8! on [-ln2/2, ln2/2] for exp), every step one
+ *              rounded binary32 operation: within 2 ulp (log) and 1.5 ulp
+ *              (exp) of the true functions, and reproducible bit for bit.
  *   q = round(t) (nearest-even) or floor(t) + [u < t - floor(t)]
  *   (stochastic), clamped to [0, top]; scale == 0 gives q = 0.
  *   The draw u of element i is word (i mod 4) of Philox-4x32-10 (Salmon et
@@ -229,9 +244,10 @@ GC_API gc_status gc_quant(gc_ctx* ctx, const float* x, int64_t n, int bits,
                    uint64_t step, uint8_t* codes_out, float* scales_out);
 
 /*
- * Dequantisation: x_out[i] = q * scale + min (GC_MINMAX, two roundings) or
- * +-(q * scale) (GC_QSGD / GC_TERN) -- "分布式训练中的梯度压缩算法" 二.1
- * (g_hat = q * scale + min).  Arguments as written by gc_quant.
+ * Dequantisation: x_out[i] = q * scale + min (GC_MINMAX, two roundings),
+ * +-(q * scale) (GC_QSGD / GC_TERN) or +-(exp(q * scale) - 1) (GC_LOG) --
+ * "分布式训练中的梯度压缩算法" 二.1 (g_hat = q * scale + min; g_hat =
+ * sign(q) (exp(|q| scale) - 1)).  Arguments as written by gc_quant.
  */
 GC_API gc_status gc_dequant(gc_ctx* ctx, const uint8_t* codes, const float* scales,
                      int64_t n, int bits, int64_t group, int mode,
@@ -249,6 +265,37 @@ GC_API gc_status gc_ef_quant(gc_ctx* ctx, const float* grad, float* err, int64_t
                       int bits, int64_t group, int mode, int rounding,
                       uint64_t seed, uint64_t step, uint8_t* codes_out,
                       float* scales_out);
+
+/*
+ * Differential quantisation with error feedback.
+ * Page: "分布式训练中的梯度压缩算法" 二.4 差分量化 (send only the change
+ * from the previous gradient, at low precision; both sides keep a history;
+ * errors pile up unless corrected from time to time).  The history ref is
+ * the gradient the receiver reconstructed last (the same on both sides, so
+ * quantisation errors do not pile up in it); refresh != 0 is the periodic
+ * correction and treats ref as 0 (the full gradient is sent):
+ *   c = grad + err (err may be NULL: c = grad);  r = refresh ? 0 : ref;
+ *   d = c - r;  (codes, scales) = gc_quant(d, bits, group, mode, ...);
+ *   g_hat = r + dequant(codes, scales);  err = c - g_hat (if err);
+ *   ref = g_hat.
+ * grad: fp32[n] (read); err, ref: fp32[n] (read, then overwritten).
+ * group must be a power of two in 4 .. 128 (one fused pass; else
+ * GC_ERR_UNSUPPORTED); any mode.
+ */
+GC_API gc_status gc_ef_diff_quant(gc_ctx* ctx, const float* grad, float* err, float* ref,
+                                  int64_t n, int bits, int64_t group, int mode, int rounding,
+                                  uint64_t seed, uint64_t step, int refresh,
+                                  uint8_t* codes_out, float* scales_out);
+
+/*
+ * The receiving side of gc_ef_diff_quant: ref = (refresh ? 0 : ref) +
+ * dequant(codes, scales), elementwise in binary32 -- after the same call
+ * sequence it holds exactly the sender's ref.  ref: fp32[n] (read, then
+ * overwritten).
+ */
+GC_API gc_status gc_diff_dequant(gc_ctx* ctx, const uint8_t* codes, const float* scales,
+                                 int64_t n, int bits, int64_t group, int mode, int refresh,
+                                 float* ref);
 
 /*
  * Hybrid: error feedback + Top-K, then QSGD on the kept values.
