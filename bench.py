@@ -66,14 +66,16 @@ def parse_args():
                    help="gradient elements (default: the workload's own size; for buckets a "
                         "smaller value cuts the same 25 MiB buckets from a shorter gradient)")
     p.add_argument("--workload", choices=["buckets", "quant", "tern", "powersgd", "aggregate",
-                                          "randk"],
+                                          "randk", "diff"],
                    default="buckets",
                    help="buckets: EF + Top-K + QSGD per 25 MiB bucket (the headline); quant: "
                         "EF + group quantisation of 2^30 elements; tern: EF + TernGrad per "
                         "tensor of one transformer layer; powersgd: rank-4 PowerSGD on one "
                         "layer's matrix shapes; aggregate: 8 ranks' Top-K + QSGD outputs summed "
-                        "into one dense gradient; randk: EF + random sparsification at 1%%")
-    p.add_argument("--mode", choices=["minmax", "qsgd"], default="qsgd",
+                        "into one dense gradient; randk: EF + random sparsification at 1%%; "
+                        "diff: EF + 4-bit min-max differential quantisation of the "
+                        "correlated 134M-element gradient")
+    p.add_argument("--mode", choices=["minmax", "qsgd", "log"], default="qsgd",
                    help="quant workload: quantisation rule")
     p.add_argument("--bits", type=int, default=8, help="quant workload: bits per code")
     p.add_argument("--rounding", choices=["nearest_even", "stochastic"], default="stochastic",
@@ -153,9 +155,9 @@ class ClockSampler:
 # of bk_hist on 65,536,000 elements), per element; it scales with the elements.
 # Valid only for the kernel source it was taken on (first 16 hex digits of the
 # SHA-256 of the file), else the bench reports null.
-TRAFFIC = {"bk_hist": {"bytes_per_elem": 759.1e6 / 65536000,
+TRAFFIC = {"bk_hist": {"bytes_per_elem": 759.6e6 / 65536000,
                        "source": "gradient_compression_ef_gb300/csrc/gc_buckets.cu",
-                       "sha256_16": "7c108dfa8d4803d8",
+                       "sha256_16": "f07b07135513bf08",
                        "profile": "profiles/bucketed_kernels_65M_full.md"}}
 
 
@@ -604,8 +606,48 @@ class RandKWorkload(_SimpleWorkload):
         return {"randk_mark": 12.0 * self.n, "randk_write": 8.0 * self.n * self.P}
 
 
+class DiffWorkload(_SimpleWorkload):
+    """Error feedback + differential quantisation of the correlated
+    134,217,728-element gradient: the change from the history is quantised
+    in 4-bit min-max groups of 64 with stochastic rounding; one
+    gc_ef_diff_quant call per step (the first call of the run refreshes)."""
+
+    BITS, GROUP, MODE, SEED = 4, 64, "minmax", 53
+
+    def __init__(self, torch, gc, dev, args, seed):
+        self.n = args.elems
+        self._init_common(torch, gc, dev, 0)
+        self.grads = inputs.correlated_steps_device(self.n, args.distinct, dev, seed=seed)
+        self.err = torch.zeros(self.n, dtype=torch.float32, device=dev)
+        self.ref = torch.zeros(self.n, dtype=torch.float32, device=dev)
+        self.codes = torch.empty(gc.codes_bytes(self.n, self.BITS, self.MODE),
+                                 dtype=torch.uint8, device=dev)
+        self.scales = torch.empty(gc.scales_floats(self.n, self.GROUP, self.MODE),
+                                  dtype=torch.float32, device=dev)
+        self.first = True
+
+    def outputs(self):
+        return [self.codes, self.scales]
+
+    def launch_step(self, t, grad=None, main=None, ctxs=None):
+        main = self.main if main is None else main
+        ctx = self._ctx_on(main, ctxs)
+        g = self.grads[t % len(self.grads)] if grad is None else grad
+        refresh, self.first = self.first, False
+        self.gc.ef_diff_quant(ctx, g, self.err, self.ref, self.BITS, self.GROUP, self.MODE,
+                              "stochastic", self.SEED, t, refresh, self.codes, self.scales)
+
+    def algorithmic_bytes(self):
+        """Read g, e and the history, write e' and the history (20 B per
+        element), the packed codes and the scales."""
+        return 20 * self.n + self.codes.numel() + 4 * self.scales.numel()
+
+    def algorithmic_bytes_per_launch(self):
+        return {"quant_fused": float(self.algorithmic_bytes())}
+
+
 WORKLOADS = {"quant": QuantWorkload, "tern": TernWorkload, "powersgd": PowerSGDWorkload,
-             "aggregate": AggregateWorkload, "randk": RandKWorkload}
+             "aggregate": AggregateWorkload, "randk": RandKWorkload, "diff": DiffWorkload}
 
 
 def kernel_timing(wl, steps, warmup_step):
@@ -639,6 +681,13 @@ def cpu_sample(args, seed=7):
         e = np.zeros_like(g)
         return (lambda: oracle.ef_quant(g, e, 2, 0, "tern", "stochastic", 91, 0), g.size,
                 "one 4096 x 4096 tensor of the layer, EF + TernGrad per tensor")
+    if args.workload == "diff":
+        n = 1 << 22
+        g = inputs.student_t(r, n)
+        e = np.zeros(n, np.float32)
+        ref = (0.9 * g + 0.1 * inputs.student_t(r, n)).astype(np.float32)
+        return (lambda: oracle.ef_diff_quant(g, e, ref, 4, 64, "minmax", "stochastic", 53, 1),
+                n, "4,194,304 elements, EF + 4-bit min-max differential quantisation g64")
     if args.workload == "randk":
         n = 1 << 22
         g = inputs.student_t(r, n)
@@ -705,6 +754,11 @@ def config(args, wl=None):
                            "11008, 11008 x 4096, 4096; N(0, (1e-3/sqrt(fan_in))^2)), EF + "
                            "TernGrad per tensor (scale = max|c| of the tensor), stochastic",
                "total_elems": n, "tensors": len(inputs.TRANSFORMER_SHAPES)}
+    elif args.workload == "diff":
+        cfg = {"workload": "flat fp32 gradient {:,} elements, Student-t nu=3 x 1e-3, correlated "
+                           "steps; EF + differential quantisation against the reconstructed "
+                           "history, 4-bit min-max groups of 64, stochastic".format(n),
+               "total_elems": n, "bits": 4, "group": 64, "mode": "minmax"}
     elif args.workload == "randk":
         cfg = {"workload": "flat fp32 gradient {:,} elements, Student-t nu=3 x 1e-3, correlated "
                            "steps; EF + random sparsification keeping each element with "
