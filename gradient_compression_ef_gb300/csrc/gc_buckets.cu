@@ -555,11 +555,19 @@ __device__ __forceinline__ void classify_at_T(const BucketWs& w, uint32_t key, u
   else if (key == T) atomicAdd(&w.seg_tie[seg], 1u);
 }
 
-constexpr int kScanPer = 8;  // segments per thread in the offset scan
+constexpr int kScanPer = 16;                          // segments per thread in the offset scan
+constexpr int kScanRound = kBkThreads * kScanPer;     // segments per round of the scan
+constexpr int kStashPer = kBkStash / kBkThreads;      // stash entries per thread
+constexpr uint32_t kNoSeg = 0xffffffffu;              // an empty stash slot
+// Shared-memory slot of scan entry i: one word of padding per 32 entries,
+// so that threads reading kScanPer consecutive entries hit distinct banks.
+__device__ __forceinline__ int scan_pad(int i) { return i + (i >> 5); }
+constexpr int kScanPadded = kScanRound + kScanRound / 32;
 
-__global__ void __launch_bounds__(kBkThreads) bk_refine_kernel(BucketWs w) {
+__global__ void __launch_bounds__(kBkThreads, 4) bk_refine_kernel(BucketWs w) {
   constexpr int NW = kBkThreads / 32;
   __shared__ uint32_t low[kLowBins];
+  __shared__ uint32_t adj_kept[kScanPadded], adj_tie[kScanPadded];
   __shared__ uint32_t warp_sums[NW + 1];
   __shared__ uint32_t digit, above;
   __shared__ int last;
@@ -628,28 +636,43 @@ __global__ void __launch_bounds__(kBkThreads) bk_refine_kernel(BucketWs w) {
     __syncthreads();
     if (last) {
       __threadfence();
+      // one round of independent loads: the low bins, the bucket's scalars,
+      // the stash and the first round of per-segment counts (staged in shared
+      // memory with coalesced loads)
       for (int i = threadIdx.x; i < kLowBins; i += kBkThreads) {
         low[i] = __ldcg(&lb[i]);
         lb[i] = 0u;
       }
+      const uint32_t need2 = __ldcg(&q->need2);
+      const uint32_t nst = __ldcg(&q->stash_count);
+      const bool in_stash = nst <= (uint32_t)kBkStash;
+      uint2 se[kStashPer];  // this thread's stash entries (key, segment)
+#pragma unroll
+      for (int r = 0; r < kStashPer; ++r) {
+        const uint32_t j = threadIdx.x + (uint32_t)r * kBkThreads;
+        se[r] = (in_stash && j < nst) ? __ldcg(&stash[j]) : make_uint2(0u, kNoSeg);
+      }
+      // kept counts of segments base .. base + kScanRound - 1 into adj_kept
+      // (and, after a rescan, the tie counts into adj_tie)
+      auto stage = [&](int64_t base) {
+        const int64_t nr = std::min<int64_t>(kScanRound, d.nseg - base);
+        for (int i = threadIdx.x; i < kScanRound; i += kBkThreads) {
+          const int64_t sg = d.seg_first + base + i;
+          adj_kept[scan_pad(i)] = i < nr ? __ldcg(&w.seg_kept[sg]) : 0u;
+          adj_tie[scan_pad(i)] = (i < nr && !in_stash) ? __ldcg(&w.seg_tie[sg]) : 0u;
+        }
+      };
+      if (in_stash) stage(0);
       if (threadIdx.x == 0) {
         digit = kNone;
         above = 0u;
       }
       __syncthreads();
-      const uint32_t need2 = __ldcg(&q->need2);
       find_digit<kBkThreads>(low, kLowBins, need2, warp_sums, &digit, &above);
       const uint32_t B3 = digit;
       const uint32_t T = (B << kHistShift) | (B2 << kLowBits) | (B3 & (kLowBins - 1));
       const uint32_t needT = need2 - above;
-      // the set-aside entries above T and at T, per segment
-      const uint32_t nst = __ldcg(&q->stash_count);
-      if (nst <= (uint32_t)kBkStash) {
-        for (uint32_t j = threadIdx.x; j < nst; j += kBkThreads) {
-          const uint2 e = __ldcg(&stash[j]);
-          classify_at_T(w, e.x, e.y, T);
-        }
-      } else {  // more (B, B2) entries than the stash holds: rescan the lists
+      if (!in_stash) {  // more (B, B2) entries than the stash holds: rescan the lists
         const uint32_t prefix = (B << (kHistShift - kLowBits)) | B2;
         for (int64_t seg = d.seg_first + warp; seg < (int64_t)d.seg_first + d.nseg; seg += NW) {
           const uint32_t cnt = w.seg_cnt[seg];
@@ -659,19 +682,35 @@ __global__ void __launch_bounds__(kBkThreads) bk_refine_kernel(BucketWs w) {
             if ((key >> kLowBits) == prefix) classify_at_T(w, key, (uint32_t)seg, T);
           }
         }
+        __syncthreads();
       }
-      __syncthreads();
       // output offsets: the ties at T go to the segments in index order;
-      // each thread takes kScanPer consecutive segments per round
+      // each thread takes kScanPer consecutive segments of a round from
+      // shared memory, the stash entries of the round classified at T there
       uint32_t tie_carry = 0u, out_carry = 0u;
-      for (int64_t base = 0; base < d.nseg; base += (int64_t)kBkThreads * kScanPer) {
-        const int64_t first = base + (int64_t)threadIdx.x * kScanPer;
-        uint32_t tie[kScanPer], kept[kScanPer];
+      for (int64_t base = 0; base < d.nseg; base += kScanRound) {
+        const int64_t nr = std::min<int64_t>(kScanRound, d.nseg - base);
+        if (base > 0 || !in_stash) {
+          __syncthreads();
+          stage(base);
+        }
+        __syncthreads();
+        if (in_stash) {
+#pragma unroll
+          for (int r = 0; r < kStashPer; ++r) {
+            if (se[r].y == kNoSeg) continue;
+            const int64_t rel = (int64_t)se[r].y - d.seg_first - base;
+            if (rel < 0 || rel >= nr) continue;
+            if (se[r].x > T) atomicAdd(&adj_kept[scan_pad((int)rel)], 1u);
+            else if (se[r].x == T) atomicAdd(&adj_tie[scan_pad((int)rel)], 1u);
+          }
+          __syncthreads();
+        }
+        uint32_t kept[kScanPer], tie[kScanPer];
 #pragma unroll
         for (int r = 0; r < kScanPer; ++r) {
-          const bool valid = first + r < d.nseg;
-          tie[r] = valid ? __ldcg(&w.seg_tie[d.seg_first + first + r]) : 0u;
-          kept[r] = valid ? __ldcg(&w.seg_kept[d.seg_first + first + r]) : 0u;
+          kept[r] = adj_kept[scan_pad((int)threadIdx.x * kScanPer + r)];
+          tie[r] = adj_tie[scan_pad((int)threadIdx.x * kScanPer + r)];
         }
         uint32_t tsum = 0u;
 #pragma unroll
@@ -687,15 +726,19 @@ __global__ void __launch_bounds__(kBkThreads) bk_refine_kernel(BucketWs w) {
           ksum += kept[r];
         }
         const uint32_t out0 = out_carry + block_scan<kBkThreads>(ksum, warp_sums, &ot);
+        // offsets back through shared memory, then coalesced stores
         uint32_t ro = out0, rt = tie0;
 #pragma unroll
         for (int r = 0; r < kScanPer; ++r) {
-          if (first + r < d.nseg) {
-            w.seg_out[d.seg_first + first + r] = ro;
-            w.seg_tieb[d.seg_first + first + r] = rt;
-          }
+          adj_kept[scan_pad((int)threadIdx.x * kScanPer + r)] = ro;
+          adj_tie[scan_pad((int)threadIdx.x * kScanPer + r)] = rt;
           ro += kept[r];
           rt += tie[r];
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < nr; i += kBkThreads) {
+          w.seg_out[d.seg_first + base + i] = adj_kept[scan_pad(i)];
+          w.seg_tieb[d.seg_first + base + i] = adj_tie[scan_pad(i)];
         }
         tie_carry += tt;
         out_carry += ot;
@@ -943,10 +986,11 @@ gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int
   }
   {
     LaunchScope L(ctx, GC_PHASE_BK_COLLECT);
+    const float* csrc = err ? err : grad;
     if (diag)
-      bk_collect_kernel<true><<<w.g_coll, kBkThreads, 0, s>>>(err ? err : grad, w);
+      bk_collect_kernel<true><<<w.g_coll, kBkThreads, 0, s>>>(csrc, w);
     else
-      bk_collect_kernel<false><<<w.g_coll, kBkThreads, 0, s>>>(err ? err : grad, w);
+      bk_collect_kernel<false><<<w.g_coll, kBkThreads, 0, s>>>(csrc, w);
   }
   {
     LaunchScope L(ctx, GC_PHASE_BK_REFINE);
