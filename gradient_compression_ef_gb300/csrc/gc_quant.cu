@@ -403,6 +403,9 @@ __global__ void __launch_bounds__(kQThreads) quant_stats_kernel(
   // 16-byte loads need every group to start on a 4-element boundary (or a
   // single group starting at element 0)
   const bool vec_ok = (G % 4) == 0 || G >= n;
+  constexpr int NA = IO == IO_EF ? 2 : 1;
+  __shared__ float4 stage[kQThreads / 32][kQStages][NA][32];
+  const int warp = threadIdx.x >> 5;
   for (int64_t ch = warp_id; ch < nchunks; ch += nwarps) {
     const int64_t g = ch / cpg, cc = ch % cpg;
     const int64_t g_begin = g * G;
@@ -412,13 +415,35 @@ __global__ void __launch_bounds__(kQThreads) quant_stats_kernel(
     float mn = INFINITY, mx = -INFINITY, amax = 0.0f;
     TreeAcc tree;
     tree.init();
-    for (int64_t b = begin; b < end; b += 128) {
-      const int64_t i0 = b + 4 * lane;
+    // the chunk's 128-element rows with kQStages - 1 of them in flight as
+    // asynchronous copies
+    const int niter = (int)((end - begin + 127) >> 7);
+    auto issue = [&](int it, int st) {
+      const int64_t i0 = begin + ((int64_t)it << 7) + 4 * lane;
+      if (it < niter && vec_ok && i0 + 3 < end) {
+        cp_async16(&stage[warp][st][0][lane], x + i0);
+        if (IO == IO_EF) cp_async16(&stage[warp][st][NA - 1][lane], err + i0);
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int k = 0; k < kQStages - 1; ++k) issue(k, k);
+    int st = 0;
+    for (int it = 0; it < niter; ++it) {
+      cp_async_wait<kQStages - 2>();
+      const int64_t i0 = begin + ((int64_t)it << 7) + 4 * lane;
       float c[4];
-      if (vec_ok && i0 + 3 < end) {
-        float4 v = __ldcs(reinterpret_cast<const float4*>(x + i0));
+      const bool vec = vec_ok && i0 + 3 < end;
+      float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f), ev = v;
+      if (vec) {
+        v = stage[warp][st][0][lane];
+        if (IO == IO_EF) ev = stage[warp][st][NA - 1][lane];
+      }
+      issue(it + kQStages - 1, st == 0 ? kQStages - 1 : st - 1);
+      st = st + 1 == kQStages ? 0 : st + 1;
+      if (vec) {
         if (IO == IO_EF) {
-          const float4 e = *reinterpret_cast<const float4*>(err + i0);
+          const float4 e = ev;
           v.x = __fadd_rn(v.x, e.x);
           v.y = __fadd_rn(v.y, e.y);
           v.z = __fadd_rn(v.z, e.z);
@@ -453,6 +478,7 @@ __global__ void __launch_bounds__(kQThreads) quant_stats_kernel(
         tree.push(warp_sum_tree(s, 32));
       }
     }
+    cp_async_wait<0>();
 #pragma unroll
     for (int o2 = 1; o2 < 32; o2 <<= 1) {
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o2));
@@ -469,38 +495,75 @@ __global__ void __launch_bounds__(kQThreads) quant_stats_kernel(
   }
 }
 
+// One block per group.  min / max / max|c| do not depend on the order, so
+// every warp takes a share of the group's chunks; the QSGD sum of squares
+// keeps its tree order and runs in warp 0.
 template <int MODE>
 __global__ void __launch_bounds__(kQThreads) quant_combine_kernel(
     const float4* __restrict__ partials, int64_t cpg, int64_t nchunks,
     int64_t ngroups, uint32_t top, float* __restrict__ scales) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warp_id = ((int64_t)blockIdx.x * kQThreads + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * kQThreads) >> 5;
-  for (int64_t g = warp_id; g < ngroups; g += nwarps) {
+  constexpr int NW = kQThreads / 32;
+  __shared__ float red[3][NW];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x) {
     const int64_t first = g * cpg;
     const int64_t last = std::min<int64_t>(first + cpg, nchunks);
-    float mn = INFINITY, mx = -INFINITY, amax = 0.0f;
-    TreeAcc tree;
-    tree.init();
-    for (int64_t b = first; b < last; b += 32) {
-      float s = 0.0f;
-      if (b + lane < last) {
-        const float4 p = partials[b + lane];
+    float mn = INFINITY, mx = -INFINITY, amax = 0.0f, ss = 0.0f;
+    if (MODE == GC_QSGD) {
+      if (warp == 0) {
+        TreeAcc tree;
+        tree.init();
+        for (int64_t b = first; b < last; b += 32) {
+          const float s = b + lane < last ? partials[b + lane].w : 0.0f;
+          tree.push(warp_sum_tree(s, 32));
+        }
+        ss = tree.finish();
+      }
+    } else {
+      int64_t b = first + threadIdx.x;
+      for (; b + 3 * kQThreads < last; b += 4 * kQThreads) {
+        float4 p[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) p[u] = partials[b + u * kQThreads];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          mn = fminf(mn, p[u].x);
+          mx = fmaxf(mx, p[u].y);
+          amax = fmaxf(amax, p[u].z);
+        }
+      }
+      for (; b < last; b += kQThreads) {
+        const float4 p = partials[b];
         mn = fminf(mn, p.x);
         mx = fmaxf(mx, p.y);
         amax = fmaxf(amax, p.z);
-        s = p.w;
       }
-      if (MODE == GC_QSGD) tree.push(warp_sum_tree(s, 32));
-    }
 #pragma unroll
-    for (int o2 = 1; o2 < 32; o2 <<= 1) {
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o2));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+      for (int o2 = 1; o2 < 32; o2 <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+      }
+      if (lane == 0) {
+        red[0][warp] = mn;
+        red[1][warp] = mx;
+        red[2][warp] = amax;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        mn = lane < NW ? red[0][lane] : INFINITY;
+        mx = lane < NW ? red[1][lane] : -INFINITY;
+        amax = lane < NW ? red[2][lane] : 0.0f;
+#pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) {
+          mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o2));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+        }
+      }
+      __syncthreads();
     }
-    const float ss = MODE == GC_QSGD ? tree.finish() : 0.0f;
-    if (lane == 0) finalize_group<MODE>(mn, mx, amax, ss, top, scales, g);
+    if (threadIdx.x == 0) finalize_group<MODE>(mn, mx, amax, ss, top, scales, g);
   }
 }
 
@@ -508,8 +571,9 @@ __global__ void __launch_bounds__(kQThreads) quant_combine_kernel(
 // G >= 4 at most one group boundary falls inside the 4 elements.
 struct GroupOf4 {
   int64_t g0, r0, G;
-  __device__ __forceinline__ GroupOf4(int64_t i0, int64_t G_) : G(G_) {
-    g0 = i0 / G_;
+  // one group of all n (G >= n) needs no division
+  __device__ __forceinline__ GroupOf4(int64_t i0, int64_t G_, int64_t n) : G(G_) {
+    g0 = G_ >= n ? 0 : i0 / G_;
     r0 = i0 - g0 * G_;
   }
   __device__ __forceinline__ int64_t operator()(int j) const {
@@ -550,7 +614,7 @@ __global__ void __launch_bounds__(kQThreads) quant_apply_kernel(
     uint32_t q[4];
     bool neg[4];
     float r[4];
-    const GroupOf4 group_of(i0, G);
+    const GroupOf4 group_of(i0, G, n);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       q[j] = 0u;
@@ -612,7 +676,7 @@ __global__ void __launch_bounds__(kQThreads) dequant_kernel(
     uint32_t sbits = 0u;
     if (MODE == GC_QSGD) sbits = (uint32_t)(signs[i0 >> 3] >> ((v & 1) * 4)) & 0xfu;
     float r[4];
-    const GroupOf4 group_of(i0, G);
+    const GroupOf4 group_of(i0, G, n);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       r[j] = 0.0f;
@@ -761,12 +825,18 @@ gc_status run_multipass(gc_ctx* ctx, const float* x, float* err, int64_t n,
   const int warps_per_block = kQThreads / 32;
   {
     LaunchScope L(ctx, GC_PHASE_QUANT_STATS);
-    quant_stats_kernel<MODE, IO><<<grid_for(ctx, p.nchunks, warps_per_block, 8), kQThreads, 0, s>>>(
+    auto kernel = quant_stats_kernel<MODE, IO>;
+    static const int per_sm = [&] {
+      cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      cudaGetLastError();
+      return blocks_per_sm(kernel, kQThreads);
+    }();
+    kernel<<<grid_for(ctx, p.nchunks, warps_per_block, per_sm), kQThreads, 0, s>>>(
         x, err, n, p.G, p.chunk, p.chunks_per_group, p.nchunks, top, ctx->ws.partials, o.scales);
   }
   if (p.chunks_per_group > 1) {
     LaunchScope L(ctx, GC_PHASE_QUANT_COMBINE);
-    quant_combine_kernel<MODE><<<grid_for(ctx, p.ngroups, warps_per_block, 8), kQThreads, 0, s>>>(
+    quant_combine_kernel<MODE><<<grid_for(ctx, p.ngroups, 1, 8), kQThreads, 0, s>>>(
         ctx->ws.partials, p.chunks_per_group, p.nchunks, p.ngroups, top, o.scales);
   }
   const float* c_src = IO == IO_EF ? err : x;
