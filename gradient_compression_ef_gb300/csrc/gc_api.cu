@@ -284,7 +284,9 @@ gc_status gc_ctx_reserve_powersgd(gc_ctx* ctx, int64_t max_m, int64_t max_n, int
     ctx->psgd = gc::PsgdWorkspace{};
     return e == cudaErrorMemoryAllocation ? GC_ERR_NO_MEMORY : GC_ERR_CUDA;
   }
-  if (cudaMemset(base, 0, (size_t)bytes) != cudaSuccess) {
+  // the memset runs on the legacy stream: finish it before any launch
+  if (cudaMemset(base, 0, (size_t)bytes) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(base);
     return GC_ERR_CUDA;
   }

@@ -11,18 +11,21 @@
 // the tensor-core ridge point, so the products run as fp32 FMAs on the CUDA
 // cores and the kernels are organised around HBM streaming:
 //   pass 1  mq       : M = G + E written over E; P = M Q (Q staged in shared
-//                      memory); each block also forms the Gram matrix of its
-//                      rows of P in fp64.  The last block sums the Gram
-//                      partials in block order, factors P^T P = U^T U
-//                      (Cholesky, fp64) and stores W = U^-1.  P W is the
-//                      Gram-Schmidt orthonormalisation of P: both give the
-//                      unique QR factor with a positive diagonal.
+//                      memory).  Blocks own 16 rows and a range of columns
+//                      (enough blocks to fill the GPU); the last block of a
+//                      row range adds the column ranges' partial rows of P in
+//                      order and forms their Gram matrix in fp64.  The last
+//                      row range sums the Gram partials in order, factors
+//                      P^T P = U^T U (Cholesky, fp64) and stores W = U^-1.
+//                      P W is the Gram-Schmidt orthonormalisation of P: both
+//                      give the unique QR factor with a positive diagonal.
 //   pass 2  mtp      : Q' = M^T P_hat.  Blocks own a 128-column strip and a
 //                      slice of rows; P_hat = P W for the slice is formed in
 //                      shared memory (strip 0 also writes it out).  Partial
 //                      sums are reduced in a fixed order by the last block of
 //                      each strip, so results are deterministic.
-//   pass 3  residual : E' = M - P_hat Q'^T (Q' staged in shared memory).
+//   pass 3  residual : E' = M - P_hat Q'^T (Q' staged in shared memory),
+//                      blocks over rows and column ranges as in pass 1.
 // Traffic: 12 + 4 + 8 = 24 bytes per element.
 #include <algorithm>
 
@@ -38,6 +41,7 @@ constexpr int kRowsPerBlock = kPWarps * kRowsPerWarp;  // 16
 constexpr int kQChunk = 512;                           // columns of Q per stage
 constexpr int kStrip = 128;                            // columns per pass-2 block
 constexpr int kPhRows = 512;                           // P_hat rows staged per pass-2 step
+constexpr int kMaxColSplits = 8;                       // column ranges of passes 1 and 3
 
 struct PsgdState {
   uint32_t ticket_mq;
@@ -46,6 +50,8 @@ struct PsgdState {
 
 struct PsgdBufs {
   float* praw;        // [m][r] raw P
+  float* ppart;       // [splits][m][r] partial rows of P per column range
+  uint32_t* rb_tickets;  // [row blocks] last-block tickets of pass 1
   double* gram_part;  // [blocks][r][r]
   float* w;           // [r][r] W = U^-1 (upper triangular)
   float* q_part;      // [splits][n][r]
@@ -91,20 +97,23 @@ __device__ __forceinline__ void stage_q(float* qs, const float* Q, int64_t col0,
 template <int R, bool VEC>
 __global__ void __launch_bounds__(kPThreads) psgd_mq_kernel(
     const float* __restrict__ G, float* __restrict__ E, int64_t m, int64_t n,
-    const float* __restrict__ Q, PsgdBufs b) {
+    const float* __restrict__ Q, PsgdBufs b, int64_t cols_per_split) {
   __shared__ float qs[kQChunk * R];
   __shared__ float prow[kRowsPerBlock][R];
   __shared__ double gram[R * R];
   __shared__ bool last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t row0 = (int64_t)blockIdx.x * kRowsPerBlock + warp * kRowsPerWarp;
+  const int split = blockIdx.y, splits = gridDim.y;
+  const int64_t c_lo = (int64_t)split * cols_per_split;
+  const int64_t c_hi = std::min<int64_t>(n, c_lo + cols_per_split);
   float acc[kRowsPerWarp][R];
 #pragma unroll
   for (int rr = 0; rr < kRowsPerWarp; ++rr)
 #pragma unroll
     for (int c = 0; c < R; ++c) acc[rr][c] = 0.0f;
 
-  for (int64_t col0 = 0; col0 < n; col0 += kQChunk) {
+  for (int64_t col0 = c_lo; col0 < c_hi; col0 += kQChunk) {
     __syncthreads();
     stage_q<R>(qs, Q, col0, n);
     __syncthreads();
@@ -112,7 +121,7 @@ __global__ void __launch_bounds__(kPThreads) psgd_mq_kernel(
     for (int s = 0; s < kQChunk / 128; ++s) {
       const int jl = s * 128 + 4 * lane;  // column within the chunk
       const int64_t j = col0 + jl;
-      if (j >= n) break;
+      if (j >= c_hi) break;
 #pragma unroll
       for (int rr = 0; rr < kRowsPerWarp; ++rr) {
         const int64_t row = row0 + rr;
@@ -139,19 +148,52 @@ __global__ void __launch_bounds__(kPThreads) psgd_mq_kernel(
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
       acc[rr][c] = v;
     }
-  if (lane == 0) {
+  if (splits == 1) {
+    if (lane == 0) {
 #pragma unroll
-    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-      const int64_t row = row0 + rr;
+      for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+        const int64_t row = row0 + rr;
 #pragma unroll
-      for (int c = 0; c < R; ++c) {
-        const float v = row < m ? acc[rr][c] : 0.0f;
-        prow[warp * kRowsPerWarp + rr][c] = v;
-        if (row < m) b.praw[row * R + c] = v;
+        for (int c = 0; c < R; ++c) {
+          const float v = row < m ? acc[rr][c] : 0.0f;
+          prow[warp * kRowsPerWarp + rr][c] = v;
+          if (row < m) b.praw[row * R + c] = v;
+        }
       }
     }
+    __syncthreads();
+  } else {
+    // partial rows of this column range; the row range's last block adds
+    // them in column-range order
+    if (lane == 0) {
+#pragma unroll
+      for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+        const int64_t row = row0 + rr;
+        if (row >= m) continue;
+#pragma unroll
+        for (int c = 0; c < R; ++c) b.ppart[((int64_t)split * m + row) * R + c] = acc[rr][c];
+      }
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+      last = atomicAdd(&b.rb_tickets[blockIdx.x], 1u) == (uint32_t)splits - 1u;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    if (threadIdx.x < kRowsPerBlock * R) {
+      const int rl = threadIdx.x / R, c = threadIdx.x % R;
+      const int64_t row = (int64_t)blockIdx.x * kRowsPerBlock + rl;
+      float v = 0.0f;
+      if (row < m) {
+        for (int sp = 0; sp < splits; ++sp) v += __ldcg(&b.ppart[((int64_t)sp * m + row) * R + c]);
+        b.praw[row * R + c] = v;
+      }
+      prow[rl][c] = v;
+    }
+    if (threadIdx.x == 0) b.rb_tickets[blockIdx.x] = 0u;
+    __syncthreads();
   }
-  __syncthreads();
   if (threadIdx.x < R * R) {
     const int a = threadIdx.x / R, c = threadIdx.x % R;
     double s = 0.0;
@@ -294,16 +336,18 @@ __global__ void __launch_bounds__(kPThreads) psgd_mtp_kernel(
 template <int R, bool VEC>
 __global__ void __launch_bounds__(kPThreads) psgd_residual_kernel(
     float* __restrict__ E, int64_t m, int64_t n, const float* __restrict__ P,
-    const float* __restrict__ Q) {
+    const float* __restrict__ Q, int64_t cols_per_split) {
   __shared__ float qs[kQChunk * R];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t row0 = (int64_t)blockIdx.x * kRowsPerBlock + warp * kRowsPerWarp;
+  const int64_t c_lo = (int64_t)blockIdx.y * cols_per_split;
+  const int64_t c_hi = std::min<int64_t>(n, c_lo + cols_per_split);
   float p[kRowsPerWarp][R];
 #pragma unroll
   for (int rr = 0; rr < kRowsPerWarp; ++rr)
 #pragma unroll
     for (int c = 0; c < R; ++c) p[rr][c] = (row0 + rr < m) ? P[(row0 + rr) * R + c] : 0.0f;
-  for (int64_t col0 = 0; col0 < n; col0 += kQChunk) {
+  for (int64_t col0 = c_lo; col0 < c_hi; col0 += kQChunk) {
     __syncthreads();
     stage_q<R>(qs, Q, col0, n);
     __syncthreads();
@@ -311,7 +355,7 @@ __global__ void __launch_bounds__(kPThreads) psgd_residual_kernel(
     for (int s = 0; s < kQChunk / 128; ++s) {
       const int jl = s * 128 + 4 * lane;
       const int64_t j = col0 + jl;
-      if (j >= n) break;
+      if (j >= c_hi) break;
 #pragma unroll
       for (int rr = 0; rr < kRowsPerWarp; ++rr) {
         const int64_t row = row0 + rr;
@@ -345,15 +389,25 @@ gc_status run_psgd(gc_ctx* ctx, const float* grad, float* err, int64_t m, int64_
   b.w = static_cast<float*>(take(sizeof(float) * 16 * 16));
   b.tickets = static_cast<uint32_t*>(take(sizeof(uint32_t) * ceil_div(pw.max_n, kStrip)));
   b.praw = static_cast<float*>(take(sizeof(float) * pw.max_m * pw.max_r));
+  b.ppart = static_cast<float*>(take(sizeof(float) * kMaxColSplits * pw.max_m * pw.max_r));
+  b.rb_tickets = static_cast<uint32_t*>(take(sizeof(uint32_t) * ceil_div(pw.max_m, kRowsPerBlock)));
   b.gram_part = static_cast<double*>(take(sizeof(double) * ceil_div(pw.max_m, kRowsPerBlock) * pw.max_r * pw.max_r));
   b.q_part = reinterpret_cast<float*>(base + off);
   b.status = ctx->ws.status;
   const int64_t qcap = (pw.bytes - (int64_t)off) / (int64_t)sizeof(float);
 
   const int mq_blocks = (int)ceil_div(m, kRowsPerBlock);
+  // column ranges (multiples of kQChunk) so that passes 1 and 3 have about
+  // 8 blocks per SM
+  const int64_t chunks = ceil_div(n, kQChunk);
+  int64_t csplits = std::min<int64_t>(
+      {(int64_t)kMaxColSplits, chunks, std::max<int64_t>(1, ceil_div((int64_t)ctx->num_sms * 8, mq_blocks))});
+  const int64_t cps = ceil_div(chunks, csplits) * kQChunk;
+  csplits = ceil_div(n, cps);
   {
     LaunchScope L(ctx, GC_PHASE_PSGD_MQ);
-    psgd_mq_kernel<R, VEC><<<mq_blocks, kPThreads, 0, s>>>(grad, err, m, n, Q_inout, b);
+    psgd_mq_kernel<R, VEC><<<dim3(mq_blocks, (unsigned)csplits), kPThreads, 0, s>>>(
+        grad, err, m, n, Q_inout, b, cps);
   }
 
   const int strips = (int)ceil_div(n, kStrip);
@@ -376,7 +430,8 @@ gc_status run_psgd(gc_ctx* ctx, const float* grad, float* err, int64_t m, int64_
   }
   {
     LaunchScope L(ctx, GC_PHASE_PSGD_RESID);
-    psgd_residual_kernel<R, VEC><<<mq_blocks, kPThreads, 0, s>>>(err, m, n, P_out, Q_inout);
+    psgd_residual_kernel<R, VEC><<<dim3(mq_blocks, (unsigned)csplits), kPThreads, 0, s>>>(
+        err, m, n, P_out, Q_inout, cps);
   }
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
@@ -395,6 +450,8 @@ int64_t psgd_workspace_bytes(int64_t max_m, int64_t max_n, int max_r, int num_sm
   int64_t bytes = up(sizeof(PsgdState)) + up(sizeof(float) * 16 * 16) +
                   up(sizeof(uint32_t) * ceil_div(max_n, kStrip)) +
                   up(sizeof(float) * max_m * max_r) +
+                  up(sizeof(float) * kMaxColSplits * max_m * max_r) +
+                  up(sizeof(uint32_t) * ceil_div(max_m, kRowsPerBlock)) +
                   up(sizeof(double) * ceil_div(max_m, kRowsPerBlock) * max_r * max_r);
   // q partials: splits * n * r floats with splits * strips <= 4 * SMs + strips
   bytes += (int64_t)sizeof(float) * ((int64_t)num_sms * 4 * kStrip + max_n + kStrip) * max_r;
