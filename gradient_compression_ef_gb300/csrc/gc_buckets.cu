@@ -85,9 +85,19 @@ __device__ __forceinline__ uint32_t append4(uint2* out, uint32_t cnt, const bool
   const uint32_t b3 = __ballot_sync(0xffffffffu, ge[3]);
   // index order is (lane, j): the lanes below come first
   uint32_t pos = cnt + __popc(b0 & lt) + __popc(b1 & lt) + __popc(b2 & lt) + __popc(b3 & lt);
+  // the lists are read again by the next passes: ask L2 to keep them while
+  // the hist pass streams the gradient past
+  uint64_t pol;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    if (ge[j]) out[pos++] = make_uint2(__float_as_uint(c[j]), base + 4 * lane + j);
+  for (int j = 0; j < 4; ++j) {
+    if (ge[j]) {
+      uint2* a = out + pos++;
+      asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1, %2}, %3;" ::"l"(a),
+                   "r"(__float_as_uint(c[j])), "r"(base + 4 * lane + j), "l"(pol)
+                   : "memory");
+    }
+  }
   return cnt + __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
 }
 
