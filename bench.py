@@ -175,6 +175,34 @@ def kernel_traffic(name, elems):
     return t["bytes_per_elem"] * elems, "ncu capture scaled by elements: " + t["profile"]
 
 
+def dist_env():
+    """(world, rank, local rank) from the launcher's environment."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(rank):
+    """Each rank compresses its own gradient replica: a seed of its own."""
+    return 42 + rank
+
+
+def max_over_ranks(torch, value, world, device):
+    """The largest of every rank's value (a step time): the job is as slow
+    as its slowest rank.  One all-reduce on a one-element tensor; no
+    collective touches the gradients."""
+    if world <= 1:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(world, elems_per_rank, ms_per_step):
+    """fp32 gradient GB/s of the whole job: every rank processes
+    elems_per_rank elements per step in ms_per_step (the max over ranks)."""
+    return world * 4.0 * elems_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def pin_host_near_gpu(torch, dev):
     """Restricts this process to the host CPUs local to the GPU (from the
     PCI device's local_cpulist), so that pinned host buffers are allocated on
@@ -827,7 +855,7 @@ def config(args, wl=None):
 def run_reference(args):
     """The reference arm: the oracle (single-threaded C, the pages'
     definitions), each step one bounded sample of the workload."""
-    rank = int(os.environ.get("RANK", "0"))
+    rank = dist_env()[1]
     if rank != 0:
         return 0
     run, n, what = cpu_sample(args, seed=11)
@@ -858,9 +886,7 @@ def main():
     if args.impl == "reference":
         return run_reference(args)
     import torch
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = dist_env()
     if world > 1:
         import torch.distributed as dist
         torch.cuda.set_device(local)
@@ -872,9 +898,9 @@ def main():
 
     if args.workload == "buckets":
         wl = BucketWorkload(torch, gc, dev, args.ratio, args.streams, args.distinct,
-                            seed=42 + rank, path=args.path, n=args.elems, diag=args.diag)
+                            seed=rank_seed(rank), path=args.path, n=args.elems, diag=args.diag)
     else:
-        wl = WORKLOADS[args.workload](torch, gc, dev, args, seed=42 + rank)
+        wl = WORKLOADS[args.workload](torch, gc, dev, args, seed=rank_seed(rank))
     torch.cuda.synchronize(dev)
     for t in range(args.warmup):
         wl.launch_step(t)
@@ -897,11 +923,7 @@ def main():
         stop.record(wl.main)
         torch.cuda.synchronize(dev)
         barrier()
-        ms_ = start.elapsed_time(stop)
-        if world > 1:
-            tm = torch.tensor([ms_], device=dev)
-            torch.distributed.all_reduce(tm, op=torch.distributed.ReduceOp.MAX)
-            ms_ = float(tm.item())
+        ms_ = max_over_ranks(torch, start.elapsed_time(stop), world, dev)
         return ms_ / steps
 
     props = torch.cuda.get_device_properties(dev)
@@ -927,8 +949,8 @@ def main():
         ms_per_step, launches, launch_mode = eager_ms, eager_launches, "eager"
     else:
         ms_per_step, launches, launch_mode = graph_ms, per_step_launches * args.steps, "cuda_graph"
-    value = world * 4.0 * wl.n / (ms_per_step * 1e-3) / 1e9
-    eager_value = world * 4.0 * wl.n / (eager_ms * 1e-3) / 1e9
+    value = whole_job_value(world, wl.n, ms_per_step)
+    eager_value = whole_job_value(world, wl.n, eager_ms)
 
     # per-kernel durations (second pass over the same kind of steps)
     phases = kernel_timing(wl, args.steps, args.warmup + args.steps)
@@ -982,7 +1004,7 @@ def main():
 
         e_ms = timed(e2e_step, e2e_steps, side_streams=(copy_s,))
         h2d = wl.input_bytes() if hasattr(wl, "input_bytes") else 4 * wl.n
-        e2e = {"value": world * 4.0 * wl.n / (e_ms * 1e-3) / 1e9, "unit": UNIT,
+        e2e = {"value": whole_job_value(world, wl.n, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": wl.out_bytes(),
                "ms_per_step": e_ms, "launch": launch_mode,
                "host_cpus": host_cpus if host_cpus else "affinity unchanged"}
