@@ -42,6 +42,7 @@ constexpr int kQChunk = 512;                           // columns of Q per stage
 constexpr int kStrip = 128;                            // columns per pass-2 block
 constexpr int kPhRows = 512;                           // P_hat rows staged per pass-2 step
 constexpr int kMaxColSplits = 8;                       // column ranges of passes 1 and 3
+constexpr int kSubSteps = 2;                           // 128-column steps loaded together
 
 struct PsgdState {
   uint32_t ticket_mq;
@@ -117,25 +118,42 @@ __global__ void __launch_bounds__(kPThreads) psgd_mq_kernel(
     __syncthreads();
     stage_q<R>(qs, Q, col0, n);
     __syncthreads();
+    // two 128-column steps of both rows loaded before any store (the
+    // stores to E would otherwise order the next loads behind them)
 #pragma unroll
-    for (int s = 0; s < kQChunk / 128; ++s) {
-      const int jl = s * 128 + 4 * lane;  // column within the chunk
-      const int64_t j = col0 + jl;
-      if (j >= c_hi) break;
+    for (int s = 0; s < kQChunk / 128; s += kSubSteps) {
+      float g[kSubSteps][kRowsPerWarp][4], e[kSubSteps][kRowsPerWarp][4];
 #pragma unroll
-      for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-        const int64_t row = row0 + rr;
-        if (row >= m) continue;
-        float g[4], e[4];
-        load_row4<VEC>(G + row * n, j, n, g);
-        load_row4<VEC>(E + row * n, j, n, e);
+      for (int u = 0; u < kSubSteps; ++u) {
+        const int64_t j = col0 + (s + u) * 128 + 4 * lane;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) g[q] = __fadd_rn(g[q], e[q]);
-        store_row4<VEC>(E + row * n, j, n, g);
+        for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+          const int64_t row = row0 + rr;
+          if (row < m && j < c_hi) {
+            load_row4<VEC>(G + row * n, j, n, g[u][rr]);
+            load_row4<VEC>(E + row * n, j, n, e[u][rr]);
+          } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 4; ++q) g[u][rr][q] = e[u][rr][q] = 0.0f;
+          }
+        }
+      }
 #pragma unroll
-          for (int c = 0; c < R; ++c) acc[rr][c] = fmaf(g[q], qs[(jl + q) * R + c], acc[rr][c]);
+      for (int u = 0; u < kSubSteps; ++u) {
+        const int jl = (s + u) * 128 + 4 * lane;  // column within the chunk
+        const int64_t j = col0 + jl;
+#pragma unroll
+        for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+          const int64_t row = row0 + rr;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) g[u][rr][q] = __fadd_rn(g[u][rr][q], e[u][rr][q]);
+          if (row < m && j < c_hi) store_row4<VEC>(E + row * n, j, n, g[u][rr]);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int c = 0; c < R; ++c)
+              acc[rr][c] = fmaf(g[u][rr][q], qs[(jl + q) * R + c], acc[rr][c]);
+        }
       }
     }
   }
@@ -352,24 +370,38 @@ __global__ void __launch_bounds__(kPThreads) psgd_residual_kernel(
     stage_q<R>(qs, Q, col0, n);
     __syncthreads();
 #pragma unroll
-    for (int s = 0; s < kQChunk / 128; ++s) {
-      const int jl = s * 128 + 4 * lane;
-      const int64_t j = col0 + jl;
-      if (j >= c_hi) break;
+    for (int s = 0; s < kQChunk / 128; s += kSubSteps) {
+      float v[kSubSteps][kRowsPerWarp][4];
 #pragma unroll
-      for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-        const int64_t row = row0 + rr;
-        if (row >= m) continue;
-        float v[4];
-        load_row4<VEC>(E + row * n, j, n, v);
+      for (int u = 0; u < kSubSteps; ++u) {
+        const int64_t j = col0 + (s + u) * 128 + 4 * lane;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float a = 0.0f;
+        for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+          const int64_t row = row0 + rr;
+          if (row < m && j < c_hi) {
+            load_row4<VEC>(E + row * n, j, n, v[u][rr]);
+          } else {
 #pragma unroll
-          for (int c = 0; c < R; ++c) a = fmaf(p[rr][c], qs[(jl + q) * R + c], a);
-          v[q] = v[q] - a;
+            for (int q = 0; q < 4; ++q) v[u][rr][q] = 0.0f;
+          }
         }
-        store_row4<VEC>(E + row * n, j, n, v);
+      }
+#pragma unroll
+      for (int u = 0; u < kSubSteps; ++u) {
+        const int jl = (s + u) * 128 + 4 * lane;
+        const int64_t j = col0 + jl;
+#pragma unroll
+        for (int rr = 0; rr < kRowsPerWarp; ++rr) {
+          const int64_t row = row0 + rr;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float a = 0.0f;
+#pragma unroll
+            for (int c = 0; c < R; ++c) a = fmaf(p[rr][c], qs[(jl + q) * R + c], a);
+            v[u][rr][q] = v[u][rr][q] - a;
+          }
+          if (row < m && j < c_hi) store_row4<VEC>(E + row * n, j, n, v[u][rr]);
+        }
       }
     }
   }

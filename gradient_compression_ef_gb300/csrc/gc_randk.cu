@@ -27,7 +27,7 @@ constexpr int kRkThreads = 256;
 constexpr int kRkWarps = kRkThreads / 32;
 
 template <bool EF>
-__global__ void __launch_bounds__(kRkThreads) randk_mark_kernel(
+__global__ void __launch_bounds__(kRkThreads, 3) randk_mark_kernel(
     const float* __restrict__ grad, float* __restrict__ err, int64_t n, int64_t nseg, float p,
     uint64_t seed, uint64_t step, uint2* __restrict__ list, uint32_t* __restrict__ seg_cnt,
     uint32_t* __restrict__ block_tot) {
