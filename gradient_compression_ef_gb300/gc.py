@@ -305,14 +305,6 @@ def ef_topk_quant_buckets(ctx, grad, err, bits, group, rounding, seed, step, idx
            "gc_ef_topk_quant_buckets")
 
 
-def norm_ratio(diag):
-    """Per-bucket gradient norm ratio ||g_hat|| / ||c|| from the diagnostics
-    (a host computation on the 3 * nb values)."""
-    import math
-    d = [float(x) for x in diag]
-    return [math.sqrt(d[3 * b + 1] / d[3 * b]) if d[3 * b] > 0 else 0.0
-            for b in range(len(d) // 3)]
-
 
 def topk_aggregate(ctx, W, k, idx, val, n, out):
     """gc_topk_aggregate: out[n] = rank-ordered sum of W ranks' (idx, val)."""

@@ -181,14 +181,17 @@ def test_diagnostics_leave_results_unchanged(env):
         assert_bits_equal(b, a, what)
 
 
-def test_norm_ratio_helper(env):
+def test_norm_ratio_limits(env):
+    """Everything sent: ratio 1 and no error energy; nothing sent: ratio 0
+    and the error energy is the gradient's."""
     torch, gc, ctx = env
     ns, ks = [4096, 4096], [4096, 0]
     g, _ = make_inputs(ns, 1)
     ctx.set_buckets(ns, ks)
     _, _, _, diag = run_topk(env, ns, ks, dev_f32(torch, g), None)
-    r = gc.norm_ratio(diag)  # everything sent / nothing sent
-    assert abs(r[0] - 1.0) <= RTOL and r[1] == 0.0
+    d = diag.reshape(-1, 3)
+    assert abs(np.sqrt(d[0, 1] / d[0, 0]) - 1.0) <= RTOL and d[0, 2] == 0.0
+    assert d[1, 1] == 0.0 and d[1, 2] == d[1, 0]
 
 
 def test_validation(env):
