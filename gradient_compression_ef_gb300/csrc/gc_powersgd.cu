@@ -310,14 +310,29 @@ __global__ void __launch_bounds__(kPThreads) psgd_mtp_kernel(
     }
     __syncthreads();
     if (col < n) {
-      for (int64_t i = sa + warp; i < sb; i += kPWarps) {
-        float v[4];
-        load_row4<VEC>(M + i * n, col, n, v);
-        const float* pr = ph + (i - sa) * R;
+      // four of the warp's rows loaded before their products
+      for (int64_t i0 = sa + warp; i0 < sb; i0 += 4 * kPWarps) {
+        float v[4][4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int u = 0; u < 4; ++u) {
+          const int64_t i = i0 + (int64_t)u * kPWarps;
+          if (i < sb) {
+            load_row4<VEC>(M + i * n, col, n, v[u]);
+          } else {
 #pragma unroll
-          for (int c = 0; c < R; ++c) acc[q][c] = fmaf(v[q], pr[c], acc[q][c]);
+            for (int q = 0; q < 4; ++q) v[u][q] = 0.0f;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t i = i0 + (int64_t)u * kPWarps;
+          if (i >= sb) break;
+          const float* pr = ph + (i - sa) * R;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int c = 0; c < R; ++c) acc[q][c] = fmaf(v[u][q], pr[c], acc[q][c]);
+        }
       }
     }
   }
