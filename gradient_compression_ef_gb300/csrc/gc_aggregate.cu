@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(kAggThreads) agg_accumulate_kernel(
   const int64_t b = blockIdx.x;
   const int64_t a = b << kAggShift;
   const int len = (int)std::min<int64_t>(kAggRange, n - a);
-  for (int i = threadIdx.x; i < kAggRange; i += kAggThreads) sm.acc[i] = 0.0f;
+  for (int i = threadIdx.x; i < kAggRange / 4; i += kAggThreads)
+    reinterpret_cast<float4*>(sm.acc)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   for (int w = threadIdx.x; w < W; w += kAggThreads) {
     // clamped to [0, k): bounds from invalid (flagged) indices stay in range
     const int32_t* sw = start + (int64_t)w * (nblk + 1);
