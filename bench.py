@@ -175,6 +175,10 @@ def kernel_traffic(name, elems):
     return t["bytes_per_elem"] * elems, "ncu capture scaled by elements: " + t["profile"]
 
 
+# GB300's nominal HBM3e bandwidth (7.9 TB/s), reported beside the measured peak
+NOMINAL_HBM_GBS = 7900.0
+
+
 def dist_env():
     """(world, rank, local rank) from the launcher's environment."""
     return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
@@ -970,7 +974,8 @@ def main():
     roofline = {"bound": "hbm", "kernel": top[0], "achieved": kernels[top[0]]["achieved_gbs"],
                 "peak": peak, "unit": "GB/s", "peak_source": peak_src,
                 "frac": kernels[top[0]]["achieved_gbs"] / peak, "traffic": traffic,
-                "traffic_source": traffic_src}
+                "traffic_source": traffic_src,
+                "frac_of_nominal": kernels[top[0]]["achieved_gbs"] / NOMINAL_HBM_GBS}
     step_achieved = wl.algorithmic_bytes() / (ms_per_step * 1e-3) / 1e9
 
     # end to end through the C ABI with host buffers: every step copies its
