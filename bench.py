@@ -58,6 +58,9 @@ def parse_args():
     p.add_argument("--diag", action="store_true",
                    help="buckets workload: also compute the fused per-bucket diagnostics")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--residual", choices=["deferred", "immediate"], default="deferred",
+                   help="buckets workload: kept entries' residuals applied by the next step's "
+                        "read of e (one flush per timed run) or stored by every step")
     p.add_argument("--eager", action="store_true",
                    help="time eager launches instead of CUDA-graph replay")
     p.add_argument("--path", choices=["buckets", "per-bucket"], default="buckets",
@@ -256,7 +259,7 @@ class BucketWorkload:
     BITS, GROUP, SEED = 8, 64, 1000
 
     def __init__(self, torch, gc, dev, ratio_per_mille, streams, distinct, seed, path,
-                 n=inputs.FLAT_ELEMS, diag=False):
+                 n=inputs.FLAT_ELEMS, diag=False, residual="immediate"):
         self.torch, self.gc, self.dev, self.path = torch, gc, dev, path
         self.n = n
         self.bounds = inputs.bucket_bounds(self.n)
@@ -280,6 +283,11 @@ class BucketWorkload:
             self.streams = [torch.cuda.Stream(device=dev) for _ in range(streams)]
             self.ctxs = [gc.Context(max(l for _, l in self.bounds), stream=s)
                          for s in self.streams]
+        # deferred: each step keeps its kept entries' residuals aside and the
+        # next step applies them while it reads e; finish() flushes the last
+        self.deferred = residual == "deferred" and path == "buckets"
+        if self.deferred:
+            self.ctxs[0].set_deferred_residual(True)
 
     def out_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.outputs())
@@ -327,10 +335,26 @@ class BucketWorkload:
             j.record(s)
             main.wait_event(j)
 
+    def finish(self):
+        """Enqueues what completes the last step's results: with deferred
+        residuals, the flush of the last step's kept-entry residuals into e.
+        Returns the launches it made."""
+        if not self.deferred:
+            return 0
+        ctx = self.ctxs[0]
+        if ctx._stream_ref is not self.main:
+            ctx.set_stream(self.main)
+        ctx.bucket_flush()
+        return 1
+
     def capture(self):
         """One CUDA graph per distinct gradient buffer, each holding a whole
-        step.  Returns (graphs, launches/step)."""
+        step.  Returns (graphs, launches/step).  With deferred residuals one
+        eager step first leaves residuals pending, so that every captured
+        step applies the ones the step before it left."""
         torch = self.torch
+        if self.deferred:
+            self.launch_step(0)
         graphs = []
         cap = torch.cuda.Stream(device=self.dev)
         before = self.launches()
@@ -389,6 +413,9 @@ class _SimpleWorkload:
         if ctx._stream_ref is not main:
             ctx.set_stream(main)
         return ctx
+
+    def finish(self):
+        return 0
 
     def capture(self):
         torch = self.torch
@@ -715,6 +742,7 @@ def kernel_timing(wl, steps, warmup_step):
     ctx.enable_timing(64 * steps)
     for t in range(steps):
         wl.launch_step(warmup_step + t, ctxs=[ctx])
+    wl.finish()
     phases = {name: [ms, cnt] for name, (ms, cnt) in ctx.read_timing().items()}
     ctx.enable_timing(0)
     return phases
@@ -847,6 +875,11 @@ def config(args, wl=None):
                "quant": "qsgd 8-bit g64 stochastic", "path": args.path}
         if args.diag:
             cfg["diagnostics"] = "per-bucket sum c^2, sum g_hat^2, sum e'^2 fused into the passes"
+        if args.path == "buckets":
+            cfg["residual"] = ("deferred: each step's kept-entry residuals are applied by the "
+                               "next step's read of e; the last step's are flushed into e inside "
+                               "the timed region" if args.residual == "deferred" else
+                               "immediate: every step stores its kept-entry residuals into e")
     cfg["l2"] = l2["l2"].format(4 * n >> 20)
     cfg["parallelism"] = l2["parallelism"]
     if wl is not None:
@@ -902,7 +935,8 @@ def main():
 
     if args.workload == "buckets":
         wl = BucketWorkload(torch, gc, dev, args.ratio, args.streams, args.distinct,
-                            seed=rank_seed(rank), path=args.path, n=args.elems, diag=args.diag)
+                            seed=rank_seed(rank), path=args.path, n=args.elems, diag=args.diag,
+                            residual=args.residual)
     else:
         wl = WORKLOADS[args.workload](torch, gc, dev, args, seed=rank_seed(rank))
     torch.cuda.synchronize(dev)
@@ -924,6 +958,7 @@ def main():
             s_.wait_event(start)
         for t in range(steps):
             run_step(t)
+        wl.finish()  # inside the timed region
         stop.record(wl.main)
         torch.cuda.synchronize(dev)
         barrier()
@@ -952,7 +987,8 @@ def main():
     if args.eager:
         ms_per_step, launches, launch_mode = eager_ms, eager_launches, "eager"
     else:
-        ms_per_step, launches, launch_mode = graph_ms, per_step_launches * args.steps, "cuda_graph"
+        ms_per_step, launch_mode = graph_ms, "cuda_graph"
+        launches = per_step_launches * args.steps + (1 if getattr(wl, "deferred", False) else 0)
     value = whole_job_value(world, wl.n, ms_per_step)
     eager_value = whole_job_value(world, wl.n, eager_ms)
 

@@ -193,7 +193,7 @@ const char* gc_phase_name(int phase) {
       "ef_hist", "collect", "write", "ef_add", "quant_fused", "quant_stats",
       "quant_combine", "quant_apply", "dequant", "psgd_mq", "psgd_mtp", "psgd_resid",
       "refine", "bk_hist", "bk_collect", "bk_refine", "bk_write", "bk_quant", "agg_bounds",
-      "agg_accumulate", "randk_mark", "randk_write", "bk_diag"};
+      "agg_accumulate", "randk_mark", "randk_write", "bk_diag", "bk_flush"};
   return (phase >= 0 && phase < GC_PHASE_COUNT) ? names[phase] : "?";
 }
 
@@ -436,6 +436,17 @@ gc_status gc_powersgd_step(gc_ctx* ctx, const float* grad, float* err, int64_t m
   return gc::launch_powersgd(ctx, grad, err, m, n, r, P_out, Q_inout);
 }
 
+namespace {
+// Writes the residuals a deferred hybrid call left pending into its err.
+gc_status flush_pending(gc_ctx* ctx) {
+  if (!ctx->bk_pending) return GC_OK;
+  float* err = ctx->bk_pending;
+  ctx->bk_pending = nullptr;
+  if (!ctx->bk_base) return GC_OK;
+  return gc::launch_bucket_flush(ctx, err);
+}
+}  // namespace
+
 gc_status gc_ctx_set_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n,
                              const int64_t* bucket_k) {
   if (!ctx || nb < 1 || nb > gc::kMaxBuckets || !bucket_n || !bucket_k) return GC_ERR_INVALID_ARG;
@@ -447,8 +458,25 @@ gc_status gc_ctx_set_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n,
     if (bucket_n[b] % 4 != 0) return GC_ERR_ALIGNMENT;
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return GC_ERR_CUDA;
+  GC_TRY(flush_pending(ctx));
   if (cudaStreamSynchronize(ctx->stream) != cudaSuccess) return GC_ERR_CUDA;
   return gc::plan_buckets(ctx, nb, bucket_n, bucket_k);
+}
+
+gc_status gc_ctx_set_deferred_residual(gc_ctx* ctx, int on) {
+  if (!ctx) return GC_ERR_INVALID_ARG;
+  DeviceGuard guard(ctx->device);
+  if (!guard.ok) return GC_ERR_CUDA;
+  if (!on) GC_TRY(flush_pending(ctx));
+  ctx->bk_defer = on ? 1 : 0;
+  return GC_OK;
+}
+
+gc_status gc_bucket_flush(gc_ctx* ctx) {
+  if (!ctx) return GC_ERR_INVALID_ARG;
+  DeviceGuard guard(ctx->device);
+  if (!guard.ok) return GC_ERR_CUDA;
+  return flush_pending(ctx);
 }
 
 gc_status gc_bucket_offsets(int nb, const int64_t* bucket_k, int bits, int64_t group,
@@ -481,6 +509,7 @@ gc_status gc_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int32_t
   GC_TRY(check_buf(idx_out, w.vals_total > 0));
   GC_TRY(check_buf(val_out, w.vals_total > 0));
   if (diag_out) GC_TRY(check_buf(diag_out, true));
+  if (ctx->bk_pending) return GC_ERR_INVALID_ARG;  // flush the deferred residuals first
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return GC_ERR_CUDA;
   GC_TRY(gc::launch_ef_topk_buckets(ctx, grad, err, idx_out, val_out, true, 0, 0,
@@ -504,12 +533,18 @@ gc_status gc_ef_topk_quant_buckets(gc_ctx* ctx, const float* grad, float* err, i
   GC_TRY(check_buf(codes_out, w.vals_total > 0));
   GC_TRY(check_buf(scales_out, w.vals_total > 0));
   if (diag_out) GC_TRY(check_buf(diag_out, true));
+  // pending residuals belong to one error buffer
+  if (ctx->bk_pending && ctx->bk_pending != err) return GC_ERR_INVALID_ARG;
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return GC_ERR_CUDA;
   const bool diag = diag_out != nullptr;
-  GC_TRY(gc::launch_ef_topk_buckets(ctx, grad, err, idx_out, w.vals, false, bits, group, diag));
+  const bool patch = ctx->bk_pending != nullptr, defer = ctx->bk_defer != 0;
+  ctx->bk_pending = nullptr;
+  GC_TRY(gc::launch_ef_topk_buckets(ctx, grad, err, idx_out, w.vals, false, bits, group, diag,
+                                    patch));
   GC_TRY(gc::launch_quant_buckets(ctx, err, idx_out, bits, group, rounding, seed, step,
-                                  codes_out, scales_out, diag));
+                                  codes_out, scales_out, diag, defer));
+  if (defer) ctx->bk_pending = err;
   return diag ? gc::launch_bucket_diag(ctx, true, diag_out) : GC_OK;
 }
 

@@ -135,7 +135,15 @@ struct PassCursor {
   __device__ __forceinline__ bool valid(int32_t sub_hi) const { return seg < sub_hi; }
 };
 
-template <bool EF, bool DIAG>
+// With PATCH, e is first brought up to date with the residuals of the kept
+// entries of the previous (deferred) hybrid call: segment s's entries are
+// patch[seg_out[s] .. seg_out[s + 1]) (the last segment of a bucket ends at
+// k), sorted by position.  A warp holds a window of 64 of them in registers
+// (two per lane), fetched for its next segment while it works on the
+// current one, and writes each into the shared-memory stage of e of the
+// pass that holds its position, before c is formed.  The ragged end of a
+// bucket is read from err directly; its residuals were written there.
+template <bool EF, bool DIAG, bool PATCH = false>
 __global__ void __launch_bounds__(kH1Threads, 1) bk_hist_kernel(
     const float* __restrict__ grad, float* __restrict__ err, BucketWs w, int qbits,
     int64_t qgroup) {
@@ -199,12 +207,78 @@ __global__ void __launch_bounds__(kH1Threads, 1) bk_hist_kernel(
       issue(ic, k);
       if (ic.valid(sub_hi)) advance(ic);
     }
+
+    // pending residuals: entries [pu, pz) of the current segment are still
+    // to be applied, lane l holds entries pw + l and pw + 32 + l
+    const uint2* plist = PATCH ? w.patch + dp->idx_off : nullptr;
+    const int32_t seg_end = seg_first + dp->nseg;
+    auto seg_entries = [&](int32_t seg, uint32_t* a, uint32_t* z) {
+      const uint32_t z0 = seg + 1 < seg_end ? __ldcg(&w.seg_out[seg + 1]) : (uint32_t)bk;
+      *z = min(z0, (uint32_t)bk);  // never past the bucket's entries
+      *a = min(__ldcg(&w.seg_out[seg]), *z);
+    };
+    auto window = [&](uint32_t base, uint32_t z, uint2* e0, uint2* e1) {
+      const uint32_t j0 = base + lane, j1 = j0 + 32u;
+      *e0 = j0 < z ? __ldcg(&plist[j0]) : make_uint2(0xffffffffu, 0u);
+      *e1 = j1 < z ? __ldcg(&plist[j1]) : make_uint2(0xffffffffu, 0u);
+    };
+    int32_t p_seg = -1, n_seg = -1;
+    int n_stage = 0;  // next segment: 1 = range requested, 2 = window requested
+    uint32_t pu = 0u, pz = 0u, pw = 0u, na = 0u, nz = 0u;
+    uint2 pe0 = make_uint2(0xffffffffu, 0u), pe1 = pe0, ne0 = pe0, ne1 = pe0;
+    const bool patching = PATCH && EF && select;
     int st_use = 0, st_issue = kStages - 1;
     uint32_t cnt = 0u;
     float d_all = 0.0f, d_unl = 0.0f;  // sums of c^2: all, key below the guess
     while (uc.valid(sub_hi)) {
+      if (patching) {
+        if (uc.seg != p_seg) {
+          // a new segment: take the prefetched window, or fetch it now
+          p_seg = uc.seg;
+          if (n_seg == p_seg && n_stage == 2) {
+            pu = na; pz = nz; pe0 = ne0; pe1 = ne1;
+          } else {
+            seg_entries(p_seg, &pu, &pz);
+            window(pu, pz, &pe0, &pe1);
+          }
+          pw = pu;
+          n_seg = p_seg + kH1Warps;
+          n_stage = 0;
+          if (n_seg < sub_hi) {
+            seg_entries(n_seg, &na, &nz);
+            n_stage = 1;
+          }
+        } else if (n_stage == 1) {
+          window(na, nz, &ne0, &ne1);
+          n_stage = 2;
+        }
+      }
       cp_async_wait<kStages - 2>();  // the oldest pass has landed
       const int32_t p = uc.p, l1 = uc.l1;
+      if (patching && pu < pz) {
+        const uint32_t pend = (uint32_t)(p + kH1Pass), fend = (uint32_t)(l1 & ~3);
+        float* stg = reinterpret_cast<float*>(sm.se[warp][st_use]);
+        bool synced = false;
+        for (;;) {
+          // the entries of this pass are a run from pu (sorted positions)
+          const bool in0 = pw + lane >= pu && pw + lane < pz && pe0.x < pend;
+          const bool in1 = pw + 32u + lane >= pu && pw + 32u + lane < pz && pe1.x < pend;
+          const uint32_t b0 = __ballot_sync(0xffffffffu, in0);
+          const uint32_t b1 = __ballot_sync(0xffffffffu, in1);
+          if ((b0 | b1) == 0u) break;
+          if (!synced) {
+            __syncwarp();  // every lane's copies of this pass have landed
+            synced = true;
+          }
+          if (in0 && pe0.x >= (uint32_t)p && pe0.x < fend) stg[pe0.x - p] = __uint_as_float(pe0.y);
+          if (in1 && pe1.x >= (uint32_t)p && pe1.x < fend) stg[pe1.x - p] = __uint_as_float(pe1.y);
+          pu += __popc(b0) + __popc(b1);
+          if (pu < pw + 64u || pu >= pz) break;
+          pw += 64u;  // the window is used up inside this pass: the next 64
+          window(pw, pz, &pe0, &pe1);
+        }
+        if (synced) __syncwarp();
+      }
       float4 cv[kH1Rows];
 #pragma unroll
       for (int u = 0; u < kH1Rows; ++u) {
@@ -979,13 +1053,19 @@ __global__ void __launch_bounds__(kDiagThreads) bk_diag_kernel(BucketWs w, int q
 
 gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int32_t* idx_out,
                                  float* val_out, bool zero_err, int qbits, int64_t qgroup,
-                                 bool diag) {
+                                 bool diag, bool patch) {
   const BucketWs& w = ctx->bk;
   cudaStream_t s = ctx->stream;
   {
     LaunchScope L(ctx, GC_PHASE_BK_HIST);
     const size_t sm = sizeof(HistSmem);
-    if (err && diag)
+    if (err && patch && diag)
+      bk_hist_kernel<true, true, true><<<w.g_hist, kH1Threads, sm, s>>>(grad, err, w, qbits,
+                                                                        qgroup);
+    else if (err && patch)
+      bk_hist_kernel<true, false, true><<<w.g_hist, kH1Threads, sm, s>>>(grad, err, w, qbits,
+                                                                         qgroup);
+    else if (err && diag)
       bk_hist_kernel<true, true><<<w.g_hist, kH1Threads, sm, s>>>(grad, err, w, qbits, qgroup);
     else if (err)
       bk_hist_kernel<true, false><<<w.g_hist, kH1Threads, sm, s>>>(grad, err, w, qbits, qgroup);
@@ -1019,6 +1099,36 @@ gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int
     else
       bk_write_kernel<false, false><<<w.g_write, kBkThreads, 0, s>>>(err, w, idx_out, val_out);
   }
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+// The pending residuals of the patch list into err: one warp per chunk of
+// 128 entries of one bucket.
+__global__ void __launch_bounds__(kBkThreads) bk_flush_kernel(float* __restrict__ err,
+                                                              BucketWs w) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gwarp = ((int64_t)blockIdx.x * kBkThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kBkThreads) >> 5;
+  for (int64_t ch = gwarp; ch < w.nchunk; ch += nwarps) {
+    const BucketDesc d = w.desc[w.chunk_bucket[ch]];
+    const int64_t m0 = (ch - d.chunk_first) * kChunkVals;
+#pragma unroll
+    for (int j = 0; j < kChunkVals / 32; ++j) {
+      const int64_t m = m0 + 32 * j + lane;
+      if (m >= d.k) continue;
+      const uint2 pr = w.patch[d.idx_off + m];
+      if (pr.x < (uint32_t)d.n) err[d.start + pr.x] = __uint_as_float(pr.y);
+    }
+  }
+}
+
+gc_status launch_bucket_flush(gc_ctx* ctx, float* err) {
+  const BucketWs& w = ctx->bk;
+  if (w.nchunk == 0) return GC_OK;
+  LaunchScope L(ctx, GC_PHASE_BK_FLUSH);
+  const int grid =
+      (int)std::min<int64_t>(ceil_div(w.nchunk, kBkThreads / 32), (int64_t)ctx->num_sms * 8);
+  bk_flush_kernel<<<grid, kBkThreads, 0, ctx->stream>>>(err, w);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
 
@@ -1076,12 +1186,19 @@ gc_status plan_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n, const int64
       cudaFuncSetAttribute(bk_hist_kernel<true, true>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, hsm) != cudaSuccess ||
       cudaFuncSetAttribute(bk_hist_kernel<false, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, hsm) != cudaSuccess ||
+      cudaFuncSetAttribute(bk_hist_kernel<true, false, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, hsm) != cudaSuccess ||
+      cudaFuncSetAttribute(bk_hist_kernel<true, true, true>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, hsm) != cudaSuccess)
     return GC_ERR_CUDA;
   // every instantiation of a pass runs on the same grid (the tickets count
   // its blocks): the smallest resident count of them
-  w.g_hist = grid(std::min(blocks_per_sm(bk_hist_kernel<true, false>, kH1Threads, hsm),
-                           blocks_per_sm(bk_hist_kernel<true, true>, kH1Threads, hsm)));
+  w.g_hist = grid(std::min(
+      std::min(blocks_per_sm(bk_hist_kernel<true, false>, kH1Threads, hsm),
+               blocks_per_sm(bk_hist_kernel<true, true>, kH1Threads, hsm)),
+      std::min(blocks_per_sm(bk_hist_kernel<true, false, true>, kH1Threads, hsm),
+               blocks_per_sm(bk_hist_kernel<true, true, true>, kH1Threads, hsm))));
   w.g_coll = grid(std::min(blocks_per_sm(bk_collect_kernel<false>, kBkThreads),
                            blocks_per_sm(bk_collect_kernel<true>, kBkThreads)));
   w.g_ref = grid(blocks_per_sm(bk_refine_kernel, kBkThreads));
@@ -1116,6 +1233,7 @@ gc_status plan_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n, const int64
   const size_t o_stash = take(sizeof(uint2) * kBkStash * (size_t)nb);
   const size_t o_qoff = take(sizeof(int64_t) * 2 * (size_t)nb);
   const size_t o_vals = take(sizeof(float) * (size_t)std::max<int64_t>(voff, 1));
+  const size_t o_patch = take(sizeof(uint2) * (size_t)std::max<int64_t>(voff, 1));
   size_t o_dseg[3];
   for (int i = 0; i < 3; ++i) o_dseg[i] = take(sizeof(float) * nseg);
   const size_t o_dch = take(sizeof(float) * 2 * chunk_bucket.size());
@@ -1145,6 +1263,7 @@ gc_status plan_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n, const int64
   w.stash = reinterpret_cast<uint2*>(p + o_stash);
   w.qoff = reinterpret_cast<int64_t*>(p + o_qoff);
   w.vals = reinterpret_cast<float*>(p + o_vals);
+  w.patch = reinterpret_cast<uint2*>(p + o_patch);
   w.seg_c2 = reinterpret_cast<float*>(p + o_dseg[0]);
   w.seg_drop = reinterpret_cast<float*>(p + o_dseg[1]);
   w.seg_keep = reinterpret_cast<float*>(p + o_dseg[2]);

@@ -145,6 +145,8 @@ struct BucketWs {
   uint2* stash;         // [nb][kBkStash] (key, segment)
   int64_t* qoff;        // [nb][2] codes byte / scales float offset of each bucket
   float* vals;          // [vals_total] kept values of the hybrid call
+  uint2* patch;         // [vals_total] (position, bits of e') of the kept entries whose
+                        // residual write-back is deferred to the next call
   // per-segment / per-chunk partial sums of the diagnostics
   float* seg_c2;        // [nseg] sum of c^2
   float* seg_drop;      // [nseg] sum of c^2 over the entries not kept
@@ -189,6 +191,8 @@ struct gc_ctx {
   // bucket plan (gc_ctx_set_buckets)
   void* bk_base;
   gc::BucketWs bk;
+  int bk_defer;             // deferred residual write-back of the bucketed hybrid
+  float* bk_pending;        // error buffer whose kept-entry residuals are pending
 };
 
 namespace gc {
@@ -482,15 +486,23 @@ gc_status launch_powersgd(gc_ctx* ctx, const float* grad, float* err,
 // zero_err writes e' = +0 at the kept positions.  qbits > 0 also lays out
 // the QSGD outputs of (qbits, qgroup) for launch_quant_buckets.
 // diag also leaves the per-segment diagnostic partial sums.
+// patch applies the residuals the previous deferred hybrid call left in
+// the plan's patch list to e as it is read.
 gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int32_t* idx_out,
                                  float* val_out, bool zero_err, int qbits, int64_t qgroup,
-                                 bool diag);
+                                 bool diag, bool patch = false);
+// Writes the pending residuals of the patch list into err (the kept
+// positions of the last deferred hybrid call).
+gc_status launch_bucket_flush(gc_ctx* ctx, float* err);
 // QSGD of every bucket's kept values (from launch_ef_topk_buckets) with the
 // residual scattered to err; bucket b uses seed + b.  diag also leaves the
-// per-chunk diagnostic partial sums.
+// per-chunk diagnostic partial sums.  defer keeps the residuals in the
+// plan's patch list instead (only the ragged tail of a bucket, which the
+// next read takes directly from err, is also written to err).
 gc_status launch_quant_buckets(gc_ctx* ctx, float* err, const int32_t* idx_out, int bits,
                                int64_t group, int rounding, uint64_t seed, uint64_t step,
-                               uint8_t* codes_out, float* scales_out, bool diag);
+                               uint8_t* codes_out, float* scales_out, bool diag,
+                               bool defer = false);
 // Per-bucket diagnostics {sum c^2, sum g_hat^2, sum e'^2} into out[nb][3]
 // from the partial sums of the last bucketed call (quant: the hybrid's).
 gc_status launch_bucket_diag(gc_ctx* ctx, bool quant, double* out);

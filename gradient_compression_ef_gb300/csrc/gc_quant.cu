@@ -68,6 +68,8 @@ struct QuantOut {
   uint32_t* status;                // device status word
   float* ref;                      // differential quantisation: the history
   int refresh;                     // differential quantisation: ref taken as 0
+  uint2* patch;                    // deferred residuals: (position, bits of e') per entry
+  int64_t patch_tail;              // positions from here on are also written to err
 };
 
 __device__ __forceinline__ void zero_padding_bytes(const QuantOut& o) {
@@ -210,12 +212,40 @@ __device__ __forceinline__ void quant_fused_apply(
         if (valid[j]) err[i0 + j] = r[j];
     }
   } else if (IO == IO_SCATTER) {
+    if (o.patch) {
+      // deferred: (position, e') pairs in entry order, coalesced; the next
+      // read of e applies them.  An entry with a bad position gets one that
+      // matches no element.
+      uint2 pr[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (!valid[j]) continue;
-      const int32_t t = scatter_idx[i0 + j];
-      if (t >= 0 && (int64_t)t < o.scatter_n) err[t] = r[j];
-      else atomicOr(o.status, kStatusScatterIndex);
+      for (int j = 0; j < 4; ++j) {
+        pr[j] = make_uint2(0xffffffffu, 0u);
+        if (!valid[j]) continue;
+        const int32_t t = scatter_idx[i0 + j];
+        if (t >= 0 && (int64_t)t < o.scatter_n) {
+          pr[j] = make_uint2((uint32_t)t, __float_as_uint(r[j]));
+          if ((int64_t)t >= o.patch_tail) err[t] = r[j];
+        } else {
+          atomicOr(o.status, kStatusScatterIndex);
+        }
+      }
+      if (i0 + 3 < n) {
+        uint4* dst = reinterpret_cast<uint4*>(o.patch + i0);
+        dst[0] = make_uint4(pr[0].x, pr[0].y, pr[1].x, pr[1].y);
+        dst[1] = make_uint4(pr[2].x, pr[2].y, pr[3].x, pr[3].y);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (valid[j]) o.patch[i0 + j] = pr[j];
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (!valid[j]) continue;
+        const int32_t t = scatter_idx[i0 + j];
+        if (t >= 0 && (int64_t)t < o.scatter_n) err[t] = r[j];
+        else atomicOr(o.status, kStatusScatterIndex);
+      }
     }
   }
 }
@@ -741,17 +771,20 @@ __host__ __device__ inline QuantOut make_out(uint8_t* codes, float* scales, int6
   o.status = nullptr;
   o.ref = nullptr;
   o.refresh = 0;
+  o.patch = nullptr;
+  o.patch_tail = 0;
   return o;
 }
 
 // QSGD of the kept values of every bucket of a plan: one warp per chunk of
 // 128 values of one bucket; bucket b's codes and scales start at the offsets
-// the hist pass laid out, its residuals go to err[start_b + idx].
+// the hist pass laid out, its residuals go to err[start_b + idx] or, with
+// defer, to the plan's patch list.
 template <int BITS, int LPG, bool DIAG>
 __global__ void __launch_bounds__(kQThreads) quant_buckets_kernel(
     float* __restrict__ err, const int32_t* __restrict__ idx, BucketWs w,
     uint8_t* __restrict__ codes_out, float* __restrict__ scales_out, int stochastic,
-    uint64_t seed, uint64_t step) {
+    uint64_t seed, uint64_t step, int defer) {
   const int lane = threadIdx.x & 31;
   const int64_t warp_id = ((int64_t)blockIdx.x * kQThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kQThreads) >> 5;
@@ -763,6 +796,10 @@ __global__ void __launch_bounds__(kQThreads) quant_buckets_kernel(
                           GC_QSGD);
     o.scatter_n = d.n;
     o.status = w.status;
+    if (defer) {
+      o.patch = w.patch + d.idx_off;
+      o.patch_tail = d.n & ~3;  // the ragged end of a bucket is read from err directly
+    }
     if (lc == 0 && lane == 0) zero_padding_bytes(o);
     float dsum[2] = {0.0f, 0.0f};
     quant_fused_chunk<GC_QSGD, BITS, LPG, IO_SCATTER, DIAG>(
@@ -989,21 +1026,23 @@ gc_status launch_diff_dequant(gc_ctx* ctx, const uint8_t* codes, const float* sc
 
 gc_status launch_quant_buckets(gc_ctx* ctx, float* err, const int32_t* idx_out, int bits,
                                int64_t group, int rounding, uint64_t seed, uint64_t step,
-                               uint8_t* codes_out, float* scales_out, bool diag) {
+                               uint8_t* codes_out, float* scales_out, bool diag,
+                               bool defer) {
   const BucketWs& w = ctx->bk;
   if (w.nchunk == 0) return GC_OK;
   const int grid = grid_for(ctx, w.nchunk, kQThreads / 32, 8);
   const int st = rounding == GC_STOCHASTIC;
+  const int df = defer ? 1 : 0;
   cudaStream_t s = ctx->stream;
   LaunchScope L(ctx, GC_PHASE_BK_QUANT);
 #define GC_BQ(B, LPG)                                                                    \
   do {                                                                                   \
     if (diag)                                                                            \
       quant_buckets_kernel<B, LPG, true><<<grid, kQThreads, 0, s>>>(                     \
-          err, idx_out, w, codes_out, scales_out, st, seed, step);                       \
+          err, idx_out, w, codes_out, scales_out, st, seed, step, df);                   \
     else                                                                                 \
       quant_buckets_kernel<B, LPG, false><<<grid, kQThreads, 0, s>>>(                    \
-          err, idx_out, w, codes_out, scales_out, st, seed, step);                       \
+          err, idx_out, w, codes_out, scales_out, st, seed, step, df);                   \
   } while (0)
 #define GC_BQ_G(B)                 \
   switch (group) {                 \

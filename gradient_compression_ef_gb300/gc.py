@@ -20,7 +20,7 @@ NEAREST_EVEN, STOCHASTIC = 0, 1
 MODES = {"minmax": MINMAX, "qsgd": QSGD, "tern": TERN, "log": LOG}
 ROUNDINGS = {"nearest_even": NEAREST_EVEN, "stochastic": STOCHASTIC}
 
-PHASE_COUNT = 23
+PHASE_COUNT = 24
 
 OK = 0
 ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE = -1, -2, -3, -4
@@ -59,6 +59,8 @@ SIGNATURES = [
     ("gc_powersgd_step", _int, [_vp, _vp, _vp, _i64, _i64, _int, _vp, _vp]),
     ("gc_ef_topk_noalloc", _int, [_vp, _vp, _i64, _i64, _vp, _vp, _vp]),
     ("gc_ctx_set_buckets", _int, [_vp, _int, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
+    ("gc_ctx_set_deferred_residual", _int, [_vp, _int]),
+    ("gc_bucket_flush", _int, [_vp]),
     ("gc_bucket_offsets", _int, [_int, ctypes.POINTER(_i64), _int, _i64, ctypes.POINTER(_i64),
                                  ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
     ("gc_ef_topk_buckets", _int, [_vp, _vp, _vp, _vp, _vp, _vp]),
@@ -187,6 +189,19 @@ class Context:
         _check(lib.gc_ctx_set_buckets(self.handle, nb, an, ak), "gc_ctx_set_buckets")
         self.bucket_n = [int(v) for v in bucket_n]
         self.bucket_k = [int(v) for v in bucket_k]
+
+    def set_deferred_residual(self, on):
+        """on: the bucketed hybrid keeps the kept entries' residuals aside and
+        the next call on the same err applies them as it reads e; err is
+        exact only after bucket_flush().  off: flushes, then writes e' in
+        full again."""
+        _check(lib.gc_ctx_set_deferred_residual(self.handle, 1 if on else 0),
+               "gc_ctx_set_deferred_residual")
+
+    def bucket_flush(self):
+        """Writes the pending residuals of the last deferred hybrid call into
+        its err (asynchronous on the context's stream)."""
+        _check(lib.gc_bucket_flush(self.handle), "gc_bucket_flush")
 
     def close(self):
         if getattr(self, "handle", None) is not None and self.handle.value:

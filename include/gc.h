@@ -156,7 +156,8 @@ typedef enum gc_phase {
   GC_PHASE_RANDK_MARK = 20,  /* random sparsification: draws, residual, kept lists */
   GC_PHASE_RANDK_WRITE = 21, /* random sparsification: ordered output */
   GC_PHASE_BK_DIAG = 22,     /* bucketed: per-bucket diagnostics */
-  GC_PHASE_COUNT = 23
+  GC_PHASE_BK_FLUSH = 23,    /* bucketed: pending kept-entry residuals into e */
+  GC_PHASE_COUNT = 24
 } gc_phase;
 
 /* Name of a phase ("ef_hist", ...); "?" when out of range. */
@@ -415,6 +416,8 @@ GC_API gc_status gc_topk_quant_aggregate(gc_ctx* ctx, int W, int64_t k, const in
  * (replacing any earlier plan) and uploads the plan; synchronises the
  * context's stream first, so it must not be called while work is in flight
  * or during stream capture.  GC_ERR_NO_MEMORY when the reservation fails.
+ * Residuals still pending from a deferred hybrid call (below) are written
+ * to their error buffer first.
  */
 GC_API gc_status gc_ctx_set_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n,
                                     const int64_t* bucket_k);
@@ -481,6 +484,40 @@ GC_API gc_status gc_ef_topk_quant_buckets(gc_ctx* ctx, const float* grad, float*
                                           uint64_t seed, uint64_t step, int32_t* idx_out,
                                           uint8_t* codes_out, float* scales_out,
                                           double* diag_out);
+
+/*
+ * Deferred residual write-back of the bucketed hybrid.  The pages store the
+ * new error e' = c - g_hat after every step and add it back at the next
+ * ("gradient-compression-quantization-sparsification" 2.1, Top-K with error
+ * feedback; "4、梯度累积与梯度压缩" 4.3); they do not say when the kept
+ * entries' part has to reach memory.  Written at once it is one 4-byte store per kept entry at
+ * a random position of e, and each costs a DRAM sector read and write-back
+ * (about 40 us for 1.3 million kept entries, a tenth of the step).
+ *
+ * on = 1: gc_ef_topk_quant_buckets leaves e'_i = c_i at the kept positions
+ * and keeps their residuals c_i - g_hat_i in the plan's scratch; the next
+ * call on the same err applies them as it reads e (no extra pass, no
+ * scattered stores).  Indices, codes, scales and diagnostics of every call
+ * are bit-identical to the immediate write-back, and so is err once the
+ * residuals are flushed.  Until then err differs from e' at the last
+ * call's kept positions: call gc_bucket_flush before reading, changing or
+ * freeing err, or before handing it to any other call.
+ * on = 0 (the default): flushes pending residuals, then every call writes
+ * e' in full again.
+ * While residuals are pending: gc_ef_topk_quant_buckets with another err
+ * and gc_ef_topk_buckets return GC_ERR_INVALID_ARG (nothing launched);
+ * gc_ctx_set_buckets flushes first; gc_ctx_destroy drops them.
+ * A call captured into a CUDA graph while residuals are pending applies,
+ * at every replay, those the previous replay (or call) left.
+ */
+GC_API gc_status gc_ctx_set_deferred_residual(gc_ctx* ctx, int on);
+
+/*
+ * Writes the pending residuals of the last deferred hybrid call into its
+ * err (asynchronous on the context's stream: one small launch); a no-op when
+ * none are pending.
+ */
+GC_API gc_status gc_bucket_flush(gc_ctx* ctx);
 
 /*
  * Largest n accepted by gc_ef_topk_noalloc: its scratch is a fixed device
