@@ -155,12 +155,13 @@ class ClockSampler:
 
 # DRAM traffic of the dominant kernel from one ncu capture
 # (profiles/bucketed_kernels_65M_full.md: dram__bytes_read.sum + dram__bytes_write.sum
-# of bk_hist on 65,536,000 elements), per element; it scales with the elements.
+# of bk_hist, the variant that applies the previous step's deferred residuals,
+# on 65,536,000 elements), per element; it scales with the elements.
 # Valid only for the kernel source it was taken on (first 16 hex digits of the
 # SHA-256 of the file), else the bench reports null.
-TRAFFIC = {"bk_hist": {"bytes_per_elem": 747.9e6 / 65536000,
+TRAFFIC = {"bk_hist": {"bytes_per_elem": 751.0e6 / 65536000,
                        "source": "gradient_compression_ef_gb300/csrc/gc_buckets.cu",
-                       "sha256_16": "1e8ba159f1de6a60",
+                       "sha256_16": "4843462a706b4bc8",
                        "profile": "profiles/bucketed_kernels_65M_full.md"}}
 
 
