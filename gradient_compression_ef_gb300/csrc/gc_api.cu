@@ -538,7 +538,9 @@ gc_status gc_ef_topk_quant_buckets(gc_ctx* ctx, const float* grad, float* err, i
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return GC_ERR_CUDA;
   const bool diag = diag_out != nullptr;
-  const bool patch = ctx->bk_pending != nullptr, defer = ctx->bk_defer != 0;
+  // in deferred mode the hist pass checks the plan's ready flag itself, so a
+  // call captured into a graph applies whatever the call before it left
+  const bool defer = ctx->bk_defer != 0, patch = defer;
   ctx->bk_pending = nullptr;
   GC_TRY(gc::launch_ef_topk_buckets(ctx, grad, err, idx_out, w.vals, false, bits, group, diag,
                                     patch));

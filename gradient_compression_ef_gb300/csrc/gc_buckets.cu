@@ -136,7 +136,9 @@ struct PassCursor {
 };
 
 // With PATCH, e is first brought up to date with the residuals of the kept
-// entries of the previous (deferred) hybrid call: segment s's entries are
+// entries of the previous (deferred) hybrid call, when the plan's ready flag
+// says the patch list holds any (the collect pass clears the flag, the
+// deferred QSGD pass sets it, a flush clears it): segment s's entries are
 // patch[seg_out[s] .. seg_out[s + 1]) (the last segment of a bucket ends at
 // k), sorted by position.  A warp holds a window of 64 of them in registers
 // (two per lane), fetched for its next segment while it works on the
@@ -152,6 +154,7 @@ __global__ void __launch_bounds__(kH1Threads, 1) bk_hist_kernel(
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t lt = lanemask_lt();
   if (blockIdx.x == 0 && warp == 0 && qbits > 0) layout_quant_outputs(w, qbits, qgroup, lane);
+  const bool patch_ready = PATCH && __ldcg(w.patch_ready) != 0u;
   for (int i = threadIdx.x; i < kHistBins; i += kH1Threads) sm.h[i] = 0u;
   if (threadIdx.x == 0) sm.listed = 0u;
   __syncthreads();
@@ -226,7 +229,7 @@ __global__ void __launch_bounds__(kH1Threads, 1) bk_hist_kernel(
     int n_stage = 0;  // next segment: 1 = range requested, 2 = window requested
     uint32_t pu = 0u, pz = 0u, pw = 0u, na = 0u, nz = 0u;
     uint2 pe0 = make_uint2(0xffffffffu, 0u), pe1 = pe0, ne0 = pe0, ne1 = pe0;
-    const bool patching = PATCH && EF && select;
+    const bool patching = PATCH && EF && select && patch_ready;
     int st_use = 0, st_issue = kStages - 1;
     uint32_t cnt = 0u;
     float d_all = 0.0f, d_unl = 0.0f;  // sums of c^2: all, key below the guess
@@ -465,6 +468,8 @@ __global__ void __launch_bounds__(kBkThreads, 4) bk_collect_kernel(const float* 
   __shared__ int last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t lt = lanemask_lt();
+  // the hist pass before this one has applied any pending residuals
+  if (blockIdx.x == 0 && threadIdx.x == 0) *w.patch_ready = 0u;
   for (int i = threadIdx.x; i < kMidBins; i += kBkThreads) mid[i] = 0u;
   __syncthreads();
   int64_t s, s_hi;
@@ -1103,13 +1108,16 @@ gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int
 }
 
 // The pending residuals of the patch list into err: one warp per chunk of
-// 128 entries of one bucket.
+// 128 entries of one bucket.  Nothing is written unless the ready flag is
+// set; the last block to finish (every block has read the flag by then)
+// clears it.
 __global__ void __launch_bounds__(kBkThreads) bk_flush_kernel(float* __restrict__ err,
                                                               BucketWs w) {
   const int lane = threadIdx.x & 31;
   const int64_t gwarp = ((int64_t)blockIdx.x * kBkThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kBkThreads) >> 5;
-  for (int64_t ch = gwarp; ch < w.nchunk; ch += nwarps) {
+  const bool ready = __ldcg(w.patch_ready) != 0u;
+  for (int64_t ch = gwarp; ready && ch < w.nchunk; ch += nwarps) {
     const BucketDesc d = w.desc[w.chunk_bucket[ch]];
     const int64_t m0 = (ch - d.chunk_first) * kChunkVals;
 #pragma unroll
@@ -1118,6 +1126,14 @@ __global__ void __launch_bounds__(kBkThreads) bk_flush_kernel(float* __restrict_
       if (m >= d.k) continue;
       const uint2 pr = w.patch[d.idx_off + m];
       if (pr.x < (uint32_t)d.n) err[d.start + pr.x] = __uint_as_float(pr.y);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(w.flush_ticket, 1u) == gridDim.x - 1u) {
+      *w.patch_ready = 0u;
+      *w.flush_ticket = 0u;
     }
   }
 }
@@ -1222,6 +1238,7 @@ gc_status plan_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n, const int64
   auto take = [&](size_t bytes) { size_t o = off; off += (bytes + 255) / 256 * 256; return o; };
   const size_t o_desc = take(sizeof(BucketDesc) * nb);
   const size_t o_sel = take(sizeof(BucketSel) * nb);
+  const size_t o_flag = take(2 * sizeof(uint32_t));  // zeroed with the selection records
   const size_t o_segb = take(sizeof(int32_t) * nseg);
   const size_t o_chb = take(sizeof(int32_t) * chunk_bucket.size());
   const size_t o_hist = take(sizeof(uint32_t) * kHistBins * (size_t)nb);
@@ -1248,6 +1265,8 @@ gc_status plan_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n, const int64
   char* p = static_cast<char*>(base);
   w.desc = reinterpret_cast<BucketDesc*>(p + o_desc);
   w.sel = reinterpret_cast<BucketSel*>(p + o_sel);
+  w.patch_ready = reinterpret_cast<uint32_t*>(p + o_flag);
+  w.flush_ticket = w.patch_ready + 1;
   w.seg_bucket = reinterpret_cast<int32_t*>(p + o_segb);
   w.chunk_bucket = reinterpret_cast<int32_t*>(p + o_chb);
   w.hist = reinterpret_cast<uint32_t*>(p + o_hist);

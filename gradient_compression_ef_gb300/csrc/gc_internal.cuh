@@ -147,6 +147,8 @@ struct BucketWs {
   float* vals;          // [vals_total] kept values of the hybrid call
   uint2* patch;         // [vals_total] (position, bits of e') of the kept entries whose
                         // residual write-back is deferred to the next call
+  uint32_t* patch_ready;   // 1 while the patch list holds residuals not yet in e
+  uint32_t* flush_ticket;  // last-block ticket of the flush pass
   // per-segment / per-chunk partial sums of the diagnostics
   float* seg_c2;        // [nseg] sum of c^2
   float* seg_drop;      // [nseg] sum of c^2 over the entries not kept

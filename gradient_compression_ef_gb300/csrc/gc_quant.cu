@@ -799,6 +799,7 @@ __global__ void __launch_bounds__(kQThreads) quant_buckets_kernel(
     if (defer) {
       o.patch = w.patch + d.idx_off;
       o.patch_tail = d.n & ~3;  // the ragged end of a bucket is read from err directly
+      if (ch == 0 && lane == 0) *w.patch_ready = 1u;  // read by the next call's hist pass
     }
     if (lc == 0 && lane == 0) zero_padding_bytes(o);
     float dsum[2] = {0.0f, 0.0f};

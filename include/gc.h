@@ -507,8 +507,10 @@ GC_API gc_status gc_ef_topk_quant_buckets(gc_ctx* ctx, const float* grad, float*
  * While residuals are pending: gc_ef_topk_quant_buckets with another err
  * and gc_ef_topk_buckets return GC_ERR_INVALID_ARG (nothing launched);
  * gc_ctx_set_buckets flushes first; gc_ctx_destroy drops them.
- * A call captured into a CUDA graph while residuals are pending applies,
- * at every replay, those the previous replay (or call) left.
+ * The plan also records on the device whether residuals are pending, so a
+ * call captured into a CUDA graph applies, at every replay, those the call
+ * or replay before it left (none on the first call of a plan or after a
+ * flush); gc_bucket_flush after replays writes those of the last one.
  */
 GC_API gc_status gc_ctx_set_deferred_residual(gc_ctx* ctx, int on);
 

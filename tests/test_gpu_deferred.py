@@ -263,3 +263,68 @@ def test_deferred_full_size_workload(env):
     now.check()
     later.check()
     assert torch.equal(e_now.view(torch.int32), e_later.view(torch.int32))
+
+
+def test_deferred_graph_captured_first(env):
+    """A deferred call captured before any call of the plan ran: the first
+    replay finds nothing pending, every later one applies the residuals of
+    the replay before it; a flush after the replays completes e'."""
+    torch, gc, now, later = env
+    ns, ks = LAYOUTS["segments"]
+    g, e0 = make_inputs(ns, 19)
+    gd = dev_f32(torch, g)
+    now.set_buckets(ns, ks)
+    later.set_buckets(ns, ks)
+    on, ol = Outs(torch, gc, ks, 8, 64, False), Outs(torch, gc, ks, 8, 64, False)
+    e_now, e_later = dev_f32(torch, e0), dev_f32(torch, e0)
+    for _ in range(4):
+        gc.ef_topk_quant_buckets(now, gd, e_now, 8, 64, "stochastic", 6, 2, on.idx, on.codes,
+                                 on.scales)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    later.set_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        gc.ef_topk_quant_buckets(later, gd, e_later, 8, 64, "stochastic", 6, 2, ol.idx,
+                                 ol.codes, ol.scales)
+    torch.cuda.current_stream().wait_stream(s)
+    later.set_stream(torch.cuda.current_stream())
+    for _ in range(4):
+        graph.replay()
+    later.bucket_flush()
+    torch.cuda.synchronize()
+    later.check()
+    now.check()
+    compare(on.snapshot(), ol.snapshot(), ks, on.offs, "captured first")
+    assert_bits_equal(host(e_later), host(e_now), "captured first err")
+
+
+def test_deferred_flush_then_new_error_buffer_contents(env):
+    """After a flush the plan holds nothing pending: new contents written into
+    e (a checkpoint restored, say) are not overwritten by old residuals."""
+    torch, gc, now, later = env
+    ns, ks = LAYOUTS["mixed"]
+    g, e0 = make_inputs(ns, 23)
+    _, e1 = make_inputs(ns, 24)
+    gd = dev_f32(torch, g)
+    now.set_buckets(ns, ks)
+    later.set_buckets(ns, ks)
+    on, ol = Outs(torch, gc, ks, 8, 64, False), Outs(torch, gc, ks, 8, 64, False)
+    ed = dev_f32(torch, e0)
+    for step in range(2):
+        gc.ef_topk_quant_buckets(later, gd, ed, 8, 64, "stochastic", 3, step, ol.idx, ol.codes,
+                                 ol.scales)
+    later.bucket_flush()
+    ed.copy_(dev_f32(torch, e1))
+    e_now = dev_f32(torch, e1)
+    for step in range(2, 4):
+        gc.ef_topk_quant_buckets(now, gd, e_now, 8, 64, "stochastic", 3, step, on.idx, on.codes,
+                                 on.scales)
+        gc.ef_topk_quant_buckets(later, gd, ed, 8, 64, "stochastic", 3, step, ol.idx, ol.codes,
+                                 ol.scales)
+        compare(on.snapshot(), ol.snapshot(), ks, on.offs, "restored step %d" % step)
+    later.bucket_flush()
+    torch.cuda.synchronize()
+    later.check()
+    now.check()
+    assert_bits_equal(host(ed), host(e_now), "restored err")
