@@ -123,3 +123,6 @@ def test_bucket_calls_validate_on_the_host(gc):
     assert L.gc_bucket_offsets(2, k, 3, 64, out, out, None) == gc.ERR_UNSUPPORTED
     bad = (ctypes.c_int64 * 2)(1, -1)
     assert L.gc_bucket_offsets(2, bad, 8, 64, out, None, None) == gc.ERR_INVALID_ARG
+    assert L.gc_ctx_set_deferred_residual(None, 1) == gc.ERR_INVALID_ARG
+    assert L.gc_ctx_set_deferred_residual(None, 0) == gc.ERR_INVALID_ARG
+    assert L.gc_bucket_flush(None) == gc.ERR_INVALID_ARG
