@@ -159,9 +159,9 @@ class ClockSampler:
 # on 65,536,000 elements), per element; it scales with the elements.
 # Valid only for the kernel source it was taken on (first 16 hex digits of the
 # SHA-256 of the file), else the bench reports null.
-TRAFFIC = {"bk_hist": {"bytes_per_elem": 750.7e6 / 65536000,
+TRAFFIC = {"bk_hist": {"bytes_per_elem": 750.4e6 / 65536000,
                        "source": "gradient_compression_ef_gb300/csrc/gc_buckets.cu",
-                       "sha256_16": "cc63fce1bfcc4f50",
+                       "sha256_16": "6bfff760bd11984f",
                        "profile": "profiles/bucketed_kernels_65M_full.md"}}
 
 

@@ -509,11 +509,15 @@ gc_status gc_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int32_t
   GC_TRY(check_buf(idx_out, w.vals_total > 0));
   GC_TRY(check_buf(val_out, w.vals_total > 0));
   if (diag_out) GC_TRY(check_buf(diag_out, true));
-  if (ctx->bk_pending) return GC_ERR_INVALID_ARG;  // flush the deferred residuals first
+  // pending residuals belong to one error buffer
+  if (ctx->bk_pending && ctx->bk_pending != err) return GC_ERR_INVALID_ARG;
   DeviceGuard guard(ctx->device);
   if (!guard.ok) return GC_ERR_CUDA;
+  const bool defer = ctx->bk_defer != 0 && err != nullptr;
+  ctx->bk_pending = nullptr;
   GC_TRY(gc::launch_ef_topk_buckets(ctx, grad, err, idx_out, val_out, true, 0, 0,
-                                    diag_out != nullptr));
+                                    diag_out != nullptr, defer, defer));
+  if (defer) ctx->bk_pending = err;
   return diag_out ? gc::launch_bucket_diag(ctx, false, diag_out) : GC_OK;
 }
 

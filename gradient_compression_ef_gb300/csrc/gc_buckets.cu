@@ -863,12 +863,18 @@ __global__ void __launch_bounds__(kBkThreads, 4) bk_refine_kernel(BucketWs w) {
 // write: ordered (index, value) of the kept entries, four segments per warp
 // (lane r < 4 holds segment r's bookkeeping).
 // ---------------------------------------------------------------------------
+// With ZERO and defer, the kept entries' e' = +0 goes to the plan's patch
+// list as (position, 0) pairs in output order, for the next call's hist
+// pass, instead of a store at each random position of e (the ragged end of
+// a bucket, which the hist pass reads from e directly, is stored at once).
 template <bool ZERO, bool DIAG>
 __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict__ err,
                                                               BucketWs w,
                                                               int32_t* __restrict__ idx_out,
-                                                              float* __restrict__ val_out) {
+                                                              float* __restrict__ val_out,
+                                                              int defer) {
   const int lane = threadIdx.x & 31;
+  if (ZERO && defer && blockIdx.x == 0 && threadIdx.x == 0) *w.patch_ready = 1u;
   const uint32_t lt = lanemask_lt();
   const int64_t gwarp = ((int64_t)blockIdx.x * kBkThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kBkThreads) >> 5;
@@ -939,7 +945,14 @@ __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict_
             if (pos < bk && e[r][u].y < bn) {
               idx_out[off + pos] = (int32_t)e[r][u].y;
               val_out[off + pos] = __uint_as_float(e[r][u].x);
-              if (ZERO) err[start + e[r][u].y] = 0.0f;
+              if (ZERO) {
+                if (!defer) {
+                  err[start + e[r][u].y] = 0.0f;
+                } else {
+                  w.patch[off + pos] = make_uint2(e[r][u].y, 0u);
+                  if (e[r][u].y >= (bn & ~3u)) err[start + e[r][u].y] = 0.0f;
+                }
+              }
             } else {
               atomicOr(w.status, kStatusTopkOverflow);
             }
@@ -1058,7 +1071,7 @@ __global__ void __launch_bounds__(kDiagThreads) bk_diag_kernel(BucketWs w, int q
 
 gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int32_t* idx_out,
                                  float* val_out, bool zero_err, int qbits, int64_t qgroup,
-                                 bool diag, bool patch) {
+                                 bool diag, bool patch, bool defer_zero) {
   const BucketWs& w = ctx->bk;
   cudaStream_t s = ctx->stream;
   {
@@ -1094,15 +1107,15 @@ gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int
   {
     LaunchScope L(ctx, GC_PHASE_BK_WRITE);
     const bool z = zero_err && err;
-    const int gd = w.g_write_diag;
+    const int gd = w.g_write_diag, df = (z && defer_zero) ? 1 : 0;
     if (z && diag)
-      bk_write_kernel<true, true><<<gd, kBkThreads, 0, s>>>(err, w, idx_out, val_out);
+      bk_write_kernel<true, true><<<gd, kBkThreads, 0, s>>>(err, w, idx_out, val_out, df);
     else if (z)
-      bk_write_kernel<true, false><<<w.g_write, kBkThreads, 0, s>>>(err, w, idx_out, val_out);
+      bk_write_kernel<true, false><<<w.g_write, kBkThreads, 0, s>>>(err, w, idx_out, val_out, df);
     else if (diag)
-      bk_write_kernel<false, true><<<gd, kBkThreads, 0, s>>>(err, w, idx_out, val_out);
+      bk_write_kernel<false, true><<<gd, kBkThreads, 0, s>>>(err, w, idx_out, val_out, 0);
     else
-      bk_write_kernel<false, false><<<w.g_write, kBkThreads, 0, s>>>(err, w, idx_out, val_out);
+      bk_write_kernel<false, false><<<w.g_write, kBkThreads, 0, s>>>(err, w, idx_out, val_out, 0);
   }
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }

@@ -488,11 +488,13 @@ gc_status launch_powersgd(gc_ctx* ctx, const float* grad, float* err,
 // zero_err writes e' = +0 at the kept positions.  qbits > 0 also lays out
 // the QSGD outputs of (qbits, qgroup) for launch_quant_buckets.
 // diag also leaves the per-segment diagnostic partial sums.
-// patch applies the residuals the previous deferred hybrid call left in
-// the plan's patch list to e as it is read.
+// patch applies the residuals a previous deferred call left in the plan's
+// patch list to e as it is read (when the plan's ready flag says there are
+// any); defer_zero (with zero_err) puts the kept entries' e' = +0 into the
+// patch list instead of storing it.
 gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int32_t* idx_out,
                                  float* val_out, bool zero_err, int qbits, int64_t qgroup,
-                                 bool diag, bool patch = false);
+                                 bool diag, bool patch = false, bool defer_zero = false);
 // Writes the pending residuals of the patch list into err (the kept
 // positions of the last deferred hybrid call).
 gc_status launch_bucket_flush(gc_ctx* ctx, float* err);

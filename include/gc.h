@@ -486,27 +486,29 @@ GC_API gc_status gc_ef_topk_quant_buckets(gc_ctx* ctx, const float* grad, float*
                                           double* diag_out);
 
 /*
- * Deferred residual write-back of the bucketed hybrid.  The pages store the
- * new error e' = c - g_hat after every step and add it back at the next
- * ("gradient-compression-quantization-sparsification" 2.1, Top-K with error
- * feedback; "4、梯度累积与梯度压缩" 4.3); they do not say when the kept
- * entries' part has to reach memory.  Written at once it is one 4-byte store per kept entry at
- * a random position of e, and each costs a DRAM sector read and write-back
- * (about 40 us for 1.3 million kept entries, a tenth of the step).
+ * Deferred residual write-back of the bucketed calls with error feedback.
+ * The pages store the new error e' after every step and add it back at the
+ * next ("gradient-compression-quantization-sparsification" 2.1, Top-K with
+ * error feedback; "4、梯度累积与梯度压缩" 4.3); they do not say when the
+ * kept entries' part has to reach memory.  Written at once it is one 4-byte
+ * store per kept entry at a random position of e, and each costs a DRAM
+ * sector read and write-back (about 40 us for 1.3 million kept entries, a
+ * tenth of the hybrid's step).
  *
- * on = 1: gc_ef_topk_quant_buckets leaves e'_i = c_i at the kept positions
- * and keeps their residuals c_i - g_hat_i in the plan's scratch; the next
- * call on the same err applies them as it reads e (no extra pass, no
- * scattered stores).  Indices, codes, scales and diagnostics of every call
- * are bit-identical to the immediate write-back, and so is err once the
+ * on = 1: gc_ef_topk_quant_buckets (e' = c - g_hat) and gc_ef_topk_buckets
+ * with err (e' = +0) leave e'_i = c_i at the kept positions and keep the
+ * kept entries' e' in the plan's scratch; the next bucketed call on the
+ * same err applies them as it reads e (no extra pass, no scattered stores).
+ * Indices, values, codes, scales and diagnostics of every call are
+ * bit-identical to the immediate write-back, and so is err once the
  * residuals are flushed.  Until then err differs from e' at the last
  * call's kept positions: call gc_bucket_flush before reading, changing or
  * freeing err, or before handing it to any other call.
  * on = 0 (the default): flushes pending residuals, then every call writes
  * e' in full again.
- * While residuals are pending: gc_ef_topk_quant_buckets with another err
- * and gc_ef_topk_buckets return GC_ERR_INVALID_ARG (nothing launched);
- * gc_ctx_set_buckets flushes first; gc_ctx_destroy drops them.
+ * While residuals are pending, a bucketed call with another err (or none)
+ * returns GC_ERR_INVALID_ARG (nothing launched); gc_ctx_set_buckets
+ * flushes first; gc_ctx_destroy drops them.
  * The plan also records on the device whether residuals are pending, so a
  * call captured into a CUDA graph applies, at every replay, those the call
  * or replay before it left (none on the first call of a plan or after a
@@ -515,7 +517,7 @@ GC_API gc_status gc_ef_topk_quant_buckets(gc_ctx* ctx, const float* grad, float*
 GC_API gc_status gc_ctx_set_deferred_residual(gc_ctx* ctx, int on);
 
 /*
- * Writes the pending residuals of the last deferred hybrid call into its
+ * Writes the pending residuals of the last deferred bucketed call into its
  * err (asynchronous on the context's stream: one small launch); a no-op when
  * none are pending.
  */

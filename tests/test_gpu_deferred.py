@@ -209,15 +209,16 @@ def test_deferred_rules(env):
     assert later.launch_count() == before
     gc.ef_topk_quant_buckets(later, gd, ed, 8, 64, "nearest_even", 0, 0, o.idx, o.codes, o.scales)
     assert later.launch_count() - before == 5
-    # pending residuals belong to ed: another buffer or the Top-K call is refused
+    # pending residuals belong to ed: a call on another buffer, or on none, is refused
     with pytest.raises(gc.GCError) as ex:
         gc.ef_topk_quant_buckets(later, gd, other, 8, 64, "nearest_even", 0, 0, o.idx, o.codes,
                                  o.scales)
     assert ex.value.status == gc.ERR_INVALID_ARG
     val = torch.empty(o.idx.numel(), dtype=torch.float32, device="cuda")
-    with pytest.raises(gc.GCError) as ex:
-        gc.ef_topk_buckets(later, gd, ed, o.idx, val)
-    assert ex.value.status == gc.ERR_INVALID_ARG
+    for e_arg in (other, None):
+        with pytest.raises(gc.GCError) as ex:
+            gc.ef_topk_buckets(later, gd, e_arg, o.idx, val)
+        assert ex.value.status == gc.ERR_INVALID_ARG
     assert later.launch_count() - before == 5
     # the second call applies the first one's residuals
     gc.ef_topk_quant_buckets(later, gd, ed, 8, 64, "nearest_even", 0, 0, o.idx, o.codes, o.scales)
@@ -328,3 +329,59 @@ def test_deferred_flush_then_new_error_buffer_contents(env):
     later.check()
     now.check()
     assert_bits_equal(host(ed), host(e_now), "restored err")
+
+
+def run_topk_pair(env, ns, ks, grads, e0, calls, diag=False):
+    """Top-K-only (and, where calls says so, hybrid) bucketed steps on both
+    contexts; compares every output and the flushed err."""
+    torch, gc, now, later = env
+    now.set_buckets(ns, ks)
+    later.set_buckets(ns, ks)
+    oi, _, _ = gc.bucket_offsets(ks)
+    on, ol = Outs(torch, gc, ks, 8, 64, diag), Outs(torch, gc, ks, 8, 64, diag)
+    vals = [torch.full((max(oi[-1], 4),), -7.0, dtype=torch.float32, device="cuda")
+            for _ in range(2)]
+    e_now, e_later = dev_f32(torch, e0), dev_f32(torch, e0)
+    for step, (g, kind) in enumerate(zip(grads, calls)):
+        gd = dev_f32(torch, g)
+        for ctx, o, v, e in ((now, on, vals[0], e_now), (later, ol, vals[1], e_later)):
+            if kind == "topk":
+                gc.ef_topk_buckets(ctx, gd, e, o.idx, v, diag=o.diag)
+            else:
+                gc.ef_topk_quant_buckets(ctx, gd, e, 8, 64, "stochastic", 9, step, o.idx,
+                                         o.codes, o.scales, diag=o.diag)
+        now.check()
+        later.check()
+        a, b = on.snapshot(), ol.snapshot()
+        for b_, k in enumerate(ks):
+            assert_bits_equal(b[0][oi[b_]:oi[b_] + k], a[0][oi[b_]:oi[b_] + k],
+                              "step %d bucket %d idx" % (step, b_))
+            if kind == "topk":
+                assert_bits_equal(host(vals[1])[oi[b_]:oi[b_] + k],
+                                  host(vals[0])[oi[b_]:oi[b_] + k], "step %d val" % step)
+        if kind != "topk":
+            compare(a, b, ks, on.offs, "step %d" % step)
+        elif diag:
+            assert np.array_equal(a[3].view(np.uint64), b[3].view(np.uint64)), "diag"
+    later.bucket_flush()
+    later.check()
+    assert_bits_equal(host(e_later), host(e_now), "flushed err")
+
+
+@pytest.mark.parametrize("name", ["tiny", "segments", "mixed", "one_element"])
+@pytest.mark.parametrize("diag", [False, True])
+def test_deferred_topk_steps_match_immediate(env, name, diag):
+    """Top-K only: the kept entries' e' = +0 is deferred the same way."""
+    ns, ks = LAYOUTS[name]
+    grads = list(inputs.correlated_steps(sum(ns), 4, seed=30 + len(name)))
+    _, e0 = make_inputs(ns, 31)
+    run_topk_pair(env, ns, ks, grads, e0, ["topk"] * 4, diag)
+
+
+def test_deferred_topk_and_hybrid_interleaved(env):
+    """Top-K and hybrid steps on one error buffer: each applies what the call
+    before it left, whichever kind that was."""
+    ns, ks = many_buckets(33, nb=60)
+    grads = list(inputs.correlated_steps(sum(ns), 5, seed=33))
+    _, e0 = make_inputs(ns, 33)
+    run_topk_pair(env, ns, ks, grads, e0, ["topk", "quant", "quant", "topk", "quant"])
