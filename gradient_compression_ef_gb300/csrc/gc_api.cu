@@ -437,7 +437,7 @@ gc_status gc_powersgd_step(gc_ctx* ctx, const float* grad, float* err, int64_t m
 }
 
 namespace {
-// Writes the residuals a deferred hybrid call left pending into its err.
+// Writes the residuals a deferred bucketed call left pending into its err.
 gc_status flush_pending(gc_ctx* ctx) {
   if (!ctx->bk_pending) return GC_OK;
   float* err = ctx->bk_pending;

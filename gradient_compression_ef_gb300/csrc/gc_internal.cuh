@@ -496,7 +496,7 @@ gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int
                                  float* val_out, bool zero_err, int qbits, int64_t qgroup,
                                  bool diag, bool patch = false, bool defer_zero = false);
 // Writes the pending residuals of the patch list into err (the kept
-// positions of the last deferred hybrid call).
+// positions of the last deferred bucketed call).
 gc_status launch_bucket_flush(gc_ctx* ctx, float* err);
 // QSGD of every bucket's kept values (from launch_ef_topk_buckets) with the
 // residual scattered to err; bucket b uses seed + b.  diag also leaves the

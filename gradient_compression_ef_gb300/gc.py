@@ -191,15 +191,15 @@ class Context:
         self.bucket_k = [int(v) for v in bucket_k]
 
     def set_deferred_residual(self, on):
-        """on: the bucketed hybrid keeps the kept entries' residuals aside and
-        the next call on the same err applies them as it reads e; err is
-        exact only after bucket_flush().  off: flushes, then writes e' in
-        full again."""
+        """on: the bucketed calls with error feedback keep the kept entries'
+        residuals aside and the next bucketed call on the same err applies
+        them as it reads e; err is exact only after bucket_flush().  off:
+        flushes, then writes e' in full again."""
         _check(lib.gc_ctx_set_deferred_residual(self.handle, 1 if on else 0),
                "gc_ctx_set_deferred_residual")
 
     def bucket_flush(self):
-        """Writes the pending residuals of the last deferred hybrid call into
+        """Writes the pending residuals of the last deferred bucketed call into
         its err (asynchronous on the context's stream)."""
         _check(lib.gc_bucket_flush(self.handle), "gc_bucket_flush")
 

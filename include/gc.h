@@ -416,7 +416,7 @@ GC_API gc_status gc_topk_quant_aggregate(gc_ctx* ctx, int W, int64_t k, const in
  * (replacing any earlier plan) and uploads the plan; synchronises the
  * context's stream first, so it must not be called while work is in flight
  * or during stream capture.  GC_ERR_NO_MEMORY when the reservation fails.
- * Residuals still pending from a deferred hybrid call (below) are written
+ * Residuals still pending from a deferred bucketed call (below) are written
  * to their error buffer first.
  */
 GC_API gc_status gc_ctx_set_buckets(gc_ctx* ctx, int nb, const int64_t* bucket_n,
