@@ -153,16 +153,16 @@ class ClockSampler:
                 "source": "nvml"}
 
 
-# DRAM traffic of the dominant kernel from one ncu capture
-# (profiles/bucketed_kernels_65M_full.md: dram__bytes_read.sum + dram__bytes_write.sum
-# of bk_hist, the variant that applies the previous step's deferred residuals,
-# on 65,536,000 elements), per element; it scales with the elements.
-# Valid only for the kernel source it was taken on (first 16 hex digits of the
-# SHA-256 of the file), else the bench reports null.
+# DRAM traffic of the dominant kernel from one ncu capture:
+# dram__bytes_read.sum + dram__bytes_write.sum of bk_hist (the variant that
+# applies the previous step's deferred residuals) on 65,536,000 elements, per
+# element; the pass streams each element once, so it scales with the
+# elements.  Valid only for the kernel source it was taken on (first 16 hex
+# digits of the SHA-256 of the file), else the bench reports null.
 TRAFFIC = {"bk_hist": {"bytes_per_elem": 750.4e6 / 65536000,
                        "source": "gradient_compression_ef_gb300/csrc/gc_buckets.cu",
                        "sha256_16": "6bfff760bd11984f",
-                       "profile": "profiles/bucketed_kernels_65M_full.md"}}
+                       "captured_on": "65,536,000 elements"}}
 
 
 def kernel_traffic(name, elems):
@@ -176,7 +176,8 @@ def kernel_traffic(name, elems):
         return None, "kernel source missing"
     if digest[:16] != t["sha256_16"]:
         return None, "kernel changed since the ncu capture"
-    return t["bytes_per_elem"] * elems, "ncu capture scaled by elements: " + t["profile"]
+    return t["bytes_per_elem"] * elems, ("ncu dram bytes of one launch on %s, scaled by "
+                                         "elements" % t["captured_on"])
 
 
 # GB300's nominal HBM3e bandwidth (7.9 TB/s), reported beside the measured peak
@@ -328,7 +329,7 @@ class BucketWorkload:
         for b, ((start, length), k) in enumerate(zip(self.bounds, self.ks)):
             ctx = ctxs[b % len(ctxs)]
             gc.ef_topk_quant(ctx, g[start:start + length], self.err[start:start + length], k,
-                             self.BITS, self.GROUP, "stochastic", self.SEED + b, t,
+                             self.BITS, self.GROUP, "stochastic", gc.bucket_seed(self.SEED, b), t,
                              self.idx[oi[b]:oi[b] + k], self.codes[oc[b]:oc[b + 1]],
                              self.scales[os_[b]:os_[b + 1]], n=length)
         for s in streams:

@@ -44,7 +44,10 @@ def _stale(target, deps):
 def build(force=False, verbose=False, extra=()):
     """Compiles the CUDA sources (only what changed) and links libgc.so."""
     os.makedirs(OUT_DIR, exist_ok=True)
-    headers = [os.path.join(CSRC, "gc_internal.cuh"), os.path.join(INCLUDE, "gc.h")]
+    # every source includes gc.h and some of the csrc headers: any change to
+    # one of them rebuilds every object
+    headers = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh"))
+    headers.append(os.path.join(INCLUDE, "gc.h"))
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)

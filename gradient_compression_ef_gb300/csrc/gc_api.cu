@@ -93,7 +93,9 @@ const char* gc_status_string(int status) {
     case GC_ERR_INVALID_ARG: return "invalid argument";
     case GC_ERR_UNSUPPORTED: return "unsupported bit width or mode";
     case GC_ERR_ALIGNMENT: return "buffer not 16-byte aligned";
-    case GC_ERR_WORKSPACE: return "size exceeds the context's reserved scratch";
+    case GC_ERR_WORKSPACE:
+      return "size exceeds the reserved scratch (the context's, or the fixed array of "
+             "the allocation-free call)";
     case GC_ERR_CUDA: return "CUDA runtime error";
     case GC_ERR_DEVICE_CHECK: return "device-side self check failed";
     case GC_ERR_NO_MEMORY: return "device allocation failed";
@@ -478,6 +480,8 @@ gc_status gc_bucket_flush(gc_ctx* ctx) {
   if (!guard.ok) return GC_ERR_CUDA;
   return flush_pending(ctx);
 }
+
+uint64_t gc_bucket_seed(uint64_t seed, int b) { return gc::bucket_seed(seed, b); }
 
 gc_status gc_bucket_offsets(int nb, const int64_t* bucket_k, int bits, int64_t group,
                             int64_t* idx_off, int64_t* codes_off, int64_t* scales_off) {

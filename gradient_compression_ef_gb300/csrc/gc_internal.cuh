@@ -239,6 +239,15 @@ __device__ __forceinline__ void uniform4(uint64_t block, uint64_t seed,
   u[3] = __fmul_rn(__uint2float_rn(r.w >> 8), 0x1p-24f);
 }
 
+// Philox key of bucket b of a bucketed call: the call's seed with b times
+// the 64-bit golden-ratio constant xor-ed in.  Bucket 0 keeps the seed, and a
+// caller that changes the seed by small steps between calls never makes one
+// bucket reuse another bucket's draws (seed + b would: bucket b + 1 under
+// seed s would draw what bucket b draws under seed s + 1).
+__host__ __device__ __forceinline__ uint64_t bucket_seed(uint64_t seed, int b) {
+  return seed ^ ((uint64_t)b * 0x9E3779B97F4A7C15ull);
+}
+
 // Natural logarithm and exponential of the logarithmic quantiser, by the
 // Cody-Waite method (W. J. Cody, W. Waite, "Software Manual for the
 // Elementary Functions", 1980, ALOG and EXP), every step one rounded
@@ -499,7 +508,7 @@ gc_status launch_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err, int
 // positions of the last deferred bucketed call).
 gc_status launch_bucket_flush(gc_ctx* ctx, float* err);
 // QSGD of every bucket's kept values (from launch_ef_topk_buckets) with the
-// residual scattered to err; bucket b uses seed + b.  diag also leaves the
+// residual scattered to err; bucket b uses bucket_seed(seed, b).  diag also leaves the
 // per-chunk diagnostic partial sums.  defer keeps the residuals in the
 // plan's patch list instead (only the ragged tail of a bucket, which the
 // next read takes directly from err, is also written to err).

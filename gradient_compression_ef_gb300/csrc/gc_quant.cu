@@ -805,7 +805,7 @@ __global__ void __launch_bounds__(kQThreads) quant_buckets_kernel(
     float dsum[2] = {0.0f, 0.0f};
     quant_fused_chunk<GC_QSGD, BITS, LPG, IO_SCATTER, DIAG>(
         w.vals + d.idx_off, err + d.start, idx + d.idx_off, d.k, o, stochastic,
-        seed + (uint64_t)b, step, lc * kChunkVals, lane, dsum);
+        bucket_seed(seed, b), step, lc * kChunkVals, lane, dsum);
     if (DIAG) {
       const float g2 = warp_allsum(dsum[0]), r2 = warp_allsum(dsum[1]);
       if (lane == 0) {

@@ -58,6 +58,7 @@ SIGNATURES = [
     ("gc_diff_dequant", _int, [_vp, _vp, _vp, _i64, _int, _i64, _int, _int, _vp]),
     ("gc_powersgd_step", _int, [_vp, _vp, _vp, _i64, _i64, _int, _vp, _vp]),
     ("gc_ef_topk_noalloc", _int, [_vp, _vp, _i64, _i64, _vp, _vp, _vp]),
+    ("gc_bucket_seed", _u64, [_u64, _int]),
     ("gc_ctx_set_buckets", _int, [_vp, _int, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
     ("gc_ctx_set_deferred_residual", _int, [_vp, _int]),
     ("gc_bucket_flush", _int, [_vp]),
@@ -287,6 +288,11 @@ def ef_topk_noalloc(grad, err, k, idx_out, val_out, stream=None, n=None):
     n = grad.numel() if n is None else n
     _check(lib.gc_ef_topk_noalloc(_ptr(grad), _ptr(err), n, k, _ptr(idx_out), _ptr(val_out),
                                   handle), "gc_ef_topk_noalloc")
+
+
+def bucket_seed(seed, b):
+    """The Philox key the bucketed calls give bucket b for ``seed``."""
+    return int(lib.gc_bucket_seed(seed, b))
 
 
 def bucket_offsets(bucket_k, bits=None, group=None):

@@ -71,7 +71,9 @@ typedef enum gc_status {
   GC_ERR_UNSUPPORTED = -2,  /* bits not in {1,2,4,8}; TERN with bits != 2;
                                LOG with bits == 1 */
   GC_ERR_ALIGNMENT = -3,    /* a buffer is not 16-byte aligned */
-  GC_ERR_WORKSPACE = -4,    /* n above the context's reserved capacity */
+  GC_ERR_WORKSPACE = -4,    /* n above the reserved scratch: the context's
+                               capacity, or GC_NOALLOC_MAX_N for
+                               gc_ef_topk_noalloc */
   GC_ERR_CUDA = -5,         /* a CUDA runtime call or launch failed */
   GC_ERR_DEVICE_CHECK = -6, /* a device-side self check failed */
   GC_ERR_NO_MEMORY = -7     /* gc_ctx_create could not reserve scratch */
@@ -324,8 +326,11 @@ GC_API gc_status gc_ef_topk_quant(gc_ctx* ctx, const float* grad, float* err,
  * "梯度聚合通信优化实战方案" 梯度压缩原理 (error compensation is what makes
  * PowerSGD work).  Steps (Vogels et al., NeurIPS 2019, Algorithm 1):
  *   M = grad + err  (stored into err);  P = M Q;
- *   P_hat = modified Gram-Schmidt(P);  Q' = M^T P_hat;
- *   err = M - P_hat Q'^T.
+ *   P_hat = the orthonormal factor of P (the page's Gram-Schmidt step):
+ *     computed as a Cholesky QR, G = P^T P in binary64, G = U^T U with U
+ *     upper triangular and positive diagonal, P_hat = P U^-1 -- the same
+ *     factor Gram-Schmidt gives, up to rounding; a zero column stays zero;
+ *   Q' = M^T P_hat;  err = M - P_hat Q'^T.
  * grad, err: fp32 m x n row-major;  P_out: fp32 m x r (receives P_hat);
  * Q_inout: fp32 n x r (read as Q, overwritten with Q').  1 <= r <= 16;
  * requires gc_ctx_reserve_powersgd with limits covering (m, n, r).
@@ -403,8 +408,20 @@ GC_API gc_status gc_topk_quant_aggregate(gc_ctx* ctx, int W, int64_t k, const in
  * elements [start_b, start_b + bucket_n[b]) with start_b = sum of the
  * earlier sizes, and keeps bucket_k[b] entries.  Per bucket the result is
  * bit-identical to the single-bucket call on the slice (gc_ef_topk, or
- * gc_ef_topk_quant with seed + b); indices are bucket-local.
+ * gc_ef_topk_quant with the key gc_bucket_seed(seed, b)); indices are
+ * bucket-local.  The flat array may hold more than 2^31 elements (up to
+ * 65536 buckets of up to 2^31 - 2^16 elements each).
  */
+
+/*
+ * Philox key of bucket b in a bucketed call with `seed`: seed XOR (b *
+ * 0x9E3779B97F4A7C15), the 64-bit golden-ratio constant floor(2^64 / phi).
+ * Bucket 0 keeps the seed; calls whose seeds differ by small amounts never
+ * give two buckets the same key (seed + b would: bucket b + 1 under seed s
+ * would repeat bucket b under seed s + 1).  The pages compress bucket by
+ * bucket and fix no random stream per bucket ("4、梯度累积与梯度压缩" 4.3).
+ */
+GC_API uint64_t gc_bucket_seed(uint64_t seed, int b);
 
 /*
  * Sets the context's bucket plan: nb (1 .. 65536) buckets of bucket_n[b]
@@ -472,8 +489,8 @@ GC_API gc_status gc_ef_topk_buckets(gc_ctx* ctx, const float* grad, float* err,
 
 /*
  * gc_ef_topk_quant on every bucket of the plan: bucket b is compressed as
- * gc_ef_topk_quant(slice_b, bucket_k[b], bits, group, rounding, seed + b,
- * step) with its indices at idx_out + idx_off[b], its codes at codes_out +
+ * gc_ef_topk_quant(slice_b, bucket_k[b], bits, group, rounding,
+ * gc_bucket_seed(seed, b), step) with its indices at idx_out + idx_off[b], its codes at codes_out +
  * codes_off[b] and its scales at scales_out + scales_off[b]
  * (gc_bucket_offsets).  group must be a power of two in 4 .. 128
  * (GC_ERR_UNSUPPORTED otherwise); err must not be NULL.  diag_out: NULL, or
@@ -548,7 +565,10 @@ GC_API gc_status gc_bucket_flush(gc_ctx* ctx);
  * the library's module is loaded on that GPU and held until the process
  * exits.  The first call on each device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  Every call on a device shares the one
+ * call before any stream capture.  The address is kept for the life of the
+ * process: after cudaDeviceReset (or any reset of the device's primary
+ * context) the module is loaded again elsewhere, so do not call this entry
+ * point on that device after such a reset.  Every call on a device shares the one
  * array, and each call first clears the part that must start at zero;
  * calls that overlap on the GPU (other streams, other host threads) race on
  * it and give wrong results, so serialise them.  Device self-check status

@@ -118,6 +118,18 @@ float orc_uniform(uint64_t seed, uint64_t step, uint64_t i) {
   return (float)(word >> 8) * 0x1p-24f;
 }
 
+/*
+ * Key of bucket b of a bucketed call (reading: the pages compress bucket by
+ * bucket [P3 4.3, P4 通信计算重叠] and fix no stream per bucket).  Bucket b
+ * draws with the key seed XOR (b * 0x9E3779B97F4A7C15), the 64-bit
+ * golden-ratio constant floor(2^64 / phi): bucket 0 keeps the call's seed,
+ * and buckets of calls whose seeds differ by small amounts never share a
+ * key.
+ */
+uint64_t orc_bucket_seed(uint64_t seed, int64_t b) {
+  return seed ^ ((uint64_t)b * UINT64_C(0x9E3779B97F4A7C15));
+}
+
 /* ------------------------------------------------------------------------ */
 /* Sizes of the compressed formats.                                          */
 /* ------------------------------------------------------------------------ */

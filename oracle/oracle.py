@@ -47,6 +47,8 @@ def lib():
         L.orc_philox4x32_10.restype = None
         L.orc_uniform.argtypes = [_u64, _u64, _u64]
         L.orc_uniform.restype = ctypes.c_float
+        L.orc_bucket_seed.argtypes = [_u64, _i64]
+        L.orc_bucket_seed.restype = _u64
         L.orc_codes_bytes.argtypes = [_i64, _int, _int]
         L.orc_codes_bytes.restype = _i64
         L.orc_scales_floats.argtypes = [_i64, _i64, _int]
@@ -127,6 +129,11 @@ def philox4x32_10(counter, key):
 def uniform(seed, step, i):
     """The stochastic-rounding draw u in [0, 1) of element i."""
     return float(lib().orc_uniform(seed, step, i))
+
+
+def bucket_seed(seed, b):
+    """The Philox key bucket b of a bucketed call draws with."""
+    return int(lib().orc_bucket_seed(seed, b))
 
 
 def codes_bytes(n, bits, mode):

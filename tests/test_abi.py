@@ -126,3 +126,10 @@ def test_bucket_calls_validate_on_the_host(gc):
     assert L.gc_ctx_set_deferred_residual(None, 1) == gc.ERR_INVALID_ARG
     assert L.gc_ctx_set_deferred_residual(None, 0) == gc.ERR_INVALID_ARG
     assert L.gc_bucket_flush(None) == gc.ERR_INVALID_ARG
+
+
+def test_bucket_seed_matches_the_oracle(gc):
+    import oracle
+    for seed in (0, 1, 1000, 0xFFFFFFFFFFFFFFFF, 0x123456789ABCDEF0):
+        for b in (0, 1, 2, 20, 255, 65535):
+            assert gc.bucket_seed(seed, b) == oracle.bucket_seed(seed, b)

@@ -135,7 +135,7 @@ def check_quant(ns, ks, g, e, bits, group, rounding, seed, step, offs, idx, code
     for b, (n, k) in enumerate(zip(ns, ks)):
         sl = slice(st[b], st[b + 1])
         o_idx, o_codes, o_scales, o_err = oracle.ef_topk_quant(
-            g[sl], e[sl], k, bits, group, rounding, seed + b, step)
+            g[sl], e[sl], k, bits, group, rounding, oracle.bucket_seed(seed, b), step)
         w = "%s bucket %d" % (what, b)
         assert_bits_equal(idx[oi[b]:oi[b] + k], o_idx, w + " idx")
         assert o_codes.size == oc[b + 1] - oc[b]

@@ -126,8 +126,8 @@ def check_quant(ns, ks, g, e, bits, group, rounding, seed, step, offs, idx, code
     for b in (range(len(ns)) if buckets is None else buckets):
         k = ks[b]
         sl = slice(st[b], st[b + 1])
-        o_idx, o_codes, o_scales, _ = oracle.ef_topk_quant(g[sl], e[sl].copy(), k, bits, group,
-                                                           rounding, seed + b, step)
+        o_idx, o_codes, o_scales, _ = oracle.ef_topk_quant(
+            g[sl], e[sl].copy(), k, bits, group, rounding, oracle.bucket_seed(seed, b), step)
         w = "%s bucket %d" % (what, b)
         assert_bits_equal(idx[oi[b]:oi[b] + k], o_idx, w + " idx")
         assert_bits_equal(codes[oc[b]:oc[b + 1]], o_codes, w + " codes")

@@ -82,3 +82,29 @@ def test_uniform_distribution():
     v = np.array([oracle.uniform(42, 4, i) for i in range(256)])
     w = np.array([oracle.uniform(43, 3, i) for i in range(256)])
     assert not np.array_equal(u[:256], v) and not np.array_equal(u[:256], w)
+
+
+def test_bucket_seed_golden_ratio_key():
+    """Bucket b of a bucketed call draws with seed XOR b * floor(2^64 / phi).
+    The constant is derived here from sqrt(5) in exact integer arithmetic,
+    not retyped: floor(2^64 (sqrt(5) - 1) / 2)."""
+    from math import isqrt
+    # floor(2^64 * (sqrt(5) - 1) / 2) = floor((sqrt(5 * 4^64) - 2^64) / 2)
+    phi64 = (isqrt(5 << 128) - (1 << 64)) // 2
+    mask = (1 << 64) - 1
+    for seed in (0, 1, 42, 0xDEADBEEF12345678, mask):
+        assert oracle.bucket_seed(seed, 0) == seed
+        for b in (1, 2, 3, 255, 65535):
+            assert oracle.bucket_seed(seed, b) == seed ^ ((b * phi64) & mask)
+
+
+def test_bucket_seeds_do_not_collide_across_nearby_calls():
+    """A caller that steps its seed by small amounts (s, s + 1, ...) never
+    gives two (seed, bucket) pairs the same key, as seed + b would
+    (bucket b + 1 under seed s = bucket b under seed s + 1)."""
+    keys = {}
+    for seed in range(1000, 1064):
+        for b in range(300):
+            k = oracle.bucket_seed(seed, b)
+            assert k not in keys, (seed, b, keys.get(k))
+            keys[k] = (seed, b)
