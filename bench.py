@@ -1,15 +1,19 @@
 #!/usr/bin/env python3
 """Throughput of the GB300 error-feedback gradient compressor.
 
-Default workload: a flat fp32 gradient of 134,217,728 elements (512 MiB) cut
-into 25 MiB buckets (20 x 6,553,600 + 1 x 3,145,728), Student-t (nu = 3)
-values x 1e-3 with temporally correlated steps g_t = 0.9 g_{t-1} + 0.436
-fresh_t.  One step is one pass of the whole compressor over every bucket:
-error feedback + Top-K 1 % + 8-bit QSGD (groups of 64, stochastic rounding)
-on the kept values + dequantisation + residual write-back.  By default the
-step is one gc_ef_topk_quant_buckets call (every bucket in one launch per
-pass); --path per-bucket calls gc_ef_topk_quant once per bucket, spread over
-several contexts / CUDA streams.
+Default workload (--workload layers): the gradient set of a 32-layer
+transformer, each layer {4096x4096 x4, 4096x11008 x2, 11008x4096, 4096},
+6,476,136,448 fp32 elements (25.9 GB) drawn N(0, (1e-3/sqrt(fan_in))^2) per
+tensor, with temporally correlated steps g_t = 0.9 g_{t-1} + 0.436 fresh_t.
+One step is one pass of the whole compressor over every tensor: error
+feedback + Top-K 1 % of the tensor + 8-bit QSGD (groups of 64, stochastic
+rounding) on the kept values + dequantisation + residual write-back, each
+of the 256 tensors its own bucket of one gc_ef_topk_quant_buckets call
+(every tensor in one launch per pass).  --path per-bucket calls
+gc_ef_topk_quant once per tensor, spread over several contexts / CUDA
+streams.  --workload buckets runs the same compressor on a flat gradient of
+134,217,728 Student-t (nu = 3) elements cut into 25 MiB buckets; the other
+workloads are the other compressors of the library.
 
 The metric is fp32 gradient GB/s through the compressor (4 bytes per
 gradient element per step), whole job over all GPUs.  Also reported: the
@@ -53,7 +57,8 @@ def parse_args():
     p.add_argument("--impl", choices=["gc", "reference"], default="gc")
     p.add_argument("--streams", type=int, default=4, help="contexts/streams for the buckets")
     p.add_argument("--ratio", type=int, default=10, help="Top-K ratio in per mille")
-    p.add_argument("--distinct", type=int, default=3, help="distinct correlated gradients")
+    p.add_argument("--distinct", type=int, default=None,
+                   help="distinct correlated gradients (default 2 for layers, else 3)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--diag", action="store_true",
                    help="buckets workload: also compute the fused per-bucket diagnostics")
@@ -68,12 +73,16 @@ def parse_args():
     p.add_argument("--elems", type=int, default=None,
                    help="gradient elements (default: the workload's own size; for buckets a "
                         "smaller value cuts the same 25 MiB buckets from a shorter gradient)")
-    p.add_argument("--workload", choices=["buckets", "quant", "tern", "powersgd", "aggregate",
-                                          "randk", "diff"],
-                   default="buckets",
-                   help="buckets: EF + Top-K + QSGD per 25 MiB bucket (the headline); quant: "
+    p.add_argument("--layers", type=int, default=inputs.TRANSFORMER_LAYERS,
+                   help="layers workloads: transformer layers in the gradient set")
+    p.add_argument("--workload", choices=["layers", "buckets", "quant", "tern", "powersgd",
+                                          "aggregate", "randk", "diff"],
+                   default="layers",
+                   help="layers: EF + Top-K 1%% + 8-bit QSGD per tensor of the 32-layer "
+                        "transformer gradient set (the headline); buckets: the same "
+                        "compressor per 25 MiB bucket of a flat gradient; quant: "
                         "EF + group quantisation of 2^30 elements; tern: EF + TernGrad per "
-                        "tensor of one transformer layer; powersgd: rank-4 PowerSGD on one "
+                        "tensor of the transformer layer set; powersgd: rank-4 PowerSGD on one "
                         "layer's matrix shapes; aggregate: 8 ranks' Top-K + QSGD outputs summed "
                         "into one dense gradient; randk: EF + random sparsification at 1%%; "
                         "diff: EF + 4-bit min-max differential quantisation of the "
@@ -86,6 +95,9 @@ def parse_args():
     args = p.parse_args()
     if args.elems is None:
         args.elems = inputs.GROUP_ELEMS if args.workload == "quant" else inputs.FLAT_ELEMS
+    if args.distinct is None:
+        # two correlated gradients of the layer set are 52 GB already
+        args.distinct = 2 if args.workload in ("layers", "tern") else 3
     return args
 
 
@@ -250,8 +262,9 @@ def measured_peaks():
 # the default workload
 # ---------------------------------------------------------------------------
 class BucketWorkload:
-    """134,217,728 fp32 elements in 25 MiB buckets; one step = EF + Top-K +
-    8-bit QSGD over every bucket.
+    """One step = EF + Top-K + 8-bit QSGD over every bucket: either the
+    134,217,728-element flat gradient in 25 MiB buckets, or (layers) the
+    transformer layer set with one bucket per tensor.
 
     path "buckets": one bucket plan on one context, the whole step is one
     gc_ef_topk_quant_buckets call (one launch per pass over all buckets).
@@ -261,12 +274,21 @@ class BucketWorkload:
     BITS, GROUP, SEED = 8, 64, 1000
 
     def __init__(self, torch, gc, dev, ratio_per_mille, streams, distinct, seed, path,
-                 n=inputs.FLAT_ELEMS, diag=False, residual="immediate"):
+                 n=inputs.FLAT_ELEMS, diag=False, residual="immediate", layers=None):
         self.torch, self.gc, self.dev, self.path = torch, gc, dev, path
-        self.n = n
-        self.bounds = inputs.bucket_bounds(self.n)
+        if layers is None:
+            # the flat gradient cut into 25 MiB buckets
+            self.n = n
+            self.bounds = inputs.bucket_bounds(self.n)
+            self.grads = inputs.correlated_steps_device(self.n, distinct, dev, seed=seed)
+        else:
+            # one bucket per tensor of the transformer layer set
+            sizes = [n_ for n_, _ in inputs.transformer_set_sizes(layers)]
+            self.n = sum(sizes)
+            starts = np.concatenate([[0], np.cumsum(sizes)]).tolist()
+            self.bounds = [(int(a), int(l)) for a, l in zip(starts, sizes)]
+            self.grads = inputs.transformer_set_device(layers, distinct, dev, seed=seed)
         self.ks = [inputs.ratio_k(length, ratio_per_mille, 1000) for _, length in self.bounds]
-        self.grads = inputs.correlated_steps_device(self.n, distinct, dev, seed=seed)
         self.err = torch.zeros(self.n, dtype=torch.float32, device=dev)
         # outputs of all buckets in three contiguous buffers (16-byte aligned slices)
         self.oi, self.oc, self.os = gc.bucket_offsets(self.ks, self.BITS, self.GROUP)
@@ -481,24 +503,20 @@ class QuantWorkload(_SimpleWorkload):
 
 
 class TernWorkload(_SimpleWorkload):
-    """TernGrad with error feedback on the tensors of one transformer layer
-    (4 x 4096^2, 2 x 4096 x 11008, 11008 x 4096, 4096), one scale per tensor
-    (max |c|), stochastic rounding: one gc_ef_quant call per tensor."""
+    """TernGrad with error feedback on the transformer layer set (--layers
+    layers of 4 x 4096^2, 2 x 4096 x 11008, 11008 x 4096, 4096), one scale
+    per tensor (max |c|), stochastic rounding: one gc_ef_quant call per
+    tensor, tensor t keyed by gc_bucket_seed(SEED, t)."""
 
     SEED = 91
 
     def __init__(self, torch, gc, dev, args, seed):
-        sizes = [int(np.prod(s)) for s in inputs.TRANSFORMER_SHAPES]
+        sizes = [n_ for n_, _ in inputs.transformer_set_sizes(args.layers)]
         self.sizes = sizes
         self.n = sum(sizes)
         self._init_common(torch, gc, dev, max(sizes))
         self.starts = np.concatenate([[0], np.cumsum(sizes)]).tolist()
-        self.grads = []
-        for d in range(args.distinct):
-            flat = torch.empty(self.n, dtype=torch.float32, device=dev)
-            for w_, (a, b) in enumerate(zip(self.starts, self.starts[1:])):
-                flat[a:b] = inputs.transformer_tensor_device(d, w_, dev, seed=seed)
-            self.grads.append(flat)
+        self.grads = inputs.transformer_set_device(args.layers, args.distinct, dev, seed=seed)
         self.err = torch.zeros(self.n, dtype=torch.float32, device=dev)
         self.cb = [gc.codes_bytes(n_, 2, "tern") for n_ in sizes]
         self.coff = np.concatenate([[0], np.cumsum(self.cb)]).tolist()
@@ -514,7 +532,8 @@ class TernWorkload(_SimpleWorkload):
         g = self.grads[t % len(self.grads)] if grad is None else grad
         for w_, (a, b) in enumerate(zip(self.starts, self.starts[1:])):
             self.gc.ef_quant(ctx, g[a:b], self.err[a:b], 2, 0, "tern", "stochastic",
-                             self.SEED + w_, t, self.codes[self.coff[w_]:self.coff[w_ + 1]],
+                             self.gc.bucket_seed(self.SEED, w_), t,
+                             self.codes[self.coff[w_]:self.coff[w_ + 1]],
                              self.scales[4 * w_:4 * w_ + 4])
 
     def algorithmic_bytes(self):
@@ -526,7 +545,7 @@ class TernWorkload(_SimpleWorkload):
     def algorithmic_bytes_per_launch(self):
         """quant_stats reads g, e and writes c (12 B per element); quant_apply
         reads c, writes e' and the codes (8.25 B per element); averaged over
-        the layer's 8 tensors."""
+        the set's tensors."""
         k = len(self.sizes)
         return {"quant_stats": 12.0 * self.n / k,
                 "quant_apply": (8.0 * self.n + self.codes.numel()) / k}
@@ -764,10 +783,10 @@ def cpu_sample(args, seed=7):
                 n, "4,194,304 elements of the 2^30-element gradient, EF + %s %d-bit g64 %s"
                 % (args.mode, args.bits, args.rounding))
     if args.workload == "tern":
-        g = inputs.transformer_tensor(0, 0)
+        g = inputs.transformer_tensor(0, 0)  # one 4096 x 4096 tensor
         e = np.zeros_like(g)
         return (lambda: oracle.ef_quant(g, e, 2, 0, "tern", "stochastic", 91, 0), g.size,
-                "one 4096 x 4096 tensor of the layer, EF + TernGrad per tensor")
+                "one 4096 x 4096 tensor of the layer set, EF + TernGrad per tensor")
     if args.workload == "diff":
         n = 1 << 22
         g = inputs.student_t(r, n)
@@ -802,6 +821,13 @@ def cpu_sample(args, seed=7):
         E = np.zeros_like(M)
         return (lambda: oracle.powersgd_step(M, E, Q0, 4), M.size,
                 "one 4096 x 4096 matrix of the layer, rank-4 PowerSGD step (fp64)")
+    if args.workload == "layers":
+        g = inputs.transformer_tensor(0, 0)
+        e = (0.1 * inputs.transformer_tensor(1, 0)).astype(np.float32)
+        k = inputs.ratio_k(g.size, args.ratio, 1000)
+        return (lambda: oracle.ef_topk_quant(g, e, k, 8, 64, "stochastic", 1000, 0), g.size,
+                "one 4096 x 4096 tensor of the layer set, EF + Top-K %g%% + 8-bit QSGD"
+                % (args.ratio / 10))
     length = inputs.BUCKET_ELEMS
     k = inputs.ratio_k(length, args.ratio, 1000)
     g = inputs.student_t(r, length)
@@ -836,11 +862,13 @@ def config(args, wl=None):
                "total_elems": n, "group": 64, "mode": args.mode, "bits": args.bits,
                "rounding": args.rounding}
     elif args.workload == "tern":
-        n = sum(int(np.prod(s_)) for s_ in inputs.TRANSFORMER_SHAPES)
-        cfg = {"workload": "one transformer layer's gradient tensors (4 x 4096^2, 2 x 4096 x "
-                           "11008, 11008 x 4096, 4096; N(0, (1e-3/sqrt(fan_in))^2)), EF + "
-                           "TernGrad per tensor (scale = max|c| of the tensor), stochastic",
-               "total_elems": n, "tensors": len(inputs.TRANSFORMER_SHAPES)}
+        sizes = [n_ for n_, _ in inputs.transformer_set_sizes(args.layers)]
+        n = sum(sizes)
+        cfg = {"workload": "transformer gradient set, {} layers x {{4096x4096 x4, 4096x11008 x2, "
+                           "11008x4096, 4096}} = {:,} fp32 elements, N(0, (1e-3/sqrt(fan_in))^2), "
+                           "correlated steps; EF + TernGrad per tensor (scale = max|c| of the "
+                           "tensor), stochastic, 2-bit codes".format(args.layers, n),
+               "total_elems": n, "layers": args.layers, "tensors": len(sizes)}
     elif args.workload == "diff":
         cfg = {"workload": "flat fp32 gradient {:,} elements, Student-t nu=3 x 1e-3, correlated "
                            "steps; EF + differential quantisation against the reconstructed "
@@ -856,6 +884,22 @@ def config(args, wl=None):
                            "a {:,}-element Student-t gradient, summed in rank order into one "
                            "dense fp32 gradient".format(n),
                "total_elems": n, "ranks": 8, "topk_percent": 1, "quant": "qsgd 8-bit g64"}
+    elif args.workload == "layers":
+        sizes = [n_ for n_, _ in inputs.transformer_set_sizes(args.layers)]
+        n = sum(sizes)
+        cfg = {"workload": "transformer gradient set, {} layers x {{4096x4096 x4, 4096x11008 x2, "
+                           "11008x4096, 4096}} = {:,} fp32 elements, N(0, (1e-3/sqrt(fan_in))^2), "
+                           "correlated steps; per tensor (one bucket each) EF + Top-K {:g}% + 8-bit "
+                           "QSGD (groups of 64, stochastic) on the kept values".format(
+                               args.layers, n, args.ratio / 10),
+               "total_elems": n, "layers": args.layers, "tensors": len(sizes),
+               "topk_per_mille": args.ratio, "quant": "qsgd 8-bit g64 stochastic",
+               "path": args.path}
+        if args.path == "buckets":
+            cfg["residual"] = ("deferred: each step's kept-entry residuals are applied by the "
+                               "next step's read of e; the last step's are flushed into e inside "
+                               "the timed region" if args.residual == "deferred" else
+                               "immediate: every step stores its kept-entry residuals into e")
     elif args.workload == "powersgd":
         n = sum(m * n_ for m, n_ in inputs.POWERSGD_SHAPES)
         cfg = {"workload": "one transformer layer's matrix shapes (4096 x 4096, 4096 x 11008, "
@@ -935,10 +979,11 @@ def main():
     host_cpus = pin_host_near_gpu(torch, dev)
     from gradient_compression_ef_gb300 import gc
 
-    if args.workload == "buckets":
+    if args.workload in ("buckets", "layers"):
         wl = BucketWorkload(torch, gc, dev, args.ratio, args.streams, args.distinct,
                             seed=rank_seed(rank), path=args.path, n=args.elems, diag=args.diag,
-                            residual=args.residual)
+                            residual=args.residual,
+                            layers=args.layers if args.workload == "layers" else None)
     else:
         wl = WORKLOADS[args.workload](torch, gc, dev, args, seed=rank_seed(rank))
     torch.cuda.synchronize(dev)
@@ -1008,7 +1053,8 @@ def main():
                          "algorithmic_bytes_per_launch": algo.get(name),
                          "achieved_gbs": algo[name] / avg_s / 1e9 if algo.get(name) else None}
     traffic, traffic_src = kernel_traffic(top[0], wl.n) \
-        if args.workload == "buckets" and args.path == "buckets" else (None, "no ncu capture")
+        if args.workload in ("buckets", "layers") and args.path == "buckets" \
+        else (None, "no ncu capture")
     roofline = {"bound": "hbm", "kernel": top[0], "achieved": kernels[top[0]]["achieved_gbs"],
                 "peak": peak, "unit": "GB/s", "peak_source": peak_src,
                 "frac": kernels[top[0]]["achieved_gbs"] / peak, "traffic": traffic,
@@ -1022,7 +1068,14 @@ def main():
     e2e = None
     if not args.no_e2e:
         T = len(wl.grads)
-        hosts = [g.cpu().pin_memory() for g in wl.grads]
+        # one pinned host copy per distinct gradient; above 8 GB of gradient
+        # one host buffer serves every step (the bytes copied are the same)
+        nh = T if 4 * wl.n * T <= (8 << 30) else 1
+        hosts = []
+        for g in wl.grads[:nh]:
+            h_ = torch.empty(g.numel(), dtype=g.dtype, pin_memory=True)
+            h_.copy_(g)
+            hosts.append(h_)
         outs_h = [torch.empty(t.numel(), dtype=t.dtype).pin_memory() for t in wl.outputs()]
         copy_s = torch.cuda.Stream(device=dev)
         ready = [torch.cuda.Event() for _ in range(T)]
@@ -1034,7 +1087,7 @@ def main():
             if t >= T:
                 copy_s.wait_event(done[d])
             with torch.cuda.stream(copy_s):
-                wl.grads[d].copy_(hosts[d], non_blocking=True)
+                wl.grads[d].copy_(hosts[d % nh], non_blocking=True)
             ready[d].record(copy_s)
             wl.main.wait_event(ready[d])
             if args.eager:

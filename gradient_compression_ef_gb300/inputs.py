@@ -153,6 +153,41 @@ def transformer_tensor_device(layer, which, device, seed=42, scale=1e-3):
                        dtype=torch.float32).mul_(scale / float(np.sqrt(shape[0])))
 
 
+def transformer_set_sizes(layers=TRANSFORMER_LAYERS):
+    """[(elements, fan_in)] of every tensor of the layer set, layer by layer."""
+    one = [(int(np.prod(s)), s[0]) for s in TRANSFORMER_SHAPES]
+    return one * int(layers)
+
+
+def transformer_set_device(layers, steps, device, seed=42, scale=1e-3, rho=0.9, fresh=0.436):
+    """``steps`` flat float32 gradients of the whole layer set (tensors laid
+    end to end, layer by layer), drawn by torch on ``device`` (seeded).
+    Tensor t of step 0 is N(0, (scale / sqrt(fan_in_t))^2); later steps are
+    temporally correlated, g_s = rho g_{s-1} + fresh * (a new draw of the
+    same distribution), so each tensor keeps its distribution (rho^2 +
+    fresh^2 = 1.0001)."""
+    import torch
+    sizes = transformer_set_sizes(layers)
+    total = sum(n for n, _ in sizes)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+
+    def draw():
+        x = torch.randn(total, generator=gen, device=device, dtype=torch.float32)
+        a = 0
+        for n, fan_in in sizes:
+            x[a:a + n].mul_(scale / float(np.sqrt(fan_in)))
+            a += n
+        return x
+
+    out = [draw()]
+    for _ in range(1, steps):
+        g = draw().mul_(fresh)
+        g.add_(out[-1], alpha=rho)
+        out.append(g)
+    return out
+
+
 def transformer_tensor(layer, which, seed=42, scale=1e-3):
     """Tensor ``which`` (0..7) of ``layer`` as a flat float32 array."""
     shape = TRANSFORMER_SHAPES[which]
