@@ -755,12 +755,12 @@ WORKLOADS = {"quant": QuantWorkload, "tern": TernWorkload, "powersgd": PowerSGDW
              "aggregate": AggregateWorkload, "randk": RandKWorkload, "diff": DiffWorkload}
 
 
-def kernel_timing(wl, steps, warmup_step):
+def kernel_timing(wl, steps, warmup_step, launches_per_step):
     """Per-phase CUDA-event durations over `steps` more steps run with all
     buckets on one context / stream, so that each kernel runs alone and its
-    events bracket its own execution."""
+    events bracket its own execution (room for every launch of the steps)."""
     ctx = wl.ctxs[0]
-    ctx.enable_timing(64 * steps)
+    ctx.enable_timing(max(64, launches_per_step + 8) * steps)
     for t in range(steps):
         wl.launch_step(warmup_step + t, ctxs=[ctx])
     wl.finish()
@@ -1040,7 +1040,7 @@ def main():
     eager_value = whole_job_value(world, wl.n, eager_ms)
 
     # per-kernel durations (second pass over the same kind of steps)
-    phases = kernel_timing(wl, args.steps, args.warmup + args.steps)
+    phases = kernel_timing(wl, args.steps, args.warmup + args.steps, per_step_launches)
     # dominant kernel: the largest total time among kernels that move
     # gradient bytes (the selection passes in between move almost none)
     algo = wl.algorithmic_bytes_per_launch()

@@ -195,7 +195,7 @@ const char* gc_phase_name(int phase) {
       "ef_hist", "collect", "write", "ef_add", "quant_fused", "quant_stats",
       "quant_combine", "quant_apply", "dequant", "psgd_mq", "psgd_mtp", "psgd_resid",
       "refine", "bk_hist", "bk_collect", "bk_refine", "bk_write", "bk_quant", "agg_bounds",
-      "agg_accumulate", "randk_mark", "randk_write", "bk_diag", "bk_flush"};
+      "agg_accumulate", "randk_mark", "randk_write", "bk_diag", "bk_flush", "psgd_thin"};
   return (phase >= 0 && phase < GC_PHASE_COUNT) ? names[phase] : "?";
 }
 

@@ -32,6 +32,7 @@ constexpr uint32_t kStatusTopkCount = 1u << 0;   // candidate count mismatch
 constexpr uint32_t kStatusTopkSelect = 1u << 1;  // threshold search failed
 constexpr uint32_t kStatusTopkOverflow = 1u << 2;  // more than k entries kept
 constexpr uint32_t kStatusScatterIndex = 1u << 3;  // residual index out of range
+constexpr uint32_t kStatusWaitTimeout = 1u << 4;   // a bounded wait on an mbarrier ran out
 
 // Per-context Top-K selection state in device memory.
 struct TopkSel {

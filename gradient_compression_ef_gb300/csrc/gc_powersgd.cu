@@ -27,9 +27,13 @@
 //   pass 3  residual : E' = M - P_hat Q'^T (Q' staged in shared memory),
 //                      blocks over rows and column ranges as in pass 1.
 // Traffic: 12 + 4 + 8 = 24 bytes per element.
+#include <cudaTypedefs.h>
+
 #include <algorithm>
+#include <mutex>
 
 #include "gc_internal.cuh"
+#include "gc_sm100.cuh"
 
 namespace gc {
 namespace {
@@ -90,6 +94,44 @@ __device__ __forceinline__ void stage_q(float* qs, const float* Q, int64_t col0,
   const float* src = Q + col0 * R;
   for (int64_t t = threadIdx.x; t < (int64_t)kQChunk * R; t += kPThreads)
     qs[t] = t < cols * R ? src[t] : 0.0f;
+}
+
+// Cholesky P^T P = U^T U (U upper, positive diagonal) of the binary64 Gram
+// matrix, and w = U^-1 (upper triangular, row-major R x R floats): P U^-1 is
+// the orthonormal factor Gram-Schmidt gives.  A column whose remaining norm
+// is 0 is dropped (its P_hat column is left zero), as Gram-Schmidt leaves a
+// zero column zero.  One thread.
+template <int R>
+__device__ void cholesky_inverse(const double* gram, float* w) {
+  double U[R][R], W[R][R];
+  bool zero[R];
+  for (int i = 0; i < R; ++i)
+    for (int j = 0; j < R; ++j) U[i][j] = W[i][j] = 0.0;
+  for (int j = 0; j < R; ++j) {
+    for (int i = 0; i < j; ++i) {
+      if (zero[i]) { U[i][j] = 0.0; continue; }
+      double s = gram[i * R + j];
+      for (int k = 0; k < i; ++k) s -= U[k][i] * U[k][j];
+      U[i][j] = s / U[i][i];
+    }
+    double d = gram[j * R + j];
+    for (int k = 0; k < j; ++k) d -= U[k][j] * U[k][j];
+    zero[j] = !(d > 0.0);
+    U[j][j] = zero[j] ? 1.0 : sqrt(d);
+  }
+  // W = U^-1 by back substitution, columns of dropped directions zero
+  for (int j = R - 1; j >= 0; --j) {
+    if (zero[j]) continue;
+    W[j][j] = 1.0 / U[j][j];
+    for (int i = j - 1; i >= 0; --i) {
+      if (zero[i]) continue;
+      double s = 0.0;
+      for (int k = i + 1; k <= j; ++k) s += U[i][k] * W[k][j];
+      W[i][j] = -s / U[i][i];
+    }
+  }
+  for (int i = 0; i < R; ++i)
+    for (int j = 0; j < R; ++j) w[i * R + j] = (float)W[i][j];
 }
 
 // ---------------------------------------------------------------------------
@@ -232,38 +274,7 @@ __global__ void __launch_bounds__(kPThreads) psgd_mq_kernel(
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    // Cholesky P^T P = U^T U (U upper, positive diagonal).  A column whose
-    // remaining norm is 0 is dropped (its P_hat column is left zero), as
-    // Gram-Schmidt leaves a zero column zero.
-    double U[R][R], W[R][R];
-    bool zero[R];
-    for (int i = 0; i < R; ++i)
-      for (int j = 0; j < R; ++j) U[i][j] = W[i][j] = 0.0;
-    for (int j = 0; j < R; ++j) {
-      for (int i = 0; i < j; ++i) {
-        if (zero[i]) { U[i][j] = 0.0; continue; }
-        double s = gram[i * R + j];
-        for (int k = 0; k < i; ++k) s -= U[k][i] * U[k][j];
-        U[i][j] = s / U[i][i];
-      }
-      double d = gram[j * R + j];
-      for (int k = 0; k < j; ++k) d -= U[k][j] * U[k][j];
-      zero[j] = !(d > 0.0);
-      U[j][j] = zero[j] ? 1.0 : sqrt(d);
-    }
-    // W = U^-1 by back substitution, columns of dropped directions zero
-    for (int j = R - 1; j >= 0; --j) {
-      if (zero[j]) continue;
-      W[j][j] = 1.0 / U[j][j];
-      for (int i = j - 1; i >= 0; --i) {
-        if (zero[i]) continue;
-        double s = 0.0;
-        for (int k = i + 1; k <= j; ++k) s += U[i][k] * W[k][j];
-        W[i][j] = -s / U[i][i];
-      }
-    }
-    for (int i = 0; i < R; ++i)
-      for (int j = 0; j < R; ++j) b.w[i * R + j] = (float)W[i][j];
+    cholesky_inverse<R>(gram, b.w);
     b.state->ticket_mq = 0u;
   }
 }
@@ -422,6 +433,1009 @@ __global__ void __launch_bounds__(kPThreads) psgd_residual_kernel(
   }
 }
 
+// ===========================================================================
+// Tensor-core path (n a multiple of 4, so that every row of G, E and M
+// starts on a 16-byte boundary as the TMA requires).
+//
+// Pass 1, P = M Q (K = n, N = r), runs as tcgen05.mma kind::tf32 with the
+// accumulator (128 lanes of fp32) in tensor memory.  TF32 keeps 10 mantissa
+// bits, so every operand is split as x = hi + lo (hi = x rounded to TF32,
+// lo = x - hi exactly, of which the tensor core keeps the top 11 bits) and
+// hi*hi + hi*lo + lo*hi is accumulated: about 2^-21 relative error per
+// product instead of 2^-11, close to fp32.
+//
+// The memory system wants long runs of each matrix row (a pass that read
+// 128 bytes of each of 128 rows per step reached 61 % of the bandwidth, the
+// same pass reading 2 KB of each of 8 rows 89 %), while the MMA wants 128
+// operand rows.  So an operand tile of 128 rows is made of SG segments of
+// 32 columns from each of 128 / SG matrix rows (a 3-D TMA box: 32 columns x
+// SG segments x 128 / SG rows, with the 128-byte swizzle), and the thin
+// operand carries the segments along N: image row s r + c holds column c of
+// Q for the segment s (rows SG r .. of hi, then as many of lo).  Operand
+// row (row, s) times image row (s', c) is the segment-s part of P[row][c]
+// when s' = s; the read-out keeps those and adds them over the segments.
+// With SG = 4 (r <= 4) each step reads 512 bytes of each of 32 rows
+// (16 segments, 2 KB per row, made the pass tensor-bound: the MMA work
+// grows with SG); matrices whose columns are not a multiple of 32 use
+// SG = 1 (128 rows x 32 columns, a 2-D box).
+//
+// Work: the pass cuts its K range into units of 32 SG columns per tile of
+// 128 / SG rows; units are numbered tile-major and every CTA (one per SM)
+// takes a contiguous run of them, so each CTA contributes a partial result
+// to at most a few tiles.  CTA c's partial for tile t goes to slot c + t
+// (the (CTA, tile) pairs, taken in unit order, advance one of the two at a
+// time, so the slots are distinct), and the last contributor of a tile
+// (ticket) adds the tile's slots in CTA order: deterministic.
+//
+// Roles in a CTA of 320 threads: warps 0-7 convert the staged tiles (M = G
+// + E stored to global, then the hi/lo split in place), warps 0-3 also read
+// the accumulator out (tcgen05.ld: warp w reads lanes 32w .. 32w + 31);
+// warp 8 lane 0 issues the TMA and bulk copies; warp 9 owns the tensor
+// memory and its lane 0 issues the MMAs.  Stages are handed on by
+// mbarriers: full (copies landed), conv (operands converted), empty (the
+// MMAs reading the stage are done); acc_full / acc_empty hand the
+// accumulator to the read-out and back.  Every wait is bounded; the
+// converter warps take each abort decision together (one flag behind a
+// named barrier), so no barrier is left waiting for a thread that gave up.
+//
+// Passes 2 (Q' = M^T P_hat) and 3 (E' = M - P_hat Q'^T) stream M on the
+// CUDA cores; see their kernels.
+// ===========================================================================
+namespace tcp {
+constexpr int kConv = 256;             // converter threads (warps 0-7)
+constexpr int kEpi = 128;              // accumulator read-out threads (warps 0-3)
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kRows = 128;             // MMA M: operand rows of a tile
+constexpr int kKBlk = 32;              // K per operand row of a unit (one 128-byte row)
+constexpr uint32_t kTileBytes = kRows * kKBlk * 4;  // 16 KB
+constexpr uint32_t kTmemCols = 256;
+constexpr int kResidConv = 512;        // passes 2 and 3: compute threads (warps 0-15)
+constexpr int kResidThreads = 544;     // passes 2 and 3: warps 0-15 compute, warp 16 loads
+constexpr int kStagesR = 10;           // passes 2 and 3: stages
+constexpr long long kWaitCycles = 4000000000ll;  // bound on each wait: ~2 s at 2 GHz
+
+// Segments per operand tile for rank R: 4 (512 contiguous bytes of each of
+// 32 rows per step) while 4 r image rows fit a 16-row half; the MMA work
+// grows with SG (the off-diagonal products are wasted), and 16 segments
+// made the pass tensor-bound.
+__host__ __device__ constexpr int segs_for(int R) { return R <= 4 ? 4 : R <= 8 ? 2 : 1; }
+// Image rows per half (hi or lo): SG r rounded up to 16.
+__host__ __device__ constexpr int img_half(int R, int SG) { return (SG * R + 15) / 16 * 16; }
+// Stages of pass 1: G and E tiles (32 KB) plus the image.
+__host__ __device__ constexpr int stages_p(int R, int SG) {
+  return 2 * img_half(R, SG) * 128 > 8192 ? 4 : 5;
+}
+
+// First unit of CTA c of C over U units, and the CTA that owns unit u.
+__host__ __device__ __forceinline__ int64_t unit_lo(int c, int C, int64_t U) {
+  return U * c / C;
+}
+__device__ __forceinline__ int unit_owner(int64_t u, int C, int64_t U) {
+  int lo = 0, hi = C - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (unit_lo(mid, C, U) <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Unit u of a tile-major numbering with `per` units per tile, stepped
+// without a division per unit (64-bit division is a long instruction
+// sequence on the GPU), and the stage ring position of the i-th unit of a
+// run: stage st, parity ph of its use.
+struct UnitCursor {
+  int64_t tile, blk, per;
+  __device__ __forceinline__ UnitCursor(int64_t u, int64_t per_)
+      : tile(u / per_), blk(u % per_), per(per_) {}
+  __device__ __forceinline__ void next() {
+    if (++blk == per) {
+      blk = 0;
+      ++tile;
+    }
+  }
+};
+template <int S>
+struct Ring {
+  int st = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next() {
+    if (++st == S) {
+      st = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
+// Barrier of the converter warps only (the loader and MMA warps run on).
+__device__ __forceinline__ void conv_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConv) : "memory");
+}
+__device__ __forceinline__ void resid_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kResidConv) : "memory");
+}
+
+struct Smem {
+  uint32_t a_hi;     // [S] tiles: G, then hi(M) (shared addresses)
+  uint32_t a_lo;     // [S] tiles: E, then lo(M)
+  uint32_t img;      // [S] thin-operand images
+  uint64_t* full;
+  uint64_t* conv;
+  uint64_t* empty;
+  uint64_t* acc_full;
+  uint64_t* acc_empty;
+  uint64_t* drain;
+  uint32_t* tmem_slot;
+  volatile int* abort_flag;
+  int* last1;
+  int* last2;
+  float* rows;   // [kRows][16]
+  double* gram;  // [16 * 16]
+};
+
+__host__ __device__ constexpr size_t smem_bytes_p(int S, uint32_t img_bytes) {
+  return 1024 + (size_t)S * (2 * kTileBytes + img_bytes) + (size_t)(3 * S + 3) * 8 + 64 +
+         (size_t)kRows * 16 * 4 + 16 * 16 * 8;
+}
+
+__device__ __forceinline__ Smem carve_smem(unsigned char* raw, int S, uint32_t img_bytes) {
+  using namespace sm100;
+  // the 128-byte swizzle repeats every 1024 bytes: tiles start on 1024
+  unsigned char* p = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Smem s;
+  s.a_hi = smem_u32(p); p += (size_t)S * kTileBytes;
+  s.a_lo = smem_u32(p); p += (size_t)S * kTileBytes;
+  s.img = smem_u32(p); p += (size_t)S * img_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(p);
+  s.full = bars;
+  s.conv = bars + S;
+  s.empty = bars + 2 * S;
+  s.acc_full = bars + 3 * S;
+  s.acc_empty = s.acc_full + 1;
+  s.drain = s.acc_full + 2;
+  p += (size_t)(3 * S + 3) * 8;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(p);
+  s.abort_flag = reinterpret_cast<volatile int*>(p + 16);
+  s.last1 = reinterpret_cast<int*>(p + 32);
+  s.last2 = reinterpret_cast<int*>(p + 48);
+  p += 64;
+  s.rows = reinterpret_cast<float*>(p); p += (size_t)kRows * 16 * 4;
+  s.gram = reinterpret_cast<double*>(p);
+  return s;
+}
+
+// The converter warps' common abort decision: any thread that saw a wait
+// run out raises the flag; all read it after the named barrier.
+__device__ __forceinline__ bool conv_abort(const Smem& s, bool ok) {
+  if (!ok) *s.abort_flag = 1;
+  conv_sync();
+  return *s.abort_flag != 0;
+}
+
+struct TcBufs {
+  float* praw;           // [m][R] P = M Q
+  float* part;           // [(C + tiles)][rows of a tile][R] partials per (CTA, tile)
+  float* qimg;           // [units along K][image] the Q images
+  uint32_t* rt_tickets;  // [row tiles]
+  double* gram_part;     // [row tiles][R][R]
+  float* w;              // [R][R] U^-1
+  PsgdState* state;
+  uint32_t* status;
+};
+
+// ---------------------------------------------------------------------------
+// pass 0: the images of Q for pass 1, one per 32 SG rows of Q (one thread
+// per row of Q): row i = 32 SG kb + 32 s + k is column k of the image of
+// block kb, where it fills rows s R + c (hi(Q[i][c])) and H + s R + c
+// (lo), H = the half height; the threads of segment 0 also clear the
+// padding rows.
+// ---------------------------------------------------------------------------
+template <int R, int SG>
+__global__ void __launch_bounds__(256) psgd_qimage_kernel(const float* __restrict__ Q, int64_t n,
+                                                          float* __restrict__ img, int64_t rows) {
+  using namespace sm100;
+  constexpr int H = img_half(R, SG);
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= rows) return;
+  const int64_t kb = i / (kKBlk * SG);
+  const uint32_t sgm = (uint32_t)((i / kKBlk) % SG), k = (uint32_t)(i % kKBlk);
+  float* im = img + kb * (2 * H * kKBlk);
+#pragma unroll
+  for (int c = 0; c < R; ++c) {
+    const float v = i < n ? Q[i * R + c] : 0.0f;
+    const float h = to_tf32(v);
+    im[sw128_offset(sgm * R + c, k) >> 2] = h;
+    im[sw128_offset(H + sgm * R + c, k) >> 2] = v - h;
+  }
+  if (sgm == 0) {
+    for (int row = SG * R; row < H; ++row) {
+      im[sw128_offset(row, k) >> 2] = 0.0f;
+      im[sw128_offset(H + row, k) >> 2] = 0.0f;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// pass 1 on the tensor cores: M = G + E (written over E) and P = M Q; the
+// last contributor of a row tile adds its partial rows and writes the
+// tile's Gram partial; the last row tile factors the Gram matrix.
+// ---------------------------------------------------------------------------
+template <int R, int SG>
+__global__ void __launch_bounds__(kThreads, 1) psgd_p_tc_kernel(
+    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmE,
+    float* __restrict__ E, int64_t m, int64_t n, TcBufs b) {
+  using namespace sm100;
+  constexpr int RG = kRows / SG;                  // matrix rows per tile
+  constexpr int KU = SG * kKBlk;                  // matrix columns per unit
+  constexpr int H = img_half(R, SG);              // image rows per half
+  constexpr uint32_t kImg = 2 * H * kKBlk * 4;    // image bytes
+  constexpr int S = stages_p(R, SG);
+  extern __shared__ unsigned char tc_smem[];
+  const Smem s = carve_smem(tc_smem, S, kImg);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int C = gridDim.x, cta = blockIdx.x;
+  const int64_t RT = (m + RG - 1) / RG, KB = (n + KU - 1) / KU, U = RT * KB;
+  const int64_t u0 = unit_lo(cta, C, U), u1 = unit_lo(cta + 1, C, U);
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.conv[i], kConv);
+      mbar_init(&s.empty[i], 1);
+    }
+    mbar_init(s.acc_full, 1);
+    mbar_init(s.acc_empty, kEpi);
+    mbar_init(s.drain, 1);
+    *s.abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(s.tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *s.tmem_slot;
+  bool ok = true, mma_issued = false;
+  int64_t loads = 0;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      tma_prefetch_map(&tmG);
+      tma_prefetch_map(&tmE);
+      UnitCursor cur(u0, KB);
+      Ring<S> ring;
+      for (int64_t i = 0; i < u1 - u0; ++i, cur.next(), ring.next()) {
+        const int st = ring.st;
+        if (i >= S && !mbar_wait(&s.empty[st], ring.ph ^ 1u, kWaitCycles)) {
+          ok = false;
+          break;
+        }
+        const int64_t kb = cur.blk, rt = cur.tile;
+        mbar_arrive_expect_tx(&s.full[st], 2 * kTileBytes + kImg);
+        if (SG == 1) {
+          tma_load_2d(s.a_hi + st * kTileBytes, &tmG, (int32_t)(kb * kKBlk), (int32_t)(rt * RG),
+                      &s.full[st]);
+          tma_load_2d(s.a_lo + st * kTileBytes, &tmE, (int32_t)(kb * kKBlk), (int32_t)(rt * RG),
+                      &s.full[st]);
+        } else {
+          tma_load_3d(s.a_hi + st * kTileBytes, &tmG, 0, (int32_t)(kb * SG), (int32_t)(rt * RG),
+                      &s.full[st]);
+          tma_load_3d(s.a_lo + st * kTileBytes, &tmE, 0, (int32_t)(kb * SG), (int32_t)(rt * RG),
+                      &s.full[st]);
+        }
+        bulk_load_s(s.img + st * kImg, b.qimg + kb * (kImg / 4), kImg, &s.full[st]);
+        ++loads;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      // per K = 8 step: A_hi x [B_hi | B_lo] into columns [0, 2H), A_lo x
+      // B_hi into [2H, 3H)
+      constexpr uint32_t id1 = idesc_tf32(kRows, 2 * H, 0), id2 = idesc_tf32(kRows, H, 0);
+      int seg = 0;
+      UnitCursor cur(u0, KB);
+      Ring<S> ring;
+      for (int64_t i = 0; i < u1 - u0; ++i, cur.next(), ring.next()) {
+        const int st = ring.st;
+        if (!mbar_wait(&s.conv[st], ring.ph, kWaitCycles) ||
+            !mbar_wait(&s.full[st], ring.ph, kWaitCycles)) {
+          ok = false;
+          break;
+        }
+        const bool first = i == 0 || cur.blk == 0;
+        if (first && seg > 0 &&
+            !mbar_wait(s.acc_empty, (uint32_t)((seg - 1) & 1), kWaitCycles)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t ah = s.a_hi + st * kTileBytes, al = s.a_lo + st * kTileBytes;
+        const uint32_t im = s.img + st * kImg;
+#pragma unroll
+        for (int kk = 0; kk < kKBlk / 8; ++kk) {
+          const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+          // operand rows of 128 bytes, 8-row groups 1024 bytes apart; a K = 8
+          // step is 32 bytes along the rows
+          const uint64_t db = smem_desc_sw128(im + kk * 32, 16, 1024);
+          mma_tf32(tmem, smem_desc_sw128(ah + kk * 32, 16, 1024), db, id1, acc);
+          mma_tf32(tmem + 2 * H, smem_desc_sw128(al + kk * 32, 16, 1024), db, id2, acc);
+        }
+        mma_issued = true;
+        mma_commit(&s.empty[st]);
+        if (cur.blk == KB - 1 || i == u1 - u0 - 1) {
+          mma_commit(s.acc_full);
+          ++seg;
+        }
+      }
+    }
+  } else {
+    int seg = 0;
+    constexpr int kPasses = kRows * 8 / kConv;  // operand rows per thread
+    const uint32_t ch = lane & 7;
+    UnitCursor cur(u0, KB);
+    Ring<S> ring;
+    for (int64_t i = 0; i < u1 - u0; ++i, cur.next(), ring.next()) {
+      const int st = ring.st;
+      const bool got = mbar_wait(&s.full[st], ring.ph, kWaitCycles);
+      if (conv_abort(s, got)) { ok = false; break; }
+      const int64_t rt = cur.tile, kb = cur.blk;
+      const uint32_t ah = s.a_hi + st * kTileBytes, al = s.a_lo + st * kTileBytes;
+      // M = G + E; lanes 8q .. 8q + 7 cover one operand row (128 bytes, a
+      // segment of a matrix row; the warp's four rows are consecutive
+      // segments, 512 contiguous bytes).  Loads, then arithmetic, then stores.
+      float4 g[kPasses], e[kPasses];
+      uint32_t off[kPasses];
+#pragma unroll
+      for (int p = 0; p < kPasses; ++p) {
+        const uint32_t a = p * (kConv / 8) + warp * 4 + (lane >> 3);
+        off[p] = sw128_offset(a, 4 * ch);
+        g[p] = lds128(ah + off[p]);
+        e[p] = lds128(al + off[p]);
+      }
+      float4 hi[kPasses], lo[kPasses];
+#pragma unroll
+      for (int p = 0; p < kPasses; ++p) {
+        g[p] = make_float4(__fadd_rn(g[p].x, e[p].x), __fadd_rn(g[p].y, e[p].y),
+                           __fadd_rn(g[p].z, e[p].z), __fadd_rn(g[p].w, e[p].w));
+        hi[p] = make_float4(to_tf32(g[p].x), to_tf32(g[p].y), to_tf32(g[p].z), to_tf32(g[p].w));
+        lo[p] = make_float4(g[p].x - hi[p].x, g[p].y - hi[p].y, g[p].z - hi[p].z,
+                            g[p].w - hi[p].w);
+      }
+#pragma unroll
+      for (int p = 0; p < kPasses; ++p) {
+        sts128(ah + off[p], hi[p]);
+        sts128(al + off[p], lo[p]);
+      }
+#pragma unroll
+      for (int p = 0; p < kPasses; ++p) {
+        const uint32_t a = p * (kConv / 8) + warp * 4 + (lane >> 3);
+        const int64_t grow = rt * RG + a / SG;
+        const int64_t col = kb * KU + (a % SG) * kKBlk + 4 * ch;
+        if (grow < m && col < n) *reinterpret_cast<float4*>(E + grow * n + col) = g[p];
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&s.conv[st]);
+      if (cur.blk != KB - 1 && i != u1 - u0 - 1) continue;
+      // read-out of this CTA's partial P rows of row tile rt: lane (row,
+      // segment) keeps image rows s R .. s R + R - 1 of each product, the
+      // segments of a row are added by shuffles (fixed order)
+      const bool acc = mbar_wait(s.acc_full, (uint32_t)(seg & 1), kWaitCycles);
+      if (conv_abort(s, acc)) { ok = false; break; }
+      ++seg;
+      if (tid < kEpi) {
+        const uint32_t sgm = tid % SG, lo_col = sgm * R;
+        float prod[3][R];
+#pragma unroll
+        for (int x = 0; x < 3; ++x)
+#pragma unroll
+          for (int c = 0; c < R; ++c) prod[x][c] = 0.0f;
+        tc_fence_after_sync();
+        const uint32_t base = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll
+        for (int x = 0; x < 3; ++x) {
+#pragma unroll
+          for (int j = 0; j < H / 16; ++j) {
+            float v[16];
+            tmem_ld16(base + x * H + 16 * j, v);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const uint32_t col = 16 * j + q;
+#pragma unroll
+              for (int c = 0; c < R; ++c)
+                if (col == lo_col + c) prod[x][c] = v[q];
+            }
+          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive(s.acc_empty);
+        float v[R];
+#pragma unroll
+        for (int c = 0; c < R; ++c) {
+          float t = (prod[0][c] + prod[1][c]) + prod[2][c];
+#pragma unroll
+          for (int o = SG / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+          v[c] = t;
+        }
+        if (sgm == 0) {
+          float* dst = b.part + ((int64_t)(cta + rt) * RG + tid / SG) * R;
+#pragma unroll
+          for (int c = 0; c < R; ++c) dst[c] = v[c];
+        }
+      }
+      __threadfence();
+      conv_sync();
+      const int c_first = unit_owner(rt * KB, C, U), c_last = unit_owner(rt * KB + KB - 1, C, U);
+      if (tid == 0)
+        *s.last1 = atomicAdd(&b.rt_tickets[rt], 1u) == (uint32_t)(c_last - c_first);
+      conv_sync();
+      if (!*s.last1) continue;
+      __threadfence();
+      // the row tile's P rows: partials added in CTA order
+      if (tid < RG) {
+        const int64_t grow = rt * RG + tid;
+        float pr[R];
+#pragma unroll
+        for (int c = 0; c < R; ++c) pr[c] = 0.0f;
+        for (int cc = c_first; cc <= c_last; ++cc) {
+          const float* src = b.part + ((int64_t)(cc + rt) * RG + tid) * R;
+#pragma unroll
+          for (int c = 0; c < R; ++c) pr[c] += __ldcg(src + c);
+        }
+#pragma unroll
+        for (int c = 0; c < R; ++c) {
+          s.rows[tid * 16 + c] = grow < m ? pr[c] : 0.0f;
+          if (grow < m) b.praw[grow * R + c] = pr[c];
+        }
+      }
+      if (tid == 0) b.rt_tickets[rt] = 0u;
+      conv_sync();
+      for (int t = tid; t < R * R; t += kConv) {
+        const int a = t / R, c = t % R;
+        double acc2 = 0.0;
+        for (int r = 0; r < RG; ++r) acc2 += (double)s.rows[r * 16 + a] * (double)s.rows[r * 16 + c];
+        b.gram_part[rt * R * R + t] = acc2;
+      }
+      __threadfence();
+      conv_sync();
+      if (tid == 0) *s.last2 = atomicAdd(&b.state->ticket_mq, 1u) == (uint32_t)(RT - 1);
+      conv_sync();
+      if (!*s.last2) continue;
+      __threadfence();
+      for (int t = tid; t < R * R; t += kConv) {
+        double acc2 = 0.0;
+        for (int64_t r = 0; r < RT; ++r) acc2 += __ldcg(&b.gram_part[r * R * R + t]);
+        s.gram[t] = acc2;
+      }
+      conv_sync();
+      if (tid == 0) {
+        cholesky_inverse<R>(s.gram, b.w);
+        b.state->ticket_mq = 0u;
+      }
+    }
+  }
+  // end: the loader waits for its copies still in flight, the MMA issuer
+  // for its MMAs, then warp 9 frees the tensor memory
+  if (warp == kProducerWarp && lane == 0) {
+    for (int64_t j = std::max<int64_t>(0, loads - S); j < loads; ++j)
+      if (!mbar_wait(&s.full[j % S], (uint32_t)((j / S) & 1), kWaitCycles))
+        ok = false;
+  }
+  if (warp == kMmaWarp && lane == 0 && mma_issued) {
+    mma_commit(s.drain);
+    if (!mbar_wait(s.drain, 0, kWaitCycles)) ok = false;
+  }
+  if (!ok) atomicOr(b.status, kStatusWaitTimeout);
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// P_hat = P W for every row (written to P_out and to a copy padded with zero
+// rows to a multiple of 8, which pass 3 copies in whole blocks).
+// ---------------------------------------------------------------------------
+template <int R>
+__global__ void __launch_bounds__(256) psgd_phat_kernel(const float* __restrict__ praw,
+                                                        const float* __restrict__ W, int64_t m,
+                                                        int64_t m_pad, float* __restrict__ P_out,
+                                                        float* __restrict__ phat) {
+  __shared__ float w[R * R];
+  for (int t = threadIdx.x; t < R * R; t += blockDim.x) w[t] = W[t];
+  __syncthreads();
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= m_pad) return;
+  float pr[R];
+#pragma unroll
+  for (int a = 0; a < R; ++a) pr[a] = i < m ? praw[i * R + a] : 0.0f;
+#pragma unroll
+  for (int c = 0; c < R; ++c) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int a = 0; a <= c; ++a) acc = fmaf(pr[a], w[a * R + c], acc);
+    phat[i * R + c] = acc;
+    if (i < m) P_out[i * R + c] = acc;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// pass 3: E' = M - P_hat Q'^T, fp32 FMAs on the CUDA cores (r products per
+// element).  The matrix streams in units of 8 rows x 512 columns (2 KB
+// contiguous per row, two TMA boxes of 8 x 256 without swizzle) together
+// with the unit's 8 rows of P_hat; units run column block by column block,
+// so a thread keeps the Q' rows of its four columns in registers for as
+// long as its CTA stays in one column block.
+// ---------------------------------------------------------------------------
+constexpr int kRGRows = 8;            // rows per unit
+constexpr int kRGCols = 512;          // columns per unit
+constexpr uint32_t kRGTile = kRGRows * kRGCols * 4;  // 16 KB
+
+template <int R>
+__global__ void __launch_bounds__(kResidThreads, 1) psgd_resid_tma_kernel(
+    const __grid_constant__ CUtensorMap tmE, float* __restrict__ E, int64_t m, int64_t n,
+    const float* __restrict__ phat, const float* __restrict__ Qn, uint32_t* status) {
+  using namespace sm100;
+  constexpr int S = kStagesR;
+  constexpr uint32_t kPBytes = kRGRows * R * 4;  // P_hat rows of one unit
+  constexpr uint32_t kStageBytes = kRGTile + ((kPBytes + 127) / 128) * 128;
+  constexpr int kLoader = kResidConv / 32;       // the loader warp
+  extern __shared__ unsigned char tc_smem[];
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(tc_smem) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)S * kStageBytes);
+  uint64_t* empty = full + S;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int C = gridDim.x, cta = blockIdx.x;
+  const int64_t RG = (m + kRGRows - 1) / kRGRows, CB = (n + kRGCols - 1) / kRGCols, U = RG * CB;
+  const int64_t u0 = unit_lo(cta, C, U), u1 = unit_lo(cta + 1, C, U);
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kResidConv / 32);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  bool ok = true;
+  int64_t loads = 0;
+  if (warp == kLoader) {
+    if (lane == 0) {
+      tma_prefetch_map(&tmE);
+      UnitCursor cur(u0, RG);
+      Ring<S> ring;
+      for (int64_t i = 0; i < u1 - u0; ++i, cur.next(), ring.next()) {
+        const int st = ring.st;
+        if (i >= S && !mbar_wait(&empty[st], ring.ph ^ 1u, kWaitCycles)) {
+          ok = false;
+          break;
+        }
+        const int64_t cb = cur.tile, rg = cur.blk;
+        unsigned char* stage = base + (size_t)st * kStageBytes;
+        mbar_arrive_expect_tx(&full[st], kRGTile + kPBytes);
+        tma_load_2d(stage, &tmE, (int32_t)(cb * kRGCols), (int32_t)(rg * kRGRows), &full[st]);
+        tma_load_2d(stage + kRGTile / 2, &tmE, (int32_t)(cb * kRGCols + kRGCols / 2),
+                    (int32_t)(rg * kRGRows), &full[st]);
+        bulk_load(stage + kRGTile, phat + rg * kRGRows * R, kPBytes, &full[st]);
+        ++loads;
+      }
+      for (int64_t j = std::max<int64_t>(0, loads - S); j < loads; ++j)
+        if (!mbar_wait(&full[j % S], (uint32_t)((j / S) & 1), kWaitCycles))
+          ok = false;
+    }
+  } else {
+    // thread t: column chunk t % 128 (four columns), rows t / 128 and t / 128 + 4
+    const uint32_t chunk = tid & 127, r0 = tid >> 7;
+    int64_t cur_cb = -1;
+    float qv[4][R];
+    UnitCursor cur(u0, RG);
+    Ring<S> ring;
+    for (int64_t i = 0; i < u1 - u0; ++i, cur.next(), ring.next()) {
+      const int st = ring.st;
+      const int64_t cb = cur.tile, rg = cur.blk;
+      const int64_t col = cb * kRGCols + 4 * chunk;
+      if (cb != cur_cb) {
+        // Q' rows of this thread's four columns for the new column block
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int c = 0; c < R; ++c) qv[q][c] = (col + q < n) ? __ldg(&Qn[(col + q) * R + c]) : 0.0f;
+        cur_cb = cb;
+      }
+      // a wait that runs out ends the warp's loop (the warp decides as one,
+      // as it meets at __syncwarp below; no other barrier follows)
+      bool bad = *abort_flag != 0 || !mbar_wait(&full[st], ring.ph, kWaitCycles);
+      if (__any_sync(0xffffffffu, bad)) {
+        *abort_flag = 1;
+        ok = false;
+        break;
+      }
+      const uint32_t t = smem_u32(base + (size_t)st * kStageBytes);
+      const uint32_t ps = t + kRGTile;
+      // box (chunk / 64) holds columns 256 (chunk / 64) ..; rows 1 KB apart
+      const uint32_t cofs = (chunk >> 6) * (kRGTile / 2) + (chunk & 63) * 16;
+      float4 mv[2];
+      float pr[2][R];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t row = r0 + 4 * h;
+        mv[h] = lds128(t + cofs + row * 1024);
+#pragma unroll
+        for (int c = 0; c < R; ++c) pr[h][c] = lds32(ps + (row * R + c) * 4);
+      }
+      float4 out[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float x[4] = {mv[h].x, mv[h].y, mv[h].z, mv[h].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float a = 0.0f;
+#pragma unroll
+          for (int c = 0; c < R; ++c) a = fmaf(pr[h][c], qv[q][c], a);
+          x[q] = x[q] - a;
+        }
+        out[h] = make_float4(x[0], x[1], x[2], x[3]);
+      }
+      // the stage can be refilled once every warp has read it: each lane's
+      // loaded values have been used by the arithmetic above (so its loads
+      // are complete) before the warp's one arrival
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t grow = rg * kRGRows + r0 + 4 * h;
+        if (grow < m && col < n) *reinterpret_cast<float4*>(E + grow * n + col) = out[h];
+      }
+    }
+  }
+  if (!ok) atomicOr(status, kStatusWaitTimeout);
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// pass 2: Q' = M^T P_hat, fp32 FMAs on the CUDA cores (r products per
+// element).  The tensor core cannot take this contraction's operand from M
+// as it lies in memory: the sum runs over M's rows, so M would be the
+// transposed (MN-major) operand, which kind::tf32 does not accept (it reads
+// as zero), and transposing every tile through shared memory, plus one
+// M = 128 MMA per 4 KB of M, held a tensor-core version of this pass near a
+// third of the memory bandwidth.  Here M streams exactly as in pass 3 (units
+// of 8 rows x 512 columns, column block by column block, with the unit's
+// rows of P_hat), and each thread keeps the sums of four columns in
+// registers while its CTA stays in one column block.  Thread t holds
+// columns 4 (t / 4) .. + 3 of rows t % 4 and t % 4 + 4 of each unit; at the
+// end of a column block the four row phases are added by shuffles (fixed
+// order), each CTA writes its partial Q' of the block to slot CTA + block,
+// and the block's last contributor adds the slots in CTA order.
+// ---------------------------------------------------------------------------
+template <int R>
+__global__ void __launch_bounds__(kResidThreads, 1) psgd_qstream_kernel(
+    const __grid_constant__ CUtensorMap tmM, int64_t m, int64_t n, const float* __restrict__ phat,
+    float* __restrict__ Q_out, float* __restrict__ part, uint32_t* __restrict__ tickets,
+    uint32_t* status) {
+  using namespace sm100;
+  constexpr int S = kStagesR;
+  constexpr uint32_t kPBytes = kRGRows * R * 4;
+  constexpr uint32_t kStageBytes = kRGTile + ((kPBytes + 127) / 128) * 128;
+  constexpr int kLoader = kResidConv / 32;
+  extern __shared__ unsigned char tc_smem[];
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(tc_smem) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)S * kStageBytes);
+  uint64_t* empty = full + S;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
+  volatile int* last = abort_flag + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int C = gridDim.x, cta = blockIdx.x;
+  const int64_t RG = (m + kRGRows - 1) / kRGRows, CB = (n + kRGCols - 1) / kRGCols, U = RG * CB;
+  const int64_t u0 = unit_lo(cta, C, U), u1 = unit_lo(cta + 1, C, U);
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kResidConv / 32);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  bool ok = true;
+  int64_t loads = 0;
+  if (warp == kLoader) {
+    if (lane == 0) {
+      tma_prefetch_map(&tmM);
+      UnitCursor cur(u0, RG);
+      Ring<S> ring;
+      for (int64_t i = 0; i < u1 - u0; ++i, cur.next(), ring.next()) {
+        const int st = ring.st;
+        if (i >= S && !mbar_wait(&empty[st], ring.ph ^ 1u, kWaitCycles)) {
+          ok = false;
+          break;
+        }
+        const int64_t cb = cur.tile, rg = cur.blk;
+        unsigned char* stage = base + (size_t)st * kStageBytes;
+        mbar_arrive_expect_tx(&full[st], kRGTile + kPBytes);
+        tma_load_2d(stage, &tmM, (int32_t)(cb * kRGCols), (int32_t)(rg * kRGRows), &full[st]);
+        tma_load_2d(stage + kRGTile / 2, &tmM, (int32_t)(cb * kRGCols + kRGCols / 2),
+                    (int32_t)(rg * kRGRows), &full[st]);
+        bulk_load(stage + kRGTile, phat + rg * kRGRows * R, kPBytes, &full[st]);
+        ++loads;
+      }
+      for (int64_t j = std::max<int64_t>(0, loads - S); j < loads; ++j)
+        if (!mbar_wait(&full[j % S], (uint32_t)((j / S) & 1), kWaitCycles))
+          ok = false;
+    }
+  } else {
+    const uint32_t r0 = tid & 3, chunk = tid >> 2;
+    const uint32_t cofs = (chunk >> 6) * (kRGTile / 2) + (chunk & 63) * 16;
+    float acc[4][R];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int c = 0; c < R; ++c) acc[q][c] = 0.0f;
+    UnitCursor cur(u0, RG);
+    Ring<S> ring;
+    for (int64_t i = 0; i < u1 - u0; ++i, cur.next(), ring.next()) {
+      const int st = ring.st;
+      const int64_t cb = cur.tile;
+      // a wait that runs out makes the warp (deciding as one) skip its work
+      // from then on; it still meets the barriers at the ends of column blocks
+      bool bad = *abort_flag != 0;
+      if (!bad) bad = !mbar_wait(&full[st], ring.ph, kWaitCycles);
+      const bool skip = __any_sync(0xffffffffu, bad);
+      if (skip) {
+        *abort_flag = 1;
+        ok = false;
+      }
+      const uint32_t t = smem_u32(base + (size_t)st * kStageBytes);
+      const uint32_t ps = t + kRGTile;
+      float4 mv[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+      float pr[2][R];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < R; ++c) pr[h][c] = 0.0f;
+      if (!skip) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t row = r0 + 4 * h;
+          mv[h] = lds128(t + cofs + row * 1024);
+#pragma unroll
+          for (int c = 0; c < R; ++c) pr[h][c] = lds32(ps + (row * R + c) * 4);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float x[4] = {mv[h].x, mv[h].y, mv[h].z, mv[h].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int c = 0; c < R; ++c) acc[q][c] = fmaf(x[q], pr[h][c], acc[q][c]);
+      }
+      if (!skip) {
+        // the stage can be refilled once every warp has read it: each lane's
+        // loaded values have been used above (so its loads are complete)
+        // before the warp's one arrival
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+      if (cur.blk != RG - 1 && i != u1 - u0 - 1) continue;
+      // end of this CTA's part of column block cb: its partial sums
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int c = 0; c < R; ++c) {
+          float v = acc[q][c];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          acc[q][c] = v;
+        }
+      if (r0 == 0) {
+        float* dst = part + ((int64_t)(cta + cb) * kRGCols + 4 * chunk) * R;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int c = 0; c < R; ++c) dst[q * R + c] = acc[q][c];
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int c = 0; c < R; ++c) acc[q][c] = 0.0f;
+      __threadfence();
+      resid_sync();
+      const int c_first = unit_owner(cb * RG, C, U), c_last = unit_owner(cb * RG + RG - 1, C, U);
+      if (tid == 0) *last = atomicAdd(&tickets[cb], 1u) == (uint32_t)(c_last - c_first);
+      resid_sync();
+      if (!*last) continue;
+      __threadfence();
+      // the block's columns: slots added in CTA order
+      const int64_t col = cb * kRGCols + tid;
+      if (col < n) {
+        float q[R];
+#pragma unroll
+        for (int c = 0; c < R; ++c) q[c] = 0.0f;
+        for (int cc = c_first; cc <= c_last; ++cc) {
+          const float* src = part + ((int64_t)(cc + cb) * kRGCols + tid) * R;
+#pragma unroll
+          for (int c = 0; c < R; ++c) q[c] += __ldcg(src + c);
+        }
+#pragma unroll
+        for (int c = 0; c < R; ++c) Q_out[col * R + c] = q[c];
+      }
+      if (tid == 0) tickets[cb] = 0u;
+    }
+  }
+  if (!ok) atomicOr(status, kStatusWaitTimeout);
+  __syncthreads();
+}
+
+template <int R>
+__host__ constexpr size_t resid_smem_bytes() {
+  return 1024 + (size_t)kStagesR * (kRGTile + ((kRGRows * R * 4 + 127) / 128) * 128) +
+         (size_t)2 * kStagesR * 8 + 16;
+}
+
+}  // namespace tcp
+
+// cuTensorMapEncodeTiled from the driver (looked up once).
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// A rows x cols fp32 row-major matrix (cols a multiple of 4) read in boxes
+// of box_rows x box_cols, with the 128-byte swizzle (box_cols <= 32) or
+// rows stored one after the other; out-of-range parts of a box read as
+// zero.
+bool make_map(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, uint32_t box_cols,
+              uint32_t box_rows, bool swizzle) {
+  const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same matrix (cols a multiple of 32) seen as 32 columns x cols / 32
+// segments x rows, read in boxes of 32 x sg x rg with the 128-byte swizzle:
+// box row (r, s) is segment s of matrix row r, 128 bytes.
+bool make_map_segments(CUtensorMap* map, const float* base, int64_t rows, int64_t cols,
+                       uint32_t sg, uint32_t rg) {
+  const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {32, (cuuint64_t)(cols / 32), (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {128, (cuuint64_t)cols * 4};
+  const cuuint32_t box[3] = {32, sg, rg};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Bytes of the tensor-core path's data area for matrices up to max_m x
+// max_n: pass 1 partials and Q images, pass 2 partials, P_hat padded.
+int64_t tc_area_bytes(int64_t max_m, int64_t max_n, int max_r, int num_sms) {
+  auto up = [](int64_t b) { return (b + 255) / 256 * 256; };
+  return up((int64_t)sizeof(float) * ((int64_t)num_sms * tcp::kRows + max_m + tcp::kRows) *
+            max_r) +
+         up(round_up(max_n, 512) * 128 + 16384) +
+         up((int64_t)sizeof(float) * (num_sms + ceil_div(max_n, tcp::kRGCols)) * tcp::kRGCols *
+            max_r) +
+         up((int64_t)sizeof(float) * round_up(max_m, tcp::kRGRows) * max_r);
+}
+
+// Pass 0 and pass 1 with SG segments per operand tile.
+template <int R, int SG>
+gc_status launch_pass1(gc_ctx* ctx, const float* grad, float* err, int64_t m, int64_t n,
+                       const float* Q, const tcp::TcBufs& b) {
+  constexpr int RG = tcp::kRows / SG, KU = SG * tcp::kKBlk, H = tcp::img_half(R, SG);
+  constexpr uint32_t kImg = 2 * H * tcp::kKBlk * 4;
+  CUtensorMap tm_g, tm_e;
+  const bool maps = SG == 1 ? make_map(&tm_g, grad, m, n, tcp::kKBlk, RG, true) &&
+                                  make_map(&tm_e, err, m, n, tcp::kKBlk, RG, true)
+                            : make_map_segments(&tm_g, grad, m, n, SG, RG) &&
+                                  make_map_segments(&tm_e, err, m, n, SG, RG);
+  if (!maps) return GC_ERR_CUDA;
+  const int64_t KB = ceil_div(n, KU), U = ceil_div(m, RG) * KB;
+  const size_t smem = tcp::smem_bytes_p(tcp::stages_p(R, SG), kImg);
+  if (cudaFuncSetAttribute(tcp::psgd_p_tc_kernel<R, SG>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return GC_ERR_CUDA;
+  {
+    LaunchScope L(ctx, GC_PHASE_PSGD_THIN);
+    const int64_t rows = KB * KU;
+    tcp::psgd_qimage_kernel<R, SG><<<(unsigned)ceil_div(rows, 256), 256, 0, ctx->stream>>>(
+        Q, n, b.qimg, rows);
+  }
+  {
+    LaunchScope L(ctx, GC_PHASE_PSGD_MQ);
+    const int c1 = (int)std::min<int64_t>(ctx->num_sms, U);
+    tcp::psgd_p_tc_kernel<R, SG><<<c1, tcp::kThreads, smem, ctx->stream>>>(tm_g, tm_e, err, m, n,
+                                                                             b);
+  }
+  return GC_OK;
+}
+
+template <int R>
+gc_status run_psgd_tc(gc_ctx* ctx, const float* grad, float* err, int64_t m, int64_t n,
+                      float* P_out, float* Q_inout, const PsgdBufs& pb, char* area) {
+  cudaStream_t s = ctx->stream;
+  const PsgdWorkspace& pw = ctx->psgd;
+  auto up = [](int64_t v) { return (v + 255) / 256 * 256; };
+  tcp::TcBufs b;
+  b.praw = pb.praw;
+  b.part = reinterpret_cast<float*>(area);
+  area += up((int64_t)sizeof(float) * ((int64_t)ctx->num_sms * tcp::kRows + pw.max_m + tcp::kRows) *
+             pw.max_r);
+  b.qimg = reinterpret_cast<float*>(area);
+  area += up(round_up(pw.max_n, 512) * 128 + 16384);
+  float* qpart = reinterpret_cast<float*>(area);
+  area += up((int64_t)sizeof(float) * (ctx->num_sms + ceil_div(pw.max_n, tcp::kRGCols)) *
+             tcp::kRGCols * pw.max_r);
+  float* phat = reinterpret_cast<float*>(area);  // P_hat, rows padded to a multiple of 8
+  b.rt_tickets = pb.rb_tickets;
+  b.gram_part = pb.gram_part;
+  b.w = pb.w;
+  b.state = pb.state;
+  b.status = pb.status;
+
+  // pass 1: segment tiles when the rows split into 32-column segments
+  const gc_status st1 = n % 32 == 0
+                            ? launch_pass1<R, tcp::segs_for(R)>(ctx, grad, err, m, n, Q_inout, b)
+                            : launch_pass1<R, 1>(ctx, grad, err, m, n, Q_inout, b);
+  if (st1 != GC_OK) return st1;
+
+  // P_hat = P W; passes 2 and 3 stream M in units of 8 rows x 512 columns
+  CUtensorMap tm_r;
+  if (!make_map(&tm_r, err, m, n, tcp::kRGCols / 2, tcp::kRGRows, false)) return GC_ERR_CUDA;
+  const int64_t m_pad = round_up(m, tcp::kRGRows);
+  const int c3 = (int)std::min<int64_t>(ctx->num_sms,
+                                        (m_pad / tcp::kRGRows) * ceil_div(n, tcp::kRGCols));
+  const size_t sm3 = tcp::resid_smem_bytes<R>();
+  if (cudaFuncSetAttribute(tcp::psgd_qstream_kernel<R>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3) != cudaSuccess ||
+      cudaFuncSetAttribute(tcp::psgd_resid_tma_kernel<R>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3) != cudaSuccess)
+    return GC_ERR_CUDA;
+  {
+    LaunchScope L(ctx, GC_PHASE_PSGD_THIN);
+    tcp::psgd_phat_kernel<R><<<(unsigned)ceil_div(m_pad, 256), 256, 0, s>>>(b.praw, b.w, m, m_pad,
+                                                                           P_out, phat);
+  }
+  {
+    LaunchScope L(ctx, GC_PHASE_PSGD_MTP);
+    tcp::psgd_qstream_kernel<R><<<c3, tcp::kResidThreads, sm3, s>>>(tm_r, m, n, phat, Q_inout,
+                                                                      qpart, pb.tickets, b.status);
+  }
+  {
+    LaunchScope L(ctx, GC_PHASE_PSGD_RESID);
+    tcp::psgd_resid_tma_kernel<R><<<c3, tcp::kResidThreads, sm3, s>>>(tm_r, err, m, n, phat,
+                                                                        Q_inout, b.status);
+  }
+  return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
 template <int R, bool VEC>
 gc_status run_psgd(gc_ctx* ctx, const float* grad, float* err, int64_t m, int64_t n,
                    float* P_out, float* Q_inout) {
@@ -432,15 +1446,22 @@ gc_status run_psgd(gc_ctx* ctx, const float* grad, float* err, int64_t m, int64_
   // carve the reserved scratch (see gc_ctx_reserve_powersgd)
   size_t off = 0;
   auto take = [&](size_t bytes) { void* p = base + off; off += (bytes + 255) / 256 * 256; return p; };
+  // tickets and state first (zero between calls, shared by both paths),
+  // then the data both paths write before they read
   b.state = static_cast<PsgdState*>(take(sizeof(PsgdState)));
   b.w = static_cast<float*>(take(sizeof(float) * 16 * 16));
   b.tickets = static_cast<uint32_t*>(take(sizeof(uint32_t) * ceil_div(pw.max_n, kStrip)));
+  // (row tickets and Gram partials: one per 8 rows covers both paths)
+  b.rb_tickets = static_cast<uint32_t*>(take(sizeof(uint32_t) * ceil_div(pw.max_m, 8)));
   b.praw = static_cast<float*>(take(sizeof(float) * pw.max_m * pw.max_r));
-  b.ppart = static_cast<float*>(take(sizeof(float) * kMaxColSplits * pw.max_m * pw.max_r));
-  b.rb_tickets = static_cast<uint32_t*>(take(sizeof(uint32_t) * ceil_div(pw.max_m, kRowsPerBlock)));
-  b.gram_part = static_cast<double*>(take(sizeof(double) * ceil_div(pw.max_m, kRowsPerBlock) * pw.max_r * pw.max_r));
-  b.q_part = reinterpret_cast<float*>(base + off);
+  b.gram_part = static_cast<double*>(take(sizeof(double) * ceil_div(pw.max_m, 8) * pw.max_r * pw.max_r));
   b.status = ctx->ws.status;
+  if constexpr (VEC) {
+    // rows start on 16-byte boundaries: the tensor-core path
+    return run_psgd_tc<R>(ctx, grad, err, m, n, P_out, Q_inout, b, base + off);
+  }
+  b.ppart = static_cast<float*>(take(sizeof(float) * kMaxColSplits * pw.max_m * pw.max_r));
+  b.q_part = reinterpret_cast<float*>(base + off);
   const int64_t qcap = (pw.bytes - (int64_t)off) / (int64_t)sizeof(float);
 
   const int mq_blocks = (int)ceil_div(m, kRowsPerBlock);
@@ -494,15 +1515,18 @@ gc_status run_psgd_r(gc_ctx* ctx, const float* grad, float* err, int64_t m, int6
 
 int64_t psgd_workspace_bytes(int64_t max_m, int64_t max_n, int max_r, int num_sms) {
   auto up = [](int64_t b) { return (b + 255) / 256 * 256; };
-  int64_t bytes = up(sizeof(PsgdState)) + up(sizeof(float) * 16 * 16) +
-                  up(sizeof(uint32_t) * ceil_div(max_n, kStrip)) +
-                  up(sizeof(float) * max_m * max_r) +
-                  up(sizeof(float) * kMaxColSplits * max_m * max_r) +
-                  up(sizeof(uint32_t) * ceil_div(max_m, kRowsPerBlock)) +
-                  up(sizeof(double) * ceil_div(max_m, kRowsPerBlock) * max_r * max_r);
-  // q partials: splits * n * r floats with splits * strips <= 4 * SMs + strips
-  bytes += (int64_t)sizeof(float) * ((int64_t)num_sms * 4 * kStrip + max_n + kStrip) * max_r;
-  return bytes;
+  const int64_t common = up(sizeof(PsgdState)) + up(sizeof(float) * 16 * 16) +
+                         up(sizeof(uint32_t) * ceil_div(max_n, kStrip)) +
+                         up(sizeof(uint32_t) * ceil_div(max_m, 8)) +
+                         up(sizeof(float) * max_m * max_r) +
+                         up(sizeof(double) * ceil_div(max_m, 8) * max_r * max_r);
+  // CUDA-core path: partial rows of P per column range, then the q
+  // partials (splits * n * r floats with splits * strips <= 4 * SMs + strips)
+  const int64_t cuda_core = up(sizeof(float) * kMaxColSplits * max_m * max_r) +
+                            (int64_t)sizeof(float) * ((int64_t)num_sms * 4 * kStrip + max_n + kStrip) * max_r;
+  // tensor-core path: one 128-row partial per (CTA, tile) pair, the images
+  const int64_t tensor_core = tc_area_bytes(max_m, max_n, max_r, num_sms);
+  return common + std::max(cuda_core, tensor_core);
 }
 
 gc_status launch_powersgd(gc_ctx* ctx, const float* grad, float* err, int64_t m,

@@ -20,7 +20,7 @@ NEAREST_EVEN, STOCHASTIC = 0, 1
 MODES = {"minmax": MINMAX, "qsgd": QSGD, "tern": TERN, "log": LOG}
 ROUNDINGS = {"nearest_even": NEAREST_EVEN, "stochastic": STOCHASTIC}
 
-PHASE_COUNT = 24
+PHASE_COUNT = 25
 
 OK = 0
 ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_WORKSPACE = -1, -2, -3, -4

@@ -194,7 +194,7 @@ def test_error_feedback_steps_match_single_calls(env):
         for b, (nb_, kb) in enumerate(zip(ns, ks)):
             s0 = int(st[b])
             gc.ef_topk_quant(ctx, gd[s0:s0 + nb_], e_one[s0:s0 + nb_], kb, 8, 64, "stochastic",
-                             50 + b, step, idx_one[oi[b]:oi[b] + kb],
+                             gc.bucket_seed(50, b), step, idx_one[oi[b]:oi[b] + kb],
                              codes_one[oc[b]:oc[b + 1]], scales_one[os_[b]:os_[b + 1]])
         ctx.check()
         assert_bits_equal(host(e_bk), host(e_one), "step %d err" % step)
@@ -321,7 +321,8 @@ def test_full_size_workload(env):
         gc.ef_topk_quant_buckets(ctx, gd, e_bk, 8, 64, "stochastic", 1000, step, *out_bk)
         for b, ((s0, length), kb) in enumerate(zip(bounds, ks)):
             gc.ef_topk_quant(ctx, gd[s0:s0 + length], e_one[s0:s0 + length], kb, 8, 64,
-                             "stochastic", 1000 + b, step, out_one[0][oi[b]:oi[b] + kb],
+                             "stochastic", gc.bucket_seed(1000, b), step,
+                             out_one[0][oi[b]:oi[b] + kb],
                              out_one[1][oc[b]:oc[b + 1]], out_one[2][os_[b]:os_[b + 1]])
         ctx.check()
     assert_bits_equal(host(e_bk), host(e_one), "full err")
@@ -338,7 +339,8 @@ def test_full_size_workload(env):
         s0, length = bounds[b]
         sl = slice(s0, s0 + length)
         o_idx, o_codes, o_scales, o_err = oracle.ef_topk_quant(
-            g_last[sl], e_before[sl], ks[b], 8, 64, "stochastic", 1000 + b, len(grads) - 1)
+            g_last[sl], e_before[sl], ks[b], 8, 64, "stochastic", oracle.bucket_seed(1000, b),
+            len(grads) - 1)
         assert_bits_equal(idx_h[oi[b]:oi[b] + ks[b]], o_idx, "oracle idx %d" % b)
         assert_bits_equal(codes_h[oc[b]:oc[b + 1]], o_codes, "oracle codes %d" % b)
         assert_bits_equal(scales_h[os_[b]:os_[b] + o_scales.size], o_scales, "oracle scales %d" % b)
@@ -373,7 +375,7 @@ def test_threshold_guess_paths(env, scales):
         for b, (n, k) in enumerate(zip(ns, ks)):
             sl = slice(st[b], st[b + 1])
             o_idx, o_codes, o_scales, o_err = oracle.ef_topk_quant(
-                g[sl], e[sl], k, 8, 64, "stochastic", 3 + b, step)
+                g[sl], e[sl], k, 8, 64, "stochastic", oracle.bucket_seed(3, b), step)
             w = "step %d bucket %d" % (step, b)
             assert_bits_equal(i_h[oi[b]:oi[b] + k], o_idx, w + " idx")
             assert_bits_equal(c_h[oc[b]:oc[b + 1]], o_codes, w + " codes")

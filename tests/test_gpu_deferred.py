@@ -143,7 +143,8 @@ def test_deferred_chain_against_oracle(env):
         oi, oc, os_ = ol.offs
         for b, k in enumerate(ks):
             o_idx, o_codes, o_scales, e_or[b] = oracle.ef_topk_quant(
-                g[st[b]:st[b + 1]], e_or[b], k, 8, 64, "stochastic", 40 + b, step)
+                g[st[b]:st[b + 1]], e_or[b], k, 8, 64, "stochastic", oracle.bucket_seed(40, b),
+                step)
             assert_bits_equal(idx[oi[b]:oi[b] + k], o_idx, "step %d bucket %d idx" % (step, b))
             assert_bits_equal(codes[oc[b]:oc[b + 1]], o_codes, "step %d codes" % step)
             assert_bits_equal(scales[os_[b]:os_[b] + o_scales.size], o_scales,

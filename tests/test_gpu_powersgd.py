@@ -86,3 +86,32 @@ def test_requires_reserved_scratch(env):
                          torch.zeros((8, 2), device="cuda"))
     assert ei.value.status == gc.ERR_WORKSPACE
     c.close()
+
+
+@pytest.mark.parametrize("shape", [(4096, 11008), (1000, 4100), (777, 96)])
+def test_repeatable_and_close_to_fp32(env, shape):
+    """The same step on the same inputs gives the same bits every time (the
+    passes' partial sums are added in a fixed order), and the three-term
+    TF32 products keep the reconstruction within 2e-5 of the binary64
+    oracle -- far inside the 1e-3 bar, so that a lost or doubled partial
+    sum cannot hide under it.  The shapes cover 32-column segments with a
+    partial last column block (11008 = 21.5 x 512), columns that are not a
+    multiple of 32 (4100) and a matrix smaller than one column block."""
+    torch, gc, ctx = env
+    m, n = shape
+    M, Q0 = inputs.low_rank_matrix(m, n, r=4)
+    outs = []
+    for _ in range(2):
+        Gd, Ed, Qd = dev_f32(torch, M), dev_f32(torch, np.zeros_like(M)), dev_f32(torch, Q0)
+        Pd = torch.empty((m, 4), dtype=torch.float32, device="cuda")
+        gc.powersgd_step(ctx, Gd, Ed, m, n, 4, Pd, Qd)
+        ctx.check()
+        outs.append((host(Pd), host(Qd), host(Ed)))
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    oP, oQ, oE = oracle.powersgd_step(M, np.zeros_like(M), Q0, 4)
+    P, Qn, En = outs[0]
+    approx = P.astype(np.float64) @ Qn.astype(np.float64).T
+    o_approx = oP.astype(np.float64) @ oQ.astype(np.float64).T
+    assert rel(approx, o_approx) <= 2e-5
+    assert rel(En, oE) <= 2e-5 * max(1.0, np.linalg.norm(o_approx) / np.linalg.norm(oE))
