@@ -216,6 +216,29 @@ def low_rank_matrix(m, n, rank=16, noise_std=1e-4, seed=42, r=4):
     return M, Q0
 
 
+def low_rank_matrix_device(m, n, device, seed=42, rank=16, noise_std=1e-4, r=4):
+    """The low_rank_matrix recipe with the large parts drawn by torch on
+    ``device`` (seeded): (M float32 m x n, Q0 float32 n x r) with M = U
+    diag(sigma) V^T + noise, U, V orthonormal (numpy QR of Gaussians),
+    sigma_i = 0.05^(i / (rank - 1)) -- the same distribution as the host
+    recipe, for workloads too large to draw on the host."""
+    import torch
+    # the thin orthonormal factors come from numpy's QR on the host (small)
+    generator = rng([seed, m, n, 1])
+    u, _ = np.linalg.qr(generator.standard_normal((m, rank)))
+    v, _ = np.linalg.qr(generator.standard_normal((n, rank)))
+    sigma = 0.05 ** (np.arange(rank) / max(rank - 1, 1))
+    u = torch.from_numpy(u * sigma).to(device)
+    v = torch.from_numpy(v).to(device)
+    M = (u @ v.T).to(torch.float32)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    M.add_(torch.randn(m, n, generator=gen, device=device, dtype=torch.float32),
+           alpha=noise_std)
+    Q0 = torch.randn(n, r, generator=gen, device=device, dtype=torch.float32)
+    return M, Q0
+
+
 def tiny_cases(seed=7):
     """Small edge-case vectors used by the parity tests (length, values)."""
     generator = rng(seed)
