@@ -100,38 +100,59 @@ __device__ __forceinline__ void stage_q(float* qs, const float* Q, int64_t col0,
 // matrix, and w = U^-1 (upper triangular, row-major R x R floats): P U^-1 is
 // the orthonormal factor Gram-Schmidt gives.  A column whose remaining norm
 // is 0 is dropped (its P_hat column is left zero), as Gram-Schmidt leaves a
-// zero column zero.  One thread.
+// zero column zero.
+//
+// One warp, in shared memory: A (R x R, the Gram matrix, overwritten by U
+// in its upper triangle) and rinv (R doubles).  Step k takes the pivot d =
+// A[k][k], scales row k by 1 / sqrt(d) and subtracts the outer product of
+// the scaled row from the trailing block, so every entry loses the same
+// products in the same order as in the column-by-column form; the one
+// reciprocal square root per pivot replaces the square root and the
+// divisions (binary64 division and square root are long instruction
+// sequences here, and the chain is serial).  Then lane j forms column j of
+// W by back substitution.
 template <int R>
-__device__ void cholesky_inverse(const double* gram, float* w) {
-  double U[R][R], W[R][R];
-  bool zero[R];
-  for (int i = 0; i < R; ++i)
-    for (int j = 0; j < R; ++j) U[i][j] = W[i][j] = 0.0;
-  for (int j = 0; j < R; ++j) {
-    for (int i = 0; i < j; ++i) {
-      if (zero[i]) { U[i][j] = 0.0; continue; }
-      double s = gram[i * R + j];
-      for (int k = 0; k < i; ++k) s -= U[k][i] * U[k][j];
-      U[i][j] = s / U[i][i];
+__device__ void cholesky_inverse_warp(double* A, double* rinv, float* w, int lane) {
+#pragma unroll 1
+  for (int k = 0; k < R; ++k) {
+    const double d = A[k * R + k];
+    const bool z = !(d > 0.0);
+    const double r = z ? 0.0 : rsqrt(d);
+    __syncwarp();
+    for (int j = k + 1 + lane; j < R; j += 32) A[k * R + j] = z ? 0.0 : A[k * R + j] * r;
+    if (lane == 0) rinv[k] = r;  // 0 marks a dropped direction
+    __syncwarp();
+    const int T = R - 1 - k;
+    for (int t = lane; t < T * T; t += 32) {
+      const int i = k + 1 + t / T, j = k + 1 + t % T;
+      if (i <= j) A[i * R + j] = A[i * R + j] - A[k * R + i] * A[k * R + j];
     }
-    double d = gram[j * R + j];
-    for (int k = 0; k < j; ++k) d -= U[k][j] * U[k][j];
-    zero[j] = !(d > 0.0);
-    U[j][j] = zero[j] ? 1.0 : sqrt(d);
+    __syncwarp();
   }
-  // W = U^-1 by back substitution, columns of dropped directions zero
-  for (int j = R - 1; j >= 0; --j) {
-    if (zero[j]) continue;
-    W[j][j] = 1.0 / U[j][j];
-    for (int i = j - 1; i >= 0; --i) {
-      if (zero[i]) continue;
-      double s = 0.0;
-      for (int k = i + 1; k <= j; ++k) s += U[i][k] * W[k][j];
-      W[i][j] = -s / U[i][i];
+  if (lane < R) {
+    const int j = lane;
+    double wc[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) wc[i] = 0.0;
+    const double rj = rinv[j];
+    if (rj != 0.0) {
+#pragma unroll
+      for (int i = R - 1; i >= 0; --i) {
+        if (i == j) wc[i] = rj;
+        const double ri = rinv[i];
+        if (i < j && ri != 0.0) {
+          double sum = 0.0;
+#pragma unroll
+          for (int k = 0; k < R; ++k)
+            if (k > i && k <= j) sum += A[i * R + k] * wc[k];
+          wc[i] = -sum * ri;
+        }
+      }
     }
+#pragma unroll
+    for (int i = 0; i < R; ++i) w[i * R + j] = (float)wc[i];
   }
-  for (int i = 0; i < R; ++i)
-    for (int j = 0; j < R; ++j) w[i * R + j] = (float)W[i][j];
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
@@ -144,6 +165,7 @@ __global__ void __launch_bounds__(kPThreads) psgd_mq_kernel(
   __shared__ float qs[kQChunk * R];
   __shared__ float prow[kRowsPerBlock][R];
   __shared__ double gram[R * R];
+  __shared__ double rinv[R];
   __shared__ bool last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t row0 = (int64_t)blockIdx.x * kRowsPerBlock + warp * kRowsPerWarp;
@@ -273,10 +295,8 @@ __global__ void __launch_bounds__(kPThreads) psgd_mq_kernel(
     gram[threadIdx.x] = s;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    cholesky_inverse<R>(gram, b.w);
-    b.state->ticket_mq = 0u;
-  }
+  if (warp == 0) cholesky_inverse_warp<R>(gram, rinv, b.w, lane);
+  if (threadIdx.x == 0) b.state->ticket_mq = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -435,7 +455,7 @@ __global__ void __launch_bounds__(kPThreads) psgd_residual_kernel(
 
 // ===========================================================================
 // Tensor-core path (n a multiple of 4, so that every row of G, E and M
-// starts on a 16-byte boundary as the TMA requires).
+// starts on a 16-byte boundary).
 //
 // Pass 1, P = M Q (K = n, N = r), runs as tcgen05.mma kind::tf32 with the
 // accumulator (128 lanes of fp32) in tensor memory.  TF32 keeps 10 mantissa
@@ -448,16 +468,14 @@ __global__ void __launch_bounds__(kPThreads) psgd_residual_kernel(
 // 128 bytes of each of 128 rows per step reached 61 % of the bandwidth, the
 // same pass reading 2 KB of each of 8 rows 89 %), while the MMA wants 128
 // operand rows.  So an operand tile of 128 rows is made of SG segments of
-// 32 columns from each of 128 / SG matrix rows (a 3-D TMA box: 32 columns x
-// SG segments x 128 / SG rows, with the 128-byte swizzle), and the thin
-// operand carries the segments along N: image row s r + c holds column c of
-// Q for the segment s (rows SG r .. of hi, then as many of lo).  Operand
-// row (row, s) times image row (s', c) is the segment-s part of P[row][c]
-// when s' = s; the read-out keeps those and adds them over the segments.
-// With SG = 4 (r <= 4) each step reads 512 bytes of each of 32 rows
-// (16 segments, 2 KB per row, made the pass tensor-bound: the MMA work
-// grows with SG); matrices whose columns are not a multiple of 32 use
-// SG = 1 (128 rows x 32 columns, a 2-D box).
+// 32 columns from each of 128 / SG matrix rows, and the thin operand
+// carries the segments along N: image row s r + c holds column c of Q for
+// the segment s (rows SG r .. of hi, then as many of lo).  Operand row
+// (row, s) times image row (s', c) is the segment-s part of P[row][c] when
+// s' = s; the read-out keeps those and adds them over the segments.  SG = 4
+// for r <= 4 (512 bytes of each of 32 rows per unit), 2 for r <= 8, 1
+// above; the MMA work grows with SG (the off-diagonal products are wasted:
+// 16 segments made the pass tensor-bound).
 //
 // Work: the pass cuts its K range into units of 32 SG columns per tile of
 // 128 / SG rows; units are numbered tile-major and every CTA (one per SM)
@@ -467,58 +485,63 @@ __global__ void __launch_bounds__(kPThreads) psgd_residual_kernel(
 // time, so the slots are distinct), and the last contributor of a tile
 // (ticket) adds the tile's slots in CTA order: deterministic.
 //
-// Roles in a CTA of 320 threads: warps 0-7 convert the staged tiles (M = G
-// + E stored to global, then the hi/lo split in place), warps 0-3 also read
-// the accumulator out (tcgen05.ld: warp w reads lanes 32w .. 32w + 31);
-// warp 8 lane 0 issues the TMA and bulk copies; warp 9 owns the tensor
-// memory and its lane 0 issues the MMAs.  Stages are handed on by
-// mbarriers: full (copies landed), conv (operands converted), empty (the
-// MMAs reading the stage are done); acc_full / acc_empty hand the
-// accumulator to the read-out and back.  Every wait is bounded; the
-// converter warps take each abort decision together (one flag behind a
-// named barrier), so no barrier is left waiting for a thread that gave up.
+// Roles in a CTA of 448 threads: warps 0-7 stream G and E (cp.async into
+// staging slots of their own), form M = G + E (stored to global) and write
+// hi(M), lo(M) into the swizzled operand stage; warp 8 lane 0 copies the Q
+// images (bulk copies); warp 9 owns the tensor memory and its lane 0 issues
+// the MMAs; warps 10-13 read the accumulator out (tcgen05.ld: warp w reads
+// lanes 32 (w % 4) .. + 31) and do the per-tile reductions.  Operand
+// stages are handed on by mbarriers: full (image landed), conv (operands
+// written), empty (the MMAs reading the stage are done).  The accumulator
+// is double-buffered (segment j in buffer j % 2; acc_full / acc_empty per
+// buffer), so the converters never wait for a read-out: with one buffer
+// and the read-out done by the converters, the pipeline drained at every
+// segment end and the pass ran at about half the bandwidth on matrices of
+// 4096 columns.  Every wait is bounded; the converters and the read-out
+// warps each take their abort decisions together (a flag per group behind
+// the group's named barrier), so no barrier is left waiting for a thread
+// that gave up.
 //
 // Passes 2 (Q' = M^T P_hat) and 3 (E' = M - P_hat Q'^T) stream M on the
 // CUDA cores; see their kernels.
 // ===========================================================================
 namespace tcp {
 constexpr int kConv = 256;             // converter threads (warps 0-7)
-constexpr int kEpi = 128;              // accumulator read-out threads (warps 0-3)
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kEpiWarp0 = 10;          // accumulator read-out warps 10-13
+constexpr int kEpi = 128;              // accumulator read-out threads
+constexpr int kThreads = 448;
 constexpr int kRows = 128;             // MMA M: operand rows of a tile
 constexpr int kKBlk = 32;              // K per operand row of a unit (one 128-byte row)
 constexpr uint32_t kTileBytes = kRows * kKBlk * 4;  // 16 KB
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kAccCols = 64;     // one accumulator buffer (3 H <= 64 columns)
+constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr int kResidConv = 512;        // passes 2 and 3: compute threads (warps 0-15)
 constexpr int kResidThreads = 544;     // passes 2 and 3: warps 0-15 compute, warp 16 loads
-constexpr int kStagesR = 10;           // passes 2 and 3: stages
+constexpr int kWThreads = 64;          // pass 2: warps 17-18 form W and P_hat
+constexpr int kQThreads = kResidThreads + kWThreads;
+constexpr int kGramSlots = 256;        // pass 2: partial Gram sums (max(kWThreads, r^2) doubles)
+constexpr int kStagesR = 6;            // passes 2 and 3: stages (32 KB each)
 constexpr long long kWaitCycles = 4000000000ll;  // bound on each wait: ~2 s at 2 GHz
+constexpr int kPadRows = 16;           // P and P_hat rows are padded to a multiple of this
 
-// Segments per operand tile for rank R: 4 (512 contiguous bytes of each of
-// 32 rows per step) while 4 r image rows fit a 16-row half; the MMA work
-// grows with SG (the off-diagonal products are wasted), and 16 segments
-// made the pass tensor-bound.
+// Segments per operand tile for rank R (SG r <= 16: one 16-row image half).
 __host__ __device__ constexpr int segs_for(int R) { return R <= 4 ? 4 : R <= 8 ? 2 : 1; }
 // Image rows per half (hi or lo): SG r rounded up to 16.
 __host__ __device__ constexpr int img_half(int R, int SG) { return (SG * R + 15) / 16 * 16; }
-// Stages of pass 1: G and E tiles (32 KB) plus the image.
-__host__ __device__ constexpr int stages_p(int R, int SG) {
-  return 2 * img_half(R, SG) * 128 > 8192 ? 4 : 5;
-}
+// Pass 1: operand stages (hi, lo and the image, 36 KB each) and staging
+// slots of the converters' copies of G and E (32 KB each).
+constexpr int kOpStages = 2;
+constexpr int kStgSlots = 4;
 
-// First unit of CTA c of C over U units, and the CTA that owns unit u.
+// First unit of CTA c of C over U units, and the CTA that owns unit u: the
+// largest c with floor(U c / C) <= u, i.e. U c < (u + 1) C.
 __host__ __device__ __forceinline__ int64_t unit_lo(int c, int C, int64_t U) {
   return U * c / C;
 }
-__device__ __forceinline__ int unit_owner(int64_t u, int C, int64_t U) {
-  int lo = 0, hi = C - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (unit_lo(mid, C, U) <= u) lo = mid; else hi = mid - 1;
-  }
-  return lo;
+__host__ __device__ __forceinline__ int unit_owner(int64_t u, int C, int64_t U) {
+  return (int)(((u + 1) * C - 1) / U);
 }
 
 // Unit u of a tile-major numbering with `per` units per tile, stepped
@@ -552,34 +575,43 @@ struct Ring {
 __device__ __forceinline__ void conv_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConv) : "memory");
 }
+// Barrier of the read-out warps only.
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 2, %0;" ::"n"(kEpi) : "memory");
+}
+__device__ __forceinline__ void w_sync() {
+  asm volatile("bar.sync 3, %0;" ::"n"(kWThreads) : "memory");
+}
 __device__ __forceinline__ void resid_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kResidConv) : "memory");
 }
 
 struct Smem {
-  uint32_t a_hi;     // [S] tiles: G, then hi(M) (shared addresses)
-  uint32_t a_lo;     // [S] tiles: E, then lo(M)
+  uint32_t a_hi;     // [S] operand tiles hi(M) (shared addresses)
+  uint32_t a_lo;     // [S] operand tiles lo(M)
   uint32_t img;      // [S] thin-operand images
+  uint32_t stg;      // [SS] staging slots of the converters' copies
   uint64_t* full;
   uint64_t* conv;
   uint64_t* empty;
-  uint64_t* acc_full;
-  uint64_t* acc_empty;
+  uint64_t* acc_full;   // [2] accumulator buffers
+  uint64_t* acc_empty;  // [2]
   uint64_t* drain;
   uint32_t* tmem_slot;
-  volatile int* abort_flag;
+  volatile int* abort_flag;  // the converters' abort decision
+  volatile int* epi_abort;   // the read-out warps' abort decision
   int* last1;
   int* last2;
   float* rows;   // [kRows][16]
   double* gram;  // [16 * 16]
 };
 
-__host__ __device__ constexpr size_t smem_bytes_p(int S, uint32_t img_bytes) {
-  return 1024 + (size_t)S * (2 * kTileBytes + img_bytes) + (size_t)(3 * S + 3) * 8 + 64 +
-         (size_t)kRows * 16 * 4 + 16 * 16 * 8;
+__host__ __device__ constexpr size_t smem_bytes_p(int S, uint32_t img_bytes, int SS) {
+  return 1024 + (size_t)S * (2 * kTileBytes + img_bytes) + (size_t)SS * 2 * kTileBytes +
+         (size_t)(3 * S + 5) * 8 + 64 + (size_t)kRows * 16 * 4 + 16 * 16 * 8;
 }
 
-__device__ __forceinline__ Smem carve_smem(unsigned char* raw, int S, uint32_t img_bytes) {
+__device__ __forceinline__ Smem carve_smem(unsigned char* raw, int S, uint32_t img_bytes, int SS) {
   using namespace sm100;
   // the 128-byte swizzle repeats every 1024 bytes: tiles start on 1024
   unsigned char* p = reinterpret_cast<unsigned char*>(
@@ -588,15 +620,17 @@ __device__ __forceinline__ Smem carve_smem(unsigned char* raw, int S, uint32_t i
   s.a_hi = smem_u32(p); p += (size_t)S * kTileBytes;
   s.a_lo = smem_u32(p); p += (size_t)S * kTileBytes;
   s.img = smem_u32(p); p += (size_t)S * img_bytes;
+  s.stg = smem_u32(p); p += (size_t)SS * 2 * kTileBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(p);
   s.full = bars;
   s.conv = bars + S;
   s.empty = bars + 2 * S;
   s.acc_full = bars + 3 * S;
-  s.acc_empty = s.acc_full + 1;
-  s.drain = s.acc_full + 2;
-  p += (size_t)(3 * S + 3) * 8;
+  s.acc_empty = s.acc_full + 2;
+  s.drain = s.acc_full + 4;
+  p += (size_t)(3 * S + 5) * 8;
   s.tmem_slot = reinterpret_cast<uint32_t*>(p);
+  s.epi_abort = reinterpret_cast<volatile int*>(p + 8);
   s.abort_flag = reinterpret_cast<volatile int*>(p + 16);
   s.last1 = reinterpret_cast<int*>(p + 32);
   s.last2 = reinterpret_cast<int*>(p + 48);
@@ -606,12 +640,18 @@ __device__ __forceinline__ Smem carve_smem(unsigned char* raw, int S, uint32_t i
   return s;
 }
 
-// The converter warps' common abort decision: any thread that saw a wait
-// run out raises the flag; all read it after the named barrier.
+// A group's common abort decision (converters, read-out warps; each group
+// has its own flag): any thread that saw a wait run out raises the flag,
+// all read it after the group's named barrier.
 __device__ __forceinline__ bool conv_abort(const Smem& s, bool ok) {
   if (!ok) *s.abort_flag = 1;
   conv_sync();
   return *s.abort_flag != 0;
+}
+__device__ __forceinline__ bool epi_abort_now(const Smem& s, bool ok) {
+  if (!ok) *s.epi_abort = 1;
+  epi_sync();
+  return *s.epi_abort != 0;
 }
 
 struct TcBufs {
@@ -661,33 +701,44 @@ __global__ void __launch_bounds__(256) psgd_qimage_kernel(const float* __restric
 // pass 1 on the tensor cores: M = G + E (written over E) and P = M Q; the
 // last contributor of a row tile adds its partial rows and writes the
 // tile's Gram partial; the last row tile factors the Gram matrix.
+//
+// Each converter thread streams its own 16-byte pieces of G and E (four
+// operand rows, one 16-byte column chunk) through a ring of SS staging
+// slots with cp.async, SS - 1 units ahead, and reads back only its own
+// pieces (no barrier for the staging); it then writes hi(M) and lo(M) into
+// the swizzled operand stage the MMAs read, and M to global memory.  The
+// loader warp only copies the Q images (bulk copies).
 // ---------------------------------------------------------------------------
 template <int R, int SG>
 __global__ void __launch_bounds__(kThreads, 1) psgd_p_tc_kernel(
-    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmE,
-    float* __restrict__ E, int64_t m, int64_t n, TcBufs b) {
+    const float* __restrict__ G, float* __restrict__ E, int64_t m, int64_t n, TcBufs b) {
   using namespace sm100;
   constexpr int RG = kRows / SG;                  // matrix rows per tile
   constexpr int KU = SG * kKBlk;                  // matrix columns per unit
   constexpr int H = img_half(R, SG);              // image rows per half
   constexpr uint32_t kImg = 2 * H * kKBlk * 4;    // image bytes
-  constexpr int S = stages_p(R, SG);
+  constexpr int S = kOpStages, SS = kStgSlots;
+  constexpr int kPasses = kRows * 8 / kConv;      // operand rows per converter thread
   extern __shared__ unsigned char tc_smem[];
-  const Smem s = carve_smem(tc_smem, S, kImg);
+  const Smem s = carve_smem(tc_smem, S, kImg, SS);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int C = gridDim.x, cta = blockIdx.x;
   const int64_t RT = (m + RG - 1) / RG, KB = (n + KU - 1) / KU, U = RT * KB;
-  const int64_t u0 = unit_lo(cta, C, U), u1 = unit_lo(cta + 1, C, U);
+  const int64_t m_pad = (m + kPadRows - 1) / kPadRows * kPadRows;
+  const int64_t u0 = unit_lo(cta, C, U), u1 = unit_lo(cta + 1, C, U), nun = u1 - u0;
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&s.full[i], 1);
       mbar_init(&s.conv[i], kConv);
       mbar_init(&s.empty[i], 1);
     }
-    mbar_init(s.acc_full, 1);
-    mbar_init(s.acc_empty, kEpi);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.acc_full[i], 1);
+      mbar_init(&s.acc_empty[i], kEpi);
+    }
     mbar_init(s.drain, 1);
     *s.abort_flag = 0;
+    *s.epi_abort = 0;
     mbar_fence_init();
   }
   if (warp == kMmaWarp) {
@@ -703,30 +754,16 @@ __global__ void __launch_bounds__(kThreads, 1) psgd_p_tc_kernel(
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
-      tma_prefetch_map(&tmG);
-      tma_prefetch_map(&tmE);
       UnitCursor cur(u0, KB);
       Ring<S> ring;
-      for (int64_t i = 0; i < u1 - u0; ++i, cur.next(), ring.next()) {
+      for (int64_t i = 0; i < nun; ++i, cur.next(), ring.next()) {
         const int st = ring.st;
         if (i >= S && !mbar_wait(&s.empty[st], ring.ph ^ 1u, kWaitCycles)) {
           ok = false;
           break;
         }
-        const int64_t kb = cur.blk, rt = cur.tile;
-        mbar_arrive_expect_tx(&s.full[st], 2 * kTileBytes + kImg);
-        if (SG == 1) {
-          tma_load_2d(s.a_hi + st * kTileBytes, &tmG, (int32_t)(kb * kKBlk), (int32_t)(rt * RG),
-                      &s.full[st]);
-          tma_load_2d(s.a_lo + st * kTileBytes, &tmE, (int32_t)(kb * kKBlk), (int32_t)(rt * RG),
-                      &s.full[st]);
-        } else {
-          tma_load_3d(s.a_hi + st * kTileBytes, &tmG, 0, (int32_t)(kb * SG), (int32_t)(rt * RG),
-                      &s.full[st]);
-          tma_load_3d(s.a_lo + st * kTileBytes, &tmE, 0, (int32_t)(kb * SG), (int32_t)(rt * RG),
-                      &s.full[st]);
-        }
-        bulk_load_s(s.img + st * kImg, b.qimg + kb * (kImg / 4), kImg, &s.full[st]);
+        mbar_arrive_expect_tx(&s.full[st], kImg);
+        bulk_load_s(s.img + st * kImg, b.qimg + cur.blk * (kImg / 4), kImg, &s.full[st]);
         ++loads;
       }
     }
@@ -738,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1) psgd_p_tc_kernel(
       int seg = 0;
       UnitCursor cur(u0, KB);
       Ring<S> ring;
-      for (int64_t i = 0; i < u1 - u0; ++i, cur.next(), ring.next()) {
+      for (int64_t i = 0; i < nun; ++i, cur.next(), ring.next()) {
         const int st = ring.st;
         if (!mbar_wait(&s.conv[st], ring.ph, kWaitCycles) ||
             !mbar_wait(&s.full[st], ring.ph, kWaitCycles)) {
@@ -746,8 +783,11 @@ __global__ void __launch_bounds__(kThreads, 1) psgd_p_tc_kernel(
           break;
         }
         const bool first = i == 0 || cur.blk == 0;
-        if (first && seg > 0 &&
-            !mbar_wait(s.acc_empty, (uint32_t)((seg - 1) & 1), kWaitCycles)) {
+        // a segment accumulates into buffer seg & 1, free once the read-out
+        // of segment seg - 2 is done
+        const uint32_t d = tmem + (uint32_t)(seg & 1) * kAccCols;
+        if (first && seg >= 2 &&
+            !mbar_wait(&s.acc_empty[seg & 1], (uint32_t)(((seg - 2) >> 1) & 1), kWaitCycles)) {
           ok = false;
           break;
         }
@@ -760,40 +800,53 @@ __global__ void __launch_bounds__(kThreads, 1) psgd_p_tc_kernel(
           // operand rows of 128 bytes, 8-row groups 1024 bytes apart; a K = 8
           // step is 32 bytes along the rows
           const uint64_t db = smem_desc_sw128(im + kk * 32, 16, 1024);
-          mma_tf32(tmem, smem_desc_sw128(ah + kk * 32, 16, 1024), db, id1, acc);
-          mma_tf32(tmem + 2 * H, smem_desc_sw128(al + kk * 32, 16, 1024), db, id2, acc);
+          mma_tf32(d, smem_desc_sw128(ah + kk * 32, 16, 1024), db, id1, acc);
+          mma_tf32(d + 2 * H, smem_desc_sw128(al + kk * 32, 16, 1024), db, id2, acc);
         }
         mma_issued = true;
         mma_commit(&s.empty[st]);
-        if (cur.blk == KB - 1 || i == u1 - u0 - 1) {
-          mma_commit(s.acc_full);
+        if (cur.blk == KB - 1 || i == nun - 1) {
+          mma_commit(&s.acc_full[seg & 1]);
           ++seg;
         }
       }
     }
-  } else {
-    int seg = 0;
-    constexpr int kPasses = kRows * 8 / kConv;  // operand rows per thread
+  } else if (warp < kProducerWarp) {
     const uint32_t ch = lane & 7;
-    UnitCursor cur(u0, KB);
-    Ring<S> ring;
-    for (int64_t i = 0; i < u1 - u0; ++i, cur.next(), ring.next()) {
-      const int st = ring.st;
-      const bool got = mbar_wait(&s.full[st], ring.ph, kWaitCycles);
-      if (conv_abort(s, got)) { ok = false; break; }
-      const int64_t rt = cur.tile, kb = cur.blk;
-      const uint32_t ah = s.a_hi + st * kTileBytes, al = s.a_lo + st * kTileBytes;
-      // M = G + E; lanes 8q .. 8q + 7 cover one operand row (128 bytes, a
-      // segment of a matrix row; the warp's four rows are consecutive
-      // segments, 512 contiguous bytes).  Loads, then arithmetic, then stores.
-      float4 g[kPasses], e[kPasses];
-      uint32_t off[kPasses];
+    // staging slot q holds piece j (0..3: G of operand row p = j, 4..7: E)
+    // of thread t at stg + ((q * 8 + j) * kConv + t) * 16
+    auto stage_unit = [&](int64_t rt, int64_t kb, int q) {
 #pragma unroll
       for (int p = 0; p < kPasses; ++p) {
         const uint32_t a = p * (kConv / 8) + warp * 4 + (lane >> 3);
-        off[p] = sw128_offset(a, 4 * ch);
-        g[p] = lds128(ah + off[p]);
-        e[p] = lds128(al + off[p]);
+        const int64_t grow = rt * RG + a / SG;
+        const int64_t col = kb * KU + (a % SG) * kKBlk + 4 * ch;
+        const bool in = grow < m && col < n;  // n % 4 == 0: a chunk is in or out
+        const int64_t off = in ? grow * n + col : 0;
+        cp_async16_zfill(s.stg + ((q * 8 + p) * kConv + tid) * 16, G + off, in ? 16u : 0u);
+        cp_async16_zfill(s.stg + ((q * 8 + 4 + p) * kConv + tid) * 16, E + off, in ? 16u : 0u);
+      }
+      cp_async_commit();
+    };
+    UnitCursor icur(u0, KB);
+    for (int q = 0; q < SS - 1; ++q, icur.next()) {
+      if (q < nun) stage_unit(icur.tile, icur.blk, q);
+      else cp_async_commit();
+    }
+    UnitCursor cur(u0, KB);
+    Ring<S> ring;
+    int q = 0;  // staging slot of unit i
+    for (int64_t i = 0; i < nun; ++i, cur.next(), ring.next(), icur.next(), q = (q + 1) % SS) {
+      // unit i + SS - 1 goes into the slot unit i - 1 used
+      if (i + SS - 1 < nun) stage_unit(icur.tile, icur.blk, (q + SS - 1) % SS);
+      else cp_async_commit();
+      cp_async_wait<SS - 1>();  // this thread's pieces of unit i have landed
+      const int64_t rt = cur.tile, kb = cur.blk;
+      float4 g[kPasses], e[kPasses];
+#pragma unroll
+      for (int p = 0; p < kPasses; ++p) {
+        g[p] = lds128(s.stg + ((q * 8 + p) * kConv + tid) * 16);
+        e[p] = lds128(s.stg + ((q * 8 + 4 + p) * kConv + tid) * 16);
       }
       float4 hi[kPasses], lo[kPasses];
 #pragma unroll
@@ -804,11 +857,8 @@ __global__ void __launch_bounds__(kThreads, 1) psgd_p_tc_kernel(
         lo[p] = make_float4(g[p].x - hi[p].x, g[p].y - hi[p].y, g[p].z - hi[p].z,
                             g[p].w - hi[p].w);
       }
-#pragma unroll
-      for (int p = 0; p < kPasses; ++p) {
-        sts128(ah + off[p], hi[p]);
-        sts128(al + off[p], lo[p]);
-      }
+      // M to global memory: lanes 8q .. 8q + 7 write one 128-byte piece of a
+      // matrix row, the warp's four operand rows being consecutive pieces
 #pragma unroll
       for (int p = 0; p < kPasses; ++p) {
         const uint32_t a = p * (kConv / 8) + warp * 4 + (lane >> 3);
@@ -816,104 +866,139 @@ __global__ void __launch_bounds__(kThreads, 1) psgd_p_tc_kernel(
         const int64_t col = kb * KU + (a % SG) * kKBlk + 4 * ch;
         if (grow < m && col < n) *reinterpret_cast<float4*>(E + grow * n + col) = g[p];
       }
+      // the operand stage is free once the MMAs of unit i - S are done
+      const int st = ring.st;
+      const bool got = i < S || mbar_wait(&s.empty[st], ring.ph ^ 1u, kWaitCycles);
+      if (conv_abort(s, got)) { ok = false; break; }
+      const uint32_t ah = s.a_hi + st * kTileBytes, al = s.a_lo + st * kTileBytes;
+#pragma unroll
+      for (int p = 0; p < kPasses; ++p) {
+        const uint32_t a = p * (kConv / 8) + warp * 4 + (lane >> 3);
+        const uint32_t off = sw128_offset(a, 4 * ch);
+        sts128(ah + off, hi[p]);
+        sts128(al + off, lo[p]);
+      }
       fence_proxy_async_smem();
       mbar_arrive(&s.conv[st]);
-      if (cur.blk != KB - 1 && i != u1 - u0 - 1) continue;
-      // read-out of this CTA's partial P rows of row tile rt: lane (row,
-      // segment) keeps image rows s R .. s R + R - 1 of each product, the
-      // segments of a row are added by shuffles (fixed order)
-      const bool acc = mbar_wait(s.acc_full, (uint32_t)(seg & 1), kWaitCycles);
-      if (conv_abort(s, acc)) { ok = false; break; }
-      ++seg;
-      if (tid < kEpi) {
-        const uint32_t sgm = tid % SG, lo_col = sgm * R;
-        float prod[3][R];
+    }
+    cp_async_wait<0>();  // no copy of this thread may outlive the CTA
+  } else {
+    // read-out warps: warp w reads tensor-memory lanes 32 (w % 4) .. + 31,
+    // lane = operand row (row / SG of the tile, segment row % SG).  Per
+    // segment of this CTA (one per row tile it touches), in order: keep
+    // image rows s R .. s R + R - 1 of each product, add the segments of a
+    // row by shuffles (fixed order) and write the CTA's partial P rows.
+    const int e = tid - kEpiWarp0 * 32;
+    const uint32_t quarter = (uint32_t)warp & 3u, orow = quarter * 32 + lane;
+    const uint32_t sgm = orow % SG, lo_col = sgm * R;
+    // this CTA's Gram partial: the Gram matrices of the row tiles it
+    // finishes, added in tile order (entry e + kEpi j in gacc[j])
+    constexpr int kGE = (R * R + kEpi - 1) / kEpi;
+    double gacc[kGE];
 #pragma unroll
-        for (int x = 0; x < 3; ++x)
+    for (int j = 0; j < kGE; ++j) gacc[j] = 0.0;
+    const int64_t t_first = u0 / KB, t_last = nun > 0 ? (u1 - 1) / KB : t_first - 1;
+    int seg = 0;
+    for (int64_t rt = t_first; rt <= t_last; ++rt, ++seg) {
+      const uint32_t buf = (uint32_t)(seg & 1);
+      const bool got = mbar_wait(&s.acc_full[buf], (uint32_t)((seg >> 1) & 1), kWaitCycles);
+      if (epi_abort_now(s, got)) { ok = false; break; }
+      float prod[3][R];
 #pragma unroll
-          for (int c = 0; c < R; ++c) prod[x][c] = 0.0f;
-        tc_fence_after_sync();
-        const uint32_t base = tmem + ((uint32_t)(warp * 32) << 16);
+      for (int x = 0; x < 3; ++x)
 #pragma unroll
-        for (int x = 0; x < 3; ++x) {
+        for (int c = 0; c < R; ++c) prod[x][c] = 0.0f;
+      tc_fence_after_sync();
+      const uint32_t base = tmem + ((quarter * 32) << 16) + buf * kAccCols;
 #pragma unroll
-          for (int j = 0; j < H / 16; ++j) {
-            float v[16];
-            tmem_ld16(base + x * H + 16 * j, v);
+      for (int x = 0; x < 3; ++x) {
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              const uint32_t col = 16 * j + q;
+        for (int j = 0; j < H / 16; ++j) {
+          float v[16];
+          tmem_ld16(base + x * H + 16 * j, v);
 #pragma unroll
-              for (int c = 0; c < R; ++c)
-                if (col == lo_col + c) prod[x][c] = v[q];
-            }
+          for (int q = 0; q < 16; ++q) {
+            const uint32_t col = 16 * j + q;
+#pragma unroll
+            for (int c = 0; c < R; ++c)
+              if (col == lo_col + c) prod[x][c] = v[q];
           }
         }
-        tc_fence_before_sync();
-        mbar_arrive(s.acc_empty);
-        float v[R];
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&s.acc_empty[buf]);
+      float v[R];
 #pragma unroll
-        for (int c = 0; c < R; ++c) {
-          float t = (prod[0][c] + prod[1][c]) + prod[2][c];
+      for (int c = 0; c < R; ++c) {
+        float t = (prod[0][c] + prod[1][c]) + prod[2][c];
 #pragma unroll
-          for (int o = SG / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-          v[c] = t;
-        }
-        if (sgm == 0) {
-          float* dst = b.part + ((int64_t)(cta + rt) * RG + tid / SG) * R;
+        for (int o = SG / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        v[c] = t;
+      }
+      if (sgm == 0) {
+        float* dst = b.part + ((int64_t)(cta + rt) * RG + orow / SG) * R;
 #pragma unroll
-          for (int c = 0; c < R; ++c) dst[c] = v[c];
-        }
+        for (int c = 0; c < R; ++c) dst[c] = v[c];
       }
       __threadfence();
-      conv_sync();
+      epi_sync();
       const int c_first = unit_owner(rt * KB, C, U), c_last = unit_owner(rt * KB + KB - 1, C, U);
-      if (tid == 0)
+      if (e == 0)
         *s.last1 = atomicAdd(&b.rt_tickets[rt], 1u) == (uint32_t)(c_last - c_first);
-      conv_sync();
+      epi_sync();
       if (!*s.last1) continue;
       __threadfence();
-      // the row tile's P rows: partials added in CTA order
-      if (tid < RG) {
-        const int64_t grow = rt * RG + tid;
+      // the row tile's P rows: partials added in CTA order (loads issued in
+      // batches, the additions in order)
+      if (e < RG) {
+        const int64_t grow = rt * RG + e;
+        constexpr int kB = R <= 4 ? 8 : R <= 8 ? 4 : 2;
         float pr[R];
 #pragma unroll
         for (int c = 0; c < R; ++c) pr[c] = 0.0f;
-        for (int cc = c_first; cc <= c_last; ++cc) {
-          const float* src = b.part + ((int64_t)(cc + rt) * RG + tid) * R;
+        for (int c0 = c_first; c0 <= c_last; c0 += kB) {
+          float v[kB][R];
 #pragma unroll
-          for (int c = 0; c < R; ++c) pr[c] += __ldcg(src + c);
+          for (int j = 0; j < kB; ++j) {
+            const float* src = b.part + ((int64_t)(c0 + j + rt) * RG + e) * R;
+#pragma unroll
+            for (int c = 0; c < R; ++c) v[j][c] = c0 + j <= c_last ? __ldcg(src + c) : 0.0f;
+          }
+#pragma unroll
+          for (int j = 0; j < kB; ++j)
+            if (c0 + j <= c_last) {
+#pragma unroll
+              for (int c = 0; c < R; ++c) pr[c] += v[j][c];
+            }
         }
+        // rows m .. m_pad - 1 of the padded P are zero
 #pragma unroll
         for (int c = 0; c < R; ++c) {
-          s.rows[tid * 16 + c] = grow < m ? pr[c] : 0.0f;
-          if (grow < m) b.praw[grow * R + c] = pr[c];
+          s.rows[e * 16 + c] = grow < m ? pr[c] : 0.0f;
+          if (grow < m_pad) b.praw[grow * R + c] = grow < m ? pr[c] : 0.0f;
         }
       }
-      if (tid == 0) b.rt_tickets[rt] = 0u;
-      conv_sync();
-      for (int t = tid; t < R * R; t += kConv) {
-        const int a = t / R, c = t % R;
-        double acc2 = 0.0;
-        for (int r = 0; r < RG; ++r) acc2 += (double)s.rows[r * 16 + a] * (double)s.rows[r * 16 + c];
-        b.gram_part[rt * R * R + t] = acc2;
+      if (e == 0) b.rt_tickets[rt] = 0u;
+      epi_sync();
+      // the tile's Gram matrix (fp64) into this CTA's partial
+#pragma unroll
+      for (int j = 0; j < kGE; ++j) {
+        const int t = e + j * kEpi;
+        if (t < R * R) {
+          const int a = t / R, c = t % R;
+          double acc2 = 0.0;
+          for (int r = 0; r < RG; ++r)
+            acc2 += (double)s.rows[r * 16 + a] * (double)s.rows[r * 16 + c];
+          gacc[j] += acc2;
+        }
       }
-      __threadfence();
-      conv_sync();
-      if (tid == 0) *s.last2 = atomicAdd(&b.state->ticket_mq, 1u) == (uint32_t)(RT - 1);
-      conv_sync();
-      if (!*s.last2) continue;
-      __threadfence();
-      for (int t = tid; t < R * R; t += kConv) {
-        double acc2 = 0.0;
-        for (int64_t r = 0; r < RT; ++r) acc2 += __ldcg(&b.gram_part[r * R * R + t]);
-        s.gram[t] = acc2;
-      }
-      conv_sync();
-      if (tid == 0) {
-        cholesky_inverse<R>(s.gram, b.w);
-        b.state->ticket_mq = 0u;
-      }
+    }
+    // every CTA writes its partial (zero if it finished no tile); pass 2
+    // adds them in CTA order
+#pragma unroll
+    for (int j = 0; j < kGE; ++j) {
+      const int t = e + j * kEpi;
+      if (t < R * R) b.gram_part[(int64_t)cta * R * R + t] = gacc[j];
     }
   }
   // end: the loader waits for its copies still in flight, the MMA issuer
@@ -937,43 +1022,17 @@ __global__ void __launch_bounds__(kThreads, 1) psgd_p_tc_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// P_hat = P W for every row (written to P_out and to a copy padded with zero
-// rows to a multiple of 8, which pass 3 copies in whole blocks).
-// ---------------------------------------------------------------------------
-template <int R>
-__global__ void __launch_bounds__(256) psgd_phat_kernel(const float* __restrict__ praw,
-                                                        const float* __restrict__ W, int64_t m,
-                                                        int64_t m_pad, float* __restrict__ P_out,
-                                                        float* __restrict__ phat) {
-  __shared__ float w[R * R];
-  for (int t = threadIdx.x; t < R * R; t += blockDim.x) w[t] = W[t];
-  __syncthreads();
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= m_pad) return;
-  float pr[R];
-#pragma unroll
-  for (int a = 0; a < R; ++a) pr[a] = i < m ? praw[i * R + a] : 0.0f;
-#pragma unroll
-  for (int c = 0; c < R; ++c) {
-    float acc = 0.0f;
-#pragma unroll
-    for (int a = 0; a <= c; ++a) acc = fmaf(pr[a], w[a * R + c], acc);
-    phat[i * R + c] = acc;
-    if (i < m) P_out[i * R + c] = acc;
-  }
-}
-
-// ---------------------------------------------------------------------------
 // pass 3: E' = M - P_hat Q'^T, fp32 FMAs on the CUDA cores (r products per
-// element).  The matrix streams in units of 8 rows x 512 columns (2 KB
-// contiguous per row, two TMA boxes of 8 x 256 without swizzle) together
-// with the unit's 8 rows of P_hat; units run column block by column block,
+// element).  The matrix streams in units of 16 rows x 512 columns (2 KB
+// contiguous per row, two TMA boxes of 16 x 256 without swizzle) together
+// with the unit's 16 rows of P_hat; units run column block by column block,
 // so a thread keeps the Q' rows of its four columns in registers for as
 // long as its CTA stays in one column block.
 // ---------------------------------------------------------------------------
-constexpr int kRGRows = 8;            // rows per unit
+constexpr int kRGRows = 16;           // rows per unit
+constexpr int kRGPer = kRGRows / 4;   // rows per thread (4 row phases)
 constexpr int kRGCols = 512;          // columns per unit
-constexpr uint32_t kRGTile = kRGRows * kRGCols * 4;  // 16 KB
+constexpr uint32_t kRGTile = kRGRows * kRGCols * 4;  // 32 KB
 
 template <int R>
 __global__ void __launch_bounds__(kResidThreads, 1) psgd_resid_tma_kernel(
@@ -1030,7 +1089,7 @@ __global__ void __launch_bounds__(kResidThreads, 1) psgd_resid_tma_kernel(
           ok = false;
     }
   } else {
-    // thread t: column chunk t % 128 (four columns), rows t / 128 and t / 128 + 4
+    // thread t: column chunk t % 128 (four columns), rows t / 128 + 4 h
     const uint32_t chunk = tid & 127, r0 = tid >> 7;
     int64_t cur_cb = -1;
     float qv[4][R];
@@ -1060,18 +1119,18 @@ __global__ void __launch_bounds__(kResidThreads, 1) psgd_resid_tma_kernel(
       const uint32_t ps = t + kRGTile;
       // box (chunk / 64) holds columns 256 (chunk / 64) ..; rows 1 KB apart
       const uint32_t cofs = (chunk >> 6) * (kRGTile / 2) + (chunk & 63) * 16;
-      float4 mv[2];
-      float pr[2][R];
+      float4 mv[kRGPer];
+      float pr[kRGPer][R];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < kRGPer; ++h) {
         const uint32_t row = r0 + 4 * h;
         mv[h] = lds128(t + cofs + row * 1024);
 #pragma unroll
         for (int c = 0; c < R; ++c) pr[h][c] = lds32(ps + (row * R + c) * 4);
       }
-      float4 out[2];
+      float4 out[kRGPer];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < kRGPer; ++h) {
         float x[4] = {mv[h].x, mv[h].y, mv[h].z, mv[h].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -1088,7 +1147,7 @@ __global__ void __launch_bounds__(kResidThreads, 1) psgd_resid_tma_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < kRGPer; ++h) {
         const int64_t grow = rg * kRGRows + r0 + 4 * h;
         if (grow < m && col < n) *reinterpret_cast<float4*>(E + grow * n + col) = out[h];
       }
@@ -1106,31 +1165,37 @@ __global__ void __launch_bounds__(kResidThreads, 1) psgd_resid_tma_kernel(
 // as zero), and transposing every tile through shared memory, plus one
 // M = 128 MMA per 4 KB of M, held a tensor-core version of this pass near a
 // third of the memory bandwidth.  Here M streams exactly as in pass 3 (units
-// of 8 rows x 512 columns, column block by column block, with the unit's
+// of 16 rows x 512 columns, column block by column block, with the unit's
 // rows of P_hat), and each thread keeps the sums of four columns in
 // registers while its CTA stays in one column block.  Thread t holds
-// columns 4 (t / 4) .. + 3 of rows t % 4 and t % 4 + 4 of each unit; at the
+// columns 4 (t / 4) .. + 3 of rows t % 4 + 4 h of each unit; at the
 // end of a column block the four row phases are added by shuffles (fixed
 // order), each CTA writes its partial Q' of the block to slot CTA + block,
 // and the block's last contributor adds the slots in CTA order.
 // ---------------------------------------------------------------------------
 template <int R>
-__global__ void __launch_bounds__(kResidThreads, 1) psgd_qstream_kernel(
-    const __grid_constant__ CUtensorMap tmM, int64_t m, int64_t n, const float* __restrict__ phat,
-    float* __restrict__ Q_out, float* __restrict__ part, uint32_t* __restrict__ tickets,
-    uint32_t* status) {
+__global__ void __launch_bounds__(kQThreads, 1) psgd_qstream_kernel(
+    const __grid_constant__ CUtensorMap tmM, int64_t m, int64_t n, const float* __restrict__ pp,
+    const double* __restrict__ gram_part, int64_t gram_parts, float* __restrict__ P_out,
+    float* __restrict__ phat, float* __restrict__ w_out, float* __restrict__ Q_out,
+    float* __restrict__ part, uint32_t* __restrict__ tickets, uint32_t* status) {
   using namespace sm100;
   constexpr int S = kStagesR;
   constexpr uint32_t kPBytes = kRGRows * R * 4;
   constexpr uint32_t kStageBytes = kRGTile + ((kPBytes + 127) / 128) * 128;
   constexpr int kLoader = kResidConv / 32;
+  constexpr int R2 = R * R;
   extern __shared__ unsigned char tc_smem[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(tc_smem) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)S * kStageBytes);
   uint64_t* empty = full + S;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
+  uint64_t* wbar = empty + S;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(wbar + 1);
   volatile int* last = abort_flag + 1;
+  double* sg = reinterpret_cast<double*>(wbar + 2);  // [threads per entry][R2] partial Gram sums
+  double* sgram = sg + kGramSlots;                    // [R2]
+  float* sw = reinterpret_cast<float*>(sgram + 256);  // [R2] W
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int C = gridDim.x, cta = blockIdx.x;
   const int64_t RG = (m + kRGRows - 1) / kRGRows, CB = (n + kRGCols - 1) / kRGCols, U = RG * CB;
@@ -1140,13 +1205,66 @@ __global__ void __launch_bounds__(kResidThreads, 1) psgd_qstream_kernel(
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kResidConv / 32);
     }
+    mbar_init(wbar, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
   __syncthreads();
   bool ok = true;
   int64_t loads = 0;
-  if (warp == kLoader) {
+  if (warp > kLoader) {
+    // W = U^-1, U the Cholesky factor of P^T P, from the pass-1 Gram
+    // partials (one per pass-1 CTA, added in the same fixed order in every
+    // CTA), while the other warps
+    // stream M; then this CTA's slice of P_hat = P W.
+    const int wt = tid - (kLoader + 1) * 32;
+    constexpr int HS = R2 >= kWThreads ? 1 : kWThreads / R2;  // threads per Gram entry
+    for (int j = wt; j < R2 * HS; j += kWThreads) {
+      const int t = j % R2, h = j / R2;
+      double acc2 = 0.0;
+      int64_t r = h;
+      for (; r + 7 * HS < gram_parts; r += 8 * HS) {
+        double v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = __ldcg(&gram_part[(r + q * HS) * R2 + t]);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc2 += v[q];
+      }
+      for (; r < gram_parts; r += HS) acc2 += __ldcg(&gram_part[r * R2 + t]);
+      sg[h * R2 + t] = acc2;
+    }
+    w_sync();
+    for (int t = wt; t < R2; t += kWThreads) {
+      double a = 0.0;
+      for (int h = 0; h < HS; ++h) a += sg[h * R2 + t];
+      sgram[t] = a;
+    }
+    w_sync();
+    if (wt < 32) {
+      cholesky_inverse_warp<R>(sgram, sg, sw, lane);  // (sg is free again: rinv)
+      if (lane == 0) {
+        if (cta == 0)
+          for (int t = 0; t < R2; ++t) w_out[t] = sw[t];
+        mbar_arrive(wbar);  // release: W in shared memory for the column-block ends
+      }
+    }
+    w_sync();
+    const int64_t m_pad = RG * kRGRows;
+    const int64_t ra = m_pad * cta / C, rb = m_pad * (cta + 1) / C;
+    for (int64_t row = ra + wt; row < rb; row += kWThreads) {
+      float pr[R];
+#pragma unroll
+      for (int a = 0; a < R; ++a) pr[a] = pp[row * R + a];
+#pragma unroll
+      for (int c = 0; c < R; ++c) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int a = 0; a <= c; ++a) acc = fmaf(pr[a], sw[a * R + c], acc);
+        phat[row * R + c] = acc;
+        if (row < m) P_out[row * R + c] = acc;
+      }
+    }
+  } else if (warp == kLoader) {
     if (lane == 0) {
       tma_prefetch_map(&tmM);
       UnitCursor cur(u0, RG);
@@ -1163,7 +1281,7 @@ __global__ void __launch_bounds__(kResidThreads, 1) psgd_qstream_kernel(
         tma_load_2d(stage, &tmM, (int32_t)(cb * kRGCols), (int32_t)(rg * kRGRows), &full[st]);
         tma_load_2d(stage + kRGTile / 2, &tmM, (int32_t)(cb * kRGCols + kRGCols / 2),
                     (int32_t)(rg * kRGRows), &full[st]);
-        bulk_load(stage + kRGTile, phat + rg * kRGRows * R, kPBytes, &full[st]);
+        bulk_load(stage + kRGTile, pp + rg * kRGRows * R, kPBytes, &full[st]);
         ++loads;
       }
       for (int64_t j = std::max<int64_t>(0, loads - S); j < loads; ++j)
@@ -1194,28 +1312,26 @@ __global__ void __launch_bounds__(kResidThreads, 1) psgd_qstream_kernel(
       }
       const uint32_t t = smem_u32(base + (size_t)st * kStageBytes);
       const uint32_t ps = t + kRGTile;
-      float4 mv[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-      float pr[2][R];
+      // rows one after the other (ranks above 8 keep one row's P in
+      // registers at a time)
+      constexpr int kHU = R <= 8 ? kRGPer : 1;
+#pragma unroll kHU
+      for (int h = 0; h < kRGPer; ++h) {
+        const uint32_t row = r0 + 4 * h;
+        float4 mv = make_float4(0.f, 0.f, 0.f, 0.f);
+        float pr[R];
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+        for (int c = 0; c < R; ++c) pr[c] = 0.0f;
+        if (!skip) {
+          mv = lds128(t + cofs + row * 1024);
 #pragma unroll
-        for (int c = 0; c < R; ++c) pr[h][c] = 0.0f;
-      if (!skip) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t row = r0 + 4 * h;
-          mv[h] = lds128(t + cofs + row * 1024);
-#pragma unroll
-          for (int c = 0; c < R; ++c) pr[h][c] = lds32(ps + (row * R + c) * 4);
+          for (int c = 0; c < R; ++c) pr[c] = lds32(ps + (row * R + c) * 4);
         }
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float x[4] = {mv[h].x, mv[h].y, mv[h].z, mv[h].w};
+        const float x[4] = {mv.x, mv.y, mv.z, mv.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q)
 #pragma unroll
-          for (int c = 0; c < R; ++c) acc[q][c] = fmaf(x[q], pr[h][c], acc[q][c]);
+          for (int c = 0; c < R; ++c) acc[q][c] = fmaf(x[q], pr[c], acc[q][c]);
       }
       if (!skip) {
         // the stage can be refilled once every warp has read it: each lane's
@@ -1253,19 +1369,39 @@ __global__ void __launch_bounds__(kResidThreads, 1) psgd_qstream_kernel(
       resid_sync();
       if (!*last) continue;
       __threadfence();
-      // the block's columns: slots added in CTA order
+      // the block's columns: slots added in CTA order (loads issued in
+      // batches, the additions in order), then Q' = (M^T P) W
       const int64_t col = cb * kRGCols + tid;
+      float q[R];
+#pragma unroll
+      for (int c = 0; c < R; ++c) q[c] = 0.0f;
       if (col < n) {
-        float q[R];
+        constexpr int kB = R <= 4 ? 8 : R <= 8 ? 4 : 2;
+        for (int c0 = c_first; c0 <= c_last; c0 += kB) {
+          float v[kB][R];
 #pragma unroll
-        for (int c = 0; c < R; ++c) q[c] = 0.0f;
-        for (int cc = c_first; cc <= c_last; ++cc) {
-          const float* src = part + ((int64_t)(cc + cb) * kRGCols + tid) * R;
+          for (int j = 0; j < kB; ++j) {
+            const float* src = part + ((int64_t)(c0 + j + cb) * kRGCols + tid) * R;
 #pragma unroll
-          for (int c = 0; c < R; ++c) q[c] += __ldcg(src + c);
+            for (int c = 0; c < R; ++c) v[j][c] = c0 + j <= c_last ? __ldcg(src + c) : 0.0f;
+          }
+#pragma unroll
+          for (int j = 0; j < kB; ++j)
+            if (c0 + j <= c_last) {
+#pragma unroll
+              for (int c = 0; c < R; ++c) q[c] += v[j][c];
+            }
         }
+      }
+      if (!mbar_wait(wbar, 0u, kWaitCycles)) ok = false;
+      if (col < n) {
 #pragma unroll
-        for (int c = 0; c < R; ++c) Q_out[col * R + c] = q[c];
+        for (int c = 0; c < R; ++c) {
+          float acc = 0.0f;
+#pragma unroll
+          for (int a = 0; a <= c; ++a) acc = fmaf(q[a], sw[a * R + c], acc);
+          Q_out[col * R + c] = acc;
+        }
       }
       if (tid == 0) tickets[cb] = 0u;
     }
@@ -1278,6 +1414,11 @@ template <int R>
 __host__ constexpr size_t resid_smem_bytes() {
   return 1024 + (size_t)kStagesR * (kRGTile + ((kRGRows * R * 4 + 127) / 128) * 128) +
          (size_t)2 * kStagesR * 8 + 16;
+}
+// pass 2 adds W's barrier, the Gram partial sums, the Gram matrix and W
+template <int R>
+__host__ constexpr size_t qstream_smem_bytes() {
+  return resid_smem_bytes<R>() + 16 + (size_t)(kGramSlots + 256) * 8 + 256 * 4;
 }
 
 }  // namespace tcp
@@ -1317,24 +1458,8 @@ bool make_map(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, u
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The same matrix (cols a multiple of 32) seen as 32 columns x cols / 32
-// segments x rows, read in boxes of 32 x sg x rg with the 128-byte swizzle:
-// box row (r, s) is segment s of matrix row r, 128 bytes.
-bool make_map_segments(CUtensorMap* map, const float* base, int64_t rows, int64_t cols,
-                       uint32_t sg, uint32_t rg) {
-  const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_tiled_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {32, (cuuint64_t)(cols / 32), (cuuint64_t)rows};
-  const cuuint64_t strides[2] = {128, (cuuint64_t)cols * 4};
-  const cuuint32_t box[3] = {32, sg, rg};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Bytes of the tensor-core path's data area for matrices up to max_m x
-// max_n: pass 1 partials and Q images, pass 2 partials, P_hat padded.
+// max_n: pass 1 partials and Q images, pass 2 partials, P and P_hat padded.
 int64_t tc_area_bytes(int64_t max_m, int64_t max_n, int max_r, int num_sms) {
   auto up = [](int64_t b) { return (b + 255) / 256 * 256; };
   return up((int64_t)sizeof(float) * ((int64_t)num_sms * tcp::kRows + max_m + tcp::kRows) *
@@ -1342,7 +1467,7 @@ int64_t tc_area_bytes(int64_t max_m, int64_t max_n, int max_r, int num_sms) {
          up(round_up(max_n, 512) * 128 + 16384) +
          up((int64_t)sizeof(float) * (num_sms + ceil_div(max_n, tcp::kRGCols)) * tcp::kRGCols *
             max_r) +
-         up((int64_t)sizeof(float) * round_up(max_m, tcp::kRGRows) * max_r);
+         2 * up((int64_t)sizeof(float) * round_up(max_m, tcp::kPadRows) * max_r);
 }
 
 // Pass 0 and pass 1 with SG segments per operand tile.
@@ -1351,14 +1476,8 @@ gc_status launch_pass1(gc_ctx* ctx, const float* grad, float* err, int64_t m, in
                        const float* Q, const tcp::TcBufs& b) {
   constexpr int RG = tcp::kRows / SG, KU = SG * tcp::kKBlk, H = tcp::img_half(R, SG);
   constexpr uint32_t kImg = 2 * H * tcp::kKBlk * 4;
-  CUtensorMap tm_g, tm_e;
-  const bool maps = SG == 1 ? make_map(&tm_g, grad, m, n, tcp::kKBlk, RG, true) &&
-                                  make_map(&tm_e, err, m, n, tcp::kKBlk, RG, true)
-                            : make_map_segments(&tm_g, grad, m, n, SG, RG) &&
-                                  make_map_segments(&tm_e, err, m, n, SG, RG);
-  if (!maps) return GC_ERR_CUDA;
   const int64_t KB = ceil_div(n, KU), U = ceil_div(m, RG) * KB;
-  const size_t smem = tcp::smem_bytes_p(tcp::stages_p(R, SG), kImg);
+  const size_t smem = tcp::smem_bytes_p(tcp::kOpStages, kImg, tcp::kStgSlots);
   if (cudaFuncSetAttribute(tcp::psgd_p_tc_kernel<R, SG>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return GC_ERR_CUDA;
@@ -1371,8 +1490,7 @@ gc_status launch_pass1(gc_ctx* ctx, const float* grad, float* err, int64_t m, in
   {
     LaunchScope L(ctx, GC_PHASE_PSGD_MQ);
     const int c1 = (int)std::min<int64_t>(ctx->num_sms, U);
-    tcp::psgd_p_tc_kernel<R, SG><<<c1, tcp::kThreads, smem, ctx->stream>>>(tm_g, tm_e, err, m, n,
-                                                                             b);
+    tcp::psgd_p_tc_kernel<R, SG><<<c1, tcp::kThreads, smem, ctx->stream>>>(grad, err, m, n, b);
   }
   return GC_OK;
 }
@@ -1384,7 +1502,6 @@ gc_status run_psgd_tc(gc_ctx* ctx, const float* grad, float* err, int64_t m, int
   const PsgdWorkspace& pw = ctx->psgd;
   auto up = [](int64_t v) { return (v + 255) / 256 * 256; };
   tcp::TcBufs b;
-  b.praw = pb.praw;
   b.part = reinterpret_cast<float*>(area);
   area += up((int64_t)sizeof(float) * ((int64_t)ctx->num_sms * tcp::kRows + pw.max_m + tcp::kRows) *
              pw.max_r);
@@ -1393,40 +1510,41 @@ gc_status run_psgd_tc(gc_ctx* ctx, const float* grad, float* err, int64_t m, int
   float* qpart = reinterpret_cast<float*>(area);
   area += up((int64_t)sizeof(float) * (ctx->num_sms + ceil_div(pw.max_n, tcp::kRGCols)) *
              tcp::kRGCols * pw.max_r);
-  float* phat = reinterpret_cast<float*>(area);  // P_hat, rows padded to a multiple of 8
+  const int64_t pad_bytes = up((int64_t)sizeof(float) * round_up(pw.max_m, tcp::kPadRows) * pw.max_r);
+  b.praw = reinterpret_cast<float*>(area);  // P, rows padded with zeros to a multiple of 16
+  area += pad_bytes;
+  float* phat = reinterpret_cast<float*>(area);  // P_hat, padded the same way
   b.rt_tickets = pb.rb_tickets;
   b.gram_part = pb.gram_part;
   b.w = pb.w;
   b.state = pb.state;
   b.status = pb.status;
 
-  // pass 1: segment tiles when the rows split into 32-column segments
-  const gc_status st1 = n % 32 == 0
-                            ? launch_pass1<R, tcp::segs_for(R)>(ctx, grad, err, m, n, Q_inout, b)
-                            : launch_pass1<R, 1>(ctx, grad, err, m, n, Q_inout, b);
+  const gc_status st1 = launch_pass1<R, tcp::segs_for(R)>(ctx, grad, err, m, n, Q_inout, b);
   if (st1 != GC_OK) return st1;
 
-  // P_hat = P W; passes 2 and 3 stream M in units of 8 rows x 512 columns
+  // passes 2 and 3 stream M in units of 16 rows x 512 columns; pass 2 also
+  // forms W and P_hat = P W
   CUtensorMap tm_r;
   if (!make_map(&tm_r, err, m, n, tcp::kRGCols / 2, tcp::kRGRows, false)) return GC_ERR_CUDA;
   const int64_t m_pad = round_up(m, tcp::kRGRows);
   const int c3 = (int)std::min<int64_t>(ctx->num_sms,
                                         (m_pad / tcp::kRGRows) * ceil_div(n, tcp::kRGCols));
-  const size_t sm3 = tcp::resid_smem_bytes<R>();
+  const size_t sm2 = tcp::qstream_smem_bytes<R>(), sm3 = tcp::resid_smem_bytes<R>();
   if (cudaFuncSetAttribute(tcp::psgd_qstream_kernel<R>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3) != cudaSuccess ||
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2) != cudaSuccess ||
       cudaFuncSetAttribute(tcp::psgd_resid_tma_kernel<R>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3) != cudaSuccess)
     return GC_ERR_CUDA;
   {
-    LaunchScope L(ctx, GC_PHASE_PSGD_THIN);
-    tcp::psgd_phat_kernel<R><<<(unsigned)ceil_div(m_pad, 256), 256, 0, s>>>(b.praw, b.w, m, m_pad,
-                                                                           P_out, phat);
-  }
-  {
     LaunchScope L(ctx, GC_PHASE_PSGD_MTP);
-    tcp::psgd_qstream_kernel<R><<<c3, tcp::kResidThreads, sm3, s>>>(tm_r, m, n, phat, Q_inout,
-                                                                      qpart, pb.tickets, b.status);
+    // one Gram partial per pass-1 CTA
+    const int64_t gram_parts = std::min<int64_t>(
+        ctx->num_sms,
+        ceil_div(m, tcp::kRows / tcp::segs_for(R)) * ceil_div(n, tcp::segs_for(R) * tcp::kKBlk));
+    tcp::psgd_qstream_kernel<R><<<c3, tcp::kQThreads, sm2, s>>>(
+        tm_r, m, n, b.praw, b.gram_part, gram_parts, P_out, phat, b.w, Q_inout, qpart, pb.tickets,
+        b.status);
   }
   {
     LaunchScope L(ctx, GC_PHASE_PSGD_RESID);
@@ -1434,6 +1552,12 @@ gc_status run_psgd_tc(gc_ctx* ctx, const float* grad, float* err, int64_t m, int
                                                                         Q_inout, b.status);
   }
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+}
+
+// Gram partials the workspace holds: the CUDA-core path writes one per
+// block of 8 rows, the tensor-core path one per pass-1 CTA (at most one per SM).
+int64_t gram_parts_cap(int64_t max_m, int num_sms) {
+  return std::max<int64_t>(ceil_div(max_m, 8), num_sms);
 }
 
 template <int R, bool VEC>
@@ -1451,10 +1575,12 @@ gc_status run_psgd(gc_ctx* ctx, const float* grad, float* err, int64_t m, int64_
   b.state = static_cast<PsgdState*>(take(sizeof(PsgdState)));
   b.w = static_cast<float*>(take(sizeof(float) * 16 * 16));
   b.tickets = static_cast<uint32_t*>(take(sizeof(uint32_t) * ceil_div(pw.max_n, kStrip)));
-  // (row tickets and Gram partials: one per 8 rows covers both paths)
+  // (row tickets: one per 8 rows covers both paths; Gram partials: one per
+  // 8 rows or per SM, whichever is more)
   b.rb_tickets = static_cast<uint32_t*>(take(sizeof(uint32_t) * ceil_div(pw.max_m, 8)));
   b.praw = static_cast<float*>(take(sizeof(float) * pw.max_m * pw.max_r));
-  b.gram_part = static_cast<double*>(take(sizeof(double) * ceil_div(pw.max_m, 8) * pw.max_r * pw.max_r));
+  b.gram_part = static_cast<double*>(
+      take(sizeof(double) * gram_parts_cap(pw.max_m, ctx->num_sms) * pw.max_r * pw.max_r));
   b.status = ctx->ws.status;
   if constexpr (VEC) {
     // rows start on 16-byte boundaries: the tensor-core path
@@ -1519,7 +1645,7 @@ int64_t psgd_workspace_bytes(int64_t max_m, int64_t max_n, int max_r, int num_sm
                          up(sizeof(uint32_t) * ceil_div(max_n, kStrip)) +
                          up(sizeof(uint32_t) * ceil_div(max_m, 8)) +
                          up(sizeof(float) * max_m * max_r) +
-                         up(sizeof(double) * ceil_div(max_m, 8) * max_r * max_r);
+                         up(sizeof(double) * gram_parts_cap(max_m, num_sms) * max_r * max_r);
   // CUDA-core path: partial rows of P per column range, then the q
   // partials (splits * n * r floats with splits * strips <= 4 * SMs + strips)
   const int64_t cuda_core = up(sizeof(float) * kMaxColSplits * max_m * max_r) +

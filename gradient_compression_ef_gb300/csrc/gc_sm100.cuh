@@ -129,6 +129,15 @@ __device__ __forceinline__ void bulk_load_s(uint32_t dst, const void* src, uint3
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (cp.async, cached in L2 only)
+// of `src_bytes` (16, or 0 to fill the destination with zeros without
+// reading), completed by the issuing thread's cp.async.wait_group.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
 // Shared-memory loads and stores on 32-bit shared addresses (explicit
 // shared-space instructions: a generic pointer whose address space the
 // compiler cannot prove would go through the global load/store path).

@@ -115,3 +115,20 @@ def test_repeatable_and_close_to_fp32(env, shape):
     o_approx = oP.astype(np.float64) @ oQ.astype(np.float64).T
     assert rel(approx, o_approx) <= 2e-5
     assert rel(En, oE) <= 2e-5 * max(1.0, np.linalg.norm(o_approx) / np.linalg.norm(oE))
+
+
+@pytest.mark.parametrize("m,n,r", [(16, 100_000, 4), (40, 60_000, 16)])
+def test_short_wide_matrix_in_a_tight_context(env, m, n, r):
+    """Few rows and many columns, with the scratch reserved for exactly this
+    shape: pass 1 then runs on more CTAs (one per SM) than the matrix has
+    blocks of 8 rows, and each of them writes a Gram partial."""
+    torch, gc, _ = env
+    M, _ = inputs.low_rank_matrix(m, n, r=min(r, 4))
+    rg = np.random.default_rng(m * n + r)
+    Q = rg.standard_normal((n, r)).astype(np.float32)
+    c = gc.Context(16)
+    c.reserve_powersgd(m, n, r)
+    try:
+        run_steps((torch, gc, c), M, np.zeros_like(M), Q, r, 2)
+    finally:
+        c.close()
