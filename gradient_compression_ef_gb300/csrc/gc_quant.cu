@@ -40,7 +40,10 @@ QuantPlan quant_plan(int64_t n, int64_t group) {
     p.chunk = p.G;
     p.chunks_per_group = 1;
   } else {
-    int64_t target = ceil_div(p.G, 8192);
+    // at most about 4096 chunks per group: enough warps for the statistics
+    // pass, few partials for the combine (chunk sizes stay powers of two,
+    // so the QSGD summation tree is the same for any of them)
+    int64_t target = ceil_div(p.G, 4096);
     int64_t c = 1024;
     while (c < target) c <<= 1;
     p.chunk = c;
@@ -541,22 +544,30 @@ __global__ void __launch_bounds__(kQThreads) quant_combine_kernel(
     float mn = INFINITY, mx = -INFINITY, amax = 0.0f, ss = 0.0f;
     if (MODE == GC_QSGD) {
       if (warp == 0) {
+        // eight rows of 32 partials loaded at a time, pushed in order
         TreeAcc tree;
         tree.init();
-        for (int64_t b = first; b < last; b += 32) {
-          const float s = b + lane < last ? partials[b + lane].w : 0.0f;
-          tree.push(warp_sum_tree(s, 32));
+        for (int64_t b = first; b < last; b += 8 * 32) {
+          float sv[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int64_t i = b + u * 32 + lane;
+            sv[u] = i < last ? partials[i].w : 0.0f;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if (b + u * 32 < last) tree.push(warp_sum_tree(sv[u], 32));
         }
         ss = tree.finish();
       }
     } else {
       int64_t b = first + threadIdx.x;
-      for (; b + 3 * kQThreads < last; b += 4 * kQThreads) {
-        float4 p[4];
+      for (; b + 7 * kQThreads < last; b += 8 * kQThreads) {
+        float4 p[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) p[u] = partials[b + u * kQThreads];
+        for (int u = 0; u < 8; ++u) p[u] = partials[b + u * kQThreads];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 8; ++u) {
           mn = fminf(mn, p[u].x);
           mx = fmaxf(mx, p[u].y);
           amax = fmaxf(amax, p[u].z);
@@ -622,6 +633,18 @@ __global__ void __launch_bounds__(kQThreads) quant_apply_kernel(
   const int64_t warp_id = ((int64_t)blockIdx.x * kQThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kQThreads) >> 5;
   zero_padding(o);
+  // one group of all n: its parameters once, not per element
+  const bool one_group = G >= n;
+  float scale1 = 0.0f, offset1 = 0.0f;
+  if (one_group) {
+    if (MODE == GC_MINMAX) {
+      const float2 p = reinterpret_cast<const float2*>(o.scales)[0];
+      scale1 = p.x;
+      offset1 = p.y;
+    } else {
+      scale1 = o.scales[0];
+    }
+  }
   for (int64_t base = warp_id * 128; base < n; base += nwarps * 128) {
     const int64_t i0 = base + 4 * lane;
     const bool active = i0 < n;
@@ -651,14 +674,16 @@ __global__ void __launch_bounds__(kQThreads) quant_apply_kernel(
       neg[j] = false;
       r[j] = 0.0f;
       if (valid[j]) {
-        const int64_t g = group_of(j);
-        float scale, offset = 0.0f;
-        if (MODE == GC_MINMAX) {
-          const float2 p = reinterpret_cast<const float2*>(o.scales)[g];
-          scale = p.x;
-          offset = p.y;
-        } else {
-          scale = o.scales[g];
+        float scale = scale1, offset = offset1;
+        if (!one_group) {
+          const int64_t g = group_of(j);
+          if (MODE == GC_MINMAX) {
+            const float2 p = reinterpret_cast<const float2*>(o.scales)[g];
+            scale = p.x;
+            offset = p.y;
+          } else {
+            scale = o.scales[g];
+          }
         }
         float gh;
         q[j] = quantize_one<MODE>(c[j], scale, offset, stochastic != 0, u[j], top, &neg[j], &gh);
