@@ -10,13 +10,16 @@
 //
 // Rank w's indices are strictly increasing, so no two of its entries touch
 // the same element and the rank order is the only order that matters.  The
-// output is cut into ranges of kAggRange elements, one block each:
-//   bounds     : for every rank, the first entry of each range (four entry
+// output is cut into ranges of kAggRange elements, one warp each:
+//   bounds     : for every rank, the first entry of each range (sixteen entry
 //                boundaries per thread; each range is written exactly once).
-//   accumulate : a block gathers the entries of its range, rank by rank, in
-//                chunks into shared memory (all loads of a chunk in flight at
-//                once), adds them to its shared accumulator in rank order
-//                (a barrier between ranks) and writes its range once.
+//   accumulate : a warp takes the ranks 32 at a time, gathers their entries
+//                of its range in chunks into its own shared-memory slots (all
+//                loads of a chunk in flight at once), adds them to its own
+//                accumulator rank by rank (__syncwarp between ranks) and
+//                writes its range once.  Warps share nothing, so no block
+//                barrier holds a range back and each SM keeps about forty
+//                ranges in flight.
 #include <algorithm>
 
 #include "gc_internal.cuh"
@@ -24,11 +27,12 @@
 namespace gc {
 namespace {
 
-constexpr int kAggShift = 13;
-constexpr int kAggRange = 1 << kAggShift;   // output elements per block
-constexpr int kAggThreads = 256;
-constexpr int kAggSlots = 2048;             // gathered entries per chunk
-constexpr int kAggGather = 4;               // entries per thread per gathering round
+constexpr int kAggShift = 10;
+constexpr int kAggRange = 1 << kAggShift;   // output elements per warp
+constexpr int kAggWarps = 8;                // warps (ranges) per block
+constexpr int kAggThreads = 32 * kAggWarps;
+constexpr int kAggSlots = 128;              // gathered entries per chunk of a warp
+constexpr int kAggGather = kAggSlots / 32;  // entries per lane per chunk
 constexpr int kAggMaxRanks = 1024;
 
 // Per-rank stride of the index and value arrays: k rounded up to 4 entries,
@@ -86,18 +90,18 @@ __global__ void __launch_bounds__(256) agg_bounds_kernel(const int32_t* __restri
   }
 }
 
-// Shared memory of a block: the accumulator of its range, one gathered
-// chunk, and two int32[W + 1] arrays sized by the launch (rank w's entries of
-// this range are [first[w], first[w] + pre[w+1] - pre[w])).
-struct AggSmem {
+// Shared memory of one warp: the accumulator of its range, one gathered
+// chunk, and for the current group of 32 ranks their first entries of the
+// range and the offsets of their entries in the warp's flat list.  Aligned
+// to 16 bytes: every warp's accumulator is read and written as float4.
+struct __align__(16) AggWarpSmem {
   float acc[kAggRange];
   float val[kAggSlots];
   uint16_t loc[kAggSlots];
+  int32_t first[32];
+  int32_t pre[33];
 };
-
-__host__ __device__ inline size_t agg_smem_bytes(int W) {
-  return sizeof(AggSmem) + 2 * sizeof(int32_t) * (size_t)(W + 1);
-}
+static_assert(sizeof(AggWarpSmem) % 16 == 0, "float4 access to each warp's accumulator");
 
 // Value of entry j of rank w: val[w*K + j] (K = k rounded up to 4), or for QSGD codes
 // +-fl(q * scale) with rank w's codes at w * cb and scales at w * sf (sf a
@@ -118,73 +122,78 @@ __device__ __forceinline__ float agg_value(const float* __restrict__ val,
 }
 
 template <int BITS>
-__global__ void __launch_bounds__(kAggThreads) agg_accumulate_kernel(
+__global__ void __launch_bounds__(kAggThreads, 5) agg_accumulate_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ val,
     const uint8_t* __restrict__ codes, const float* __restrict__ scales, int W, int64_t k,
     int64_t cb, int64_t mag, int64_t sf, int64_t G, int64_t n, int64_t nblk,
     const int32_t* __restrict__ start, float* __restrict__ out, uint32_t* __restrict__ status) {
-  extern __shared__ __align__(16) unsigned char agg_smem_raw[];
-  AggSmem& sm = *reinterpret_cast<AggSmem*>(agg_smem_raw);
-  int32_t* first = reinterpret_cast<int32_t*>(agg_smem_raw + sizeof(AggSmem));
-  int32_t* pre = first + (W + 1);
-  const int64_t b = blockIdx.x;
+  __shared__ AggWarpSmem warps[kAggWarps];
+  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+  const int64_t b = (int64_t)blockIdx.x * kAggWarps + wi;
+  if (b >= nblk) return;  // (no block barrier follows)
+  AggWarpSmem& sm = warps[wi];
   const int64_t a = b << kAggShift;
   const int len = (int)std::min<int64_t>(kAggRange, n - a);
-  for (int i = threadIdx.x; i < kAggRange / 4; i += kAggThreads)
-    reinterpret_cast<float4*>(sm.acc)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  for (int w = threadIdx.x; w < W; w += kAggThreads) {
-    // clamped to [0, k): bounds from invalid (flagged) indices stay in range
-    const int32_t* sw = start + (int64_t)w * (nblk + 1);
-    const int64_t f = std::min<int64_t>(std::max<int32_t>(sw[b], 0), k);
-    const int64_t l = std::min<int64_t>(std::max<int32_t>(sw[b + 1], 0), k);
-    first[w] = (int32_t)f;
-    // a range holds at most kAggRange entries of one rank (distinct indices)
-    pre[w] = (int32_t)std::min<int64_t>(l > f ? l - f : 0, kAggRange);  // scanned below
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int32_t run = 0;
-    for (int w = 0; w < W; ++w) {
-      const int32_t c = pre[w];
-      pre[w] = run;
-      run += c;
+#pragma unroll
+  for (int q = 0; q < kAggRange / 128; ++q)
+    reinterpret_cast<float4*>(sm.acc)[q * 32 + lane] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (int r0 = 0; r0 < W; r0 += 32) {
+    const int nr = min(32, W - r0);
+    // this group's ranks: first entry and count in the range (clamped to
+    // [0, k): bounds from invalid, flagged indices stay in range; a range
+    // holds at most kAggRange entries of one rank), then the offsets of
+    // their entries in the warp's flat list (a scan across the lanes)
+    int32_t f = 0, cnt = 0;
+    if (lane < nr) {
+      const int32_t* sw = start + (int64_t)(r0 + lane) * (nblk + 1);
+      const int64_t f64 = std::min<int64_t>(std::max<int32_t>(sw[b], 0), k);
+      const int64_t l64 = std::min<int64_t>(std::max<int32_t>(sw[b + 1], 0), k);
+      f = (int32_t)f64;
+      cnt = (int32_t)std::min<int64_t>(l64 > f64 ? l64 - f64 : 0, kAggRange);
     }
-    pre[W] = run;
-  }
-  __syncthreads();
-  const int32_t total = pre[W];
-  // chunks of the block's entries in rank-major order
-  for (int32_t c0 = 0; c0 < total; c0 += kAggSlots) {
-    const int32_t c1 = min(c0 + kAggSlots, total);
-    for (int32_t e0 = c0 + threadIdx.x; e0 < c1; e0 += kAggThreads * kAggGather) {
-      // rank and entry of each of this thread's flat entries, then all their
+    int32_t incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int32_t total = __shfl_sync(0xffffffffu, incl, 31);
+    __syncwarp();  // the previous group's reads of first / pre are done
+    sm.first[lane] = f;
+    sm.pre[lane] = incl - cnt;
+    if (lane == 31) sm.pre[32] = incl;
+    __syncwarp();
+    for (int32_t c0 = 0; c0 < total; c0 += kAggSlots) {
+      const int32_t c1 = min(c0 + kAggSlots, total);
+      // rank and entry of each of this lane's flat entries, then all their
       // global loads, then the shared-memory stores
       int wq[kAggGather];
       int64_t jq[kAggGather];
 #pragma unroll
       for (int u = 0; u < kAggGather; ++u) {
-        const int32_t e = e0 + u * kAggThreads;
-        int lo = 0, hi = W - 1;  // the last rank w with pre[w] <= e
+        const int32_t e = c0 + u * 32 + lane;
+        int lo = 0, hi = nr - 1;  // the last rank r of the group with pre[r] <= e
         while (lo < hi) {
           const int mid = (lo + hi + 1) >> 1;
-          if (pre[mid] <= e) lo = mid;
+          if (sm.pre[mid] <= e) lo = mid;
           else hi = mid - 1;
         }
-        wq[u] = lo;
-        jq[u] = (int64_t)first[lo] + (e - pre[lo]);
+        wq[u] = r0 + lo;
+        jq[u] = (int64_t)sm.first[lo] + (e - sm.pre[lo]);
       }
       int32_t iq[kAggGather];
       float vq[kAggGather];
 #pragma unroll
       for (int u = 0; u < kAggGather; ++u) {
-        if (e0 + u * kAggThreads < c1) {
+        if (c0 + u * 32 + lane < c1) {
           iq[u] = idx[(int64_t)wq[u] * round_up4(k) + jq[u]];
           vq[u] = agg_value<BITS>(val, codes, scales, k, cb, mag, sf, G, wq[u], jq[u]);
         }
       }
+      __syncwarp();  // the previous chunk's adds are done with the slots
 #pragma unroll
       for (int u = 0; u < kAggGather; ++u) {
-        const int32_t e = e0 + u * kAggThreads;
+        const int32_t e = c0 + u * 32 + lane;
         if (e < c1) {
           const int64_t i = (int64_t)iq[u] - a;
           const bool ok = i >= 0 && i < len;
@@ -193,27 +202,28 @@ __global__ void __launch_bounds__(kAggThreads) agg_accumulate_kernel(
           sm.val[e - c0] = vq[u];
         }
       }
-    }
-    __syncthreads();
-    // rank by rank: within a rank the locations are distinct
-    int w0 = 0;
-    while (w0 < W && pre[w0 + 1] <= c0) ++w0;
-    for (int w = w0; w < W && pre[w] < c1; ++w) {
-      const int32_t e0 = max(pre[w], c0), e1 = min(pre[w + 1], c1);
-      for (int32_t e = e0 + threadIdx.x; e < e1; e += kAggThreads) {
-        const uint16_t l = sm.loc[e - c0];
-        if (l != 0xffffu) sm.acc[l] = __fadd_rn(sm.acc[l], sm.val[e - c0]);
+      __syncwarp();
+      // rank by rank: within a rank the locations are distinct
+      for (int r = 0; r < nr; ++r) {
+        const int32_t e0 = max(sm.pre[r], c0), e1 = min(sm.pre[r + 1], c1);
+        if (e0 >= e1) continue;
+        for (int32_t e = e0 + lane; e < e1; e += 32) {
+          const uint16_t l = sm.loc[e - c0];
+          if (l != 0xffffu) sm.acc[l] = __fadd_rn(sm.acc[l], sm.val[e - c0]);
+        }
+        __syncwarp();
       }
-      __syncthreads();
     }
   }
-  __syncthreads();
+  __syncwarp();
   float* o = out + a;
   if (len == kAggRange) {
-    for (int i = threadIdx.x; i < kAggRange / 4; i += kAggThreads)
-      reinterpret_cast<float4*>(o)[i] = reinterpret_cast<const float4*>(sm.acc)[i];
+#pragma unroll
+    for (int q = 0; q < kAggRange / 128; ++q)
+      reinterpret_cast<float4*>(o)[q * 32 + lane] =
+          reinterpret_cast<const float4*>(sm.acc)[q * 32 + lane];
   } else {
-    for (int i = threadIdx.x; i < len; i += kAggThreads) o[i] = sm.acc[i];
+    for (int i = lane; i < len; i += 32) o[i] = sm.acc[i];
   }
 }
 
@@ -223,7 +233,7 @@ gc_status run_accumulate(gc_ctx* ctx, const int32_t* idx, const float* val, cons
                          int64_t sf, int64_t G, int64_t n, int64_t nblk, const int32_t* start,
                          float* out) {
   LaunchScope L(ctx, GC_PHASE_AGG_ACCUMULATE);
-  agg_accumulate_kernel<BITS><<<(unsigned)nblk, kAggThreads, agg_smem_bytes(W), ctx->stream>>>(
+  agg_accumulate_kernel<BITS><<<(unsigned)ceil_div(nblk, kAggWarps), kAggThreads, 0, ctx->stream>>>(
       idx, val, codes, scales, W, k, cb, mag, sf, G, n, nblk, start, out, ctx->ws.status);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
@@ -231,13 +241,14 @@ gc_status run_accumulate(gc_ctx* ctx, const int32_t* idx, const float* val, cons
 }  // namespace
 
 gc_status prepare_aggregate_kernels() {
-  const int bytes = (int)agg_smem_bytes(kAggMaxRanks);
+  // static shared memory only; prefer the largest carve-out so that five
+  // blocks (forty ranges) fit on an SM
   const bool ok =
-      cudaFuncSetAttribute(agg_accumulate_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
-      cudaFuncSetAttribute(agg_accumulate_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
-      cudaFuncSetAttribute(agg_accumulate_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
-      cudaFuncSetAttribute(agg_accumulate_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
-      cudaFuncSetAttribute(agg_accumulate_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+      cudaFuncSetAttribute(agg_accumulate_kernel<0>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess &&
+      cudaFuncSetAttribute(agg_accumulate_kernel<1>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess &&
+      cudaFuncSetAttribute(agg_accumulate_kernel<2>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess &&
+      cudaFuncSetAttribute(agg_accumulate_kernel<4>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess &&
+      cudaFuncSetAttribute(agg_accumulate_kernel<8>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
   return ok ? GC_OK : GC_ERR_CUDA;
 }
 

@@ -497,10 +497,10 @@ __global__ void __launch_bounds__(kPThreads) psgd_residual_kernel(
 // buffer), so the converters never wait for a read-out: with one buffer
 // and the read-out done by the converters, the pipeline drained at every
 // segment end and the pass ran at about half the bandwidth on matrices of
-// 4096 columns.  Every wait is bounded; the converters and the read-out
-// warps each take their abort decisions together (a flag per group behind
-// the group's named barrier), so no barrier is left waiting for a thread
-// that gave up.
+// 4096 columns.  Every wait is bounded.  A converter warp gives up as one
+// (a vote) and the converters share no barrier; the read-out warps take
+// each abort decision together (a flag behind their named barrier), so no
+// barrier is left waiting for a thread that gave up.
 //
 // Passes 2 (Q' = M^T P_hat) and 3 (E' = M - P_hat Q'^T) stream M on the
 // CUDA cores; see their kernels.
@@ -571,10 +571,6 @@ struct Ring {
   }
 };
 
-// Barrier of the converter warps only (the loader and MMA warps run on).
-__device__ __forceinline__ void conv_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConv) : "memory");
-}
 // Barrier of the read-out warps only.
 __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync 2, %0;" ::"n"(kEpi) : "memory");
@@ -598,7 +594,6 @@ struct Smem {
   uint64_t* acc_empty;  // [2]
   uint64_t* drain;
   uint32_t* tmem_slot;
-  volatile int* abort_flag;  // the converters' abort decision
   volatile int* epi_abort;   // the read-out warps' abort decision
   int* last1;
   int* last2;
@@ -631,7 +626,6 @@ __device__ __forceinline__ Smem carve_smem(unsigned char* raw, int S, uint32_t i
   p += (size_t)(3 * S + 5) * 8;
   s.tmem_slot = reinterpret_cast<uint32_t*>(p);
   s.epi_abort = reinterpret_cast<volatile int*>(p + 8);
-  s.abort_flag = reinterpret_cast<volatile int*>(p + 16);
   s.last1 = reinterpret_cast<int*>(p + 32);
   s.last2 = reinterpret_cast<int*>(p + 48);
   p += 64;
@@ -640,14 +634,8 @@ __device__ __forceinline__ Smem carve_smem(unsigned char* raw, int S, uint32_t i
   return s;
 }
 
-// A group's common abort decision (converters, read-out warps; each group
-// has its own flag): any thread that saw a wait run out raises the flag,
-// all read it after the group's named barrier.
-__device__ __forceinline__ bool conv_abort(const Smem& s, bool ok) {
-  if (!ok) *s.abort_flag = 1;
-  conv_sync();
-  return *s.abort_flag != 0;
-}
+// The read-out warps' common abort decision: any thread that saw a wait run
+// out raises the flag, all read it after the group's named barrier.
 __device__ __forceinline__ bool epi_abort_now(const Smem& s, bool ok) {
   if (!ok) *s.epi_abort = 1;
   epi_sync();
@@ -737,7 +725,6 @@ __global__ void __launch_bounds__(kThreads, 1) psgd_p_tc_kernel(
       mbar_init(&s.acc_empty[i], kEpi);
     }
     mbar_init(s.drain, 1);
-    *s.abort_flag = 0;
     *s.epi_abort = 0;
     mbar_fence_init();
   }
@@ -866,10 +853,12 @@ __global__ void __launch_bounds__(kThreads, 1) psgd_p_tc_kernel(
         const int64_t col = kb * KU + (a % SG) * kKBlk + 4 * ch;
         if (grow < m && col < n) *reinterpret_cast<float4*>(E + grow * n + col) = g[p];
       }
-      // the operand stage is free once the MMAs of unit i - S are done
+      // the operand stage is free once the MMAs of unit i - S are done (a
+      // warp gives up as one; no barrier of the converters follows, and the
+      // other warps' own waits run out in turn)
       const int st = ring.st;
       const bool got = i < S || mbar_wait(&s.empty[st], ring.ph ^ 1u, kWaitCycles);
-      if (conv_abort(s, got)) { ok = false; break; }
+      if (__any_sync(0xffffffffu, !got)) { ok = false; break; }
       const uint32_t ah = s.a_hi + st * kTileBytes, al = s.a_lo + st * kTileBytes;
 #pragma unroll
       for (int p = 0; p < kPasses; ++p) {

@@ -48,7 +48,7 @@ def run_plain(env, idx, val, W, k, n):
 
 @pytest.mark.parametrize("W,k,n", [(1, 100, 1000), (3, 5000, 30001), (8, 2000, 8192),
                                    (8, 9000, 100_003), (16, 300, 7), (2, 0, 5000),
-                                   (5, 1, 1)])
+                                   (5, 1, 1), (40, 700, 50_000), (33, 4000, 4096)])
 def test_random_ranks(env, W, k, n):
     k = min(k, n)
     r = np.random.default_rng(W * 31 + k)
