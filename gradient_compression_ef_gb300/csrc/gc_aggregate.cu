@@ -105,19 +105,24 @@ static_assert(sizeof(AggWarpSmem) % 16 == 0, "float4 access to each warp's accum
 
 // Value of entry j of rank w: val[w*K + j] (K = k rounded up to 4), or for QSGD codes
 // +-fl(q * scale) with rank w's codes at w * cb and scales at w * sf (sf a
-// multiple of 4).
+// multiple of 4).  Entries and groups fit 32 bits (indices are int32, so
+// k < 2^31); the group of entry j is j >> gshift for a power-of-two group
+// (gshift >= 0), else j / G.
 template <int BITS>
 __device__ __forceinline__ float agg_value(const float* __restrict__ val,
                                            const uint8_t* __restrict__ codes,
                                            const float* __restrict__ scales, int64_t k,
-                                           int64_t cb, int64_t mag, int64_t sf, int64_t G,
-                                           int w, int64_t j) {
+                                           int64_t cb, int64_t mag, int64_t sf, uint32_t G,
+                                           int gshift, int w, uint32_t j) {
   if (BITS == 0) return val[(int64_t)w * round_up4(k) + j];
   const uint8_t* cw = codes + (int64_t)w * cb;
-  const int64_t bit = j * BITS;
-  const uint32_t q = (uint32_t)(cw[bit >> 3] >> (bit & 7)) & ((1u << BITS) - 1u);
+  constexpr int kPerByte = (BITS >= 8 || BITS == 0) ? 1 : 8 / BITS;  // codes per byte
+  constexpr int kByteShift = BITS == 8 ? 0 : BITS == 4 ? 1 : BITS == 2 ? 2 : 3;
+  const uint32_t q = (uint32_t)(cw[j >> kByteShift] >> ((j & (kPerByte - 1)) * BITS)) &
+                     ((1u << BITS) - 1u);
   const bool neg = (cw[mag + (j >> 3)] >> (j & 7)) & 1u;
-  const float m = __fmul_rn((float)q, scales[(int64_t)w * sf + j / G]);
+  const uint32_t g = gshift >= 0 ? j >> gshift : j / G;
+  const float m = __fmul_rn((float)q, scales[(int64_t)w * sf + g]);
   return neg ? -m : m;
 }
 
@@ -125,7 +130,7 @@ template <int BITS>
 __global__ void __launch_bounds__(kAggThreads, 5) agg_accumulate_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ val,
     const uint8_t* __restrict__ codes, const float* __restrict__ scales, int W, int64_t k,
-    int64_t cb, int64_t mag, int64_t sf, int64_t G, int64_t n, int64_t nblk,
+    int64_t cb, int64_t mag, int64_t sf, uint32_t G, int gshift, int64_t n, int64_t nblk,
     const int32_t* __restrict__ start, float* __restrict__ out, uint32_t* __restrict__ status) {
   __shared__ AggWarpSmem warps[kAggWarps];
   const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
@@ -168,7 +173,7 @@ __global__ void __launch_bounds__(kAggThreads, 5) agg_accumulate_kernel(
       // rank and entry of each of this lane's flat entries, then all their
       // global loads, then the shared-memory stores
       int wq[kAggGather];
-      int64_t jq[kAggGather];
+      uint32_t jq[kAggGather];
 #pragma unroll
       for (int u = 0; u < kAggGather; ++u) {
         const int32_t e = c0 + u * 32 + lane;
@@ -179,7 +184,7 @@ __global__ void __launch_bounds__(kAggThreads, 5) agg_accumulate_kernel(
           else hi = mid - 1;
         }
         wq[u] = r0 + lo;
-        jq[u] = (int64_t)sm.first[lo] + (e - sm.pre[lo]);
+        jq[u] = (uint32_t)(sm.first[lo] + (e - sm.pre[lo]));
       }
       int32_t iq[kAggGather];
       float vq[kAggGather];
@@ -187,7 +192,7 @@ __global__ void __launch_bounds__(kAggThreads, 5) agg_accumulate_kernel(
       for (int u = 0; u < kAggGather; ++u) {
         if (c0 + u * 32 + lane < c1) {
           iq[u] = idx[(int64_t)wq[u] * round_up4(k) + jq[u]];
-          vq[u] = agg_value<BITS>(val, codes, scales, k, cb, mag, sf, G, wq[u], jq[u]);
+          vq[u] = agg_value<BITS>(val, codes, scales, k, cb, mag, sf, G, gshift, wq[u], jq[u]);
         }
       }
       __syncwarp();  // the previous chunk's adds are done with the slots
@@ -233,8 +238,13 @@ gc_status run_accumulate(gc_ctx* ctx, const int32_t* idx, const float* val, cons
                          int64_t sf, int64_t G, int64_t n, int64_t nblk, const int32_t* start,
                          float* out) {
   LaunchScope L(ctx, GC_PHASE_AGG_ACCUMULATE);
+  // k < 2^31 (int32 indices): G fits 32 bits once clamped to k
+  const uint32_t G32 = (uint32_t)std::min<int64_t>(std::max<int64_t>(G, 1), INT32_MAX);
+  int gshift = -1;
+  if ((G32 & (G32 - 1)) == 0)
+    for (gshift = 0; (1u << gshift) != G32; ++gshift) {}
   agg_accumulate_kernel<BITS><<<(unsigned)ceil_div(nblk, kAggWarps), kAggThreads, 0, ctx->stream>>>(
-      idx, val, codes, scales, W, k, cb, mag, sf, G, n, nblk, start, out, ctx->ws.status);
+      idx, val, codes, scales, W, k, cb, mag, sf, G32, gshift, n, nblk, start, out, ctx->ws.status);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
 

@@ -364,7 +364,15 @@ __device__ __forceinline__ uint32_t quantize_one(float c, float scale,
     const float t = (MODE == GC_MINMAX) ? __fdiv_rn(__fsub_rn(c, offset), scale)
                     : (MODE == GC_LOG)  ? __fdiv_rn(cw_logf(__fadd_rn(fabsf(c), 1.0f)), scale)
                                         : __fdiv_rn(fabsf(c), scale);
-    q = round_level(t, stochastic, u, top);
+    if (MODE == GC_TERN) {
+      // scale = max |c| of the group, so t is in [0, 1] (or NaN): the level
+      // round_level gives is [u < t] stochastically (floor(t) is 0, and
+      // u < 1 for t = 1) and [t > 1/2] to nearest (rint(1/2) = 0); NaN
+      // compares false, level 0, as there
+      q = stochastic ? (u < t ? 1u : 0u) : (t > 0.5f ? 1u : 0u);
+    } else {
+      q = round_level(t, stochastic, u, top);
+    }
   }
   float mag = __fmul_rn(level_to_float(q), scale);
   if (MODE == GC_LOG) mag = __fsub_rn(cw_expf(mag), 1.0f);
