@@ -578,9 +578,6 @@ __device__ __forceinline__ void epi_sync() {
 __device__ __forceinline__ void w_sync() {
   asm volatile("bar.sync 3, %0;" ::"n"(kWThreads) : "memory");
 }
-__device__ __forceinline__ void resid_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kResidConv) : "memory");
-}
 
 struct Smem {
   uint32_t a_hi;     // [S] operand tiles hi(M) (shared addresses)
@@ -1147,27 +1144,28 @@ __global__ void __launch_bounds__(kResidThreads, 1) psgd_resid_tma_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// pass 2: Q' = M^T P_hat, fp32 FMAs on the CUDA cores (r products per
-// element).  The tensor core cannot take this contraction's operand from M
+// pass 2: M^T P, fp32 FMAs on the CUDA cores (r products per element); the
+// final reduction and Q' = (M^T P) W follow in psgd_qfinal, W and P_hat are
+// formed here by two extra warps.  The tensor core cannot take this
+// contraction's operand from M
 // as it lies in memory: the sum runs over M's rows, so M would be the
 // transposed (MN-major) operand, which kind::tf32 does not accept (it reads
 // as zero), and transposing every tile through shared memory, plus one
 // M = 128 MMA per 4 KB of M, held a tensor-core version of this pass near a
 // third of the memory bandwidth.  Here M streams exactly as in pass 3 (units
 // of 16 rows x 512 columns, column block by column block, with the unit's
-// rows of P_hat), and each thread keeps the sums of four columns in
-// registers while its CTA stays in one column block.  Thread t holds
-// columns 4 (t / 4) .. + 3 of rows t % 4 + 4 h of each unit; at the
-// end of a column block the four row phases are added by shuffles (fixed
-// order), each CTA writes its partial Q' of the block to slot CTA + block,
-// and the block's last contributor adds the slots in CTA order.
+// rows of P), and each thread keeps the sums of four columns in registers
+// while its CTA stays in one column block.  Thread t holds columns
+// 4 (t / 4) .. + 3 of rows t % 4 + 4 h of each unit; at the end of a column
+// block the four row phases are added by shuffles (fixed order) and each
+// CTA writes its partial sums of the block to slot CTA + block.
 // ---------------------------------------------------------------------------
 template <int R>
 __global__ void __launch_bounds__(kQThreads, 1) psgd_qstream_kernel(
     const __grid_constant__ CUtensorMap tmM, int64_t m, int64_t n, const float* __restrict__ pp,
     const double* __restrict__ gram_part, int64_t gram_parts, float* __restrict__ P_out,
-    float* __restrict__ phat, float* __restrict__ w_out, float* __restrict__ Q_out,
-    float* __restrict__ part, uint32_t* __restrict__ tickets, uint32_t* status) {
+    float* __restrict__ phat, float* __restrict__ w_out, float* __restrict__ part,
+    uint32_t* status) {
   using namespace sm100;
   constexpr int S = kStagesR;
   constexpr uint32_t kPBytes = kRGRows * R * 4;
@@ -1179,9 +1177,8 @@ __global__ void __launch_bounds__(kQThreads, 1) psgd_qstream_kernel(
       (reinterpret_cast<uintptr_t>(tc_smem) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)S * kStageBytes);
   uint64_t* empty = full + S;
-  uint64_t* wbar = empty + S;
+  uint64_t* wbar = empty + S;  // (space kept: flags and the W work area follow)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(wbar + 1);
-  volatile int* last = abort_flag + 1;
   double* sg = reinterpret_cast<double*>(wbar + 2);  // [threads per entry][R2] partial Gram sums
   double* sgram = sg + kGramSlots;                    // [R2]
   float* sw = reinterpret_cast<float*>(sgram + 256);  // [R2] W
@@ -1194,7 +1191,6 @@ __global__ void __launch_bounds__(kQThreads, 1) psgd_qstream_kernel(
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kResidConv / 32);
     }
-    mbar_init(wbar, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -1231,11 +1227,8 @@ __global__ void __launch_bounds__(kQThreads, 1) psgd_qstream_kernel(
     w_sync();
     if (wt < 32) {
       cholesky_inverse_warp<R>(sgram, sg, sw, lane);  // (sg is free again: rinv)
-      if (lane == 0) {
-        if (cta == 0)
-          for (int t = 0; t < R2; ++t) w_out[t] = sw[t];
-        mbar_arrive(wbar);  // release: W in shared memory for the column-block ends
-      }
+      if (lane == 0 && cta == 0)
+        for (int t = 0; t < R2; ++t) w_out[t] = sw[t];  // for the Q' reduction
     }
     w_sync();
     const int64_t m_pad = RG * kRGRows;
@@ -1351,52 +1344,75 @@ __global__ void __launch_bounds__(kQThreads, 1) psgd_qstream_kernel(
       for (int q = 0; q < 4; ++q)
 #pragma unroll
         for (int c = 0; c < R; ++c) acc[q][c] = 0.0f;
-      __threadfence();
-      resid_sync();
-      const int c_first = unit_owner(cb * RG, C, U), c_last = unit_owner(cb * RG + RG - 1, C, U);
-      if (tid == 0) *last = atomicAdd(&tickets[cb], 1u) == (uint32_t)(c_last - c_first);
-      resid_sync();
-      if (!*last) continue;
-      __threadfence();
-      // the block's columns: slots added in CTA order (loads issued in
-      // batches, the additions in order), then Q' = (M^T P) W
-      const int64_t col = cb * kRGCols + tid;
-      float q[R];
-#pragma unroll
-      for (int c = 0; c < R; ++c) q[c] = 0.0f;
-      if (col < n) {
-        constexpr int kB = R <= 4 ? 8 : R <= 8 ? 4 : 2;
-        for (int c0 = c_first; c0 <= c_last; c0 += kB) {
-          float v[kB][R];
-#pragma unroll
-          for (int j = 0; j < kB; ++j) {
-            const float* src = part + ((int64_t)(c0 + j + cb) * kRGCols + tid) * R;
-#pragma unroll
-            for (int c = 0; c < R; ++c) v[j][c] = c0 + j <= c_last ? __ldcg(src + c) : 0.0f;
-          }
-#pragma unroll
-          for (int j = 0; j < kB; ++j)
-            if (c0 + j <= c_last) {
-#pragma unroll
-              for (int c = 0; c < R; ++c) q[c] += v[j][c];
-            }
-        }
-      }
-      if (!mbar_wait(wbar, 0u, kWaitCycles)) ok = false;
-      if (col < n) {
-#pragma unroll
-        for (int c = 0; c < R; ++c) {
-          float acc = 0.0f;
-#pragma unroll
-          for (int a = 0; a <= c; ++a) acc = fmaf(q[a], sw[a * R + c], acc);
-          Q_out[col * R + c] = acc;
-        }
-      }
-      if (tid == 0) tickets[cb] = 0u;
     }
   }
   if (!ok) atomicOr(status, kStatusWaitTimeout);
   __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Q' = (M^T P) W from pass 2's partial column sums (slot c + b holds CTA c's
+// sums over its rows of column block b).  Block (b, x) takes 64 columns of
+// column block b: four threads per column add every fourth of the block's
+// contributing slots in CTA order, the four sums are added in a fixed order
+// and W is applied.  As a grid of its own the reduction runs on every SM
+// at once; done by the last contributor of each block inside pass 2 it
+// formed a tail of about 9 us after the stream.
+// ---------------------------------------------------------------------------
+constexpr int kQFCols = 64;  // columns per block
+template <int R>
+__global__ void __launch_bounds__(256) psgd_qfinal_kernel(const float* __restrict__ part,
+                                                          int64_t m, int64_t n, int C,
+                                                          const float* __restrict__ W,
+                                                          float* __restrict__ Q_out) {
+  __shared__ float red[4][kQFCols][R];
+  __shared__ float w[R * R];
+  constexpr int kSub = kRGCols / kQFCols;
+  const int64_t RG = (m + kRGRows - 1) / kRGRows, CB = (n + kRGCols - 1) / kRGCols, U = RG * CB;
+  const int64_t cb = blockIdx.x / kSub;
+  const int cl = threadIdx.x % kQFCols, qt = threadIdx.x / kQFCols;
+  const int64_t lc = (int64_t)(blockIdx.x % kSub) * kQFCols + cl;  // column within the block
+  const int64_t col = cb * kRGCols + lc;
+  for (int t = threadIdx.x; t < R * R; t += blockDim.x) w[t] = W[t];
+  const int c_first = unit_owner(cb * RG, C, U), c_last = unit_owner(cb * RG + RG - 1, C, U);
+  float q[R];
+#pragma unroll
+  for (int c = 0; c < R; ++c) q[c] = 0.0f;
+  if (col < n) {
+    constexpr int kB = R <= 4 ? 8 : R <= 8 ? 4 : 2;
+    for (int c0 = c_first + qt; c0 <= c_last; c0 += 4 * kB) {
+      float v[kB][R];
+#pragma unroll
+      for (int j = 0; j < kB; ++j) {
+        const int cc = c0 + 4 * j;
+        const float* src = part + ((int64_t)(cc + cb) * kRGCols + lc) * R;
+#pragma unroll
+        for (int c = 0; c < R; ++c) v[j][c] = cc <= c_last ? __ldcg(src + c) : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < kB; ++j)
+        if (c0 + 4 * j <= c_last) {
+#pragma unroll
+          for (int c = 0; c < R; ++c) q[c] += v[j][c];
+        }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < R; ++c) red[qt][cl][c] = q[c];
+  __syncthreads();
+  if (qt == 0 && col < n) {
+    float t[R];
+#pragma unroll
+    for (int c = 0; c < R; ++c)
+      t[c] = ((red[0][cl][c] + red[1][cl][c]) + red[2][cl][c]) + red[3][cl][c];
+#pragma unroll
+    for (int c = 0; c < R; ++c) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int a = 0; a <= c; ++a) acc = fmaf(t[a], w[a * R + c], acc);
+      Q_out[col * R + c] = acc;
+    }
+  }
 }
 
 template <int R>
@@ -1532,8 +1548,12 @@ gc_status run_psgd_tc(gc_ctx* ctx, const float* grad, float* err, int64_t m, int
         ctx->num_sms,
         ceil_div(m, tcp::kRows / tcp::segs_for(R)) * ceil_div(n, tcp::segs_for(R) * tcp::kKBlk));
     tcp::psgd_qstream_kernel<R><<<c3, tcp::kQThreads, sm2, s>>>(
-        tm_r, m, n, b.praw, b.gram_part, gram_parts, P_out, phat, b.w, Q_inout, qpart, pb.tickets,
-        b.status);
+        tm_r, m, n, b.praw, b.gram_part, gram_parts, P_out, phat, b.w, qpart, b.status);
+  }
+  {
+    LaunchScope L(ctx, GC_PHASE_PSGD_THIN);
+    const int64_t blocks = ceil_div(n, tcp::kRGCols) * (tcp::kRGCols / tcp::kQFCols);
+    tcp::psgd_qfinal_kernel<R><<<(unsigned)blocks, 256, 0, s>>>(qpart, m, n, c3, b.w, Q_inout);
   }
   {
     LaunchScope L(ctx, GC_PHASE_PSGD_RESID);

@@ -159,7 +159,7 @@ typedef enum gc_phase {
   GC_PHASE_RANDK_WRITE = 21, /* random sparsification: ordered output */
   GC_PHASE_BK_DIAG = 22,     /* bucketed: per-bucket diagnostics */
   GC_PHASE_BK_FLUSH = 23,    /* bucketed: pending kept-entry residuals into e */
-  GC_PHASE_PSGD_THIN = 24,   /* PowerSGD: the thin operands (Q^T image, P_hat) */
+  GC_PHASE_PSGD_THIN = 24,   /* PowerSGD: Q images, the final reduction of Q' */
   GC_PHASE_COUNT = 25
 } gc_phase;
 
