@@ -525,7 +525,10 @@ class TernWorkload(_SimpleWorkload):
     """TernGrad with error feedback on the transformer layer set (--layers
     layers of 4 x 4096^2, 2 x 4096 x 11008, 11008 x 4096, 4096), one scale
     per tensor (max |c|), stochastic rounding: one gc_ef_quant call per
-    tensor, tensor t keyed by gc_bucket_seed(SEED, t)."""
+    tensor, tensor t keyed by gc_bucket_seed(SEED, t).  The tensors go round
+    robin to --streams contexts, each on its own CUDA stream, as layer-wise
+    compression would be issued: a tensor's statistics pass (memory-bound)
+    then overlaps another tensor's apply pass (issue-bound)."""
 
     SEED = 91
 
@@ -534,6 +537,11 @@ class TernWorkload(_SimpleWorkload):
         self.sizes = sizes
         self.n = sum(sizes)
         self._init_common(torch, gc, dev, max(sizes))
+        if args.streams > 1:
+            self.streams = [torch.cuda.Stream(device=dev) for _ in range(args.streams)]
+            self.ctxs = [self.ctxs[0]] + [gc.Context(max(sizes), stream=st)
+                                          for st in self.streams[1:]]
+            self.ctxs[0].set_stream(self.streams[0])
         self.starts = np.concatenate([[0], np.cumsum(sizes)]).tolist()
         self.grads = inputs.transformer_set_device(args.layers, args.distinct, dev, seed=seed)
         self.err = torch.zeros(self.n, dtype=torch.float32, device=dev)
@@ -547,13 +555,27 @@ class TernWorkload(_SimpleWorkload):
 
     def launch_step(self, t, grad=None, main=None, ctxs=None):
         main = self.main if main is None else main
-        ctx = self._ctx_on(main, ctxs)
         g = self.grads[t % len(self.grads)] if grad is None else grad
+        if ctxs is not None or len(self.ctxs) == 1:
+            ctxs = [self._ctx_on(main, ctxs)]
+            join = []
+        else:
+            # fork from main onto the contexts' streams, join back at the end
+            ctxs = self.ctxs
+            fork = self.torch.cuda.Event()
+            fork.record(main)
+            for c in ctxs:
+                c._stream_ref.wait_event(fork)
+            join = [c._stream_ref for c in ctxs]
         for w_, (a, b) in enumerate(zip(self.starts, self.starts[1:])):
-            self.gc.ef_quant(ctx, g[a:b], self.err[a:b], 2, 0, "tern", "stochastic",
-                             self.gc.bucket_seed(self.SEED, w_), t,
+            self.gc.ef_quant(ctxs[w_ % len(ctxs)], g[a:b], self.err[a:b], 2, 0, "tern",
+                             "stochastic", self.gc.bucket_seed(self.SEED, w_), t,
                              self.codes[self.coff[w_]:self.coff[w_ + 1]],
                              self.scales[4 * w_:4 * w_ + 4])
+        for st in join:
+            j = self.torch.cuda.Event()
+            j.record(st)
+            main.wait_event(j)
 
     def algorithmic_bytes(self):
         """Read g and e, write e' (12 B per element) and 2-bit codes; the
