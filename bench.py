@@ -457,6 +457,33 @@ class _SimpleWorkload:
             ctx.set_stream(main)
         return ctx
 
+    def _init_streams(self, count, make_ctx):
+        """count > 1: one context per CUDA stream, the first the common one,
+        the others made by make_ctx(stream)."""
+        if count <= 1:
+            return
+        self.streams = [self.torch.cuda.Stream(device=self.dev) for _ in range(count)]
+        self.ctxs = [self.ctxs[0]] + [make_ctx(st) for st in self.streams[1:]]
+        self.ctxs[0].set_stream(self.streams[0])
+
+    def _fork(self, main, ctxs):
+        """The contexts a step uses in turn and the streams to join back:
+        one context on `main` when given `ctxs` (the per-kernel timing) or
+        when there is only one, else every context, forked from `main`."""
+        if ctxs is not None or len(self.ctxs) == 1:
+            return [self._ctx_on(main, ctxs)], []
+        fork = self.torch.cuda.Event()
+        fork.record(main)
+        for c in self.ctxs:
+            c._stream_ref.wait_event(fork)
+        return self.ctxs, [c._stream_ref for c in self.ctxs]
+
+    def _join(self, main, streams):
+        for st in streams:
+            j = self.torch.cuda.Event()
+            j.record(st)
+            main.wait_event(j)
+
     def finish(self):
         return 0
 
@@ -537,11 +564,7 @@ class TernWorkload(_SimpleWorkload):
         self.sizes = sizes
         self.n = sum(sizes)
         self._init_common(torch, gc, dev, max(sizes))
-        if args.streams > 1:
-            self.streams = [torch.cuda.Stream(device=dev) for _ in range(args.streams)]
-            self.ctxs = [self.ctxs[0]] + [gc.Context(max(sizes), stream=st)
-                                          for st in self.streams[1:]]
-            self.ctxs[0].set_stream(self.streams[0])
+        self._init_streams(args.streams, lambda st: gc.Context(max(sizes), stream=st))
         self.starts = np.concatenate([[0], np.cumsum(sizes)]).tolist()
         self.grads = inputs.transformer_set_device(args.layers, args.distinct, dev, seed=seed)
         self.err = torch.zeros(self.n, dtype=torch.float32, device=dev)
@@ -556,26 +579,13 @@ class TernWorkload(_SimpleWorkload):
     def launch_step(self, t, grad=None, main=None, ctxs=None):
         main = self.main if main is None else main
         g = self.grads[t % len(self.grads)] if grad is None else grad
-        if ctxs is not None or len(self.ctxs) == 1:
-            ctxs = [self._ctx_on(main, ctxs)]
-            join = []
-        else:
-            # fork from main onto the contexts' streams, join back at the end
-            ctxs = self.ctxs
-            fork = self.torch.cuda.Event()
-            fork.record(main)
-            for c in ctxs:
-                c._stream_ref.wait_event(fork)
-            join = [c._stream_ref for c in ctxs]
+        ctxs, join = self._fork(main, ctxs)
         for w_, (a, b) in enumerate(zip(self.starts, self.starts[1:])):
             self.gc.ef_quant(ctxs[w_ % len(ctxs)], g[a:b], self.err[a:b], 2, 0, "tern",
                              "stochastic", self.gc.bucket_seed(self.SEED, w_), t,
                              self.codes[self.coff[w_]:self.coff[w_ + 1]],
                              self.scales[4 * w_:4 * w_ + 4])
-        for st in join:
-            j = self.torch.cuda.Event()
-            j.record(st)
-            main.wait_event(j)
+        self._join(main, join)
 
     def algorithmic_bytes(self):
         """Read g and e, write e' (12 B per element) and 2-bit codes; the
@@ -597,7 +607,10 @@ class PowerSGDWorkload(_SimpleWorkload):
     layers: --layers x {4096 x 4096, 4096 x 11008, 11008 x 4096} (96
     matrices for 32 layers), each a rank-16 signal plus N(0, 1e-4^2) noise
     with its own start Q: one gc_powersgd_step per matrix per step, every
-    matrix's Q carried from step to step."""
+    matrix's Q carried from step to step.  The matrices go round robin to
+    --streams contexts on their own CUDA streams (each with its own
+    PowerSGD scratch), so one matrix's short passes and kernel tails overlap
+    another's streaming passes."""
 
     R = 4
 
@@ -606,8 +619,14 @@ class PowerSGDWorkload(_SimpleWorkload):
         self.shapes = shapes
         self.n = sum(m * n_ for m, n_ in shapes)
         self._init_common(torch, gc, dev, 0)
-        self.ctxs[0].reserve_powersgd(max(m for m, _ in shapes), max(n_ for _, n_ in shapes),
-                                      self.R)
+        mm, mn = max(m for m, _ in shapes), max(n_ for _, n_ in shapes)
+
+        def make_ctx(st):
+            c = gc.Context(0, stream=st)
+            c.reserve_powersgd(mm, mn, self.R)
+            return c
+        self.ctxs[0].reserve_powersgd(mm, mn, self.R)
+        self._init_streams(args.streams, make_ctx)
         self.starts = np.concatenate([[0], np.cumsum([m * n_ for m, n_ in shapes])]).tolist()
         flat = torch.empty(self.n, dtype=torch.float32, device=dev)
         self.Q = []
@@ -625,12 +644,13 @@ class PowerSGDWorkload(_SimpleWorkload):
 
     def launch_step(self, t, grad=None, main=None, ctxs=None):
         main = self.main if main is None else main
-        ctx = self._ctx_on(main, ctxs)
         g = self.grads[t % len(self.grads)] if grad is None else grad
+        ctxs, join = self._fork(main, ctxs)
         for i, (m, n_) in enumerate(self.shapes):
             a, b = self.starts[i], self.starts[i + 1]
-            self.gc.powersgd_step(ctx, g[a:b], self.err[a:b], m, n_, self.R, self.P[i],
-                                  self.Q[i])
+            self.gc.powersgd_step(ctxs[i % len(ctxs)], g[a:b], self.err[a:b], m, n_, self.R,
+                                  self.P[i], self.Q[i])
+        self._join(main, join)
 
     def algorithmic_bytes(self):
         """The minimum: read G and E, write E' (12 B per element)."""
