@@ -426,14 +426,19 @@ __global__ void __launch_bounds__(kH1Threads, 1) bk_hist_kernel(
 constexpr int kWalkSegs = 8;
 constexpr int kWalkRows = 2;
 
-// List length of segment s0 + lane for lanes < nq (0 elsewhere); all
-// lengths to every lane in cnt[]; returns the largest.
-__device__ __forceinline__ uint32_t walk_counts(const BucketWs& w, int64_t s0, int nq, int lane,
-                                                uint32_t* c_l, uint32_t cnt[kWalkSegs]) {
-  *c_l = lane < nq ? __ldcg(&w.seg_cnt[s0 + lane]) : 0u;
+// The list lengths of a warp's group of segments s0 .. s0 + 7 (lane r < the
+// group's size loads segment s0 + r; 0 past hi), loaded one group ahead of
+// the walk: the walk then waits for the entries only, not for their counts
+// first.  A warp's groups belong to it alone, so the counts it reads ahead
+// are final.
+__device__ __forceinline__ uint32_t group_counts(const BucketWs& w, int64_t s0, int64_t hi,
+                                                 int lane) {
+  return (s0 < hi && s0 + lane < hi && lane < kWalkSegs) ? __ldcg(&w.seg_cnt[s0 + lane]) : 0u;
+}
+__device__ __forceinline__ uint32_t spread_counts(uint32_t c_l, uint32_t cnt[kWalkSegs]) {
 #pragma unroll
-  for (int r = 0; r < kWalkSegs; ++r) cnt[r] = __shfl_sync(0xffffffffu, *c_l, r);
-  return __reduce_max_sync(0xffffffffu, *c_l);
+  for (int r = 0; r < kWalkSegs; ++r) cnt[r] = __shfl_sync(0xffffffffu, c_l, r);
+  return __reduce_max_sync(0xffffffffu, c_l);
 }
 
 // Entries j0 + 32 u + lane (u < kWalkRows) of the lists of segments s0 ..
@@ -484,10 +489,13 @@ __global__ void __launch_bounds__(kBkThreads, 4) bk_collect_kernel(const float* 
     }
     const uint32_t B = __ldcg(&w.sel[b].B);
     if (__ldcg(&w.sel[b].list_ok)) {
+      uint32_t c_next = group_counts(w, s + kWalkSegs * warp, sub_hi, lane);
       for (int64_t s0 = s + kWalkSegs * warp; s0 < sub_hi; s0 += kWalkSegs * NW) {
         const int nq = (int)std::min<int64_t>(kWalkSegs, sub_hi - s0);
-        uint32_t c_l, cnt[kWalkSegs];
-        const uint32_t mx = walk_counts(w, s0, nq, lane, &c_l, cnt);
+        uint32_t cnt[kWalkSegs];
+        const uint32_t c_l = c_next;
+        c_next = group_counts(w, s0 + kWalkSegs * NW, sub_hi, lane);
+        const uint32_t mx = spread_counts(c_l, cnt);
         uint32_t abv_l = 0u, wpos_l = 0u;
         float drop[kWalkSegs];  // this lane's sums of c^2 of the dropped entries
 #pragma unroll
@@ -676,10 +684,13 @@ __global__ void __launch_bounds__(kBkThreads, 4) bk_refine_kernel(BucketWs w) {
     BucketSel* q = &w.sel[b];
     const uint32_t B = __ldcg(&q->B), B2 = __ldcg(&q->B2);
     uint2* stash = w.stash + (int64_t)b * kBkStash;
+    uint32_t c_next = group_counts(w, s + kWalkSegs * warp, sub_hi, lane);
     for (int64_t s0 = s + kWalkSegs * warp; s0 < sub_hi; s0 += kWalkSegs * NW) {
       const int nq = (int)std::min<int64_t>(kWalkSegs, sub_hi - s0);
-      uint32_t c_l, cnt[kWalkSegs];
-      const uint32_t mx = walk_counts(w, s0, nq, lane, &c_l, cnt);
+      uint32_t cnt[kWalkSegs];
+      const uint32_t c_l = c_next;
+      c_next = group_counts(w, s0 + kWalkSegs * NW, sub_hi, lane);
+      const uint32_t mx = spread_counts(c_l, cnt);
       uint32_t strict_l = 0u;
       for (uint32_t j0 = 0; j0 < mx; j0 += 32 * kWalkRows) {
         uint2 e[kWalkSegs][kWalkRows];
@@ -878,23 +889,42 @@ __global__ void __launch_bounds__(kBkThreads) bk_write_kernel(float* __restrict_
   const uint32_t lt = lanemask_lt();
   const int64_t gwarp = ((int64_t)blockIdx.x * kBkThreads + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * kBkThreads) >> 5;
+  // the per-segment words of a group (bucket, count, output offset, ties
+  // before) are loaded one group ahead, so that a group waits for its list
+  // entries only; the bucket's words that depend on them stay in L1
+  auto seg_words = [&](int64_t s0, int& b, uint32_t& c, uint32_t& o, uint32_t& t) {
+    b = -1;
+    c = o = t = 0u;
+    if (s0 < w.nseg && s0 + lane < w.nseg && lane < kWalkSegs) {
+      const int64_t sg = s0 + lane;
+      b = w.seg_bucket[sg];
+      c = w.seg_cnt[sg];
+      o = w.seg_out[sg];
+      t = w.seg_tieb[sg];
+    }
+  };
+  int b_nx;
+  uint32_t c_nx, o_nx, t_nx;
+  seg_words(kWalkSegs * gwarp, b_nx, c_nx, o_nx, t_nx);
   for (int64_t s0 = kWalkSegs * gwarp; s0 < w.nseg; s0 += kWalkSegs * nwarps) {
     const int nq = (int)std::min<int64_t>(kWalkSegs, w.nseg - s0);
+    const int b_cur = b_nx;
+    const uint32_t c_cur = c_nx, o_cur = o_nx, t_cur = t_nx;
+    seg_words(s0 + kWalkSegs * nwarps, b_nx, c_nx, o_nx, t_nx);
     // lane r < nq: segment s0 + r
     uint32_t cnt_l = 0u, out_l = 0u, rem_l = 0u, T_l = 0u, k_l = 0u, n_l = 0u;
     int64_t off_l = 0, start_l = 0;
     if (lane < nq) {
-      const int64_t sg = s0 + lane;
-      const int b = w.seg_bucket[sg];
+      const int b = b_cur;
       const BucketDesc* dp = w.desc + b;
       k_l = (uint32_t)dp->k;
       n_l = (uint32_t)dp->n;
       off_l = dp->idx_off;
       start_l = dp->start;
       if (k_l != 0u) {
-        cnt_l = w.seg_cnt[sg];
-        out_l = w.seg_out[sg];
-        const uint32_t tieb = w.seg_tieb[sg];
+        cnt_l = c_cur;
+        out_l = o_cur;
+        const uint32_t tieb = t_cur;
         const uint32_t needT = w.sel[b].needT;
         T_l = w.sel[b].T;
         rem_l = needT > tieb ? needT - tieb : 0u;
