@@ -318,25 +318,10 @@ __host__ __device__ constexpr uint32_t mode_top() {
 // Level of one element: t >= 0 is its position on the level grid.
 // Nearest-even: rint(t).  Stochastic: floor(t) + [u < t - floor(t)].
 // Clamped to [0, top].
-// For 0 <= t < 2^22 the sum t + 2^23 lies in [2^23, 2^24), where adjacent
-// floats are 1 apart: the sum rounded down is 2^23 + floor(t), rounded to
-// nearest (ties to even) 2^23 + rint(t), and the integer is the low bits of
-// its encoding -- the same levels as the conversions below, with additions
-// only.  Elsewhere the conversions saturate and take NaN to 0, so a NaN t
-// gives level 0 and a t beyond the grid gives top.
+// The conversions saturate and take NaN to 0, so a NaN t gives level 0 and
+// a t beyond the grid gives top.
 __device__ __forceinline__ uint32_t round_level(float t, bool stochastic,
                                                 float u, uint32_t top) {
-  if (t >= 0.0f && t < 0x1p22f) {
-    uint32_t q;
-    if (stochastic) {
-      const float big = __fadd_rd(t, 0x1p23f);
-      const float fl = __fsub_rn(big, 0x1p23f);
-      q = (__float_as_uint(big) - 0x4B000000u) + ((u < __fsub_rn(t, fl)) ? 1u : 0u);
-    } else {
-      q = __float_as_uint(__fadd_rn(t, 0x1p23f)) - 0x4B000000u;
-    }
-    return min(q, top);
-  }
   int q;
   if (stochastic) {
     const float fl = floorf(t);
@@ -347,10 +332,6 @@ __device__ __forceinline__ uint32_t round_level(float t, bool stochastic,
   return (uint32_t)min(max(q, 0), (int)top);
 }
 
-// A level (q < 2^23) as a float, exactly: 2^23 + q encoded, minus 2^23.
-__device__ __forceinline__ float level_to_float(uint32_t q) {
-  return __fsub_rn(__uint_as_float(0x4B000000u + q), 0x1p23f);
-}
 
 // Quantise one value c against its group parameters; returns the code
 // level, the sign flag (QSGD/TernGrad, only when q != 0) and g_hat.
@@ -374,7 +355,7 @@ __device__ __forceinline__ uint32_t quantize_one(float c, float scale,
       q = round_level(t, stochastic, u, top);
     }
   }
-  float mag = __fmul_rn(level_to_float(q), scale);
+  float mag = __fmul_rn((float)q, scale);
   if (MODE == GC_LOG) mag = __fsub_rn(cw_expf(mag), 1.0f);
   if (MODE == GC_MINMAX) {
     *negative = false;
