@@ -173,15 +173,28 @@ class ClockSampler:
 # element; the pass streams each element once, so it scales with the
 # elements.  Valid only for the kernel source it was taken on (first 16 hex
 # digits of the SHA-256 of the file), else the bench reports null.
-TRAFFIC = {"bk_hist": {"bytes_per_elem": 750.4e6 / 65536000,
-                       "source": "gradient_compression_ef_gb300/csrc/gc_buckets.cu",
-                       "sha256_16": "6bfff760bd11984f",
-                       "captured_on": "65,536,000 elements"}}
+# DRAM bytes (read + write) of one launch of a workload's dominant kernel
+# from a one-kernel ncu capture (profiles/), per element of the launch, with
+# a hash of the kernel's source at the time of the capture.
+TRAFFIC = {
+    ("layers", "bk_hist"): {"bytes_per_elem": (1639.077e6 + 886.405e6) / 202379264,
+                            "source": "gradient_compression_ef_gb300/csrc/gc_buckets.cu",
+                            "sha256_16": "684a39e10dd37a08",
+                            "captured_on": "one transformer layer, 202,379,264 elements"},
+    ("buckets", "bk_hist"): {"bytes_per_elem": (530.639e6 + 220.218e6) / 65536000,
+                             "source": "gradient_compression_ef_gb300/csrc/gc_buckets.cu",
+                             "sha256_16": "684a39e10dd37a08",
+                             "captured_on": "65,536,000 elements"},
+    ("powersgd", "psgd_mq"): {"bytes_per_elem": (361.216e6 + 134.917e6) / 45088768,
+                              "source": "gradient_compression_ef_gb300/csrc/gc_powersgd.cu",
+                              "sha256_16": "617985f4be80d3d0",
+                              "captured_on": "one 4096 x 11008 matrix, 45,088,768 elements"},
+}
 
 
-def kernel_traffic(name, elems):
+def kernel_traffic(workload, name, elems):
     import hashlib
-    t = TRAFFIC.get(name)
+    t = TRAFFIC.get((workload, name))
     if t is None:
         return None, "no ncu capture for this kernel"
     try:
@@ -1215,9 +1228,11 @@ def main():
         kernels[name] = {"launches": cnt, "total_ms": ms_, "avg_us": avg_s * 1e6,
                          "algorithmic_bytes_per_launch": algo.get(name),
                          "achieved_gbs": algo[name] / avg_s / 1e9 if algo.get(name) else None}
-    traffic, traffic_src = kernel_traffic(top[0], wl.n) \
-        if args.workload in ("buckets", "layers", "topk") and args.path == "buckets" \
-        else (None, "no ncu capture")
+    # elements of one launch of the dominant kernel: the whole gradient for
+    # the bucketed passes, one matrix on average for PowerSGD
+    launch_elems = wl.n / len(wl.shapes) if hasattr(wl, "shapes") else wl.n
+    traffic, traffic_src = kernel_traffic(args.workload, top[0], launch_elems) \
+        if args.path == "buckets" else (None, "no ncu capture")
     roofline = {"bound": "hbm", "kernel": top[0], "achieved": kernels[top[0]]["achieved_gbs"],
                 "peak": peak, "unit": "GB/s", "peak_source": peak_src,
                 "frac": kernels[top[0]]["achieved_gbs"] / peak, "traffic": traffic,
