@@ -11,7 +11,7 @@
 // Rank w's indices are strictly increasing, so no two of its entries touch
 // the same element and the rank order is the only order that matters.  The
 // output is cut into ranges of kAggRange elements, one warp each:
-//   bounds     : for every rank, the first entry of each range (sixteen entry
+//   bounds     : for every rank, the first entry of each range (four entry
 //                boundaries per thread; each range is written exactly once).
 //   accumulate : a warp takes the ranks 32 at a time, gathers their entries
 //                of its range in chunks into its own shared-memory slots (all
@@ -43,19 +43,21 @@ __host__ __device__ __forceinline__ int64_t round_up4(int64_t k) { return (k + 3
 // b or later (k when none).  Boundary position j (0 .. k) of rank w owns the
 // ranges (range(idx[j-1]), range(idx[j])], so every range is written by
 // exactly one position.
-constexpr int kBoundsPer = 16;  // boundary positions per thread (four 16-byte loads)
+constexpr int kBoundsPer = 4;   // boundary positions per thread (one 16-byte load)
 
 __global__ void __launch_bounds__(256) agg_bounds_kernel(const int32_t* __restrict__ idx, int W,
                                                          int64_t k, int64_t n, int64_t nblk,
                                                          int32_t* __restrict__ start,
                                                          uint32_t* __restrict__ status) {
-  // rank w = blockIdx.y; positions 0 .. k fit 32 bits
-  const int32_t j0 = (int32_t)(blockIdx.x * blockDim.x + threadIdx.x) * kBoundsPer;
-  if ((int64_t)j0 > k) return;
+  // rank w = blockIdx.y; positions 0 .. k fit 32 bits (the surplus
+  // threads of the last block are dropped before the narrowing)
+  const int64_t j64 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * kBoundsPer;
+  if (j64 > k) return;
+  const int32_t j0 = (int32_t)j64;
   const int64_t w = blockIdx.y;
   const int32_t* iw = idx + w * round_up4(k);
   int32_t* sw = start + w * (nblk + 1);
-  // indices of positions j0 - 1 .. j0 + 15, all loads issued first
+  // indices of positions j0 - 1 .. j0 + kBoundsPer - 1, all loads issued first
   int32_t v[kBoundsPer + 1];
   v[0] = j0 > 0 ? iw[j0 - 1] : 0;
 #pragma unroll
