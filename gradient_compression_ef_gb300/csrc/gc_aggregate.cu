@@ -178,6 +178,9 @@ __global__ void __launch_bounds__(kAggThreads, 5) agg_accumulate_kernel(
       uint32_t jq[kAggGather];
 #pragma unroll
       for (int u = 0; u < kAggGather; ++u) {
+        wq[u] = 0;
+        jq[u] = 0u;
+        if (c0 + u * 32 >= c1) continue;  // warp-uniform: the chunk ends before this row
         const int32_t e = c0 + u * 32 + lane;
         int lo = 0, hi = nr - 1;  // the last rank r of the group with pre[r] <= e
         while (lo < hi) {
