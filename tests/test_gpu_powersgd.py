@@ -132,3 +132,14 @@ def test_short_wide_matrix_in_a_tight_context(env, m, n, r):
         run_steps((torch, gc, c), M, np.zeros_like(M), Q, r, 2)
     finally:
         c.close()
+
+
+@pytest.mark.parametrize("m,n,r", [(1, 4, 1), (3, 8, 2), (17, 12, 3), (2, 1024, 2), (33, 4, 4)])
+def test_tiny_shapes_on_the_tensor_core_path(env, m, n, r):
+    """Rows of a 16-byte multiple (n % 4 == 0) take the tensor-core passes:
+    a single row, fewer rows than one padded block of 16, four columns."""
+    rg = np.random.default_rng(m * 1000 + n * 10 + r)
+    G = rg.standard_normal((m, n)).astype(np.float32)
+    E = (0.1 * rg.standard_normal((m, n))).astype(np.float32)
+    Q = rg.standard_normal((n, r)).astype(np.float32)
+    run_steps(env, G, E, Q, r, 2)
