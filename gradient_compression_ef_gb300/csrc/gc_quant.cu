@@ -645,6 +645,8 @@ __global__ void __launch_bounds__(kQThreads) quant_apply_kernel(
       scale1 = o.scales[0];
     }
   }
+  // two chunks per round: their Philox chains interleave
+#pragma unroll 2
   for (int64_t base = warp_id * 128; base < n; base += nwarps * 128) {
     const int64_t i0 = base + 4 * lane;
     const bool active = i0 < n;
