@@ -8,17 +8,26 @@
 //
 // At rank r the step moves >= 12 bytes per element and performs 6r flops
 // per element: about 2 flop/byte at r = 4, two orders of magnitude below
-// the tensor-core ridge point, so the products run as fp32 FMAs on the CUDA
-// cores and the kernels are organised around HBM streaming:
+// the tensor-core ridge point, so every pass is organised around HBM
+// streaming.  Two paths:
+//
+// Rows of a 16-byte multiple (n % 4 == 0): pass 1 (M = G + E, P = M Q)
+// runs on the tensor cores (tcgen05, TF32 in three products), passes 2 and
+// 3 on the CUDA cores; W = U^-1 and P_hat = P W are formed inside pass 2
+// and the final reduction of Q' is a small grid of its own.  The section
+// "Tensor-core path" below describes it.
+//
+// Other column counts, all on the CUDA cores:
 //   pass 1  mq       : M = G + E written over E; P = M Q (Q staged in shared
 //                      memory).  Blocks own 16 rows and a range of columns
 //                      (enough blocks to fill the GPU); the last block of a
 //                      row range adds the column ranges' partial rows of P in
 //                      order and forms their Gram matrix in fp64.  The last
 //                      row range sums the Gram partials in order, factors
-//                      P^T P = U^T U (Cholesky, fp64) and stores W = U^-1.
-//                      P W is the Gram-Schmidt orthonormalisation of P: both
-//                      give the unique QR factor with a positive diagonal.
+//                      P^T P = U^T U (Cholesky, fp64, one warp) and stores
+//                      W = U^-1.  P W is the Gram-Schmidt orthonormalisation
+//                      of P: both give the unique QR factor with a positive
+//                      diagonal.
 //   pass 2  mtp      : Q' = M^T P_hat.  Blocks own a 128-column strip and a
 //                      slice of rows; P_hat = P W for the slice is formed in
 //                      shared memory (strip 0 also writes it out).  Partial
@@ -502,8 +511,9 @@ __global__ void __launch_bounds__(kPThreads) psgd_residual_kernel(
 // each abort decision together (a flag behind their named barrier), so no
 // barrier is left waiting for a thread that gave up.
 //
-// Passes 2 (Q' = M^T P_hat) and 3 (E' = M - P_hat Q'^T) stream M on the
-// CUDA cores; see their kernels.
+// Pass 2 (the column sums of M^T P, with W = U^-1 and P_hat = P W formed
+// beside them; psgd_qfinal adds the sums and applies W) and pass 3 (E' =
+// M - P_hat Q'^T) stream M on the CUDA cores; see their kernels.
 // ===========================================================================
 namespace tcp {
 constexpr int kConv = 256;             // converter threads (warps 0-7)
@@ -684,8 +694,9 @@ __global__ void __launch_bounds__(256) psgd_qimage_kernel(const float* __restric
 
 // ---------------------------------------------------------------------------
 // pass 1 on the tensor cores: M = G + E (written over E) and P = M Q; the
-// last contributor of a row tile adds its partial rows and writes the
-// tile's Gram partial; the last row tile factors the Gram matrix.
+// last contributor of a row tile adds its partial rows, writes the tile's
+// P rows (zero-padded) and adds the tile's Gram matrix to its CTA's Gram
+// partial, which every CTA writes at the end (pass 2 factors the sum).
 //
 // Each converter thread streams its own 16-byte pieces of G and E (four
 // operand rows, one 16-byte column chunk) through a ring of SS staging
