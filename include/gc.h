@@ -335,7 +335,11 @@ GC_API gc_status gc_ef_topk_quant(gc_ctx* ctx, const float* grad, float* err,
  * grad, err: fp32 m x n row-major;  P_out: fp32 m x r (receives P_hat);
  * Q_inout: fp32 n x r (read as Q, overwritten with Q').  1 <= r <= 16;
  * requires gc_ctx_reserve_powersgd with limits covering (m, n, r).
- * Tolerance-based: fp32 CUDA-core accumulation.
+ * Tolerance-based, deterministic: when n is a multiple of 4 (rows of a
+ * 16-byte multiple) P = M Q runs on the tensor cores with TF32 operands
+ * split in three products (near-fp32 products, fp32 accumulation) and the
+ * other products as fp32 FMAs; otherwise every product is an fp32 FMA.
+ * Every sum is added in a fixed order, so equal inputs give equal bits.
  */
 GC_API gc_status gc_powersgd_step(gc_ctx* ctx, const float* grad, float* err,
                            int64_t m, int64_t n, int r, float* P_out,
