@@ -1031,6 +1031,28 @@ constexpr int kRGPer = kRGRows / 4;   // rows per thread (4 row phases)
 constexpr int kRGCols = 512;          // columns per unit
 constexpr uint32_t kRGTile = kRGRows * kRGCols * 4;  // 32 KB
 
+// One unit row of P_hat (R floats, rows R * 4 bytes apart from a 128-byte
+// aligned start) into registers: 16-byte loads when R is a multiple of 4
+// (every row then starts on a 16-byte boundary), 8-byte loads when it is
+// even, else one float at a time.
+template <int R>
+__device__ __forceinline__ void lds_prow(uint32_t a, float (&p)[R]) {
+  if constexpr (R % 4 == 0) {
+#pragma unroll
+    for (int c = 0; c < R; c += 4) {
+      const float4 v = sm100::lds128(a + c * 4);
+      p[c] = v.x; p[c + 1] = v.y; p[c + 2] = v.z; p[c + 3] = v.w;
+    }
+  } else if constexpr (R % 2 == 0) {
+#pragma unroll
+    for (int c = 0; c < R; c += 2)
+      asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(p[c]), "=f"(p[c + 1]) : "r"(a + c * 4));
+  } else {
+#pragma unroll
+    for (int c = 0; c < R; ++c) p[c] = sm100::lds32(a + c * 4);
+  }
+}
+
 template <int R>
 __global__ void __launch_bounds__(kResidThreads, 1) psgd_resid_tma_kernel(
     const __grid_constant__ CUtensorMap tmE, float* __restrict__ E, int64_t m, int64_t n,
@@ -1122,8 +1144,7 @@ __global__ void __launch_bounds__(kResidThreads, 1) psgd_resid_tma_kernel(
       for (int h = 0; h < kRGPer; ++h) {
         const uint32_t row = r0 + 4 * h;
         mv[h] = lds128(t + cofs + row * 1024);
-#pragma unroll
-        for (int c = 0; c < R; ++c) pr[h][c] = lds32(ps + (row * R + c) * 4);
+        lds_prow<R>(ps + row * R * 4, pr[h]);
       }
       float4 out[kRGPer];
 #pragma unroll
@@ -1317,8 +1338,7 @@ __global__ void __launch_bounds__(kQThreads, 1) psgd_qstream_kernel(
         for (int c = 0; c < R; ++c) pr[c] = 0.0f;
         if (!skip) {
           mv = lds128(t + cofs + row * 1024);
-#pragma unroll
-          for (int c = 0; c < R; ++c) pr[c] = lds32(ps + (row * R + c) * 4);
+          lds_prow<R>(ps + row * R * 4, pr);
         }
         const float x[4] = {mv.x, mv.y, mv.z, mv.w};
 #pragma unroll
