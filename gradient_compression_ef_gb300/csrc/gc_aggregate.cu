@@ -13,13 +13,16 @@
 // output is cut into ranges of kAggRange elements, one warp each:
 //   bounds     : for every rank, the first entry of each range (four entry
 //                boundaries per thread; each range is written exactly once).
-//   accumulate : a warp takes the ranks 32 at a time, gathers their entries
-//                of its range in chunks into its own shared-memory slots (all
-//                loads of a chunk in flight at once), adds them to its own
-//                accumulator rank by rank (__syncwarp between ranks) and
-//                writes its range once.  Warps share nothing, so no block
-//                barrier holds a range back and each SM keeps about forty
-//                ranges in flight.
+//   accumulate : a warp takes the ranks 32 at a time and packs their
+//                entries of its range into one flat list, rank after rank,
+//                read in rows of 32 (lane e of a row finds its rank from a
+//                ballot of the ranks that start before the row and a
+//                redux of those that start in it; four rows of loads in
+//                flight at once).  It adds each row to its own accumulator
+//                one rank at a time (__syncwarp between ranks) and writes
+//                its range once.  Warps share nothing, so no block barrier
+//                holds a range back and each SM keeps forty-eight ranges in
+//                flight.
 #include <algorithm>
 
 #include "gc_internal.cuh"
@@ -31,8 +34,6 @@ constexpr int kAggShift = 10;
 constexpr int kAggRange = 1 << kAggShift;   // output elements per warp
 constexpr int kAggWarps = 8;                // warps (ranges) per block
 constexpr int kAggThreads = 32 * kAggWarps;
-constexpr int kAggSlots = 128;              // gathered entries per chunk of a warp
-constexpr int kAggGather = kAggSlots / 32;  // entries per lane per chunk
 constexpr int kAggMaxRanks = 1024;
 
 // Per-rank stride of the index and value arrays: k rounded up to 4 entries,
@@ -92,16 +93,13 @@ __global__ void __launch_bounds__(256) agg_bounds_kernel(const int32_t* __restri
   }
 }
 
-// Shared memory of one warp: the accumulator of its range, one gathered
-// chunk, and for the current group of 32 ranks their first entries of the
-// range and the offsets of their entries in the warp's flat list.  Aligned
-// to 16 bytes: every warp's accumulator is read and written as float4.
+// Shared memory of one warp: the accumulator of its range, and for the
+// current group of 32 ranks the non-empty ones in rank order (their lane in
+// the group and the offset from a flat-list position to the rank's entry).
+// Aligned to 16 bytes: the accumulator is cleared and written as float4.
 struct __align__(16) AggWarpSmem {
   float acc[kAggRange];
-  float val[kAggSlots];
-  uint16_t loc[kAggSlots];
-  int32_t first[32];
-  int32_t pre[33];
+  int2 nz[32];
 };
 static_assert(sizeof(AggWarpSmem) % 16 == 0, "float4 access to each warp's accumulator");
 
@@ -109,132 +107,150 @@ static_assert(sizeof(AggWarpSmem) % 16 == 0, "float4 access to each warp's accum
 // +-fl(q * scale) with rank w's codes at w * cb and scales at w * sf (sf a
 // multiple of 4).  Entries and groups fit 32 bits (indices are int32, so
 // k < 2^31); the group of entry j is j >> gshift for a power-of-two group
-// (gshift >= 0), else j / G.
-template <int BITS>
+// (POW2), else j / G.
+template <int BITS, bool POW2>
 __device__ __forceinline__ float agg_value(const float* __restrict__ val,
                                            const uint8_t* __restrict__ codes,
-                                           const float* __restrict__ scales, int64_t k,
+                                           const float* __restrict__ scales, int64_t K,
                                            int64_t cb, int64_t mag, int64_t sf, uint32_t G,
-                                           int gshift, int w, uint32_t j) {
-  if (BITS == 0) return val[(int64_t)w * round_up4(k) + j];
-  const uint8_t* cw = codes + (int64_t)w * cb;
+                                           int gshift, int64_t w, uint32_t j) {
+  if (BITS == 0) return val[w * K + j];
+  const uint8_t* cw = codes + w * cb;
   constexpr int kPerByte = (BITS >= 8 || BITS == 0) ? 1 : 8 / BITS;  // codes per byte
   constexpr int kByteShift = BITS == 8 ? 0 : BITS == 4 ? 1 : BITS == 2 ? 2 : 3;
   const uint32_t q = (uint32_t)(cw[j >> kByteShift] >> ((j & (kPerByte - 1)) * BITS)) &
                      ((1u << BITS) - 1u);
   const bool neg = (cw[mag + (j >> 3)] >> (j & 7)) & 1u;
-  const uint32_t g = gshift >= 0 ? j >> gshift : j / G;
-  const float m = __fmul_rn((float)q, scales[(int64_t)w * sf + g]);
+  const uint32_t g = POW2 ? j >> gshift : j / G;
+  const float m = __fmul_rn((float)q, scales[w * sf + g]);
   return neg ? -m : m;
 }
 
+constexpr int kAggRows = 3;  // rows of 32 flat entries whose loads are in flight together
 template <int BITS>
-__global__ void __launch_bounds__(kAggThreads, 5) agg_accumulate_kernel(
+constexpr int agg_blocks_per_sm() { return BITS == 0 ? 5 : 6; }
+
+template <int BITS, bool POW2>
+__global__ void __launch_bounds__(kAggThreads, agg_blocks_per_sm<BITS>()) agg_accumulate_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ val,
     const uint8_t* __restrict__ codes, const float* __restrict__ scales, int W, int64_t k,
     int64_t cb, int64_t mag, int64_t sf, uint32_t G, int gshift, int64_t n, int64_t nblk,
     const int32_t* __restrict__ start, float* __restrict__ out, uint32_t* __restrict__ status) {
   __shared__ AggWarpSmem warps[kAggWarps];
   const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
-  const int64_t b = (int64_t)blockIdx.x * kAggWarps + wi;
-  if (b >= nblk) return;  // (no block barrier follows)
   AggWarpSmem& sm = warps[wi];
-  const int64_t a = b << kAggShift;
-  const int len = (int)std::min<int64_t>(kAggRange, n - a);
-#pragma unroll
-  for (int q = 0; q < kAggRange / 128; ++q)
-    reinterpret_cast<float4*>(sm.acc)[q * 32 + lane] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  for (int r0 = 0; r0 < W; r0 += 32) {
-    const int nr = min(32, W - r0);
-    // this group's ranks: first entry and count in the range (clamped to
-    // [0, k): bounds from invalid, flagged indices stay in range; a range
-    // holds at most kAggRange entries of one rank), then the offsets of
-    // their entries in the warp's flat list (a scan across the lanes)
-    int32_t f = 0, cnt = 0;
-    if (lane < nr) {
+  const int64_t K = round_up4(k);
+  const int64_t stride = (int64_t)gridDim.x * kAggWarps;
+  const uint32_t lanes_le = 0xffffffffu >> (31 - lane);
+  bool bad = false;
+  // lane r: the first entries of rank r0 + r in ranges bb and bb + 1
+  // (0, 0 past the last rank or range)
+  auto load_bounds = [&](int r0, int64_t bb, int32_t& lo, int32_t& hi) {
+    lo = 0;
+    hi = 0;
+    if (bb < nblk && lane < min(32, W - r0)) {
       const int32_t* sw = start + (int64_t)(r0 + lane) * (nblk + 1);
-      const int64_t f64 = std::min<int64_t>(std::max<int32_t>(sw[b], 0), k);
-      const int64_t l64 = std::min<int64_t>(std::max<int32_t>(sw[b + 1], 0), k);
-      f = (int32_t)f64;
-      cnt = (int32_t)std::min<int64_t>(l64 > f64 ? l64 - f64 : 0, kAggRange);
+      lo = sw[bb];
+      hi = sw[bb + 1];
     }
-    int32_t incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const int32_t total = __shfl_sync(0xffffffffu, incl, 31);
-    __syncwarp();  // the previous group's reads of first / pre are done
-    sm.first[lane] = f;
-    sm.pre[lane] = incl - cnt;
-    if (lane == 31) sm.pre[32] = incl;
-    __syncwarp();
-    for (int32_t c0 = 0; c0 < total; c0 += kAggSlots) {
-      const int32_t c1 = min(c0 + kAggSlots, total);
-      // rank and entry of each of this lane's flat entries, then all their
-      // global loads, then the shared-memory stores
-      int wq[kAggGather];
-      uint32_t jq[kAggGather];
-#pragma unroll
-      for (int u = 0; u < kAggGather; ++u) {
-        wq[u] = 0;
-        jq[u] = 0u;
-        if (c0 + u * 32 >= c1) continue;  // warp-uniform: the chunk ends before this row
-        const int32_t e = c0 + u * 32 + lane;
-        int lo = 0, hi = nr - 1;  // the last rank r of the group with pre[r] <= e
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (sm.pre[mid] <= e) lo = mid;
-          else hi = mid - 1;
-        }
-        wq[u] = r0 + lo;
-        jq[u] = (uint32_t)(sm.first[lo] + (e - sm.pre[lo]));
-      }
-      int32_t iq[kAggGather];
-      float vq[kAggGather];
-#pragma unroll
-      for (int u = 0; u < kAggGather; ++u) {
-        if (c0 + u * 32 + lane < c1) {
-          iq[u] = idx[(int64_t)wq[u] * round_up4(k) + jq[u]];
-          vq[u] = agg_value<BITS>(val, codes, scales, k, cb, mag, sf, G, gshift, wq[u], jq[u]);
-        }
-      }
-      __syncwarp();  // the previous chunk's adds are done with the slots
-#pragma unroll
-      for (int u = 0; u < kAggGather; ++u) {
-        const int32_t e = c0 + u * 32 + lane;
-        if (e < c1) {
-          const int64_t i = (int64_t)iq[u] - a;
-          const bool ok = i >= 0 && i < len;
-          if (!ok) atomicOr(status, kStatusScatterIndex);
-          sm.loc[e - c0] = ok ? (uint16_t)i : (uint16_t)0xffffu;
-          sm.val[e - c0] = vq[u];
-        }
-      }
-      __syncwarp();
-      // rank by rank: within a rank the locations are distinct
-      for (int r = 0; r < nr; ++r) {
-        const int32_t e0 = max(sm.pre[r], c0), e1 = min(sm.pre[r + 1], c1);
-        if (e0 >= e1) continue;
-        for (int32_t e = e0 + lane; e < e1; e += 32) {
-          const uint16_t l = sm.loc[e - c0];
-          if (l != 0xffffu) sm.acc[l] = __fadd_rn(sm.acc[l], sm.val[e - c0]);
-        }
-        __syncwarp();
-      }
-    }
-  }
-  __syncwarp();
-  float* o = out + a;
-  if (len == kAggRange) {
+  };
+  // persistent warps: the first group's bounds of the next range load while
+  // the warp works on this one
+  int64_t b = (int64_t)blockIdx.x * kAggWarps + wi;
+  int32_t next_lo, next_hi;
+  load_bounds(0, b, next_lo, next_hi);
+  for (; b < nblk; b += stride) {
+    int32_t blo = next_lo, bhi = next_hi;
+    load_bounds(0, b + stride, next_lo, next_hi);
+    const int64_t a = b << kAggShift;
+    const int32_t a32 = (int32_t)a;  // n <= 2^31 - 1
+    const uint32_t len = (uint32_t)std::min<int64_t>(kAggRange, n - a);
+    __syncwarp();  // the previous range's output reads are done
 #pragma unroll
     for (int q = 0; q < kAggRange / 128; ++q)
-      reinterpret_cast<float4*>(o)[q * 32 + lane] =
-          reinterpret_cast<const float4*>(sm.acc)[q * 32 + lane];
-  } else {
-    for (int i = lane; i < len; i += 32) o[i] = sm.acc[i];
+      reinterpret_cast<float4*>(sm.acc)[q * 32 + lane] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int r0 = 0; r0 < W; r0 += 32) {
+      if (r0 > 0) load_bounds(r0, b, blo, bhi);
+      // lane r: rank r0 + r's first entry and count in the range (clamped to
+      // [0, k): bounds from invalid, flagged indices stay in range; a range
+      // holds at most kAggRange entries of one rank), and the position of
+      // its entries in the warp's flat list (a scan)
+      const int64_t f64 = std::min<int64_t>(std::max<int32_t>(blo, 0), k);
+      const int64_t l64 = std::min<int64_t>(std::max<int32_t>(bhi, 0), k);
+      const int32_t f = (int32_t)f64;
+      const int32_t cnt = (int32_t)std::min<int64_t>(l64 > f64 ? l64 - f64 : 0, kAggRange);
+      int32_t incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const int32_t total = __shfl_sync(0xffffffffu, incl, 31);
+      const int32_t pre = incl - cnt;
+      const bool nonempty = cnt > 0;
+      // the non-empty ranks in order: the i-th one covers flat positions
+      // [pre, pre + cnt) and its entry j = position + (f - pre)
+      const uint32_t ne = __ballot_sync(0xffffffffu, nonempty);
+      __syncwarp();  // the previous group's reads of nz (and the clearing) are done
+      if (nonempty) sm.nz[__popc(ne & (lanes_le >> 1))] = make_int2(lane, f - pre);
+      __syncwarp();
+      for (int32_t c0 = 0; c0 < total; c0 += 32 * kAggRows) {
+        // each lane's flat entries of this chunk: their rank (the non-empty
+        // ranks that start before a row, plus those that start in it at or
+        // before the lane), then all loads in flight
+        int32_t iq[kAggRows], rq[kAggRows];
+        float vq[kAggRows];
+#pragma unroll
+        for (int t = 0; t < kAggRows; ++t) {
+          const int32_t row = c0 + 32 * t;
+          iq[t] = 0;
+          vq[t] = 0.0f;
+          rq[t] = -1;
+          if (row >= total) continue;  // warp-uniform
+          const bool in_row = nonempty && pre >= row && pre < row + 32;
+          const uint32_t starts = __reduce_or_sync(0xffffffffu, in_row ? 1u << (pre - row) : 0u);
+          const int before = __popc(__ballot_sync(0xffffffffu, nonempty && pre < row));
+          const int e = row + lane;
+          if (e < total) {
+            const int ri = before + __popc(starts & lanes_le) - 1;
+            const int2 z = sm.nz[ri];
+            const int64_t w = r0 + z.x;
+            const uint32_t j = (uint32_t)(e + z.y);
+            iq[t] = idx[w * K + j];
+            vq[t] = agg_value<BITS, POW2>(val, codes, scales, K, cb, mag, sf, G, gshift, w, j);
+            rq[t] = ri;
+          }
+        }
+        // adds in rank order: one round per rank present in the row (within
+        // a rank the locations are distinct; the warp meets between ranks)
+#pragma unroll
+        for (int t = 0; t < kAggRows; ++t) {
+          const int32_t row = c0 + 32 * t;
+          if (row >= total) break;  // warp-uniform
+          const int lo = __shfl_sync(0xffffffffu, rq[t], 0);
+          const int hi = __shfl_sync(0xffffffffu, rq[t], min(31, total - 1 - row));
+          for (int r = lo; r <= hi; ++r) {
+            if (rq[t] == r) {
+              const uint32_t i = (uint32_t)iq[t] - (uint32_t)a32;
+              if (iq[t] >= 0 && i < len) sm.acc[i] = __fadd_rn(sm.acc[i], vq[t]);
+              else bad = true;
+            }
+            __syncwarp();
+          }
+        }
+      }
+    }
+    float* o = out + a;
+    if (len == kAggRange) {
+#pragma unroll
+      for (int q = 0; q < kAggRange / 128; ++q)
+        reinterpret_cast<float4*>(o)[q * 32 + lane] =
+            reinterpret_cast<const float4*>(sm.acc)[q * 32 + lane];
+    } else {
+      for (int i = lane; i < (int)len; i += 32) o[i] = sm.acc[i];
+    }
   }
+  if (bad) atomicOr(status, kStatusScatterIndex);
 }
 
 template <int BITS>
@@ -248,22 +264,37 @@ gc_status run_accumulate(gc_ctx* ctx, const int32_t* idx, const float* val, cons
   int gshift = -1;
   if ((G32 & (G32 - 1)) == 0)
     for (gshift = 0; (1u << gshift) != G32; ++gshift) {}
-  agg_accumulate_kernel<BITS><<<(unsigned)ceil_div(nblk, kAggWarps), kAggThreads, 0, ctx->stream>>>(
-      idx, val, codes, scales, W, k, cb, mag, sf, G32, gshift, n, nblk, start, out, ctx->ws.status);
+  // persistent: as many blocks as fit on the GPU at once, at most one range a warp
+  const unsigned grid = (unsigned)std::min<int64_t>(
+      ceil_div(nblk, kAggWarps), (int64_t)std::max(ctx->num_sms, 1) * agg_blocks_per_sm<BITS>());
+  if constexpr (BITS != 0) {
+    if (gshift < 0) {
+      agg_accumulate_kernel<BITS, false><<<grid, kAggThreads, 0, ctx->stream>>>(
+          idx, val, codes, scales, W, k, cb, mag, sf, G32, gshift, n, nblk, start, out,
+          ctx->ws.status);
+      return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
+    }
+  }
+  agg_accumulate_kernel<BITS, true><<<grid, kAggThreads, 0, ctx->stream>>>(
+      idx, val, codes, scales, W, k, cb, mag, sf, G32, std::max(gshift, 0), n, nblk, start, out,
+      ctx->ws.status);
   return cudaGetLastError() == cudaSuccess ? GC_OK : GC_ERR_CUDA;
 }
 
 }  // namespace
 
 gc_status prepare_aggregate_kernels() {
-  // static shared memory only; prefer the largest carve-out so that five
-  // blocks (forty ranges) fit on an SM
-  const bool ok =
-      cudaFuncSetAttribute(agg_accumulate_kernel<0>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess &&
-      cudaFuncSetAttribute(agg_accumulate_kernel<1>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess &&
-      cudaFuncSetAttribute(agg_accumulate_kernel<2>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess &&
-      cudaFuncSetAttribute(agg_accumulate_kernel<4>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess &&
-      cudaFuncSetAttribute(agg_accumulate_kernel<8>, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
+  // static shared memory only (34 KB a block); prefer the largest carve-out
+  // so that six blocks (forty-eight ranges) fit on an SM
+  auto carve = [](auto kernel) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) ==
+           cudaSuccess;
+  };
+  const bool ok = carve(agg_accumulate_kernel<0, true>) && carve(agg_accumulate_kernel<1, true>) &&
+                  carve(agg_accumulate_kernel<2, true>) && carve(agg_accumulate_kernel<4, true>) &&
+                  carve(agg_accumulate_kernel<8, true>) && carve(agg_accumulate_kernel<1, false>) &&
+                  carve(agg_accumulate_kernel<2, false>) && carve(agg_accumulate_kernel<4, false>) &&
+                  carve(agg_accumulate_kernel<8, false>);
   return ok ? GC_OK : GC_ERR_CUDA;
 }
 

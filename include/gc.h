@@ -380,8 +380,10 @@ GC_API gc_status gc_ef_randk(gc_ctx* ctx, const float* grad, float* err, int64_t
  * GC_ERR_DEVICE_CHECK from gc_ctx_check, with the offending entries left
  * out).  val: fp32[W*K], laid out the same way.  out: fp32[n], fully
  * written.  1 <= W <= 1024;
- * 0 <= k <= n <= 2^31 - 1.  Scratch: W * (ceil(n / 8192) + 1) int32 of the
- * context's Top-K scratch, i.e. at most 2 * max_n (GC_ERR_WORKSPACE).
+ * 0 <= k <= n <= 2^31 - 1.  Scratch: W * (ceil(n / 1024) + 1) int32 (the
+ * first entry of every rank in every 1024-element range of the output) of
+ * the context's Top-K scratch, which holds 2 * max_n of them; a larger call
+ * returns GC_ERR_WORKSPACE.
  */
 GC_API gc_status gc_topk_aggregate(gc_ctx* ctx, int W, int64_t k, const int32_t* idx,
                                    const float* val, int64_t n, float* out);

@@ -69,6 +69,51 @@ def test_dense_ranks_take_several_chunks(env):
     assert_bits_equal(got, oracle.topk_aggregate(idx, val, W, n, n), "dense")
 
 
+def clustered_ranks(r, W, k, n):
+    """Ranks of mixed density: rank w draws its k indices from a window of
+    2k, 5k, n / 2 or n elements (by w mod 4) at a random offset, so some
+    ranks have hundreds of entries in a 1024-element range where others
+    have a few, in the same group of ranks."""
+    rows = []
+    for w in range(W):
+        span = min(n, (2 * k, 5 * k, n // 2, n)[w % 4])
+        lo = int(r.integers(0, n - span + 1))
+        rows.append(np.sort(lo + r.choice(span, size=k, replace=False)))
+    return np.stack(rows).astype(np.int32)
+
+
+@pytest.mark.parametrize("W,k,n", [(11, 3000, 200_000), (37, 2500, 120_000), (8, 600, 4096)])
+def test_ranks_of_mixed_density(env, W, k, n):
+    r = np.random.default_rng(W + 7 * k)
+    idx = clustered_ranks(r, W, k, n)
+    val = r.standard_normal((W, k)).astype(np.float32)
+    got = run_plain(env, idx, val, W, k, n)
+    assert_bits_equal(got, oracle.topk_aggregate(idx, val, W, k, n),
+                      "mixed W=%d k=%d n=%d" % (W, k, n))
+
+
+@pytest.mark.parametrize("bits,group", [(8, 48), (2, 100), (4, 0), (1, 7)])
+def test_quant_ranks_any_group(env, bits, group):
+    """Codes and scales drawn at random (the aggregation takes any bytes),
+    groups that are not a power of two (a division per entry) or one group
+    of all k, ranks of mixed density."""
+    torch, gc, ctx = env
+    W, n, k = 13, 150_000, 2000
+    r = np.random.default_rng(bits * 1000 + group)
+    idx = clustered_ranks(r, W, k, n)
+    cb = gc.codes_bytes(k, bits, "qsgd")
+    sf = -(-gc.scales_floats(k, group, "qsgd") // 4) * 4
+    codes = r.integers(0, 256, size=W * cb, dtype=np.uint8)
+    scales = r.uniform(0.5, 2.0, size=W * sf).astype(np.float32)
+    out = torch.full((n,), 7.0, dtype=torch.float32, device="cuda")
+    di = torch.from_numpy(padded(idx, W, k, np.int32)).cuda()
+    gc.topk_quant_aggregate(ctx, W, k, di, torch.from_numpy(codes).cuda(),
+                            dev_f32(torch, scales), bits, group, n, out)
+    ctx.check()
+    want = oracle.topk_quant_aggregate(idx, codes, scales, W, k, bits, group, n)
+    assert_bits_equal(host(out), want, "bits=%d group=%d" % (bits, group))
+
+
 def test_hand_cases(env, golden_dir):
     data = json.load(open(os.path.join(golden_dir, "aggregate_hand.json")))
     for case in data["cases"]:
