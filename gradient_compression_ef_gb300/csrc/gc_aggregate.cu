@@ -44,53 +44,83 @@ __host__ __device__ __forceinline__ int64_t round_up4(int64_t k) { return (k + 3
 // b or later (k when none).  Boundary position j (0 .. k) of rank w owns the
 // ranges (range(idx[j-1]), range(idx[j])], so every range is written by
 // exactly one position.
-constexpr int kBoundsPer = 4;   // boundary positions per thread (one 16-byte load)
+constexpr int kBoundsPer = 4;   // boundary positions per thread and step (one 16-byte load)
+constexpr int kBoundsThreads = 256;
+constexpr int kBoundsBlocksPerSm = 8;
 
-__global__ void __launch_bounds__(256) agg_bounds_kernel(const int32_t* __restrict__ idx, int W,
-                                                         int64_t k, int64_t n, int64_t nblk,
-                                                         int32_t* __restrict__ start,
-                                                         uint32_t* __restrict__ status) {
-  // rank w = blockIdx.y; positions 0 .. k fit 32 bits (the surplus
-  // threads of the last block are dropped before the narrowing)
-  const int64_t j64 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * kBoundsPer;
-  if (j64 > k) return;
-  const int32_t j0 = (int32_t)j64;
+__global__ void __launch_bounds__(kBoundsThreads, kBoundsBlocksPerSm) agg_bounds_kernel(
+    const int32_t* __restrict__ idx, int W, int64_t k, int64_t n, int64_t nblk,
+    int32_t* __restrict__ start, uint32_t* __restrict__ status) {
+  // rank w = blockIdx.y; the blocks of a rank stride over its positions
+  // 0 .. k, kBoundsPer at a time, loading the next step's indices while
+  // they write this step's boundaries
   const int64_t w = blockIdx.y;
   const int32_t* iw = idx + w * round_up4(k);
   int32_t* sw = start + w * (nblk + 1);
-  // indices of positions j0 - 1 .. j0 + kBoundsPer - 1, all loads issued first
-  int32_t v[kBoundsPer + 1];
-  v[0] = j0 > 0 ? iw[j0 - 1] : 0;
+  // positions and strides in 32 bits: k < 2^31 and a stride < 2^31, so
+  // j0 + stride < 2^32
+  const uint32_t kk = (uint32_t)k, nb = (uint32_t)nblk, n32 = (uint32_t)n;
+  const uint32_t stride = gridDim.x * kBoundsThreads * kBoundsPer;
+  // indices of positions j0 - 1 .. j0 + kBoundsPer - 1 (0 where absent)
+  auto load = [&](uint32_t j0, int32_t (&v)[kBoundsPer + 1]) {
 #pragma unroll
-  for (int q = 0; q < kBoundsPer / 4; ++q) {
-    const int64_t jq = j0 + 4 * q;
-    if (jq + 3 < k) {
-      const int4 x = *reinterpret_cast<const int4*>(iw + jq);
-      v[4 * q + 1] = x.x; v[4 * q + 2] = x.y; v[4 * q + 3] = x.z; v[4 * q + 4] = x.w;
+    for (int u = 0; u <= kBoundsPer; ++u) v[u] = 0;
+    if (j0 > kk) return;
+    if (j0 > 0) v[0] = iw[j0 - 1];
+    if (j0 + kBoundsPer <= kk) {
+      const int4 x = *reinterpret_cast<const int4*>(iw + j0);
+      v[1] = x.x; v[2] = x.y; v[3] = x.z; v[4] = x.w;
     } else {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) v[4 * q + 1 + u] = jq + u < k ? iw[jq + u] : 0;
+      for (int u = 0; u < kBoundsPer; ++u)
+        if (j0 + u < kk) v[1 + u] = iw[j0 + u];
     }
-  }
-  auto range_of = [&](int32_t x) -> int64_t {
-    if (x < 0 || (int64_t)x >= n) {
-      atomicOr(status, kStatusScatterIndex);
-      return x < 0 ? 0 : nblk - 1;
-    }
-    return (int64_t)x >> kAggShift;
   };
-  const int32_t nb = (int32_t)nblk, kk = (int32_t)k;  // ranges < 2^18, k < 2^31
-  int32_t prev = j0 > 0 ? (int32_t)range_of(v[0]) : -1;
+  // the range of an index; one outside [0, n) (negative ones are large as
+  // unsigned) is flagged and taken as the last range
+  bool bad = false;
+  auto range_of = [&](int32_t x) -> uint32_t {
+    bad |= (uint32_t)x >= n32;
+    return min((uint32_t)x >> kAggShift, nb - 1);
+  };
+  uint32_t j0 = (blockIdx.x * kBoundsThreads + threadIdx.x) * kBoundsPer;
+  int32_t v[kBoundsPer + 1], nv[kBoundsPer + 1];
+  load(j0, v);
+  for (; j0 <= kk; j0 += stride) {
+    load(j0 + stride, nv);
+    // c[u] = the range of position j0 + u - 1 (nb for position k, and the
+    // one before it past k), c[0] that of position j0 - 1 (-1 before 0)
+    int32_t c[kBoundsPer + 1];
+    if (j0 > 0 && j0 + kBoundsPer <= kk) {
+      // a quad inside the rank's entries: no position is 0 or k
 #pragma unroll
-  for (int u = 1; u <= kBoundsPer; ++u) {
-    const int32_t j = j0 + u - 1;
-    if (j > kk) break;
-    const int32_t cur = j < kk ? (int32_t)range_of(v[u]) : nb;
-    if (j > 0 && j < kk && v[u] <= v[u - 1]) atomicOr(status, kStatusScatterIndex);
-    const int32_t hi = min(cur, nb);
-    for (int32_t b = max(prev + 1, 0); b <= hi; ++b) sw[b] = j;
-    prev = cur;
+      for (int u = 0; u <= kBoundsPer; ++u) c[u] = (int32_t)range_of(v[u]);
+#pragma unroll
+      for (int u = 1; u <= kBoundsPer; ++u) bad |= v[u] <= v[u - 1];
+    } else {
+      c[0] = j0 > 0 ? (int32_t)range_of(v[0]) : -1;
+#pragma unroll
+      for (int u = 1; u <= kBoundsPer; ++u) {
+        const uint32_t j = j0 + u - 1;
+        c[u] = j < kk ? (int32_t)range_of(v[u]) : j == kk ? (int32_t)nb : c[u - 1];
+        bad |= j > 0 && j < kk && v[u] <= v[u - 1];
+      }
+    }
+    int32_t hi = c[0];
+#pragma unroll
+    for (int u = 1; u <= kBoundsPer; ++u) hi = max(hi, c[u]);
+    // ranges c[0] + 1 .. max c (at most nb): each starts at the first
+    // position whose range reaches it
+    for (int32_t b = c[0] + 1; b <= hi; ++b) {
+      uint32_t j = j0 + kBoundsPer - 1;
+#pragma unroll
+      for (int u = kBoundsPer - 1; u >= 1; --u) j = c[u] >= b ? j0 + u - 1 : j;
+      sw[b] = (int32_t)j;
+    }
+#pragma unroll
+    for (int u = 0; u <= kBoundsPer; ++u) v[u] = nv[u];
   }
+  if (bad) atomicOr(status, kStatusScatterIndex);
 }
 
 // Shared memory of one warp: the accumulator of its range, and for the
@@ -312,9 +342,14 @@ gc_status launch_aggregate(gc_ctx* ctx, int W, int64_t k, const int32_t* idx, co
   int32_t* start = reinterpret_cast<int32_t*>(ctx->ws.cand);
   {
     LaunchScope L(ctx, GC_PHASE_AGG_BOUNDS);
-    const dim3 grid((unsigned)ceil_div(ceil_div(k + 1, kBoundsPer), 256), (unsigned)W);
-    agg_bounds_kernel<<<grid, 256, 0, ctx->stream>>>(idx, W, k, n, nblk, start,
-                                                      ctx->ws.status);
+    // enough blocks over all ranks to fill the GPU once, at most one step a thread
+    const int64_t per_rank = std::max<int64_t>(
+        1, (int64_t)std::max(ctx->num_sms, 1) * kBoundsBlocksPerSm / W);
+    const dim3 grid((unsigned)std::min<int64_t>(
+                        ceil_div(ceil_div(k + 1, kBoundsPer), kBoundsThreads), per_rank),
+                    (unsigned)W);
+    agg_bounds_kernel<<<grid, kBoundsThreads, 0, ctx->stream>>>(idx, W, k, n, nblk, start,
+                                                                 ctx->ws.status);
   }
   if (cudaGetLastError() != cudaSuccess) return GC_ERR_CUDA;
   if (bits == 0)
