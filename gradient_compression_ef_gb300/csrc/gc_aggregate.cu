@@ -11,18 +11,20 @@
 // Rank w's indices are strictly increasing, so no two of its entries touch
 // the same element and the rank order is the only order that matters.  The
 // output is cut into ranges of kAggRange elements, one warp each:
-//   bounds     : for every rank, the first entry of each range (four entry
-//                boundaries per thread; each range is written exactly once).
+//   bounds     : for every rank, the first entry of each range (threads
+//                stride over the rank's entry boundaries four at a time,
+//                loading the next four while they write; each range is
+//                written exactly once).
 //   accumulate : a warp takes the ranks 32 at a time and packs their
 //                entries of its range into one flat list, rank after rank,
 //                read in rows of 32 (lane e of a row finds its rank from a
 //                ballot of the ranks that start before the row and a
-//                redux of those that start in it; four rows of loads in
+//                redux of those that start in it; three rows of loads in
 //                flight at once).  It adds each row to its own accumulator
 //                one rank at a time (__syncwarp between ranks) and writes
 //                its range once.  Warps share nothing, so no block barrier
-//                holds a range back and each SM keeps forty-eight ranges in
-//                flight.
+//                holds a range back; each SM keeps forty-eight warps, each
+//                loading its next range's bounds while it works on one.
 #include <algorithm>
 
 #include "gc_internal.cuh"
