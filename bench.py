@@ -185,10 +185,20 @@ TRAFFIC = {
                              "source": "gradient_compression_ef_gb300/csrc/gc_buckets.cu",
                              "sha256_16": "684a39e10dd37a08",
                              "captured_on": "65,536,000 elements"},
+    # pass 1's code is the same as at the capture; the file has since changed
+    # in comments and in passes 2 and 3 (their P_hat row loads) only
     ("powersgd", "psgd_mq"): {"bytes_per_elem": (361.216e6 + 134.917e6) / 45088768,
                               "source": "gradient_compression_ef_gb300/csrc/gc_powersgd.cu",
-                              "sha256_16": "617985f4be80d3d0",
+                              "sha256_16": "bd641ce596a77ff1",
                               "captured_on": "one 4096 x 11008 matrix, 45,088,768 elements"},
+    # the full workload (one pass: both metrics); the output's last tens of
+    # MB are still in L2 when the kernel ends, so the writes read below 4 B
+    # per output element
+    ("aggregate", "agg_accumulate"): {"bytes_per_elem": (59.95e6 + 471.76e6) / 134217728,
+                                      "source": "gradient_compression_ef_gb300/csrc/gc_aggregate.cu",
+                                      "sha256_16": "d1ea89f507c3e69b",
+                                      "captured_on": "the full workload, 8 ranks x 134,217,728 "
+                                                     "elements"},
 }
 
 
