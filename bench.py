@@ -191,10 +191,11 @@ TRAFFIC = {
                               "captured_on": "one 4096 x 11008 matrix, 45,088,768 elements"},
     # the full workload (one pass: both metrics); the output's last tens of
     # MB are still in L2 when the kernel ends, so the writes read below 4 B
-    # per output element
+    # per output element.  The file has changed since in the bounds kernel
+    # only (eight positions a step).
     ("aggregate", "agg_accumulate"): {"bytes_per_elem": (59.95e6 + 471.76e6) / 134217728,
                                       "source": "gradient_compression_ef_gb300/csrc/gc_aggregate.cu",
-                                      "sha256_16": "d1ea89f507c3e69b",
+                                      "sha256_16": "174459dedb864e6b",
                                       "captured_on": "the full workload, 8 ranks x 134,217,728 "
                                                      "elements"},
 }

@@ -12,8 +12,8 @@
 // the same element and the rank order is the only order that matters.  The
 // output is cut into ranges of kAggRange elements, one warp each:
 //   bounds     : for every rank, the first entry of each range (threads
-//                stride over the rank's entry boundaries four at a time,
-//                loading the next four while they write; each range is
+//                stride over the rank's entry boundaries eight at a time,
+//                loading the next eight while they write; each range is
 //                written exactly once).
 //   accumulate : a warp takes the ranks 32 at a time and packs their
 //                entries of its range into one flat list, rank after rank,
@@ -46,9 +46,9 @@ __host__ __device__ __forceinline__ int64_t round_up4(int64_t k) { return (k + 3
 // b or later (k when none).  Boundary position j (0 .. k) of rank w owns the
 // ranges (range(idx[j-1]), range(idx[j])], so every range is written by
 // exactly one position.
-constexpr int kBoundsPer = 4;   // boundary positions per thread and step (one 16-byte load)
+constexpr int kBoundsPer = 8;   // boundary positions per thread and step (two 16-byte loads)
 constexpr int kBoundsThreads = 256;
-constexpr int kBoundsBlocksPerSm = 8;
+constexpr int kBoundsBlocksPerSm = 6;
 
 __global__ void __launch_bounds__(kBoundsThreads, kBoundsBlocksPerSm) agg_bounds_kernel(
     const int32_t* __restrict__ idx, int W, int64_t k, int64_t n, int64_t nblk,
@@ -70,8 +70,11 @@ __global__ void __launch_bounds__(kBoundsThreads, kBoundsBlocksPerSm) agg_bounds
     if (j0 > kk) return;
     if (j0 > 0) v[0] = iw[j0 - 1];
     if (j0 + kBoundsPer <= kk) {
-      const int4 x = *reinterpret_cast<const int4*>(iw + j0);
-      v[1] = x.x; v[2] = x.y; v[3] = x.z; v[4] = x.w;
+#pragma unroll
+      for (int q = 0; q < kBoundsPer / 4; ++q) {
+        const int4 x = *reinterpret_cast<const int4*>(iw + j0 + 4 * q);
+        v[4 * q + 1] = x.x; v[4 * q + 2] = x.y; v[4 * q + 3] = x.z; v[4 * q + 4] = x.w;
+      }
     } else {
 #pragma unroll
       for (int u = 0; u < kBoundsPer; ++u)
