@@ -1051,7 +1051,7 @@ __device__ __forceinline__ void lds_prow(uint32_t a, float (&p)[R]) {
   } else if constexpr (R % 2 == 0) {
 #pragma unroll
     for (int c = 0; c < R; c += 2)
-      asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(p[c]), "=f"(p[c + 1]) : "r"(a + c * 4));
+      sm100::lds64(a + c * 4, p[c], p[c + 1]);
   } else {
 #pragma unroll
     for (int c = 0; c < R; ++c) p[c] = sm100::lds32(a + c * 4);
@@ -1169,8 +1169,10 @@ __global__ void __launch_bounds__(kResidThreads, 1) psgd_resid_tma_kernel(
         out[h] = make_float4(x[0], x[1], x[2], x[3]);
       }
       // the stage can be refilled once every warp has read it: each lane's
-      // loaded values have been used by the arithmetic above (so its loads
-      // are complete) before the warp's one arrival
+      // results are computed here, so its loads from the stage have
+      // returned, before the warp's one arrival
+#pragma unroll
+      for (int h = 0; h < kRGPer; ++h) settle(out[h]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
 #pragma unroll
@@ -1315,11 +1317,19 @@ __global__ void __launch_bounds__(kQThreads, 1) psgd_qstream_kernel(
           ok = false;
     }
   } else {
-    const uint32_t r0 = tid & 3, chunk = tid >> 2;
-    const uint32_t cofs = (chunk >> 6) * (kRGTile / 2) + (chunk & 63) * 16;
-    float acc[4][R];
+    // ranks up to 8: thread t takes four columns (chunk t / 4) and rows
+    // t % 4 + 4 h of a unit; above 8, two columns (chunk t / 2) and rows
+    // t % 2 + 2 h, so that the accumulators (columns x R) stay in registers
+    constexpr int NC = R <= 8 ? 4 : 2;    // columns per thread
+    constexpr int RP = NC == 4 ? 4 : 2;   // row phases
+    constexpr int NH = kRGRows / RP;      // rows per thread and unit
+    const uint32_t r0 = tid % RP, chunk = tid / RP;
+    // chunks of NC columns; box (chunk / (256 / NC)) holds columns 256 (chunk / (256 / NC)) ..
+    constexpr uint32_t kPerBox = 256 / NC;
+    const uint32_t cofs = (chunk / kPerBox) * (kRGTile / 2) + (chunk % kPerBox) * (4 * NC);
+    float acc[NC][R];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+    for (int q = 0; q < NC; ++q)
 #pragma unroll
       for (int c = 0; c < R; ++c) acc[q][c] = 0.0f;
     UnitCursor cur(u0, RG);
@@ -1340,51 +1350,62 @@ __global__ void __launch_bounds__(kQThreads, 1) psgd_qstream_kernel(
       const uint32_t ps = t + kRGTile;
       // rows one after the other (ranks above 8 keep one row's P in
       // registers at a time)
-      constexpr int kHU = R <= 8 ? kRGPer : 1;
+      constexpr int kHU = R <= 8 ? NH : 1;
 #pragma unroll kHU
-      for (int h = 0; h < kRGPer; ++h) {
-        const uint32_t row = r0 + 4 * h;
-        float4 mv = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int h = 0; h < NH; ++h) {
+        const uint32_t row = r0 + RP * h;
+        float x[NC];
+#pragma unroll
+        for (int q = 0; q < NC; ++q) x[q] = 0.0f;
         float pr[R];
 #pragma unroll
         for (int c = 0; c < R; ++c) pr[c] = 0.0f;
         if (!skip) {
-          mv = lds128(t + cofs + row * 1024);
+          if constexpr (NC == 4) {
+            const float4 mv = lds128(t + cofs + row * 1024);
+            x[0] = mv.x; x[1] = mv.y; x[2] = mv.z; x[3] = mv.w;
+          } else {
+            lds64(t + cofs + row * 1024, x[0], x[1]);
+          }
           lds_prow<R>(ps + row * R * 4, pr);
         }
-        const float x[4] = {mv.x, mv.y, mv.z, mv.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < NC; ++q)
 #pragma unroll
           for (int c = 0; c < R; ++c) acc[q][c] = fmaf(x[q], pr[c], acc[q][c]);
       }
       if (!skip) {
         // the stage can be refilled once every warp has read it: each lane's
-        // loaded values have been used above (so its loads are complete)
-        // before the warp's one arrival
+        // sums are brought up to date here, so its loads from the stage
+        // have returned, before the warp's one arrival
+#pragma unroll
+        for (int q = 0; q < NC; ++q)
+#pragma unroll
+          for (int c = 0; c < R; ++c) settle(acc[q][c]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
       }
       if (cur.blk != RG - 1 && i != u1 - u0 - 1) continue;
-      // end of this CTA's part of column block cb: its partial sums
+      // end of this CTA's part of column block cb: its partial sums (the
+      // row phases are adjacent lanes)
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
+      for (int q = 0; q < NC; ++q)
 #pragma unroll
         for (int c = 0; c < R; ++c) {
           float v = acc[q][c];
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
+#pragma unroll
+          for (int o = 1; o < RP; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
           acc[q][c] = v;
         }
       if (r0 == 0) {
-        float* dst = part + ((int64_t)(cta + cb) * kRGCols + 4 * chunk) * R;
+        float* dst = part + ((int64_t)(cta + cb) * kRGCols + NC * chunk) * R;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < NC; ++q)
 #pragma unroll
           for (int c = 0; c < R; ++c) dst[q * R + c] = acc[q][c];
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
+      for (int q = 0; q < NC; ++q)
 #pragma unroll
         for (int c = 0; c < R; ++c) acc[q][c] = 0.0f;
     }

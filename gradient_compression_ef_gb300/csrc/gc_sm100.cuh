@@ -186,18 +186,35 @@ __device__ __forceinline__ void cp_async16_zfill_hint(uint32_t dst, const void* 
 // Shared-memory loads and stores on 32-bit shared addresses (explicit
 // shared-space instructions: a generic pointer whose address space the
 // compiler cannot prove would go through the global load/store path).
+// The loads carry a memory clobber: a stage is handed back to its producer
+// by an mbarrier arrival, and a load the compiler moved past that arrival
+// could read the stage after the next copy into it has begun.
 __device__ __forceinline__ float4 lds128(uint32_t a) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(a));
+               : "r"(a)
+               : "memory");
   return v;
 }
 __device__ __forceinline__ float lds32(uint32_t a) {
   float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
   return v;
 }
+__device__ __forceinline__ void lds64(uint32_t a, float& x, float& y) {
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(x), "=f"(y) : "r"(a) : "memory");
+}
+// Makes the value(s) be computed at this point of the program: the compiler
+// cannot sink their arithmetic (or the loads it waits for) below it.  A
+// consumer that hands a stage back with an mbarrier arrival puts this on
+// everything it derived from the stage before the arrival, so that every
+// load from the stage has returned its data by then.
+__device__ __forceinline__ void settle(float& x) { asm volatile("" : "+f"(x)::"memory"); }
+__device__ __forceinline__ void settle(float4& v) {
+  asm volatile("" : "+f"(v.x), "+f"(v.y), "+f"(v.z), "+f"(v.w)::"memory");
+}
+
 __device__ __forceinline__ void sts128(uint32_t a, float4 v) {
   asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v.x), "f"(v.y), "f"(v.z),
                "f"(v.w)
@@ -270,7 +287,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
         "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
+      : "r"(taddr)
+      : "memory");
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
