@@ -808,9 +808,6 @@ __global__ void __launch_bounds__(kThreads, 1) psgd_p_tc_kernel(
     }
   } else if (warp < kProducerWarp) {
     const uint32_t ch = lane & 7;
-    // G and E are read once; M is read again by the next two passes: ask L2
-    // to keep M's lines and let G's and E's go first
-    const uint64_t pol_once = l2_evict_first(), pol_keep = l2_evict_last();
     // staging slot q holds piece j (0..3: G of operand row p = j, 4..7: E)
     // of thread t at stg + ((q * 8 + j) * kConv + t) * 16
     auto stage_unit = [&](int64_t rt, int64_t kb, int q) {
@@ -821,10 +818,8 @@ __global__ void __launch_bounds__(kThreads, 1) psgd_p_tc_kernel(
         const int64_t col = kb * KU + (a % SG) * kKBlk + 4 * ch;
         const bool in = grow < m && col < n;  // n % 4 == 0: a chunk is in or out
         const int64_t off = in ? grow * n + col : 0;
-        cp_async16_zfill_hint(s.stg + ((q * 8 + p) * kConv + tid) * 16, G + off, in ? 16u : 0u,
-                              pol_once);
-        cp_async16_zfill_hint(s.stg + ((q * 8 + 4 + p) * kConv + tid) * 16, E + off,
-                              in ? 16u : 0u, pol_once);
+        cp_async16_zfill(s.stg + ((q * 8 + p) * kConv + tid) * 16, G + off, in ? 16u : 0u);
+        cp_async16_zfill(s.stg + ((q * 8 + 4 + p) * kConv + tid) * 16, E + off, in ? 16u : 0u);
       }
       cp_async_commit();
     };
@@ -864,7 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1) psgd_p_tc_kernel(
         const uint32_t a = p * (kConv / 8) + warp * 4 + (lane >> 3);
         const int64_t grow = rt * RG + a / SG;
         const int64_t col = kb * KU + (a % SG) * kKBlk + 4 * ch;
-        if (grow < m && col < n) stg128_hint(E + grow * n + col, g[p], pol_keep);
+        if (grow < m && col < n) *reinterpret_cast<float4*>(E + grow * n + col) = g[p];
       }
       // the operand stage is free once the MMAs of unit i - S are done (a
       // warp gives up as one; no barrier of the converters follows, and the
@@ -1091,7 +1086,6 @@ __global__ void __launch_bounds__(kResidThreads, 1) psgd_resid_tma_kernel(
   if (warp == kLoader) {
     if (lane == 0) {
       tma_prefetch_map(&tmE);
-      const uint64_t pol_last_use = l2_evict_first();  // M's last read
       UnitCursor cur(u0, RG);
       Ring<S> ring;
       for (int64_t i = 0; i < u1 - u0; ++i, cur.next(), ring.next()) {
@@ -1103,11 +1097,9 @@ __global__ void __launch_bounds__(kResidThreads, 1) psgd_resid_tma_kernel(
         const int64_t cb = cur.tile, rg = cur.blk;
         unsigned char* stage = base + (size_t)st * kStageBytes;
         mbar_arrive_expect_tx(&full[st], kRGTile + kPBytes);
-        tma_load_2d_hint(smem_u32(stage), &tmE, (int32_t)(cb * kRGCols), (int32_t)(rg * kRGRows),
-                         &full[st], pol_last_use);
-        tma_load_2d_hint(smem_u32(stage + kRGTile / 2), &tmE,
-                         (int32_t)(cb * kRGCols + kRGCols / 2), (int32_t)(rg * kRGRows),
-                         &full[st], pol_last_use);
+        tma_load_2d(stage, &tmE, (int32_t)(cb * kRGCols), (int32_t)(rg * kRGRows), &full[st]);
+        tma_load_2d(stage + kRGTile / 2, &tmE, (int32_t)(cb * kRGCols + kRGCols / 2),
+                    (int32_t)(rg * kRGRows), &full[st]);
         bulk_load(stage + kRGTile, phat + rg * kRGRows * R, kPBytes, &full[st]);
         ++loads;
       }
@@ -1118,7 +1110,6 @@ __global__ void __launch_bounds__(kResidThreads, 1) psgd_resid_tma_kernel(
   } else {
     // thread t: column chunk t % 128 (four columns), rows t / 128 + 4 h
     const uint32_t chunk = tid & 127, r0 = tid >> 7;
-    const uint64_t pol_out = l2_evict_first();  // E' is not read again in this step
     int64_t cur_cb = -1;
     float qv[4][R];
     UnitCursor cur(u0, RG);
@@ -1178,7 +1169,7 @@ __global__ void __launch_bounds__(kResidThreads, 1) psgd_resid_tma_kernel(
 #pragma unroll
       for (int h = 0; h < kRGPer; ++h) {
         const int64_t grow = rg * kRGRows + r0 + 4 * h;
-        if (grow < m && col < n) stg128_hint(E + grow * n + col, out[h], pol_out);
+        if (grow < m && col < n) *reinterpret_cast<float4*>(E + grow * n + col) = out[h];
       }
     }
   }
@@ -1292,7 +1283,6 @@ __global__ void __launch_bounds__(kQThreads, 1) psgd_qstream_kernel(
   } else if (warp == kLoader) {
     if (lane == 0) {
       tma_prefetch_map(&tmM);
-      const uint64_t pol_keep = l2_evict_unchanged();  // M is read once more
       UnitCursor cur(u0, RG);
       Ring<S> ring;
       for (int64_t i = 0; i < u1 - u0; ++i, cur.next(), ring.next()) {
@@ -1304,11 +1294,9 @@ __global__ void __launch_bounds__(kQThreads, 1) psgd_qstream_kernel(
         const int64_t cb = cur.tile, rg = cur.blk;
         unsigned char* stage = base + (size_t)st * kStageBytes;
         mbar_arrive_expect_tx(&full[st], kRGTile + kPBytes);
-        tma_load_2d_hint(smem_u32(stage), &tmM, (int32_t)(cb * kRGCols), (int32_t)(rg * kRGRows),
-                         &full[st], pol_keep);
-        tma_load_2d_hint(smem_u32(stage + kRGTile / 2), &tmM,
-                         (int32_t)(cb * kRGCols + kRGCols / 2), (int32_t)(rg * kRGRows),
-                         &full[st], pol_keep);
+        tma_load_2d(stage, &tmM, (int32_t)(cb * kRGCols), (int32_t)(rg * kRGRows), &full[st]);
+        tma_load_2d(stage + kRGTile / 2, &tmM, (int32_t)(cb * kRGCols + kRGCols / 2),
+                    (int32_t)(rg * kRGRows), &full[st]);
         bulk_load(stage + kRGTile, pp + rg * kRGRows * R, kPBytes, &full[st]);
         ++loads;
       }

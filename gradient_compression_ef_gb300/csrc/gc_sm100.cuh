@@ -109,43 +109,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// L2 eviction priorities (createpolicy): lines touched under evict_first
-// leave L2 first when it needs room, evict_last ones last; evict_unchanged
-// keeps a resident line's priority.  Hints only: results never depend on
-// them.
-__device__ __forceinline__ uint64_t l2_evict_first() {
-  uint64_t p;
-  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t l2_evict_last() {
-  uint64_t p;
-  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t l2_evict_unchanged() {
-  uint64_t p;
-  asm("createpolicy.fractional.L2::evict_unchanged.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-// tma_load_2d (shared-space destination) under an L2 policy.
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int32_t x,
-                                                 int32_t y, uint64_t* bar, uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
-      : "memory");
-}
-
-// A 16-byte global store under an L2 policy.
-__device__ __forceinline__ void stg128_hint(float* p, float4 v, uint64_t pol) {
-  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x),
-               "f"(v.y), "f"(v.z), "f"(v.w), "l"(pol)
-               : "memory");
-}
-
 // Contiguous global -> shared copy of `bytes` (a multiple of 16; both
 // addresses 16-byte aligned), completing `bar`'s transactions.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
@@ -172,14 +135,6 @@ __device__ __forceinline__ void bulk_load_s(uint32_t dst, const void* src, uint3
 __device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
                "r"(src_bytes)
-               : "memory");
-}
-
-// cp_async16_zfill under an L2 policy.
-__device__ __forceinline__ void cp_async16_zfill_hint(uint32_t dst, const void* src,
-                                                      uint32_t src_bytes, uint64_t pol) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst),
-               "l"(src), "r"(src_bytes), "l"(pol)
                : "memory");
 }
 

@@ -70,10 +70,12 @@ def test_workload_shapes_five_steps(env, shape):
 def test_residual_matches_its_own_factors_elementwise(env):
     """E' = M - P_hat Q'^T holds element by element, with the step's own
     P_hat and Q', at every step of two five-step runs on the 4096 x 11008
-    workload matrix.  A residual pass that read part of a staged tile after
-    its next refill had begun gives wrong values in one row of a few hundred
-    columns: far below the Frobenius bar of the comparisons with the oracle,
-    but of the elements' own size here."""
+    workload matrix, and Q' = M^T P_hat column by column.  A residual pass
+    that read part of a staged tile after its next refill had begun gives
+    wrong values in one row of a few hundred columns: far below the
+    Frobenius bar of the comparisons with the oracle, but of the elements'
+    own size here; the same fault in the Q' pass would move a column sum by
+    one row's term of 4096 (about 1/64 of it)."""
     torch, gc, ctx = env
     m, n, r = 4096, 11008, 4
     M0, Q0 = inputs.low_rank_matrix(m, n, r=r)
@@ -91,7 +93,13 @@ def test_residual_matches_its_own_factors_elementwise(env):
             worst = D.abs().max().item()
             assert worst <= 1e-3 * rms, "step %d: |E' - (M - P_hat Q'^T)| up to %.3e (rms %.3e)" % (
                 step, worst, rms)
-            del M, D
+            del D
+            Qx = M.double().T @ P.double()
+            dq = (Q.double() - Qx).abs().max(dim=0).values
+            scale = Qx.abs().max(dim=0).values
+            assert bool((dq <= 1e-4 * scale).all()), "step %d: |Q' - M^T P_hat| / max |col| = %s" % (
+                step, (dq / scale).tolist())
+            del M, Qx
 
 
 def test_zero_gradient(env):
