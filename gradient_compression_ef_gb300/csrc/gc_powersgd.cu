@@ -1094,6 +1094,10 @@ __global__ void __launch_bounds__(kResidThreads, 1) psgd_resid_tma_kernel(
           ok = false;
           break;
         }
+        // the warps read the stage through the generic proxy and the refill
+        // writes it through the asynchronous one: order those reads (made
+        // visible to this thread by the barrier) before the copy
+        fence_proxy_async_smem();
         const int64_t cb = cur.tile, rg = cur.blk;
         unsigned char* stage = base + (size_t)st * kStageBytes;
         mbar_arrive_expect_tx(&full[st], kRGTile + kPBytes);
@@ -1291,6 +1295,10 @@ __global__ void __launch_bounds__(kQThreads, 1) psgd_qstream_kernel(
           ok = false;
           break;
         }
+        // the warps read the stage through the generic proxy and the refill
+        // writes it through the asynchronous one: order those reads (made
+        // visible to this thread by the barrier) before the copy
+        fence_proxy_async_smem();
         const int64_t cb = cur.tile, rg = cur.blk;
         unsigned char* stage = base + (size_t)st * kStageBytes;
         mbar_arrive_expect_tx(&full[st], kRGTile + kPBytes);
